@@ -1,0 +1,172 @@
+"""CPU oracle for the Q4_K / Q6_K x Q8 matmul path (numpy front end over plain C).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the bench's ``cpu_baseline`` / ``--impl reference`` legs, never by the
+package.  It shares no code with the CUDA library.
+
+Every function here is a thin marshalling layer over ``mq_oracle.c``; the
+arithmetic, and the citation of the passage each step follows, live there.
+Arrays use the oracle's own logical layouts:
+
+* weights: raw GGML block bytes, ``[N, K/256, 144]`` (Q4_K) or ``[N, K/256, 210]`` (Q6_K)
+* Q8 plane: ``q`` int8 ``[M, K]``, ``d`` f32 ``[M, K/32]``, ``S`` int32 ``[M, K/32]``
+* outputs: f64 ``[len(ms), len(ns)]`` for the listed (token, row) index pairs
+
+Every oracle function is pinned by ``tests/test_oracle_*.py`` against hand-built
+blocks, closed forms, invariants and brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import build_oracle
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = build_oracle.build()
+        L = ctypes.CDLL(path)
+        P, I64, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+        L.oq_half_to_double.argtypes = [ctypes.c_uint16]
+        L.oq_half_to_double.restype = ctypes.c_double
+        L.oq_q4k_fields.argtypes = [P, P, P, P, P, P]
+        L.oq_q6k_fields.argtypes = [P, P, P, P]
+        L.oq_q4k_dequant.argtypes = [P, I64, I64, P]
+        L.oq_q6k_dequant.argtypes = [P, I64, I64, P]
+        L.oq_rmsnorm.argtypes = [P, I64, I64, P, F32, P]
+        L.oq_quantize_q8.argtypes = [P, I64, I64, P, P, P]
+        for f in (L.oq_q4k_blockdots, L.oq_q6k_blockdots):
+            f.argtypes = [P, I64, I64, P, I64, P, I64, P, I64, P, P]
+        for f in (L.oq_q4k_matmul, L.oq_q6k_matmul):
+            f.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, I64, P]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+BLOCK_BYTES = {"q4k": 144, "q6k": 210}
+
+
+def _weights(w: np.ndarray, fmt: str):
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    n = w.shape[0]
+    per_row = w.size // n
+    nb = per_row // BLOCK_BYTES[fmt]
+    assert nb * BLOCK_BYTES[fmt] == per_row
+    return w, n, nb * 256
+
+
+def half_to_double(bits: int) -> float:
+    return lib().oq_half_to_double(int(bits) & 0xFFFF)
+
+
+def q4k_fields(block: np.ndarray):
+    """Decode one 144-byte Q4_K block -> (d, dmin, sc[8], m[8], q[256])."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8).reshape(144)
+    d, dmin = ctypes.c_double(), ctypes.c_double()
+    sc, mn, q = np.zeros(8, np.int32), np.zeros(8, np.int32), np.zeros(256, np.int32)
+    lib().oq_q4k_fields(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(mn), _p(q))
+    return d.value, dmin.value, sc, mn, q
+
+
+def q6k_fields(block: np.ndarray):
+    """Decode one 210-byte Q6_K block -> (d, sc[16], q[256])."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8).reshape(210)
+    d = ctypes.c_double()
+    sc, q = np.zeros(16, np.int32), np.zeros(256, np.int32)
+    lib().oq_q6k_fields(_p(blk), ctypes.byref(d), _p(sc), _p(q))
+    return d.value, sc, q
+
+
+def dequantize(w: np.ndarray, fmt: str) -> np.ndarray:
+    """Dequantized weights [N, K] in f64."""
+    w, n, k = _weights(w, fmt)
+    out = np.empty((n, k), np.float64)
+    (lib().oq_q4k_dequant if fmt == "q4k" else lib().oq_q6k_dequant)(_p(w), n, k, _p(out))
+    return out
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    m, k = x.shape
+    y = np.empty_like(x)
+    lib().oq_rmsnorm(_p(x), m, k, _p(w), float(eps), _p(y))
+    return y
+
+
+def quantize_q8(x: np.ndarray, rms_w: np.ndarray | None = None, eps: float = 1e-6):
+    """Q8 plane of x (optionally after the RMSNorm producer) -> (q, d, S)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if rms_w is not None:
+        x = rmsnorm(x, rms_w, eps)
+    m, k = x.shape
+    assert k % 32 == 0
+    q = np.empty((m, k), np.int8)
+    d = np.empty((m, k // 32), np.float32)
+    S = np.empty((m, k // 32), np.int32)
+    lib().oq_quantize_q8(_p(x), m, k, _p(q), _p(d), _p(S))
+    return q, d, S
+
+
+def _idx(v, limit):
+    v = np.ascontiguousarray(np.arange(limit) if v is None else v, dtype=np.int64)
+    assert v.ndim == 1 and (v.size == 0 or (v.min() >= 0 and v.max() < limit))
+    return v
+
+
+def blockdots(w: np.ndarray, fmt: str, q: np.ndarray, ms=None, ns=None):
+    """Integer checkpoint I[len(ms), len(ns), K/32] (and the raw dots D)."""
+    w, n, k = _weights(w, fmt)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    m = q.shape[0]
+    assert q.shape[1] == k
+    ms, ns = _idx(ms, m), _idx(ns, n)
+    I = np.zeros((ms.size, ns.size, k // 32), np.int32)
+    if fmt == "q4k":
+        D = np.zeros_like(I)
+        lib().oq_q4k_blockdots(_p(w), n, k, _p(q), m, _p(ms), ms.size, _p(ns), ns.size, _p(I), _p(D))
+    else:
+        D = np.zeros((ms.size, ns.size, k // 32, 2), np.int32)
+        lib().oq_q6k_blockdots(_p(w), n, k, _p(q), m, _p(ms), ms.size, _p(ns), ns.size, _p(I), _p(D))
+    return I, D
+
+
+def matmul(w: np.ndarray, fmt: str, plane, ms=None, ns=None, threads: int = 1) -> np.ndarray:
+    """Y[len(ms), len(ns)] (f64) from weight bytes and an oracle Q8 plane (q, d, S).
+
+    ``threads`` > 1 splits the row list ``ns`` over Python threads (the C call
+    releases the GIL); each thread runs the same plain C loop on its slice.
+    """
+    w, n, k = _weights(w, fmt)
+    q, d, S = (np.ascontiguousarray(a) for a in plane)
+    m = q.shape[0]
+    assert q.shape == (m, k) and d.shape == (m, k // 32) and S.shape == (m, k // 32)
+    assert q.dtype == np.int8 and d.dtype == np.float32 and S.dtype == np.int32
+    ms, ns = _idx(ms, m), _idx(ns, n)
+    fn = lib().oq_q4k_matmul if fmt == "q4k" else lib().oq_q6k_matmul
+    if threads <= 1 or ns.size < 2:
+        y = np.empty((ms.size, ns.size), np.float64)
+        fn(_p(w), n, k, _p(q), _p(d), _p(S), m, _p(ms), ms.size, _p(ns), ns.size, _p(y))
+        return y
+    parts = np.array_split(ns, min(threads, ns.size))
+
+    def run(part):
+        part = np.ascontiguousarray(part)
+        yp = np.empty((ms.size, part.size), np.float64)
+        fn(_p(w), n, k, _p(q), _p(d), _p(S), m, _p(ms), ms.size, _p(part), part.size, _p(yp))
+        return yp
+
+    with ThreadPoolExecutor(len(parts)) as ex:
+        return np.concatenate(list(ex.map(run, parts)), axis=1)

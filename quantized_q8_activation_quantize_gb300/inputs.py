@@ -1,0 +1,179 @@
+"""Seeded synthetic inputs for the Q4_K / Q6_K x Q8 matmul path.
+
+This module draws random numbers and lays out random bytes.  It holds none of
+the method's arithmetic: nothing here decodes a block, quantizes an
+activation or multiplies anything.  The CUDA path (through the tests and the
+bench) and the CPU oracle both consume exactly the arrays made here, so the
+two sides always see identical bytes.
+
+Workloads follow the 7B q4_K_m shapes of the minfer pages (Qwen2.5-7B: hidden
+3584, 28 query heads and 4 KV heads of dim 128, FFN 18944, vocab 152064;
+3314-token prefill prompt).  Seeds are ``20261202 + 100 * config + stream``
+with stream 0 = weights, 1 = activations, 2 = RMSNorm weight, 3 = outlier
+channel choice; matrices of one config that need separate streams add their
+(layer, matrix) index to the numpy ``SeedSequence``.
+
+Block sizes (GGML k-quant super-blocks of 256 values): Q4_K = 144 bytes
+(fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales/mins, 128 bytes of 4-bit
+quants); Q6_K = 210 bytes (128 bytes low 4 bits, 64 bytes high 2 bits,
+16 int8 scales, fp16 d).  Only the positions of the fp16 and int8 scale
+fields matter here, so that their value ranges can be drawn as stated.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SEED_BASE = 20261202
+STREAM_W, STREAM_X, STREAM_RMS_W, STREAM_OUTLIERS = 0, 1, 2, 3
+
+QK_K = 256             # values per k-quant super-block
+Q8_BLOCK = 32          # values per Q8 activation block
+Q4K_BYTES = 144
+Q6K_BYTES = 210
+
+HIDDEN = 3584
+FFN = 18944
+KV_DIM = 4 * 128
+VOCAB = 152064
+PREFILL_TOKENS = 3314
+N_LAYERS = 28
+
+
+def seed(config: int, stream: int) -> int:
+    return SEED_BASE + 100 * config + stream
+
+
+def rng(config: int, stream: int, *extra: int) -> np.random.Generator:
+    """PCG64 generator for one (config, stream[, layer, matrix]) input."""
+    if extra:
+        return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed(config, stream), *extra])))
+    return np.random.Generator(np.random.PCG64(seed(config, stream)))
+
+
+def _fp16_bytes(r: np.random.Generator, shape, lo: float, hi: float) -> np.ndarray:
+    """fp16 values drawn uniform in [lo, hi] (f64 draw, round-to-nearest-even to fp16), as LE bytes."""
+    v = r.uniform(lo, hi, size=shape).astype(np.float16)
+    return v.astype("<f2").view(np.uint8).reshape(*shape, 2)
+
+
+def q4k_weights(r: np.random.Generator, n_rows: int, k: int,
+                d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Q4_K weight matrix as raw bytes, shape [n_rows, k/256, 144].
+
+    d and dmin are fp16 drawn uniform in ``d_range``; the 12 packed scale/min
+    bytes and the 128 quant bytes are uniform random bytes (the 6-bit packing
+    maps 12 uniform bytes onto 16 uniform 6-bit fields, and a uniform byte holds
+    two uniform 4-bit quants).
+    """
+    assert k % QK_K == 0
+    nb = k // QK_K
+    w = np.frombuffer(r.bytes(n_rows * nb * Q4K_BYTES), dtype=np.uint8).reshape(n_rows, nb, Q4K_BYTES).copy()
+    w[..., 0:2] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    w[..., 2:4] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    return w
+
+
+def q6k_weights(r: np.random.Generator, n_rows: int, k: int,
+                scale_range=(-64, 63), d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Q6_K weight matrix as raw bytes, shape [n_rows, k/256, 210].
+
+    The 128 low-bit bytes and 64 high-bit bytes are uniform random bytes; the
+    16 int8 sub-block scales are uniform integers in ``scale_range``
+    (inclusive); d is fp16 drawn uniform in ``d_range``.
+    """
+    assert k % QK_K == 0
+    nb = k // QK_K
+    w = np.frombuffer(r.bytes(n_rows * nb * Q6K_BYTES), dtype=np.uint8).reshape(n_rows, nb, Q6K_BYTES).copy()
+    sc = r.integers(scale_range[0], scale_range[1] + 1, size=(n_rows, nb, 16), dtype=np.int16).astype(np.int8)
+    w[..., 192:208] = sc.view(np.uint8)
+    w[..., 208:210] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    return w
+
+
+def activations(r: np.random.Generator, m: int, k: int) -> np.ndarray:
+    """f32 activations [m, k] drawn N(0, 1)."""
+    return r.standard_normal((m, k), dtype=np.float32)
+
+
+def outlier_channels(r: np.random.Generator, k: int, fraction: float = 0.01) -> np.ndarray:
+    """Sorted channel indices (round(fraction * k) of them) from a seeded permutation."""
+    n = int(round(fraction * k))
+    return np.sort(r.permutation(k)[:n])
+
+
+def rms_weight(r: np.random.Generator, k: int) -> np.ndarray:
+    """RMSNorm weight [k] drawn N(1, 0.1) in f32."""
+    return (1.0 + 0.1 * r.standard_normal(k)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------------------------
+# The five workloads.  Each returns plain numpy arrays; sizes are in the docstrings.
+# --------------------------------------------------------------------------------------------
+
+def config0():
+    """Tiny Q4_K GEMM: W 256 x 512 (Q4_K), X 8 x 512 N(0,1); Y is 8 x 256."""
+    w = q4k_weights(rng(0, STREAM_W), 256, 512)
+    x = activations(rng(0, STREAM_X), 8, 512)
+    return {"w": w, "x": x, "fmt": "q4k"}
+
+
+def config1():
+    """q_proj prefill: W 3584 x 3584 (Q4_K), X 512 x 3584 N(0,1) with 36 channels x20."""
+    w = q4k_weights(rng(1, STREAM_W), HIDDEN, HIDDEN)
+    x = activations(rng(1, STREAM_X), 512, HIDDEN)
+    ch = outlier_channels(rng(1, STREAM_OUTLIERS), HIDDEN)
+    x[:, ch] *= np.float32(20.0)
+    return {"w": w, "x": x, "fmt": "q4k", "outlier_channels": ch}
+
+
+def config2(m: int = PREFILL_TOKENS):
+    """7B FFN prefill: gate/up W 18944 x 3584 (Q4_K), down W 3584 x 18944 (Q6_K, scales [-64, 63]).
+
+    x_hidden [m, 3584] N(0,1) goes through the RMSNorm producer (weight N(1, 0.1), eps 1e-6)
+    for gate and up; x_ffn [m, 18944] N(0,1) is the down projection's plain input.
+    """
+    return {
+        "w_gate": q4k_weights(rng(2, STREAM_W, 0), FFN, HIDDEN),
+        "w_up": q4k_weights(rng(2, STREAM_W, 1), FFN, HIDDEN),
+        "w_down": q6k_weights(rng(2, STREAM_W, 2), HIDDEN, FFN),
+        "x_hidden": activations(rng(2, STREAM_X, 0), m, HIDDEN),
+        "x_ffn": activations(rng(2, STREAM_X, 1), m, FFN),
+        "rms_w": rms_weight(rng(2, STREAM_RMS_W), HIDDEN),
+        "eps": np.float32(1e-6),
+    }
+
+
+# matrices of one decoder layer: (name, rows N, reduction K)
+LAYER_MATRICES = (("q", HIDDEN, HIDDEN), ("k", KV_DIM, HIDDEN), ("v", KV_DIM, HIDDEN),
+                  ("o", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN),
+                  ("down", HIDDEN, FFN))
+
+
+def config3_layout(n_layers: int = N_LAYERS):
+    """The decode sweep's matmul list: (layer, index, name, fmt, N, K).
+
+    q, k, o, gate, up are Q4_K.  v and down are Q6_K in even layers and Q4_K in
+    odd layers (14 of 28 layers carry a Q6_K attn_v, the q4_K_m mix).
+    """
+    out = []
+    for layer in range(n_layers):
+        for idx, (name, n, k) in enumerate(LAYER_MATRICES):
+            fmt = "q6k" if (name in ("v", "down") and layer % 2 == 0) else "q4k"
+            out.append((layer, idx, name, fmt, n, k))
+    return out
+
+
+def config3_matrix(layer: int, idx: int):
+    """Weight bytes and the 1 x K activation for one matmul of the decode sweep."""
+    _, _, name, fmt, n, k = next(e for e in config3_layout(layer + 1) if e[0] == layer and e[1] == idx)
+    gen = q6k_weights if fmt == "q6k" else q4k_weights
+    w = gen(rng(3, STREAM_W, layer, idx), n, k)
+    x = activations(rng(3, STREAM_X, layer, idx), 1, k)
+    return {"w": w, "x": x, "fmt": fmt, "name": name}
+
+
+def config4(m: int):
+    """LM head: W 152064 x 3584 (Q6_K, scales [-64, 63]), X m x 3584 N(0,1), m in {1, 16, 3314}."""
+    w = q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
+    x = activations(rng(4, STREAM_X, m), m, HIDDEN)
+    return {"w": w, "x": x, "fmt": "q6k"}
