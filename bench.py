@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the Q4_K / Q6_K x Q8 path on GB300 at 7B shapes.  Prints ONE JSON line.
+
+Step (the headline `value`): one 7B FFN prefill at the pages' 3314-token prompt length
+(config 2), every row of the hot path:
+    RMSNorm-fused Q8 quantize (x_hidden 3314 x 3584)
+    -> Q4_K tensor-core GEMM gate (18944 x 3584)  -> Q4_K GEMM up (18944 x 3584)
+    -> plain Q8 quantize (x_ffn 3314 x 18944)      -> Q6_K GEMM down (3584 x 18944)
+value = 2*M*N*K integer ops summed over the three GEMMs / step time, in TOPS.
+The step's footprint (weights 132 MB, activations 298 MB, outputs 549 MB) is far larger
+than the 129 MB L2, so consecutive steps do not hit L2 for their inputs (no flush).
+
+Also reported, measured in the same run:
+  "decode":  config 3, one decode token through all 196 per-layer matmuls of a 28-layer
+             7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph),
+             weight GB/s and tok/s; 3.9 GB of weights, far larger than L2.
+  "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
+  "roofline": the dominant kernel (Q4_K GEMM) against the measured dense bf16 tensor peak
+             (f16 MMA rate = bf16 rate); "roofline_decode": the LM-head GEMV against the
+             measured HBM copy bandwidth.
+  "e2e":     the same step through the C ABI from pinned host buffers, with the activation
+             copies in and the three outputs copied back inside the timed region.
+  "cpu_baseline": the CPU oracle on this host's cores on a token slice of the same step.
+
+--impl reference times the CPU oracle itself on the same workload (a token slice per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4_K/Q6_K MMQ prefill int8 TOPS + MMVQ decode weight GB/s at 7B shapes"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mq", "reference"], default="mq")
+    ap.add_argument("--skip-decode", action="store_true", help="prefill step only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ distributed ---
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, use_cuda: bool):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if self.pg.get_backend() == "nccl" else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+
+# ----------------------------------------------------------------------------------- clocks ---
+
+class Clocks:
+    """nvidia-smi sampler running only while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path):
+            p = [s.strip() for s in ln.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------- workloads ---
+
+def ffn_ops(M):
+    from quantized_q8_activation_quantize_gb300 import inputs as I
+    return 2 * M * (2 * I.FFN * I.HIDDEN + I.HIDDEN * I.FFN)
+
+
+class Prefill:
+    """Config 2: the 7B FFN prefill step at M = 3314, device-resident inputs."""
+
+    def __init__(self, torch, B, I):
+        self.torch, self.B = torch, B
+        c = I.config2()
+        self.M, self.H, self.F = c["x_hidden"].shape[0], I.HIDDEN, I.FFN
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.w_gate = dev(c["w_gate"].reshape(self.F, -1))
+        self.w_up = dev(c["w_up"].reshape(self.F, -1))
+        self.w_down = dev(c["w_down"].reshape(self.H, -1))
+        self.host_x_h = torch.from_numpy(c["x_hidden"]).pin_memory()
+        self.host_x_f = torch.from_numpy(c["x_ffn"]).pin_memory()
+        self.x_h, self.x_f = self.host_x_h.cuda(), self.host_x_f.cuda()
+        self.rms_w = dev(c["rms_w"])
+        self.eps = float(c["eps"])
+        self.p_h = B.alloc_plane(self.M, self.H)
+        self.p_f = B.alloc_plane(self.M, self.F)
+        self.y_gate = torch.empty((self.M, self.F), dtype=torch.float32, device="cuda")
+        self.y_up = torch.empty_like(self.y_gate)
+        self.y_down = torch.empty((self.M, self.H), dtype=torch.float32, device="cuda")
+        self.ops = ffn_ops(self.M)
+        self.gemm_q4k_ops = 2 * self.M * self.F * self.H
+        self.gemm_q6k_ops = 2 * self.M * self.H * self.F
+        self.launches = 5
+
+    def step(self, ev=None):
+        """One pass; with `ev` (list of 6 events) records event boundaries between launches."""
+        B, M, H, F = self.B, self.M, self.H, self.F
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        rec(0)
+        B.mq_quantize_q8(self.x_h, M, H, self.rms_w, self.eps, self.p_h)
+        rec(1)
+        B.mq_gemm_q4k(self.w_gate, F, H, self.p_h, M, self.y_gate)
+        rec(2)
+        B.mq_gemm_q4k(self.w_up, F, H, self.p_h, M, self.y_up)
+        rec(3)
+        B.mq_quantize_q8(self.x_f, M, F, None, 0.0, self.p_f)
+        rec(4)
+        B.mq_gemm_q6k(self.w_down, H, F, self.p_f, M, self.y_down)
+        rec(5)
+
+    def e2e_setup(self):
+        t = self.torch
+        self.host_y = [t.empty(tuple(y.shape), dtype=t.float32).pin_memory() for y in (self.y_gate, self.y_up, self.y_down)]
+        self.h2d = self.host_x_h.numel() * 4 + self.host_x_f.numel() * 4
+        self.d2h = sum(y.numel() * 4 for y in self.host_y)
+
+    def e2e_step(self):
+        self.x_h.copy_(self.host_x_h, non_blocking=True)
+        self.x_f.copy_(self.host_x_f, non_blocking=True)
+        self.step()
+        for h, d in zip(self.host_y, (self.y_gate, self.y_up, self.y_down)):
+            h.copy_(d, non_blocking=True)
+
+
+class DecodeSweep:
+    """Config 3: one decode token through the 196 matmuls of a 28-layer 7B q4_K_m stack."""
+
+    def __init__(self, torch, B, I):
+        self.torch, self.B = torch, B
+        self.items = []
+        self.weight_bytes = 0
+        self.bytes = 0
+        for (layer, idx, name, fmt, n, k) in I.config3_layout():
+            c = I.config3_matrix(layer, idx)
+            w = torch.from_numpy(c["w"].reshape(n, -1)).cuda()
+            x = torch.from_numpy(c["x"]).cuda()
+            plane = B.alloc_plane(1, k)
+            y = torch.empty((1, n), dtype=torch.float32, device="cuda")
+            self.items.append((fmt, w, x, plane, y, n, k))
+            self.weight_bytes += w.numel()
+            self.bytes += w.numel() + 1.25 * k + 4 * n + 4 * k     # weights + plane + output + activation
+        self.graph = None
+
+    def run(self):
+        B = self.B
+        for fmt, w, x, plane, y, n, k in self.items:
+            B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
+            B.GEMV[fmt](w, n, k, plane, 1, y)
+
+    def capture(self):
+        t = self.torch
+        s = t.cuda.Stream()
+        s.wait_stream(t.cuda.current_stream())
+        with t.cuda.stream(s):
+            self.run()                     # warm the launch path outside the capture
+        t.cuda.current_stream().wait_stream(s)
+        t.cuda.synchronize()
+        self.graph = t.cuda.CUDAGraph()
+        with t.cuda.graph(self.graph):
+            self.run()
+        t.cuda.synchronize()
+
+
+def time_events(torch, fn, steps, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+# ------------------------------------------------------------------------------ CPU oracle ---
+
+def cpu_oracle_ffn(budget_s: float, threads: int):
+    """The oracle on token slices of the config-2 step until `budget_s` is spent."""
+    import oracle
+    from quantized_q8_activation_quantize_gb300 import inputs as I
+    c = I.config2()
+    t_done, ops, tokens = 0.0, 0, 0
+    chunk = 4
+    while t_done < budget_s and tokens < c["x_hidden"].shape[0]:
+        sl = slice(tokens, tokens + chunk)
+        t0 = time.perf_counter()
+        ph = oracle.quantize_q8(c["x_hidden"][sl], c["rms_w"], float(c["eps"]))
+        oracle.matmul(c["w_gate"], "q4k", ph, threads=threads)
+        oracle.matmul(c["w_up"], "q4k", ph, threads=threads)
+        pf = oracle.quantize_q8(c["x_ffn"][sl])
+        oracle.matmul(c["w_down"], "q6k", pf, threads=threads)
+        t_done += time.perf_counter() - t0
+        ops += ffn_ops(chunk)
+        tokens += chunk
+    return ops / t_done / 1e12, tokens, t_done
+
+
+# ------------------------------------------------------------------------------------ main ---
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    per_step = []
+    tokens = 0
+    budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        v, tok, t = cpu_oracle_ffn(budget, threads)
+        if i >= args.warmup:
+            per_step.append((v, tok, t))
+            tokens = tok
+    value = statistics.mean(v for v, _, _ in per_step)
+    ms = statistics.mean(t for _, _, t in per_step) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8 dots, f64 scaling (CPU oracle)",
+            "data": "synthetic (seeded, 7B q4_K_m shapes)",
+            "config": {"workload": "7B FFN prefill, 3314 tokens (config 2): RMSNorm-Q8, gate/up Q4_K 18944x3584, "
+                                   "Q8, down Q6_K 3584x18944", "tokens_per_step_sample": tokens},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
+                             "sample": f"first {tokens} of 3314 tokens of the FFN step per timed step"},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        dist.init(use_cuda=False)
+        run_reference(args, dist)
+        return
+    import torch
+    torch.cuda.set_device(dist.local)
+    dist.init(use_cuda=True)
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_q8_activation_quantize_gb300 import binding as B
+    from quantized_q8_activation_quantize_gb300 import inputs as I
+
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    W = max(3, args.warmup)
+    K = max(1, args.steps)
+
+    # ---------------- prefill step (headline)
+    pf = Prefill(torch, B, I)
+    for _ in range(W):
+        pf.step()
+    torch.cuda.synchronize()
+    B.mq_device_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for k in range(K):
+        pf.step(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    B.mq_device_status()
+    ms_step = dist.max(t_start.elapsed_time(t_end) / K)
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])   # ms per launch
+    k_ms = per.mean(axis=0)
+    value = dist.world * pf.ops / (ms_step * 1e-3) / 1e12
+
+    gemm_q4k_ms = (k_ms[1] + k_ms[2]) / 2
+    q4k_tflops = pf.gemm_q4k_ops / (gemm_q4k_ms * 1e-3) / 1e12
+    q6k_tflops = pf.gemm_q6k_ops / (k_ms[4] * 1e-3) / 1e12
+    qrms_gbs = (pf.M * pf.H * 4 + pf.H * 4 + B.mq_q8_plane_bytes(pf.M, pf.H)) / (k_ms[0] * 1e-3) / 1e9
+    q_gbs = (pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (k_ms[3] * 1e-3) / 1e9
+
+    # ---------------- e2e through host buffers
+    pf.e2e_setup()
+    e2e_ms = time_events(torch, pf.e2e_step, max(2, K // 2), 1)
+    e2e_ms = dist.max(e2e_ms)
+    e2e = {"value": dist.world * pf.ops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": pf.h2d, "d2h_bytes_per_step": pf.d2h}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": dist.world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 (exact integer block dots on f16 tensor-core MMA) + f32 scaling",
+        "data": "synthetic (seeded, 7B q4_K_m shapes)",
+        "config": {"workload": "7B FFN prefill, 3314 tokens (config 2): RMSNorm-Q8, gate/up Q4_K 18944x3584, "
+                               "Q8, down Q6_K 3584x18944", "tokens": pf.M, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{dist.world}"},
+        "kernels_ms": {"rms_quantize": k_ms[0], "gemm_q4k_gate": k_ms[1], "gemm_q4k_up": k_ms[2],
+                       "quantize": k_ms[3], "gemm_q6k_down": k_ms[4]},
+        "kernels_rate": {"gemm_q4k_tops": q4k_tflops, "gemm_q6k_tops": q6k_tflops,
+                         "rms_quantize_gbs": qrms_gbs, "quantize_gbs": q_gbs},
+        "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,
+                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} dense bf16 (f16 MMA has the same nominal rate)"},
+        "e2e": e2e, "gpu_launches": pf.launches * K, "clocks": clk,
+    }
+
+    # ---------------- decode: LM head GEMV and the 28-layer sweep
+    if not args.skip_decode:
+        lm_w = torch.from_numpy(I.config4_weights().reshape(I.VOCAB, -1)).cuda()
+        lm = {}
+        for m, paths in ((1, ("gemv",)), (16, ("gemv", "gemm"))):
+            x = torch.from_numpy(I.config4_x(m)).cuda()
+            plane = B.alloc_plane(m, I.HIDDEN)
+            B.mq_quantize_q8(x, m, I.HIDDEN, None, 0.0, plane)
+            y = torch.empty((m, I.VOCAB), dtype=torch.float32, device="cuda")
+            for path in paths:
+                f = (B.GEMV if path == "gemv" else B.GEMM)["q6k"]
+                ms = time_events(torch, lambda: f(lm_w, I.VOCAB, I.HIDDEN, plane, m, y), max(5, K), W)
+                gbs = (lm_w.numel() + B.mq_q8_plane_bytes(m, I.HIDDEN) + 4 * m * I.VOCAB) / (ms * 1e-3) / 1e9
+                lm[f"m{m}_{path}"] = {"ms": ms, "GB/s": gbs, "TOPS": 2 * m * I.VOCAB * I.HIDDEN / (ms * 1e-3) / 1e12}
+        line["lm_head"] = lm
+        g = lm["m1_gemv"]["GB/s"]
+        line["roofline_decode"] = {"bound": "hbm", "kernel": "mq_gemv_q6k (152064x3584, M=1)", "achieved": g,
+                                   "peak": hbm_peak, "unit": "GB/s", "frac": g / hbm_peak, "traffic": None,
+                                   "peak_kind": f"{peak_kind} HBM copy"}
+        del lm_w
+        torch.cuda.empty_cache()
+        sw = DecodeSweep(torch, B, I)
+        sw.capture()
+        ms = time_events(torch, sw.graph.replay, max(5, K), W)
+        B.mq_device_status()
+        line["decode"] = {"workload": "config 3: 28 layers x 7 matmuls, M=1 (Q8 quantize + GEMV each, one CUDA graph)",
+                          "ms_per_token": ms, "tok_per_s": 1e3 / ms, "weight_bytes": sw.weight_bytes,
+                          "GB/s": sw.bytes / (ms * 1e-3) / 1e9, "frac_of_hbm": sw.bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                          "launches_per_token": 2 * len(sw.items)}
+
+    # ---------------- CPU baseline (oracle on the host cores, rank 0 only)
+    if dist.rank == 0 and dist.world == 1:
+        threads = os.cpu_count() or 1
+        v, tokens, secs = cpu_oracle_ffn(args.cpu_seconds, threads)
+        line["cpu_baseline"] = {"value": v, "unit": "TOPS", "cores": threads, "kind": "oracle",
+                                "sample": f"first {tokens} of 3314 tokens of the FFN step ({secs:.1f} s)"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

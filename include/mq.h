@@ -1,0 +1,178 @@
+/*
+ * mq.h -- C ABI of the GB300 (sm_103a) quantized k-quant matmul library.
+ *
+ * The hot path of quantized LLM inference over GGML k-quant weights, as the
+ * minfer pages describe it ("minfer" book print view, "Features > GPU -- CUDA";
+ * "Support Matrix > CUDA notes"):
+ *   1. f32 activations are quantized on the fly into an int8 Q8 plane
+ *      (blocks of 32, one f32 scale per block), optionally straight out of an
+ *      RMSNorm producer, so the normalized f32 rows are never written;
+ *   2. prefill (many tokens) multiplies the plane with raw Q4_K / Q6_K
+ *      super-blocks on the tensor cores (MMQ);
+ *   3. decode (one or a few tokens) streams the raw weight bytes once and
+ *      takes integer dots per block on the CUDA cores (MMVQ).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     stated otherwise.  Nothing is retained after the call returns and the
+ *     library never allocates device memory.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and returns MQ_OK or a negative mq_status.  Argument
+ *     errors are detected on the host before anything is launched;
+ *     mq_last_error() then names the offending values.  There is no fallback
+ *     path: an unsupported device or shape is an error, never a slower route.
+ *   - Weights are raw GGML block bytes, row-major [N rows][K/256 super-blocks]
+ *     (weight memory layout [out][in], "Architecture > 4.5 Core invariants",
+ *     item 3), base aligned to 16 bytes.  K must be a positive multiple of 256.
+ *   - Activations are token-major f32 [M][K]; outputs are token-major f32 [M][N].
+ *   - M == 0 or N == 0 is a valid empty call (returns MQ_OK, launches nothing).
+ *   - Kernels never wait without bound.  A device-side wait that runs out sets
+ *     a per-device error word and the kernel returns early; mq_device_status()
+ *     reports it as MQ_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MQ_API __attribute__((visibility("default")))
+#else
+#define MQ_API
+#endif
+
+typedef struct CUstream_st *mq_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+    MQ_OK = 0,
+    MQ_ERR_ARG = -1,            /* NULL pointer, negative size, bad flag */
+    MQ_ERR_SHAPE = -2,          /* K not a positive multiple of 256, size beyond the limits */
+    MQ_ERR_ALIGN = -3,          /* a pointer lacks the alignment stated for it */
+    MQ_ERR_DEVICE = -4,         /* current device is not compute capability 10.3 (sm_103) */
+    MQ_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed; text in mq_last_error() */
+    MQ_ERR_DEVICE_TIMEOUT = -6  /* a bounded device-side wait ran out (see mq_device_status) */
+} mq_status;
+
+/* Thread-local text describing the last error returned on this thread ("" if none). */
+MQ_API const char *mq_last_error(void);
+
+/* ---------------------------------------------------------------- Q8 plane ---
+ *
+ * The Q8 activation plane is this library's own format (the pages call it the
+ * "transposed q8 plane" that the producers emit).  For M tokens and K values
+ * per token, nblk = K/32 blocks per token, it holds:
+ *   q16 : f16  [M][K]     the codes q in [-127, 127] as f16 (every code is an
+ *                          exact f16 value); operand of the tensor-core GEMM
+ *   q8  : int8 [M][K]     the same codes as int8; operand of the dp4a GEMV
+ *   d   : f32  [nblk][M]  block scale d = amax/127 (block-major: "transposed")
+ *   s   : i32  [nblk][M]  block code sum S = sum q (used by the Q4_K min term)
+ * each section starting on a 256-byte boundary.  The plane base must be
+ * 256-byte aligned.  Contents are defined only after mq_quantize_q8 wrote them.
+ */
+typedef struct {
+    size_t off_q16, off_q8, off_d, off_s;
+    size_t total_bytes;
+} mq_plane_layout;
+
+/* Bytes needed for the plane of an M x K activation (0 if the shape is invalid). */
+MQ_API size_t mq_q8_plane_bytes(int64_t M, int64_t K);
+
+/* Section offsets of the plane; MQ_ERR_SHAPE for invalid M or K. Host-only, no CUDA call. */
+MQ_API int mq_q8_plane_layout(int64_t M, int64_t K, mq_plane_layout *out);
+
+/*
+ * mq_quantize_q8 -- activation quantization (MMQ activation quantize; the
+ * RMSNorm-fused producer when rms_w != NULL).  "Features > GPU -- CUDA":
+ * producer-fused activation quantization; "Compute Graph Design > 3.1": RmsNorm{eps}.
+ *
+ *   x      f32 [M][K], 16-byte aligned
+ *   rms_w  NULL: quantize x itself.
+ *          else f32 [K] (16-byte aligned): quantize y = (x * r) * rms_w with
+ *          r = 1/sqrt(mean_k(x^2) + eps) per token (sum of squares in f64,
+ *          r rounded once to f32, two f32 products).
+ *   eps    RMSNorm epsilon (ignored when rms_w == NULL); must be >= 0 and finite
+ *   plane  output, mq_q8_plane_bytes(M, K) bytes, 256-byte aligned
+ *
+ * Per token and 32-block: amax = max|y|, d = amax/127 (IEEE f32 divide),
+ * q = clamp(round_half_away_from_zero(y * (1/d)), -127, 127) (0 when d == 0),
+ * S = sum q.
+ */
+MQ_API int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, float eps,
+                   void *plane, mq_stream_t stream);
+
+/*
+ * mq_gemm_q4k / mq_gemm_q6k -- prefill GEMM (MMQ) on the tensor cores.
+ * "Features > GPU -- CUDA": raw-nibble GEMMs for q4_K and q6_K over the Q8
+ * plane; "Support Matrix > CUDA notes": prefill (nt >= 16) takes this path.
+ *
+ *   w      raw Q4_K (144 B/block) or Q6_K (210 B/block) bytes [N][K/256], 16-byte aligned
+ *   plane  Q8 plane of an M x K activation written by mq_quantize_q8
+ *   y      f32 [M][N] output (fully overwritten), 4-byte aligned
+ *
+ * Y[m][n] = sum over super-blocks of
+ *   Q4_K: d * sum_j sc_j * d_a[m][j] * D_j  -  dmin * sum_j m_j * d_a[m][j] * S[m][j]
+ *   Q6_K: d * sum_s sc_s * d_a[m][s/2] * D_s
+ * with D the exact integer dot of the weight quants and the Q8 codes over a
+ * 32-value (Q4_K sub-block) or 16-value (Q6_K sub-block) range.  The integer
+ * dots are exact; the float scaling is f32.  Any M >= 0 (tokens are tiled by
+ * 128, the tail is masked), any N >= 0.
+ */
+MQ_API int mq_gemm_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+
+/*
+ * mq_gemv_q4k / mq_gemv_q6k -- decode GEMV (MMVQ): streams every weight byte
+ * once per group of up to 8 tokens and takes dp4a int8 dots per block
+ * ("Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ kernels).
+ * Same arguments, same result definition as the GEMMs.  Meant for M < 16
+ * (any M >= 0 is accepted; each further group of 8 tokens streams W again).
+ */
+MQ_API int mq_gemv_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemv_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+
+/*
+ * mq_device_status -- synchronizes `stream`, then reads and clears this
+ * device's error word.  MQ_OK if no kernel reported a failed bounded wait
+ * since the last call, MQ_ERR_DEVICE_TIMEOUT (with the failing wait named in
+ * mq_last_error()) otherwise, MQ_ERR_CUDA if the synchronization failed.
+ */
+MQ_API int mq_device_status(mq_stream_t stream);
+
+/* ------------------------------------------------------------- test hooks ---
+ *
+ * mq_debug_blockdots -- runs the same kernel as the named entry point (same
+ * launch configuration, same y output) and also writes the integer
+ * checkpoint I for the window of tokens [m0, m0+m_cnt) x rows [n0, n0+n_cnt):
+ *   I_out int32 [m_cnt][n_cnt][K/32], per 32-value block b:
+ *     Q4_K: I = sc_j * D_j                      (j = b % 8)
+ *     Q6_K: I = sc_2b * D_2b + sc_2b+1 * D_2b+1 (16-value sub-blocks)
+ * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k.
+ * The window must lie inside [0, M) x [0, N).  Test infrastructure: slower
+ * than the plain entry points.
+ */
+MQ_API int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                       float *y, int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt,
+                       int32_t *I_out, mq_stream_t stream);
+
+/*
+ * mq_debug_forced_timeout -- launches a one-thread kernel whose only wait is on a
+ * barrier that nothing completes.  The wait gives up after timeout_us (1..10^6)
+ * and records the failure in the device error word, so the next
+ * mq_device_status() returns MQ_ERR_DEVICE_TIMEOUT.  Exercises the bounded-wait
+ * and status path without faulting or hanging the GPU.  Test infrastructure.
+ */
+MQ_API int mq_debug_forced_timeout(uint32_t timeout_us, mq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MQ_H */

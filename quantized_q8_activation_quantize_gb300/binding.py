@@ -1,0 +1,178 @@
+"""Thin ctypes binding over libmq.so (include/mq.h).  Argument marshalling only.
+
+Every function here has the name of the C entry point it calls and forwards device
+pointers (torch CUDA tensors or raw integers) plus a CUDA stream.  All arithmetic of
+the path runs in the library's CUDA kernels; there is no Python or CPU fallback: if
+the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmq.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "mq.h")
+
+MQ_OK, MQ_ERR_ARG, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_DEVICE, MQ_ERR_CUDA, MQ_ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+STATUS_NAMES = {0: "MQ_OK", -1: "MQ_ERR_ARG", -2: "MQ_ERR_SHAPE", -3: "MQ_ERR_ALIGN", -4: "MQ_ERR_DEVICE",
+                -5: "MQ_ERR_CUDA", -6: "MQ_ERR_DEVICE_TIMEOUT"}
+OP_GEMM_Q4K, OP_GEMM_Q6K, OP_GEMV_Q4K, OP_GEMV_Q6K = 0, 1, 2, 3
+
+
+class MQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class PlaneLayout(ctypes.Structure):
+    _fields_ = [("off_q16", ctypes.c_size_t), ("off_q8", ctypes.c_size_t), ("off_d", ctypes.c_size_t),
+                ("off_s", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/mq.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mq_\w+)\s*\(", text)))
+
+
+def lib():
+    """Load libmq.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} not built; run __graft_entry__.build() "
+                               "(or python -m quantized_q8_activation_quantize_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+        L.mq_last_error.restype = ctypes.c_char_p
+        L.mq_q8_plane_bytes.argtypes = [I64, I64]
+        L.mq_q8_plane_bytes.restype = ctypes.c_size_t
+        L.mq_q8_plane_layout.argtypes = [I64, I64, ctypes.POINTER(PlaneLayout)]
+        L.mq_quantize_q8.argtypes = [P, I64, I64, P, ctypes.c_float, P, P]
+        for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k"):
+            getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
+        L.mq_device_status.argtypes = [P]
+        L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
+        L.mq_debug_forced_timeout.argtypes = [U32, P]
+        for name in header_functions():
+            if name not in ("mq_last_error", "mq_q8_plane_bytes"):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().mq_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != MQ_OK:
+        raise MQError(rc, last_error())
+    return rc
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------------------------- plane ---
+
+def mq_q8_plane_bytes(M: int, K: int) -> int:
+    return lib().mq_q8_plane_bytes(M, K)
+
+
+def mq_q8_plane_layout(M: int, K: int) -> dict:
+    out = PlaneLayout()
+    _check(lib().mq_q8_plane_layout(M, K, ctypes.byref(out)))
+    return {f: getattr(out, f) for f, _ in PlaneLayout._fields_}
+
+
+def alloc_plane(M: int, K: int, device="cuda"):
+    """A uint8 device tensor big enough for the plane (torch blocks are 512-byte aligned)."""
+    import torch
+    t = torch.empty(max(mq_q8_plane_bytes(M, K), 1), dtype=torch.uint8, device=device)
+    assert t.data_ptr() % 256 == 0
+    return t
+
+
+def plane_views(plane, M: int, K: int):
+    """(q16 f16 [M,K], q8 int8 [M,K], d f32 [K/32,M], s int32 [K/32,M]) views of a plane tensor."""
+    import torch
+    L = mq_q8_plane_layout(M, K)
+    nb = K // 32
+    q16 = plane[L["off_q16"]:L["off_q16"] + 2 * M * K].view(torch.float16).view(M, K)
+    q8 = plane[L["off_q8"]:L["off_q8"] + M * K].view(torch.int8).view(M, K)
+    d = plane[L["off_d"]:L["off_d"] + 4 * nb * M].view(torch.float32).view(nb, M)
+    s = plane[L["off_s"]:L["off_s"] + 4 * nb * M].view(torch.int32).view(nb, M)
+    return q16, q8, d, s
+
+
+# ------------------------------------------------------------------------------ entry points ---
+
+def mq_quantize_q8(x, M: int, K: int, rms_w, eps: float, plane, stream=None):
+    return _check(lib().mq_quantize_q8(_ptr(x), M, K, _ptr(rms_w), float(eps), _ptr(plane), _stream(stream)))
+
+
+def _matmul(name, w, N, K, plane, M, y, stream):
+    return _check(getattr(lib(), name)(_ptr(w), N, K, _ptr(plane), M, _ptr(y), _stream(stream)))
+
+
+def mq_gemm_q4k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q4k", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q6k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q6k", w, N, K, plane, M, y, stream)
+
+
+def mq_gemv_q4k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemv_q4k", w, N, K, plane, M, y, stream)
+
+
+def mq_gemv_q6k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemv_q6k", w, N, K, plane, M, y, stream)
+
+
+def mq_device_status(stream=None):
+    return _check(lib().mq_device_status(_stream(stream)))
+
+
+def mq_debug_blockdots(op: int, w, N: int, K: int, plane, M: int, y, m0: int, m_cnt: int, n0: int, n_cnt: int,
+                       I_out, stream=None):
+    return _check(lib().mq_debug_blockdots(op, _ptr(w), N, K, _ptr(plane), M, _ptr(y), m0, m_cnt, n0, n_cnt,
+                                           _ptr(I_out), _stream(stream)))
+
+
+def mq_debug_forced_timeout(timeout_us: int, stream=None):
+    return _check(lib().mq_debug_forced_timeout(timeout_us, _stream(stream)))
+
+
+# ------------------------------------------------------------------------------- convenience ---
+
+GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k}
+GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k}
+
+
+def matmul(fmt: str, w, N: int, K: int, plane, M: int, y, stream=None):
+    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on."""
+    return (GEMV if M < 16 else GEMM)[fmt](w, N, K, plane, M, y, stream)

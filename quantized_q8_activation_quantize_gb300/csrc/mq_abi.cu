@@ -1,0 +1,296 @@
+// mq_abi.cu -- the C ABI (include/mq.h): argument validation, plane layout, per-device
+// state, status reporting.  Every check happens on the host before any launch; an
+// invalid call launches nothing and returns a negative mq_status.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "mq_device.cuh"
+#include "mq_internal.h"
+
+namespace mq {
+
+namespace {
+thread_local char g_msg[512] = "";
+
+// One error word per device (module globals are instantiated per device).
+__device__ unsigned int g_err_word;
+
+constexpr int kMaxDevices = 64;
+struct DevState {
+    bool ready = false;
+    int status = MQ_OK;
+    unsigned int *err = nullptr;
+};
+DevState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// a bounded wait on a barrier that nothing will ever complete (test hook)
+__global__ void forced_timeout_kernel(unsigned int *err, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+    const uint32_t a = smem_u32(&bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, 0)) {
+        if (global_timer_ns() - t0 > timeout_ns) {
+            atomicOr(err, ERR_TEST_FORCED);
+            return;
+        }
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+}  // namespace
+
+int set_error(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+namespace {
+int g_sm_count[kMaxDevices] = {0};
+constexpr int kAttrSlots = 64;
+bool g_attr_done[kMaxDevices][kAttrSlots] = {};
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 1;
+    }
+    return g_sm_count[dev];
+}
+
+int ensure_smem_attr(const void *kernel, int bytes, int slot) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kAttrSlots)
+        return set_error(MQ_ERR_CUDA, "ensure_smem_attr: bad device %d / slot %d", dev, slot);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_attr_done[dev][slot]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        g_attr_done[dev][slot] = true;
+    }
+    return MQ_OK;
+}
+
+int cuda_error(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MQ_OK;
+    return set_error(MQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Current device must be compute capability 10.3; resolves its error-word address once.
+static int device_state(unsigned int **err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return set_error(MQ_ERR_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevState &st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3) {
+            st.status = set_error(MQ_ERR_DEVICE, "device %d is compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                                  dev, major, minor);
+        } else {
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_err_word);
+            if (e != cudaSuccess) {
+                st.status = cuda_error(e, "cudaGetSymbolAddress(error word)");
+            } else {
+                st.err = static_cast<unsigned int *>(ptr);
+                st.status = MQ_OK;
+            }
+        }
+        st.ready = true;
+    }
+    if (st.status != MQ_OK) {
+        if (st.status == MQ_ERR_DEVICE) set_error(MQ_ERR_DEVICE, "device %d is not compute capability 10.3 (sm_103a)", dev);
+        return st.status;
+    }
+    *err = st.err;
+    return MQ_OK;
+}
+
+static int plane_from(void *base, int64_t M, int64_t K, Plane *p) {
+    mq_plane_layout L;
+    int rc = mq_q8_plane_layout(M, K, &L);
+    if (rc != MQ_OK) return rc;
+    uint8_t *b = static_cast<uint8_t *>(base);
+    p->q16 = reinterpret_cast<uint16_t *>(b + L.off_q16);
+    p->q8 = reinterpret_cast<int8_t *>(b + L.off_q8);
+    p->d = reinterpret_cast<float *>(b + L.off_d);
+    p->s = reinterpret_cast<int32_t *>(b + L.off_s);
+    return MQ_OK;
+}
+
+static int check_k(int64_t K) {
+    if (K <= 0 || K % kQK != 0 || K >= kMaxDim)
+        return set_error(MQ_ERR_SHAPE, "K=%lld must be a positive multiple of 256 below 2^31", (long long)K);
+    return MQ_OK;
+}
+
+// shared validation of the matmul entry points
+static int check_matmul(const char *fn, const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                        const float *y) {
+    if (M < 0 || N < 0) return set_error(MQ_ERR_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    if (M >= kMaxDim || N >= kMaxDim)
+        return set_error(MQ_ERR_SHAPE, "%s: M=%lld N=%lld must be below 2^31", fn, (long long)M, (long long)N);
+    if (M == 0 || N == 0) return MQ_OK;
+    if (!w || !plane || !y) return set_error(MQ_ERR_ARG, "%s: NULL pointer (w=%p plane=%p y=%p)", fn, w, plane, (const void *)y);
+    if (!aligned(w, 16)) return set_error(MQ_ERR_ALIGN, "%s: weights %p not 16-byte aligned", fn, w);
+    if (!aligned(plane, 256)) return set_error(MQ_ERR_ALIGN, "%s: plane %p not 256-byte aligned", fn, plane);
+    if (!aligned(y, 4)) return set_error(MQ_ERR_ALIGN, "%s: y %p not 4-byte aligned", fn, (const void *)y);
+    return MQ_OK;
+}
+
+static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
+                      const Dump &dump, mq_stream_t stream) {
+    static const char *names[4] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k"};
+    int rc = check_matmul(names[op], w, N, K, plane, M, y);
+    if (rc != MQ_OK || M == 0 || N == 0) return rc;
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    Plane p;
+    plane_from(const_cast<void *>(plane), M, K, &p);
+    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K : FMT_Q6K;
+    const uint8_t *wb = static_cast<const uint8_t *>(w);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (op < 2) return launch_gemm(fmt, wb, N, K, p, M, y, dump, err, s);
+    return launch_gemv(fmt, wb, N, K, p, M, y, dump, err, s);
+}
+
+}  // namespace mq
+
+using namespace mq;
+
+extern "C" {
+
+const char *mq_last_error(void) { return g_msg; }
+
+int mq_q8_plane_layout(int64_t M, int64_t K, mq_plane_layout *out) {
+    if (out == nullptr) return set_error(MQ_ERR_ARG, "mq_q8_plane_layout: NULL output");
+    if (M < 0 || M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "M=%lld out of range", (long long)M);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    const size_t m = (size_t)M, k = (size_t)K, nblk = k / kQ8;
+    out->off_q16 = 0;
+    out->off_q8 = align256(2 * m * k);
+    out->off_d = align256(out->off_q8 + m * k);
+    out->off_s = align256(out->off_d + 4 * nblk * m);
+    out->total_bytes = align256(out->off_s + 4 * nblk * m);
+    return MQ_OK;
+}
+
+size_t mq_q8_plane_bytes(int64_t M, int64_t K) {
+    mq_plane_layout L;
+    if (M < 0 || M >= kMaxDim || K <= 0 || K % kQK != 0 || K >= kMaxDim) return 0;
+    mq_q8_plane_layout(M, K, &L);
+    return L.total_bytes;
+}
+
+int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, void *plane,
+                   mq_stream_t stream) {
+    if (M < 0) return set_error(MQ_ERR_ARG, "mq_quantize_q8: negative M=%lld", (long long)M);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    if (M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "mq_quantize_q8: M=%lld must be below 2^31", (long long)M);
+    if (rms_w != nullptr && !(std::isfinite(eps) && eps >= 0.0f))
+        return set_error(MQ_ERR_ARG, "mq_quantize_q8: eps=%g must be finite and >= 0", (double)eps);
+    if (M == 0) return MQ_OK;
+    if (!x || !plane) return set_error(MQ_ERR_ARG, "mq_quantize_q8: NULL pointer (x=%p plane=%p)", (const void *)x, plane);
+    if (!aligned(x, 16)) return set_error(MQ_ERR_ALIGN, "mq_quantize_q8: x %p not 16-byte aligned", (const void *)x);
+    if (rms_w && !aligned(rms_w, 16))
+        return set_error(MQ_ERR_ALIGN, "mq_quantize_q8: rms_w %p not 16-byte aligned", (const void *)rms_w);
+    if (!aligned(plane, 256)) return set_error(MQ_ERR_ALIGN, "mq_quantize_q8: plane %p not 256-byte aligned", plane);
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    Plane p;
+    plane_from(plane, M, K, &p);
+    return launch_quantize(x, M, K, rms_w, eps, p, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mq_gemm_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(0, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(1, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(2, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(3, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
+int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
+                       int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *I_out, mq_stream_t stream) {
+    if (op < 0 || op > 3) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..3", op);
+    if (m_cnt <= 0 || n_cnt <= 0 || m0 < 0 || n0 < 0 || m0 + m_cnt > M || n0 + n_cnt > N)
+        return set_error(MQ_ERR_ARG, "mq_debug_blockdots: window [%lld,+%lld) x [%lld,+%lld) outside %lld x %lld",
+                         (long long)m0, (long long)m_cnt, (long long)n0, (long long)n_cnt, (long long)M, (long long)N);
+    if (!I_out || !aligned(I_out, 4)) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: bad I_out %p", (void *)I_out);
+    return run_matmul(op, w, N, K, plane, M, y, Dump{I_out, m0, m_cnt, n0, n_cnt}, stream);
+}
+
+int mq_device_status(mq_stream_t stream) {
+    unsigned int *errp = nullptr;
+    int rc = device_state(&errp);
+    if (rc != MQ_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "mq_device_status: stream synchronize");
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, errp, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_error(e, "mq_device_status: read error word");
+    if (v == 0) return MQ_OK;
+    const unsigned int zero = 0;
+    e = cudaMemcpy(errp, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_error(e, "mq_device_status: clear error word");
+    static const char *names[] = {"gemv stage", "gemm A stage", "gemm B stage", "gemm stage release",
+                                  "gemm raw weights", "gemm accumulator", "gemm accumulator release",
+                                  "gemm row factors", "gemm row factor release", "gemv drain"};
+    char buf[400] = "";
+    for (int i = 0; i < 10; ++i)
+        if (v & (1u << i)) {
+            strncat(buf, " ", sizeof buf - strlen(buf) - 1);
+            strncat(buf, names[i], sizeof buf - strlen(buf) - 1);
+        }
+    if (v & ERR_TEST_FORCED) strncat(buf, " forced-test-wait", sizeof buf - strlen(buf) - 1);
+    return set_error(MQ_ERR_DEVICE_TIMEOUT, "bounded device wait ran out (code 0x%x):%s", v, buf);
+}
+
+// Test hook: a kernel whose only wait can never complete; it must give up after
+// timeout_us and report through mq_device_status().
+int mq_debug_forced_timeout(uint32_t timeout_us, mq_stream_t stream) {
+    if (timeout_us == 0 || timeout_us > 1000000)
+        return set_error(MQ_ERR_ARG, "mq_debug_forced_timeout: timeout_us=%u not in 1..1000000", timeout_us);
+    unsigned int *err = nullptr;
+    int rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    forced_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, (uint64_t)timeout_us * 1000ull);
+    return cuda_error(cudaGetLastError(), "forced timeout launch");
+}
+
+}  // extern "C"

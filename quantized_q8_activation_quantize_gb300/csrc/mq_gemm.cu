@@ -1,0 +1,577 @@
+// mq_gemm.cu -- prefill GEMM (MMQ): raw Q4_K / Q6_K weights x Q8 plane on tcgen05 tensor cores.
+//
+// minfer pages, "Features > GPU -- CUDA": raw-nibble int8 GEMMs for q4_K and q6_K
+// over the producer-written q8 plane; "Support Matrix > CUDA notes": prefill
+// (nt >= 16) takes the MMQ path.  The pages' kernel (mma.m16n8k32 with weight
+// planes expanded at registration) targets GB10; this one is written for sm_103a:
+//
+//  * sm_103a has no tcgen05 int8 MMA kind, so the integer block dots run as
+//    kind::f16 MMAs on exact small integers: codes q_a in [-127, 127], Q4_K
+//    sc*q in [0, 945], Q6_K sc*q in [-2048, 2048] are all exact in f16, products are
+//    exact, and every 32-value block sum stays below 2^24, so the f32 TMEM
+//    accumulator holds the exact integer I.  Q6_K scales with |sc| > 64 and odd
+//    would need 13 bits: those rows take sc - 1 (even, exact) in the main tile and
+//    q * 1 in a correction tile that is multiplied only when the stage has such rows.
+//  * A (tokens, f16 codes) is a TMA 2-D tile with the 128-byte swizzle; B (weights)
+//    is unpacked from raw block bytes (staged by 1-D bulk copies of each row's
+//    16-byte-aligned superset) straight into the same swizzled K-major layout.
+//  * Each 32-value block's product goes to its own TMEM accumulator (3-slot ring);
+//    the epilogue warps drain it, apply the activation scale per block, the fp16 d
+//    (and the Q4_K min term dmin * sum_j m_j d_a S) per super-block, and keep the
+//    running sum in a fourth TMEM region.
+//
+// CTA = 14 warps: 0 TMA producer, 1 MMA issuer (+ TMEM owner), 2-5 unpackers (one
+// weight row per thread), 6-13 epilogue (2 per TMEM lane quadrant, 64 columns each).
+// Tile: 128 tokens x 128 weight rows, K staged 64 at a time.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "mq_device.cuh"
+#include "mq_internal.h"
+
+namespace mq {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kThreads = 448;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpUnpack0 = 2, kWarpEpi0 = 6;
+constexpr int kAccSlots = 3;
+constexpr uint32_t kTmemCols = 512, kAccCol = 384;
+constexpr int kTile = BM * BK * 2;       // one 128 x 64 f16 operand tile
+constexpr unsigned kFull = 0xffffffffu;
+
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int FMT>
+struct GmCfg {
+    static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
+    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 3;
+    static constexpr int RAW_STAGES = FMT == FMT_Q4K ? 3 : 2;
+    static constexpr int RAW_ROW = FMT == FMT_Q4K ? 144 : 224;   // 16-B aligned superset of one block
+    static constexpr bool CORR = FMT == FMT_Q6K;
+    static constexpr int INFO = FMT == FMT_Q4K ? 12 : 1;          // floats per weight row per super-block
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * kTile;
+    static constexpr int OFF_BC = OFF_B + STAGES * kTile;
+    static constexpr int OFF_RAW = OFF_BC + (CORR ? STAGES * kTile : 0);
+    static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;
+    static constexpr int OFF_FLAG = OFF_INFO + 2 * BN * INFO * 4;
+    static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
+    // a_full[S] b_full[S] ab_empty[S] raw_full[R] info_full[2] info_empty[2] acc_full[3] acc_empty[3]
+    static constexpr int NBARS = 3 * STAGES + RAW_STAGES + 4 + 2 * kAccSlots;
+    static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
+};
+
+struct Bars {
+    uint64_t *a_full, *b_full, *ab_empty, *raw_full, *info_full, *info_empty, *acc_full, *acc_empty;
+};
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// NW consecutive 32-bit words starting at a 2-byte aligned shared address
+template <int NW>
+__device__ __forceinline__ void lds_words_a2(uint32_t addr, uint32_t (&out)[NW]) {
+    const uint32_t b = addr & ~3u, sh = (addr & 3u) * 8u;
+    uint32_t prev = lds32(b);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+        const uint32_t next = lds32(b + 4 * (i + 1));
+        out[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// four quant bytes (each < 64) -> two f16x2 words holding 1024 + byte
+__device__ __forceinline__ void bytes_to_h2_biased(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    lo = __byte_perm(v, 0x64646464u, 0x4140);
+    hi = __byte_perm(v, 0x64646464u, 0x4342);
+}
+
+// swizzled (128 B) address of 16-byte chunk c of row r in a K-major operand tile
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
+    return tile + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int FMT, bool DUMP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__restrict__ w, int64_t N, int64_t K,
+                Plane p, int64_t M, float *__restrict__ y, Dump dump, unsigned int *err) {
+    using C = GmCfg<FMT>;
+    constexpr int S = C::STAGES, R = C::RAW_STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar0 = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
+    Bars bars;
+    bars.a_full = bar0;
+    bars.b_full = bars.a_full + S;
+    bars.ab_empty = bars.b_full + S;
+    bars.raw_full = bars.ab_empty + S;
+    bars.info_full = bars.raw_full + R;
+    bars.info_empty = bars.info_full + 2;
+    bars.acc_full = bars.info_empty + 2;
+    bars.acc_empty = bars.acc_full + kAccSlots;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
+    volatile uint32_t *corr_flags = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_FLAG);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    const int nsb = (int)(K / kQK);
+    const int nstages = nsb * 4;
+    const int64_t row_bytes = (int64_t)(K / kQK) * C::BB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bars.a_full[s], 1);
+            mbar_init(&bars.b_full[s], 128);
+            mbar_init(&bars.ab_empty[s], 1);
+        }
+        for (int r = 0; r < R; ++r) mbar_init(&bars.raw_full[r], 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.info_full[i], 128);
+            mbar_init(&bars.info_empty[i], 8);
+        }
+        for (int i = 0; i < kAccSlots; ++i) {
+            mbar_init(&bars.acc_full[i], 1);
+            mbar_init(&bars.acc_empty[i], 8);
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == kWarpMma) tmem_alloc(tmem_holder, kTmemCols);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ A producer
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            int st = 0;
+            for (; st < nstages; ++st) {
+                const int s = st % S;
+                if (!mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) break;
+                mbar_arrive_expect_tx(&bars.a_full[s], kTile);
+                tma_load_2d(sm + C::OFF_A + s * kTile, &tmA, st * BK, (int32_t)m0, &bars.a_full[s]);
+            }
+            if (*abort_flag) {   // leave no copy in flight: wait (bounded) for the last ones issued
+                for (int i = st - 1; i >= 0 && i >= st - S; --i)
+                    mbar_wait(&bars.a_full[i % S], (i / S) & 1, err, ERR_GEMM_A_FULL, nullptr);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            const uint32_t a_base = smem_u32(sm + C::OFF_A), b_base = smem_u32(sm + C::OFF_B);
+            const uint32_t bc_base = smem_u32(sm + C::OFF_BC);
+            int gb = 0;
+            bool ok = true;
+            for (int st = 0; st < nstages && ok; ++st) {
+                const int s = st % S;
+                const uint32_t ph = (st / S) & 1;
+                if (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag)) break;
+                if (!mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag)) break;
+                tc_fence_after();
+                bool corr = false;
+                if constexpr (C::CORR)
+                    corr = (corr_flags[4 * s] | corr_flags[4 * s + 1] | corr_flags[4 * s + 2] | corr_flags[4 * s + 3]) != 0;
+                for (int h = 0; h < 2; ++h) {
+                    const int slot = gb % kAccSlots;
+                    if (!mbar_wait(&bars.acc_empty[slot], ((gb / kAccSlots) & 1) ^ 1, err, ERR_GEMM_ACC_EMPTY,
+                                   abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (uint32_t)(slot * BN);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t koff = (uint32_t)((2 * h + kk) * 32);
+                        const uint64_t adesc = sw128_kmajor_desc(a_base + s * kTile + koff);
+                        mma_f16(d_tmem, adesc, sw128_kmajor_desc(b_base + s * kTile + koff), idesc, kk);
+                        if (corr) mma_f16(d_tmem, adesc, sw128_kmajor_desc(bc_base + s * kTile + koff), idesc, 1);
+                    }
+                    mma_commit(&bars.acc_full[slot]);
+                    ++gb;
+                }
+                mma_commit(&bars.ab_empty[s]);
+            }
+        }
+    } else if (warp < kWarpEpi0) {
+        // ------------------------------------------------------------ unpackers
+        const int r = threadIdx.x - 32 * kWarpUnpack0;     // weight row in the tile
+        const int64_t n = n0 + r;
+        const bool valid = n < N;
+        const uint8_t *wrow = w + (valid ? n : 0) * row_bytes;
+        uint8_t *raw_row0 = sm + C::OFF_RAW + r * C::RAW_ROW;
+        const uint32_t b_tile0 = smem_u32(sm + C::OFF_B), bc_tile0 = smem_u32(sm + C::OFF_BC);
+        float *info0 = reinterpret_cast<float *>(sm + C::OFF_INFO);
+
+        auto issue_raw = [&](int sb) {
+            const int slot = sb % R;
+            if (valid) {
+                const uint8_t *src = wrow + (int64_t)sb * C::BB;
+                const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15);
+                const uintptr_t a1 = (reinterpret_cast<uintptr_t>(src) + C::BB + 15) & ~uintptr_t(15);
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars.raw_full[slot], (uint32_t)(a1 - a0));
+                bulk_copy_g2s(raw_row0 + slot * BN * C::RAW_ROW, reinterpret_cast<const void *>(a0),
+                              (uint32_t)(a1 - a0), &bars.raw_full[slot]);
+            } else {
+                mbar_arrive(&bars.raw_full[slot]);
+            }
+        };
+        for (int sb = 0; sb < R && sb < nsb; ++sb) issue_raw(sb);
+
+        uint32_t dirty = (1u << S) - 1;      // Q6_K correction rows that may hold non-zero data
+        int issued = R < nsb ? R : nsb;
+        int sb = 0;
+        for (; sb < nsb; ++sb) {
+            const int slot = sb % R;
+            if (!mbar_wait(&bars.raw_full[slot], (sb / R) & 1, err, ERR_GEMM_RAW_FULL, abort_flag)) break;
+            const uint32_t blk = smem_u32(raw_row0 + slot * BN * C::RAW_ROW) +
+                                 (valid ? (uint32_t)(reinterpret_cast<uintptr_t>(wrow + (int64_t)sb * C::BB) & 15) : 0u);
+            // ---- super-block header
+            float d = 0.0f, dmin = 0.0f;
+            int sc[16];
+            int mn[8];
+            if constexpr (FMT == FMT_Q4K) {
+                const uint4 hd = valid ? lds128(blk) : make_uint4(0, 0, 0, 0);
+                d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xffff)));
+                dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+                uint32_t sbytes[12];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sbytes[i] = (hd.y >> (8 * i)) & 0xff;
+                    sbytes[4 + i] = (hd.z >> (8 * i)) & 0xff;
+                    sbytes[8 + i] = (hd.w >> (8 * i)) & 0xff;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sc[j] = sbytes[j] & 63;
+                    mn[j] = sbytes[j + 4] & 63;
+                    sc[j + 4] = (sbytes[j + 8] & 15) | ((sbytes[j] >> 6) << 4);
+                    mn[j + 4] = (sbytes[j + 8] >> 4) | ((sbytes[j + 4] >> 6) << 4);
+                }
+            } else {
+                uint32_t tail[5];                 // bytes 192..211: scales[16], d
+                if (valid) {
+                    lds_words_a2<5>(blk + 192, tail);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) tail[i] = 0;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sc[i] = (int)(int8_t)((tail[i >> 2] >> (8 * (i & 3))) & 0xff);
+                d = __half2float(__ushort_as_half((unsigned short)(tail[4] & 0xffff)));
+            }
+            // ---- per-row factors for the epilogue
+            if (!mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY, abort_flag)) break;
+            float *info = info0 + (sb & 1) * BN * C::INFO + r * C::INFO;
+            if constexpr (FMT == FMT_Q4K) {
+                reinterpret_cast<float4 *>(info)[0] = make_float4(d, dmin, (float)mn[0], (float)mn[1]);
+                reinterpret_cast<float4 *>(info)[1] = make_float4((float)mn[2], (float)mn[3], (float)mn[4], (float)mn[5]);
+                reinterpret_cast<float4 *>(info)[2] = make_float4((float)mn[6], (float)mn[7], 0.0f, 0.0f);
+            } else {
+                info[0] = d;
+            }
+            mbar_arrive(&bars.info_full[sb & 1]);
+
+            // ---- four 64-value stages of this super-block
+            bool ok = true;
+            for (int q = 0; q < 4; ++q) {
+                const int st = sb * 4 + q, s = st % S;
+                if (!mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t btile = b_tile0 + s * kTile;
+                if constexpr (FMT == FMT_Q4K) {
+                    // sub-blocks 2q (low nibbles of qs[32q..32q+32)) and 2q+1 (high nibbles)
+                    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+                    if (valid) {
+                        q0 = lds128(blk + 16 + 32 * q);
+                        q1 = lds128(blk + 16 + 32 * q + 16);
+                    }
+                    const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int hn = 0; hn < 2; ++hn) {
+                        const float scf = (float)sc[2 * q + hn];
+                        const __half2 sc2 = __float2half2_rn(scf);
+                        const __half2 neg = __float2half2_rn(-1024.0f * scf);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const uint32_t va = (wq[2 * cc] >> (4 * hn)) & 0x0f0f0f0fu;
+                            const uint32_t vb = (wq[2 * cc + 1] >> (4 * hn)) & 0x0f0f0f0fu;
+                            uint32_t h0, h1, h2, h3;
+                            bytes_to_h2_biased(va, h0, h1);
+                            bytes_to_h2_biased(vb, h2, h3);
+                            uint4 o;
+                            o.x = h2_as_u32(__hfma2(u32_as_h2(h0), sc2, neg));   // (1024 + q) sc - 1024 sc
+                            o.y = h2_as_u32(__hfma2(u32_as_h2(h1), sc2, neg));
+                            o.z = h2_as_u32(__hfma2(u32_as_h2(h2), sc2, neg));
+                            o.w = h2_as_u32(__hfma2(u32_as_h2(h3), sc2, neg));
+                            sts128(sw128_chunk(btile, r, 4 * hn + cc), o);
+                        }
+                    }
+                } else {
+                    // half h = q/2, groups g = 2(q%2), 2(q%2)+1; chunk c -> g = g0 + c/4, l = 8(c%4)
+                    const int h = q >> 1, g0 = 2 * (q & 1);
+                    uint32_t ql[16], qh[8];
+                    if (valid) {
+                        lds_words_a2<16>(blk + 64 * h, ql);
+                        lds_words_a2<8>(blk + 128 + 32 * h, qh);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ql[i] = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) qh[i] = 0x0a0a0a0au;   // q = 32 - 32 = 0 (unused: scale 0)
+                    }
+                    const int nsh = (g0 >= 2) ? 4 : 0;
+                    bool need_corr = false;
+                    const __half2 bias = __float2half2_rn(1056.0f);
+                    const uint32_t bct = bc_tile0 + s * kTile;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int g = g0 + (c >> 2), l = 8 * (c & 3);
+                        const int si = 8 * h + 2 * g + (l >= 16 ? 1 : 0);
+                        const int scv = valid ? sc[si] : 0;
+                        const bool big = (scv > 64 || scv < -64) && (scv & 1);
+                        const int se = big ? (scv & ~1) : scv;
+                        need_corr |= big;
+                        const __half2 s2 = __float2half2_rn((float)se);
+                        uint32_t o[4], oc[4];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t lw = ql[8 * (g & 1) + (l >> 2) + e];
+                            const uint32_t hw = qh[(l >> 2) + e];
+                            const uint32_t v = ((lw >> nsh) & 0x0f0f0f0fu) | (((hw >> (2 * g)) & 0x03030303u) << 4);
+                            uint32_t b0, b1;
+                            bytes_to_h2_biased(v, b0, b1);
+                            const __half2 t0 = __hsub2(u32_as_h2(b0), bias);   // q - 32, exact
+                            const __half2 t1 = __hsub2(u32_as_h2(b1), bias);
+                            o[2 * e] = h2_as_u32(__hmul2(t0, s2));
+                            o[2 * e + 1] = h2_as_u32(__hmul2(t1, s2));
+                            oc[2 * e] = big ? h2_as_u32(t0) : 0u;
+                            oc[2 * e + 1] = big ? h2_as_u32(t1) : 0u;
+                        }
+                        sts128(sw128_chunk(btile, r, c), make_uint4(o[0], o[1], o[2], o[3]));
+                        if (need_corr || ((dirty >> s) & 1)) sts128(sw128_chunk(bct, r, c), make_uint4(oc[0], oc[1], oc[2], oc[3]));
+                    }
+                    // rows written with correction data stay dirty until rewritten with zeros
+                    if (need_corr) dirty |= 1u << s; else dirty &= ~(1u << s);
+                    const bool any = __any_sync(kFull, need_corr);
+                    if (lane == 0) corr_flags[4 * s + (warp - kWarpUnpack0)] = any ? 1u : 0u;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.b_full[s]);
+            }
+            if (!ok) break;
+            if (sb + R < nsb) {
+                issue_raw(sb + R);
+                ++issued;
+            }
+        }
+        if (*abort_flag) {   // wait (bounded) for this row's copies still in flight
+            for (int i = sb; i < issued; ++i)
+                mbar_wait(&bars.raw_full[i % R], (i / R) & 1, err, ERR_GEMM_RAW_FULL, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - kWarpEpi0, qd = warp & 3, hf = e >> 2;
+        const int64_t m = m0 + 32 * qd + lane;
+        const bool valid_m = m < M;
+        const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
+        const int col0 = hf * 64;
+        const int64_t nblk32 = K / kQ8;
+        const float *info0 = reinterpret_cast<const float *>(sm + C::OFF_INFO);
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            float dS[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gb = sb * 8 + j;
+                const float da = valid_m ? __ldg(p.d + (int64_t)gb * M + m) : 0.0f;
+                if constexpr (FMT == FMT_Q4K) dS[j] = valid_m ? da * (float)__ldg(p.s + (int64_t)gb * M + m) : 0.0f;
+                const int slot = gb % kAccSlots;
+                if (!mbar_wait(&bars.acc_full[slot], (gb / kAccSlots) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[32];
+                    tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32 * hh), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(__uint_as_float(v[i]), da, acc[32 * hh + i]);
+                    if constexpr (DUMP) {
+                        if (valid_m && m >= dump.m0 && m < dump.m0 + dump.m_cnt) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int64_t n = n0 + col0 + 32 * hh + i;
+                                if (n >= dump.n0 && n < dump.n0 + dump.n_cnt && n < N)
+                                    dump.out[((m - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32 + gb] =
+                                        __float2int_rn(__uint_as_float(v[i]));
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
+            }
+            if (!ok) break;
+            // ---- super-block end: fold d (and the Q4_K min term) into the running sum
+            if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
+            const float *info = info0 + (sb & 1) * BN * C::INFO;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                if (sb > 0) {
+                    tmem_ld32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = col0 + 32 * hh + i;
+                    float add;
+                    if constexpr (FMT == FMT_Q4K) {
+                        const float4 f0 = reinterpret_cast<const float4 *>(info + col * C::INFO)[0];
+                        const float4 f1 = reinterpret_cast<const float4 *>(info + col * C::INFO)[1];
+                        const float4 f2 = reinterpret_cast<const float4 *>(info + col * C::INFO)[2];
+                        float t = f0.z * dS[0];
+                        t = fmaf(f0.w, dS[1], t);
+                        t = fmaf(f1.x, dS[2], t);
+                        t = fmaf(f1.y, dS[3], t);
+                        t = fmaf(f1.z, dS[4], t);
+                        t = fmaf(f1.w, dS[5], t);
+                        t = fmaf(f2.x, dS[6], t);
+                        t = fmaf(f2.y, dS[7], t);
+                        add = fmaf(f0.x, acc[32 * hh + i], -f0.y * t);
+                    } else {
+                        add = info[col] * acc[32 * hh + i];
+                    }
+                    v[i] = __float_as_uint(__uint_as_float(v[i]) + add);
+                    acc[32 * hh + i] = 0.0f;
+                }
+                tmem_st32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
+            }
+            tmem_st_wait();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.info_empty[sb & 1]);
+        }
+        if (ok && !*abort_flag) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                tmem_ld32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
+                tmem_ld_wait();
+                if (valid_m) {
+                    const int64_t nb0 = n0 + col0 + 32 * hh;
+                    float *dst = y + m * N + nb0;
+                    if (nb0 + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (nb0 + i < N) dst[i] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+template <int FMT, bool DUMP>
+int launch_fmt(const CUtensorMap &tm, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+               const Dump &dump, unsigned int *err, cudaStream_t stream) {
+    using C = GmCfg<FMT>;
+    auto kern = gemm_kernel<FMT, DUMP>;
+    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, FMT * 2 + (DUMP ? 1 : 0));
+    if (rc != MQ_OK) return rc;
+    const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tm, w, N, K, p, M, y, dump, err);
+    return cuda_error(cudaGetLastError(), "gemm launch");
+}
+
+}  // namespace
+
+int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+                const Dump &dump, unsigned int *err, cudaStream_t stream) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+    if ((M + BM - 1) / BM > 65535) return set_error(MQ_ERR_SHAPE, "M=%lld: more than 65535 token tiles", (long long)M);
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.q16, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for M=%lld K=%lld", (int)r,
+                                            (long long)M, (long long)K);
+    const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
+    if (fmt == FMT_Q4K)
+        return dmp ? launch_fmt<FMT_Q4K, true>(tm, w, N, K, p, M, y, dump, err, stream)
+                   : launch_fmt<FMT_Q4K, false>(tm, w, N, K, p, M, y, dump, err, stream);
+    return dmp ? launch_fmt<FMT_Q6K, true>(tm, w, N, K, p, M, y, dump, err, stream)
+               : launch_fmt<FMT_Q6K, false>(tm, w, N, K, p, M, y, dump, err, stream);
+}
+
+}  // namespace mq

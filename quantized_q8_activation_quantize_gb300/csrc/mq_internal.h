@@ -1,0 +1,50 @@
+// mq_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mq.h"
+
+namespace mq {
+
+enum Fmt : int { FMT_Q4K = 0, FMT_Q6K = 1 };
+
+constexpr int kQK = 256;     // values per k-quant super-block
+constexpr int kQ8 = 32;      // values per Q8 activation block
+
+inline int block_bytes(Fmt f) { return f == FMT_Q4K ? 144 : 210; }
+
+// device pointers to the sections of one Q8 plane
+struct Plane {
+    uint16_t *q16;     // f16 codes [M][K] (binary16 bit patterns)
+    int8_t *q8;        // int8 codes [M][K]
+    float *d;          // [K/32][M]
+    int32_t *s;        // [K/32][M]
+};
+
+// window of the integer checkpoint dump (test hook); cnt == 0 disables it
+struct Dump {
+    int32_t *out;
+    int64_t m0, m_cnt, n0, n_cnt;
+};
+
+int set_error(int code, const char *fmt, ...);
+
+// SM count of the current device (cached per device)
+int sm_count();
+
+// Sets the dynamic shared-memory limit of `kernel` once per device; returns MQ_OK or MQ_ERR_CUDA.
+int ensure_smem_attr(const void *kernel, int bytes, int slot);
+int cuda_error(cudaError_t e, const char *what);
+
+// launchers (arguments already validated); return MQ_OK or MQ_ERR_CUDA
+int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,
+                    unsigned int *err, cudaStream_t stream);
+int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+                const Dump &dump, unsigned int *err, cudaStream_t stream);
+int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+                const Dump &dump, unsigned int *err, cudaStream_t stream);
+
+}  // namespace mq

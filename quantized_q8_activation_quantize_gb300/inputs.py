@@ -172,8 +172,16 @@ def config3_matrix(layer: int, idx: int):
     return {"w": w, "x": x, "fmt": fmt, "name": name}
 
 
+def config4_weights():
+    """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
+    return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
+
+
+def config4_x(m: int):
+    """LM head activations: m x 3584 f32 N(0,1), m in {1, 16, 3314}."""
+    return activations(rng(4, STREAM_X, m), m, HIDDEN)
+
+
 def config4(m: int):
     """LM head: W 152064 x 3584 (Q6_K, scales [-64, 63]), X m x 3584 N(0,1), m in {1, 16, 3314}."""
-    w = q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
-    x = activations(rng(4, STREAM_X, m), m, HIDDEN)
-    return {"w": w, "x": x, "fmt": "q6k"}
+    return {"w": config4_weights(), "x": config4_x(m), "fmt": "q6k"}

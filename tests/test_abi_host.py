@@ -1,0 +1,127 @@
+"""Host-side tests of the C ABI: the library loads, exports every symbol include/mq.h
+declares, lays out the Q8 plane as documented, and rejects bad arguments before any
+CUDA call (these run without a GPU)."""
+import ctypes
+import subprocess
+import sys
+
+import pytest
+
+from quantized_q8_activation_quantize_gb300 import binding as B
+from quantized_q8_activation_quantize_gb300 import build as mqbuild
+
+
+@pytest.fixture(scope="session")
+def L():
+    mqbuild.build()
+    return B.lib()
+
+
+EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quantize_q8", "mq_gemm_q4k",
+            "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_device_status", "mq_debug_blockdots",
+            "mq_debug_forced_timeout"}
+
+
+def test_header_declares_the_boundary():
+    assert set(B.header_functions()) == EXPECTED
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in B.header_functions():
+        assert hasattr(L, name), name
+    # and nothing else with C linkage leaks out under the mq_ prefix
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.split() and ln.split()[-1].startswith("mq_")}
+    assert exported == EXPECTED
+
+
+@pytest.mark.parametrize("M,K", [(0, 256), (1, 256), (8, 512), (3314, 3584), (3314, 18944), (7, 768)])
+def test_plane_layout(L, M, K):
+    lay = B.mq_q8_plane_layout(M, K)
+    nb = K // 32
+    secs = [("off_q16", 2 * M * K), ("off_q8", M * K), ("off_d", 4 * nb * M), ("off_s", 4 * nb * M)]
+    end = 0
+    for name, size in secs:
+        assert lay[name] % 256 == 0 and lay[name] >= end
+        end = lay[name] + size
+    assert lay["total_bytes"] >= end and lay["total_bytes"] % 256 == 0 and lay["total_bytes"] - end < 256
+    assert B.mq_q8_plane_bytes(M, K) == lay["total_bytes"]
+
+
+@pytest.mark.parametrize("M,K", [(-1, 256), (4, 0), (4, 100), (4, 300), (4, -256), (1 << 31, 256)])
+def test_plane_layout_rejects_bad_shapes(L, M, K):
+    assert B.mq_q8_plane_bytes(M, K) == 0
+    with pytest.raises(B.MQError) as e:
+        B.mq_q8_plane_layout(M, K)
+    assert e.value.status == B.MQ_ERR_SHAPE
+
+
+def _rc(fn, *args):
+    return fn(*args)
+
+
+def test_quantize_argument_errors(L):
+    q = L.mq_quantize_q8
+    assert q(16, 4, 100, None, 0.0, 256, None) == B.MQ_ERR_SHAPE
+    assert q(16, -1, 256, None, 0.0, 256, None) == B.MQ_ERR_ARG
+    assert q(16, 0, 256, None, 0.0, 256, None) == B.MQ_OK            # empty: nothing to do
+    assert q(None, 4, 256, None, 0.0, 256, None) == B.MQ_ERR_ARG
+    assert "NULL" in B.last_error()
+    assert q(16, 4, 256, None, 0.0, None, None) == B.MQ_ERR_ARG
+    assert q(20, 4, 256, None, 0.0, 256, None) == B.MQ_ERR_ALIGN      # x not 16-byte aligned
+    assert q(16, 4, 256, 24, 1e-6, 256, None) == B.MQ_ERR_ALIGN      # rms_w not 16-byte aligned
+    assert q(16, 4, 256, None, 0.0, 128, None) == B.MQ_ERR_ALIGN     # plane not 256-byte aligned
+    assert q(16, 4, 256, 32, float("nan"), 256, None) == B.MQ_ERR_ARG
+    assert q(16, 4, 256, 32, -1.0, 256, None) == B.MQ_ERR_ARG
+
+
+@pytest.mark.parametrize("name", ["mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k"])
+def test_matmul_argument_errors(L, name):
+    f = getattr(L, name)
+    assert f(16, 8, 300, 256, 4, 16, None) == B.MQ_ERR_SHAPE          # K % 256
+    assert f(16, 8, 0, 256, 4, 16, None) == B.MQ_ERR_SHAPE
+    assert f(16, -8, 256, 256, 4, 16, None) == B.MQ_ERR_ARG
+    assert f(16, 8, 256, 256, -4, 16, None) == B.MQ_ERR_ARG
+    assert f(16, 0, 256, 256, 4, 16, None) == B.MQ_OK                 # N == 0: empty
+    assert f(16, 8, 256, 256, 0, 16, None) == B.MQ_OK                 # M == 0: empty
+    assert f(None, 8, 256, 256, 4, 16, None) == B.MQ_ERR_ARG
+    assert f(16, 8, 256, None, 4, 16, None) == B.MQ_ERR_ARG
+    assert f(16, 8, 256, 256, 4, None, None) == B.MQ_ERR_ARG
+    assert f(8, 8, 256, 256, 4, 16, None) == B.MQ_ERR_ALIGN           # weights need 16 B
+    assert f(16, 8, 256, 64, 4, 16, None) == B.MQ_ERR_ALIGN           # plane needs 256 B
+    assert f(16, 8, 256, 256, 4, 18, None) == B.MQ_ERR_ALIGN          # y needs 4 B
+    assert f(16, 1 << 31, 256, 256, 4, 16, None) == B.MQ_ERR_SHAPE
+
+
+def test_debug_window_errors(L):
+    d = L.mq_debug_blockdots
+    assert d(4, 16, 8, 256, 256, 4, 16, 0, 1, 0, 1, 16, None) == B.MQ_ERR_ARG      # op
+    assert d(0, 16, 8, 256, 256, 4, 16, 3, 2, 0, 1, 16, None) == B.MQ_ERR_ARG      # window past M
+    assert d(0, 16, 8, 256, 256, 4, 16, 0, 1, 0, 0, 16, None) == B.MQ_ERR_ARG      # empty window
+    assert d(0, 16, 8, 256, 256, 4, 16, 0, 1, 0, 1, None, None) == B.MQ_ERR_ARG
+    assert L.mq_debug_forced_timeout(0, None) == B.MQ_ERR_ARG
+
+
+def test_valid_call_without_a_device_fails_loudly(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    rc = L.mq_gemm_q4k(16, 8, 256, 256, 4, 16, None)
+    assert rc in (B.MQ_ERR_CUDA, B.MQ_ERR_DEVICE)
+    assert B.last_error()
+    with pytest.raises(B.MQError):
+        B.mq_gemm_q4k(16, 8, 256, 256, 4, 16, stream=0)
+
+
+def test_product_package_does_not_import_the_oracle():
+    code = ("import sys, quantized_q8_activation_quantize_gb300 as p, quantized_q8_activation_quantize_gb300.inputs;"
+            "import quantized_q8_activation_quantize_gb300.binding; print('oracle' in sys.modules)")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=B.PKG + "/..")
+    assert out.stdout.strip() == "False", out.stderr
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()

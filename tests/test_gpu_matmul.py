@@ -1,0 +1,183 @@
+"""GPU parity of the GEMM (tensor-core MMQ) and GEMV (dp4a MMVQ) entry points against the
+oracle, on identical seeded bytes:
+
+* the integer checkpoint I (per token, row, 32-value block) must match bit for bit;
+* outputs must satisfy max |Y_gpu - Y_ref| / ||Y_ref[m, :]||_2 <= 1e-3 (the stated bar);
+  on sampled full-size cases the stricter RMS-normalised form (divide by the RMS of the
+  reference row's sampled entries instead of its L2 norm, a factor sqrt(N) stricter) is used.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_q8_activation_quantize_gb300 import inputs
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(fmt, n, k, seed, scale_range=(-64, 63)):
+    r = np.random.default_rng(seed)
+    if fmt == "q4k":
+        return inputs.q4k_weights(r, n, k)
+    return inputs.q6k_weights(r, n, k, scale_range=scale_range)
+
+
+def _full_check(path, fmt, M, N, K, seed, scale_range=(-64, 63), dump=True):
+    w = _weights(fmt, N, K, seed, scale_range)
+    x = inputs.activations(np.random.default_rng(seed + 1), M, K)
+    plane, got = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    G.assert_plane_equal(got, ref_plane)
+    y, wd = G.run_matmul(path, fmt, w, plane, M, K, N)
+    ref = oracle.matmul(w, fmt, ref_plane, threads=8)
+    err = G.rel_err(y, ref)
+    assert err <= G.REL_TOL, f"rel err {err}"
+    if dump:
+        I, y2 = G.run_dump(path, fmt, wd, plane, M, K, N, 0, M, 0, N)
+        Iref, _ = oracle.blockdots(w, fmt, ref_plane[0])
+        assert np.array_equal(I, Iref), f"block dots differ at {np.argwhere(I != Iref)[:5]}"
+        assert np.array_equal(y2, y), "the dump variant must produce the same output"
+    return err
+
+
+SHAPES = [(1, 7, 256), (2, 65, 512), (5, 129, 768), (8, 64, 2048), (13, 33, 512), (16, 128, 256),
+          (17, 130, 512), (130, 129, 256), (200, 200, 1024), (129, 1, 512)]
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_shapes(path, fmt, M, N, K):
+    _full_check(path, fmt, M, N, K, seed=M * 7919 + N * 31 + K)
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_q6k_full_scale_range(path):
+    # real GGML Q6_K files use scales up to +-128; odd |sc| > 64 takes the correction tile
+    for seed, (M, N, K) in enumerate([(3, 40, 512), (64, 200, 768), (150, 130, 256)]):
+        _full_check(path, "q6k", M, N, K, seed=900 + seed, scale_range=(-128, 127))
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_extreme_blocks(path):
+    # every quant at its extreme with every code at +-127: the int32 headroom cases
+    M, N, K = 16, 16, 512
+    x = np.full((M, K), 1.0, np.float32)
+    x[1::2] = -1.0
+    plane, got = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    for fmt in ("q4k", "q6k"):
+        w = _weights(fmt, N, K, 5, (-128, 127))
+        if fmt == "q4k":
+            w[..., 4:] = 0xFF                  # sc = m = 63, q = 15
+        else:
+            w[..., 0:192] = 0                  # q = -32
+            w[..., 192:208] = 0x80             # sc = -128
+        y, wd = G.run_matmul(path, fmt, w, plane, M, K, N)
+        ref = oracle.matmul(w, fmt, ref_plane)
+        assert G.rel_err(y, ref) <= G.REL_TOL
+        I, _ = G.run_dump(path, fmt, wd, plane, M, K, N, 0, M, 0, N)
+        Iref, _ = oracle.blockdots(w, fmt, ref_plane[0])
+        assert np.array_equal(I, Iref)
+
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_config0(path):
+    c = inputs.config0()
+    M, K = c["x"].shape
+    N = c["w"].shape[0]
+    plane, got = G.gpu_plane(c["x"])
+    ref_plane = G.oracle_plane(c["x"])
+    y, wd = G.run_matmul(path, "q4k", c["w"], plane, M, K, N)
+    assert G.rel_err(y, oracle.matmul(c["w"], "q4k", ref_plane)) <= G.REL_TOL
+    I, _ = G.run_dump(path, "q4k", wd, plane, M, K, N, 0, M, 0, N)
+    assert np.array_equal(I, oracle.blockdots(c["w"], "q4k", ref_plane[0])[0])
+
+
+def test_config1_gemm_full():
+    c = inputs.config1()
+    M, K = c["x"].shape
+    N = c["w"].shape[0]
+    plane, got = G.gpu_plane(c["x"])
+    ref_plane = G.oracle_plane(c["x"])
+    G.assert_plane_equal(got, ref_plane)
+    y, wd = G.run_matmul("gemm", "q4k", c["w"], plane, M, K, N)
+    ref = oracle.matmul(c["w"], "q4k", ref_plane, threads=16)
+    assert G.rel_err(y, ref) <= G.REL_TOL
+    # integer checkpoint on a window crossing token and row tile borders
+    m0, mc, n0, nc = 120, 140, 100, 200
+    I, _ = G.run_dump("gemm", "q4k", wd, plane, M, K, N, m0, mc, n0, nc)
+    Iref, _ = oracle.blockdots(c["w"], "q4k", ref_plane[0], np.arange(m0, m0 + mc), np.arange(n0, n0 + nc))
+    assert np.array_equal(I, Iref)
+
+
+def _sampled(path, fmt, w, plane, ref_plane, M, K, N, ms, ns, dump_window=None):
+    y, wd = G.run_matmul(path, fmt, w, plane, M, K, N)
+    ref = oracle.matmul(w, fmt, ref_plane, ms, ns, threads=16)
+    got = y[np.ix_(ms, ns)]
+    rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+    err = float((np.abs(got - ref) / np.where(rms == 0, 1, rms)).max())
+    assert err <= G.REL_TOL, f"RMS-normalised err {err}"
+    if dump_window is not None:
+        m0, mc, n0, nc = dump_window
+        I, _ = G.run_dump(path, fmt, wd, plane, M, K, N, m0, mc, n0, nc)
+        Iref, _ = oracle.blockdots(w, fmt, ref_plane[0], np.arange(m0, m0 + mc), np.arange(n0, n0 + nc))
+        assert np.array_equal(I, Iref)
+    return err
+
+
+def _sample_idx(total, count, seed, must=()):
+    r = np.random.default_rng(seed)
+    idx = set(r.choice(total, size=min(count, total), replace=False).tolist()) | set(must)
+    return np.array(sorted(i for i in idx if 0 <= i < total))
+
+
+def test_config2_full_size_sampled():
+    c = inputs.config2()
+    M = c["x_hidden"].shape[0]
+    plane_h, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ref_h = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ms = _sample_idx(M, 48, 1, must=(0, 127, 128, M - 1))
+    for name in ("w_gate", "w_up"):
+        N = c[name].shape[0]
+        ns = _sample_idx(N, 384, 2, must=(0, N - 1))
+        _sampled("gemm", "q4k", c[name], plane_h, ref_h, M, 3584, N, ms, ns,
+                 dump_window=(M - 40, 40, N - 70, 70))
+    plane_f, _ = G.gpu_plane(c["x_ffn"])
+    ref_f = G.oracle_plane(c["x_ffn"])
+    ns = _sample_idx(3584, 384, 3, must=(0, 3583))
+    _sampled("gemm", "q6k", c["w_down"], plane_f, ref_f, M, 18944, 3584, ms, ns, dump_window=(3200, 114, 0, 40))
+
+
+def test_config3_decode_layers():
+    # two layers of the decode sweep: layer 0 (Q6_K v and down) and layer 1 (all Q4_K), full rows
+    for layer in (0, 1):
+        for idx in range(7):
+            c = inputs.config3_matrix(layer, idx)
+            N, K = c["w"].shape[0], c["x"].shape[1]
+            plane, _ = G.gpu_plane(c["x"])
+            ref_plane = G.oracle_plane(c["x"])
+            y, wd = G.run_matmul("gemv", c["fmt"], c["w"], plane, 1, K, N)
+            ref = oracle.matmul(c["w"], c["fmt"], ref_plane, threads=16)
+            assert G.rel_err(y, ref) <= G.REL_TOL, (layer, c["name"])
+            I, _ = G.run_dump("gemv", c["fmt"], wd, plane, 1, K, N, 0, 1, 0, min(N, 256))
+            assert np.array_equal(I, oracle.blockdots(c["w"], c["fmt"], ref_plane[0], None, np.arange(min(N, 256)))[0])
+
+
+@pytest.fixture(scope="module")
+def lm_head():
+    return inputs.config4_weights()
+
+
+@pytest.mark.parametrize("M,paths", [(1, ("gemv",)), (16, ("gemv", "gemm")), (3314, ("gemm",))])
+def test_config4_lm_head(lm_head, M, paths):
+    x = inputs.config4_x(M)
+    N, K = lm_head.shape[0], 3584
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    ms = _sample_idx(M, 24, 5, must=(0, M - 1))
+    ns = _sample_idx(N, 2048, 6, must=(0, N - 1))
+    for path in paths:
+        _sampled(path, "q6k", lm_head, plane, ref_plane, M, K, N, ms, ns,
+                 dump_window=(0, min(M, 8), N - 100, 100))
