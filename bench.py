@@ -52,7 +52,64 @@ def parse_args():
     ap.add_argument("--impl", choices=["mq", "reference"], default="mq")
     ap.add_argument("--skip-decode", action="store_true", help="prefill step only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--case", choices=sorted(CASES), help="run one kernel of the path a few times (profiling)")
+    ap.add_argument("--reps", type=int, default=3, help="launches of --case after 2 warm-up launches")
     return ap.parse_args()
+
+
+# single-kernel cases for profiler captures: name -> (config, kernel); inputs of the named config
+CASES = {
+    "gemm_q4k_gate": "config 2 gate GEMM: Q4_K 18944x3584, M=3314",
+    "gemm_q6k_down": "config 2 down GEMM: Q6_K 3584x18944, M=3314",
+    "gemm_q4k_qproj": "config 1 q_proj GEMM: Q4_K 3584x3584, M=512",
+    "gemv_q6k_lmhead": "config 4 LM head GEMV: Q6_K 152064x3584, M=1",
+    "gemv_q4k_gate": "config 3 layer-1 gate GEMV: Q4_K 18944x3584, M=1",
+    "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
+    "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
+}
+
+
+def run_case(args):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_q8_activation_quantize_gb300 import binding as B
+    from quantized_q8_activation_quantize_gb300 import inputs as I
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    name = args.case
+    if name.startswith("gemm_q4k_gate") or name.startswith("gemm_q6k_down") or name.startswith("quantize"):
+        c = I.config2()
+        M = c["x_hidden"].shape[0]
+        if name == "gemm_q6k_down" or name == "quantize_ffn":
+            x, K, N, w, fmt, rms = c["x_ffn"], I.FFN, I.HIDDEN, c["w_down"], "q6k", None
+        else:
+            x, K, N, w, fmt, rms = c["x_hidden"], I.HIDDEN, I.FFN, c["w_gate"], "q4k", c["rms_w"]
+    elif name == "gemm_q4k_qproj":
+        c = I.config1()
+        x, w, fmt, rms = c["x"], c["w"], "q4k", None
+        M, K, N = x.shape[0], x.shape[1], w.shape[0]
+    elif name == "gemv_q6k_lmhead":
+        x, w, fmt, rms = I.config4_x(1), I.config4_weights(), "q6k", None
+        M, K, N = 1, I.HIDDEN, I.VOCAB
+    else:
+        c = I.config3_matrix(1, 4)
+        x, w, fmt, rms = c["x"], c["w"], "q4k", None
+        M, K, N = 1, I.HIDDEN, I.FFN
+    xd, wd = dev(x), dev(w.reshape(N, -1))
+    rd = dev(rms) if rms is not None else None
+    plane = B.alloc_plane(M, K)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
+    if name.startswith("quantize"):
+        fn = lambda: B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
+    else:
+        f = (B.GEMM if name.startswith("gemm") else B.GEMV)[fmt]
+        fn = lambda: f(wd, N, K, plane, M, y)
+    for _ in range(2 + args.reps):
+        fn()
+    torch.cuda.synchronize()
+    B.mq_device_status()
+    print(json.dumps({"case": name, "what": CASES[name], "launches": 2 + args.reps}))
 
 
 # ------------------------------------------------------------------------------ distributed ---
@@ -311,6 +368,9 @@ def run_reference(args, dist):
 
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     dist = Dist()
     if args.impl == "reference":
         dist.init(use_cuda=False)

@@ -71,11 +71,15 @@ MQ_API const char *mq_last_error(void);
  *   q8  : int8 [M][K]     the same codes as int8; operand of the dp4a GEMV
  *   d   : f32  [nblk][M]  block scale d = amax/127 (block-major: "transposed")
  *   s   : i32  [nblk][M]  block code sum S = sum q (used by the Q4_K min term)
+ *   ds  : f32  [M][2*nblk] per super-block of token m, 16 values: the tf32 pair
+ *                          (hi[8], lo[8]) of d*S for its eight 32-value blocks,
+ *                          hi = tf32(d*S), lo = tf32(d*S - hi) (round to nearest);
+ *                          operand of the tensor-core Q4_K min term
  * each section starting on a 256-byte boundary.  The plane base must be
  * 256-byte aligned.  Contents are defined only after mq_quantize_q8 wrote them.
  */
 typedef struct {
-    size_t off_q16, off_q8, off_d, off_s;
+    size_t off_q16, off_q8, off_d, off_s, off_ds;
     size_t total_bytes;
 } mq_plane_layout;
 

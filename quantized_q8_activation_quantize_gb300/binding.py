@@ -29,7 +29,7 @@ class MQError(RuntimeError):
 
 class PlaneLayout(ctypes.Structure):
     _fields_ = [("off_q16", ctypes.c_size_t), ("off_q8", ctypes.c_size_t), ("off_d", ctypes.c_size_t),
-                ("off_s", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
+                ("off_s", ctypes.c_size_t), ("off_ds", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -115,8 +115,8 @@ def alloc_plane(M: int, K: int, device="cuda"):
     return t
 
 
-def plane_views(plane, M: int, K: int):
-    """(q16 f16 [M,K], q8 int8 [M,K], d f32 [K/32,M], s int32 [K/32,M]) views of a plane tensor."""
+def plane_views(plane, M: int, K: int, with_ds: bool = False):
+    """(q16 f16 [M,K], q8 int8 [M,K], d f32 [K/32,M], s int32 [K/32,M][, ds f32 [M,2K/32]]) views."""
     import torch
     L = mq_q8_plane_layout(M, K)
     nb = K // 32
@@ -124,7 +124,10 @@ def plane_views(plane, M: int, K: int):
     q8 = plane[L["off_q8"]:L["off_q8"] + M * K].view(torch.int8).view(M, K)
     d = plane[L["off_d"]:L["off_d"] + 4 * nb * M].view(torch.float32).view(nb, M)
     s = plane[L["off_s"]:L["off_s"] + 4 * nb * M].view(torch.int32).view(nb, M)
-    return q16, q8, d, s
+    if not with_ds:
+        return q16, q8, d, s
+    ds = plane[L["off_ds"]:L["off_ds"] + 8 * nb * M].view(torch.float32).view(M, 2 * nb)
+    return q16, q8, d, s, ds
 
 
 # ------------------------------------------------------------------------------ entry points ---

@@ -139,6 +139,7 @@ static int plane_from(void *base, int64_t M, int64_t K, Plane *p) {
     p->q8 = reinterpret_cast<int8_t *>(b + L.off_q8);
     p->d = reinterpret_cast<float *>(b + L.off_d);
     p->s = reinterpret_cast<int32_t *>(b + L.off_s);
+    p->ds = reinterpret_cast<float *>(b + L.off_ds);
     return MQ_OK;
 }
 
@@ -199,7 +200,8 @@ int mq_q8_plane_layout(int64_t M, int64_t K, mq_plane_layout *out) {
     out->off_q8 = align256(2 * m * k);
     out->off_d = align256(out->off_q8 + m * k);
     out->off_s = align256(out->off_d + 4 * nblk * m);
-    out->total_bytes = align256(out->off_s + 4 * nblk * m);
+    out->off_ds = align256(out->off_s + 4 * nblk * m);
+    out->total_bytes = align256(out->off_ds + 8 * nblk * m);
     return MQ_OK;
 }
 
@@ -270,9 +272,9 @@ int mq_device_status(mq_stream_t stream) {
     if (e != cudaSuccess) return cuda_error(e, "mq_device_status: clear error word");
     static const char *names[] = {"gemv stage", "gemm A stage", "gemm B stage", "gemm stage release",
                                   "gemm raw weights", "gemm accumulator", "gemm accumulator release",
-                                  "gemm row factors", "gemm row factor release", "gemv drain"};
+                                  "gemm row factors", "gemm row factor release", "gemv drain", "gemm min term"};
     char buf[400] = "";
-    for (int i = 0; i < 10; ++i)
+    for (int i = 0; i < 11; ++i)
         if (v & (1u << i)) {
             strncat(buf, " ", sizeof buf - strlen(buf) - 1);
             strncat(buf, names[i], sizeof buf - strlen(buf) - 1);

@@ -22,6 +22,7 @@ enum : unsigned int {
     ERR_GEMM_INFO_FULL = 1u << 7,
     ERR_GEMM_INFO_EMPTY = 1u << 8,
     ERR_GEMV_DRAIN = 1u << 9,
+    ERR_GEMM_MIN = 1u << 10,
     ERR_TEST_FORCED = 1u << 31,
 };
 
@@ -72,6 +73,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, but the thread may be suspended for up to `hint_ns` while the phase is incomplete
+// (it resumes as soon as the phase completes), so a waiting warp does not spin on the
+// issue slots the working warps of its SM sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (after
 // recording `code` in *err and raising *abort) if it did not complete within
 // kWaitTimeoutNs, or at once if another warp already raised *abort.
@@ -81,8 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_sleep(a, parity, 100000u)) return true;     // sleep up to 100 us
         if (abort != nullptr && *abort) return false;
         if (global_timer_ns() - t0 > kWaitTimeoutNs) {
             atomicOr(err, code);
@@ -170,6 +185,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns into r[off .. off+15]
+template <int NR>
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[NR], int off) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[off + 0]), "=r"(r[off + 1]), "=r"(r[off + 2]), "=r"(r[off + 3]), "=r"(r[off + 4]), "=r"(r[off + 5]),
+          "=r"(r[off + 6]), "=r"(r[off + 7]), "=r"(r[off + 8]), "=r"(r[off + 9]), "=r"(r[off + 10]), "=r"(r[off + 11]),
+          "=r"(r[off + 12]), "=r"(r[off + 13]), "=r"(r[off + 14]), "=r"(r[off + 15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -197,6 +225,41 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t addr) {
     d |= (uint64_t)1 << 46;                        // descriptor version (tcgen05)
     d |= (uint64_t)2 << 61;                        // swizzle mode: 128 B
     return d;
+}
+
+// Same for a K-major tile stored with the 64-byte swizzle: rows of 64 B, 8-row atoms of
+// 512 B stacked at a 512-B stride (tile base 512-B aligned).
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(512 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;                        // swizzle mode: 64 B
+    return d;
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (tf32 operands in f32 containers, f32 accumulator).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// round an f32 to the nearest tf32 value (10 explicit mantissa bits), kept in f32 format
+__device__ __forceinline__ float tf32_rn(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Instruction descriptor: kind::tf32, tf32 A and B (K-major), f32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int m, int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Instruction descriptor: kind::f16, f16 A and B (K-major), f32 D, shape M x N.

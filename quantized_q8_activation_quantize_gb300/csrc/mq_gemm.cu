@@ -16,16 +16,22 @@
 //    is unpacked from raw block bytes (staged by 1-D bulk copies of each row's
 //    16-byte-aligned superset) straight into the same swizzled K-major layout.
 //  * Each 32-value block's product goes to its own TMEM accumulator (3-slot ring);
-//    the epilogue warps drain it, apply the activation scale per block, the fp16 d
-//    (and the Q4_K min term dmin * sum_j m_j d_a S) per super-block, and keep the
-//    running sum in a fourth TMEM region.
+//    the epilogue warps drain it and apply the activation scale per block with packed
+//    f32x2 FMAs; once per super-block they fold the fp16 d into a running sum kept
+//    in a fourth TMEM region.
+//  * The Q4_K min term dmin * sum_j m_j d_a[j] S[j] runs on the tensor pipe: per
+//    super-block three tf32 MMAs (K = 8) of the plane's d_a*S and of -dmin*m_j, each held
+//    as a tf32 (hi, lo) pair (hi*hi + lo*hi + hi*lo, error below 2^-21 relative),
+//    accumulate straight into the running sum.
 //
-// CTA = 14 warps: 0 TMA producer, 1 MMA issuer (+ TMEM owner), 2-5 unpackers (one
-// weight row per thread), 6-13 epilogue (2 per TMEM lane quadrant, 64 columns each).
+// CTA = 16 warps: 0 TMA producer, 1 MMA issuer (+ TMEM owner), 2-3 idle, 4-7 unpackers
+// (one weight row per thread), 8-15 epilogue (2 per TMEM lane quadrant, 64 columns
+// each); setmaxnreg moves registers from the first two warpgroups to the epilogue.
 // Tile: 128 tokens x 128 weight rows, K staged 64 at a time.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "mq_device.cuh"
@@ -35,10 +41,13 @@ namespace mq {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kThreads = 448;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpUnpack0 = 2, kWarpEpi0 = 6;
+constexpr int kThreads = 512;   // 4 warpgroups: {TMA, MMA, -, -}, unpack, epilogue x2
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpUnpack0 = 4, kWarpEpi0 = 8;
+// per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file)
+constexpr int kRegsCtl = 32, kRegsUnpack = 80, kRegsEpi = 200;
+static_assert(128 * kRegsCtl + 128 * kRegsUnpack + 256 * kRegsEpi <= 65536, "register split exceeds the launch pool");
 constexpr int kAccSlots = 3;
-constexpr uint32_t kTmemCols = 512, kAccCol = 384;
+constexpr uint32_t kTmemCols = 512, kMinCol = 384;   // 3 block slots + the Q4_K min-term sum
 constexpr int kTile = BM * BK * 2;       // one 128 x 64 f16 operand tile
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -50,24 +59,38 @@ struct GmCfg {
     static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 3;
     static constexpr int RAW_STAGES = FMT == FMT_Q4K ? 3 : 2;
     static constexpr int RAW_ROW = FMT == FMT_Q4K ? 144 : 224;   // 16-B aligned superset of one block
-    static constexpr bool CORR = FMT == FMT_Q6K;
-    static constexpr int INFO = FMT == FMT_Q4K ? 12 : 1;          // floats per weight row per super-block
+    static constexpr bool CORR = FMT == FMT_Q6K;                  // Q6_K odd |sc| > 64 correction tile
+    static constexpr bool MIN = FMT == FMT_Q4K;                   // Q4_K min term on the tensor pipe
+    static constexpr int MIN_TILE = BM * 64;                      // 128 rows x 16 tf32 (64 B, 64-B swizzle)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * kTile;
     static constexpr int OFF_BC = OFF_B + STAGES * kTile;
-    static constexpr int OFF_RAW = OFF_BC + (CORR ? STAGES * kTile : 0);
-    static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;
-    static constexpr int OFF_FLAG = OFF_INFO + 2 * BN * INFO * 4;
+    static constexpr int OFF_AMIN = OFF_BC + (CORR ? STAGES * kTile : 0);
+    static constexpr int OFF_BMIN = OFF_AMIN + (MIN ? 2 * MIN_TILE : 0);
+    static constexpr int OFF_RAW = OFF_BMIN + (MIN ? 2 * MIN_TILE : 0);
+    static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;   // fp16 d per weight row, 2 slots
+    static constexpr int OFF_FLAG = OFF_INFO + 2 * BN * 4;
     static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
-    // a_full[S] b_full[S] ab_empty[S] raw_full[R] info_full[2] info_empty[2] acc_full[3] acc_empty[3]
-    static constexpr int NBARS = 3 * STAGES + RAW_STAGES + 4 + 2 * kAccSlots;
+    // a_full[S] b_full[S] ab_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] acc_full[3]
+    // acc_empty[3] amin_full[2] amin_empty[2] min_final[1]
+    static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
 };
 
 struct Bars {
-    uint64_t *a_full, *b_full, *ab_empty, *raw_full, *info_full, *info_empty, *acc_full, *acc_empty;
+    uint64_t *a_full, *b_full, *ab_empty, *raw_full, *raw_empty, *info_full, *info_empty, *acc_full, *acc_empty;
+    uint64_t *amin_full, *amin_empty, *min_final;
 };
+
+// 16-byte async copy global -> shared (L2 only); completion tracked by cp.async groups / mbarriers
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// arrive on `bar` (without raising its expected count) once this thread's cp.async copies land
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -109,11 +132,16 @@ __device__ __forceinline__ void bytes_to_h2_biased(uint32_t v, uint32_t &lo, uin
 __device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
     return tile + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
+// swizzled (64 B) address of 16-byte chunk c of row r
+__device__ __forceinline__ uint32_t sw64_chunk(uint32_t tile, int r, int c) {
+    return tile + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
 
 template <int FMT, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t *__restrict__ w, int64_t N, int64_t K,
-                Plane p, int64_t M, float *__restrict__ y, Dump dump, unsigned int *err) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmDS,
+                const __grid_constant__ CUtensorMap tmW, const uint8_t *__restrict__ w, int64_t N, int64_t K, Plane p, int64_t M, float *__restrict__ y,
+                Dump dump, unsigned int *err) {
     using C = GmCfg<FMT>;
     constexpr int S = C::STAGES, R = C::RAW_STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -124,10 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.b_full = bars.a_full + S;
     bars.ab_empty = bars.b_full + S;
     bars.raw_full = bars.ab_empty + S;
-    bars.info_full = bars.raw_full + R;
+    bars.raw_empty = bars.raw_full + R;
+    bars.info_full = bars.raw_empty + R;
     bars.info_empty = bars.info_full + 2;
     bars.acc_full = bars.info_empty + 2;
     bars.acc_empty = bars.acc_full + kAccSlots;
+    bars.amin_full = bars.acc_empty + kAccSlots;
+    bars.amin_empty = bars.amin_full + 2;
+    bars.min_final = bars.amin_empty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
     volatile uint32_t *corr_flags = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_FLAG);
@@ -144,11 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.b_full[s], 128);
             mbar_init(&bars.ab_empty[s], 1);
         }
-        for (int r = 0; r < R; ++r) mbar_init(&bars.raw_full[r], 128);
+        for (int r = 0; r < R; ++r) {
+            // Q4_K: one tensor copy per super-block (producer); Q6_K: each row's cp.async (unpackers)
+            mbar_init(&bars.raw_full[r], FMT == FMT_Q4K ? 1 : 128);
+            mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (Q4_K only)
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.info_full[i], 128);
-            mbar_init(&bars.info_empty[i], 8);
+            mbar_init(&bars.info_empty[i], C::MIN ? 9 : 8);    // epilogue warps (+ the min MMA)
+            mbar_init(&bars.amin_full[i], 1);
+            mbar_init(&bars.amin_empty[i], 1);
         }
+        mbar_init(bars.min_final, 1);
         for (int i = 0; i < kAccSlots; ++i) {
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], 8);
@@ -161,13 +200,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kWarpTma) {
-        // ------------------------------------------------------------ A producer
+    // Each warpgroup first rebalances the register file (all four of its warps execute the
+    // setmaxnreg), so the code of every role is compiled under its own budget.
+    if (warp < kWarpUnpack0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+      if (warp == kWarpTma) {
+        // ------------------------------------------------------------ A / d*S producer
         if (lane == 0) {
             prefetch_tmap(&tmA);
-            int st = 0;
-            for (; st < nstages; ++st) {
+            if constexpr (C::MIN) prefetch_tmap(&tmDS);
+            if constexpr (FMT == FMT_Q4K) prefetch_tmap(&tmW);
+            int st = 0, sb_issued = 0, raw_issued = 0;
+            // raw Q4_K blocks of the tile's 128 rows for one super-block: a 144 B x 128 box
+            auto issue_raw = [&](int sb) -> bool {
+                const int slot = sb % R;
+                if (!mbar_wait(&bars.raw_empty[slot], ((sb / R) & 1) ^ 1, err, ERR_GEMM_RAW_FULL, abort_flag))
+                    return false;
+                mbar_arrive_expect_tx(&bars.raw_full[slot], BN * C::RAW_ROW);
+                tma_load_2d(sm + C::OFF_RAW + slot * BN * C::RAW_ROW, &tmW, sb * C::BB, (int32_t)n0,
+                            &bars.raw_full[slot]);
+                raw_issued = sb + 1;
+                return true;
+            };
+            if constexpr (FMT == FMT_Q4K) {
+                for (int sb = 0; sb < R - 1 && sb < nsb; ++sb)
+                    if (!issue_raw(sb)) break;
+            }
+            for (; st < nstages && !*abort_flag; ++st) {
                 const int s = st % S;
+                if constexpr (FMT == FMT_Q4K) {
+                    // keep raw weights R-1 super-blocks ahead of the A stages
+                    if ((st & 3) == 0 && (st >> 2) + R - 1 < nsb)
+                        if (!issue_raw((st >> 2) + R - 1)) break;
+                }
+                if constexpr (C::MIN) {
+                    if ((st & 3) == 0) {
+                        const int sb = st >> 2;
+                        if (!mbar_wait(&bars.amin_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_MIN, abort_flag))
+                            break;
+                        mbar_arrive_expect_tx(&bars.amin_full[sb & 1], C::MIN_TILE);
+                        tma_load_2d(sm + C::OFF_AMIN + (sb & 1) * C::MIN_TILE, &tmDS, sb * 16, (int32_t)m0,
+                                    &bars.amin_full[sb & 1]);
+                        sb_issued = sb + 1;
+                    }
+                }
                 if (!mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) break;
                 mbar_arrive_expect_tx(&bars.a_full[s], kTile);
                 tma_load_2d(sm + C::OFF_A + s * kTile, &tmA, st * BK, (int32_t)m0, &bars.a_full[s]);
@@ -175,48 +251,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) {   // leave no copy in flight: wait (bounded) for the last ones issued
                 for (int i = st - 1; i >= 0 && i >= st - S; --i)
                     mbar_wait(&bars.a_full[i % S], (i / S) & 1, err, ERR_GEMM_A_FULL, nullptr);
+                for (int sb = sb_issued - 1; sb >= 0 && sb >= sb_issued - 2; --sb)
+                    mbar_wait(&bars.amin_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_MIN, nullptr);
+                for (int sb = raw_issued - 1; sb >= 0 && sb >= raw_issued - R; --sb)
+                    mbar_wait(&bars.raw_full[sb % R], (sb / R) & 1, err, ERR_GEMM_RAW_FULL, nullptr);
             }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            constexpr uint32_t idesc_min = idesc_tf32_f32(BM, BN);
             const uint32_t a_base = smem_u32(sm + C::OFF_A), b_base = smem_u32(sm + C::OFF_B);
             const uint32_t bc_base = smem_u32(sm + C::OFF_BC);
+            const uint32_t amin_base = smem_u32(sm + C::OFF_AMIN), bmin_base = smem_u32(sm + C::OFF_BMIN);
             int gb = 0;
             bool ok = true;
-            for (int st = 0; st < nstages && ok; ++st) {
-                const int s = st % S;
-                const uint32_t ph = (st / S) & 1;
-                if (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag)) break;
-                if (!mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag)) break;
-                tc_fence_after();
-                bool corr = false;
-                if constexpr (C::CORR)
-                    corr = (corr_flags[4 * s] | corr_flags[4 * s + 1] | corr_flags[4 * s + 2] | corr_flags[4 * s + 3]) != 0;
-                for (int h = 0; h < 2; ++h) {
-                    const int slot = gb % kAccSlots;
-                    if (!mbar_wait(&bars.acc_empty[slot], ((gb / kAccSlots) & 1) ^ 1, err, ERR_GEMM_ACC_EMPTY,
-                                   abort_flag)) {
+            for (int sb = 0; sb < nsb && ok; ++sb) {
+                for (int q = 0; q < 4 && ok; ++q) {
+                    const int st = sb * 4 + q, s = st % S;
+                    const uint32_t ph = (st / S) & 1;
+                    if (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag) ||
+                        !mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(slot * BN);
+                    bool corr = false;
+                    if constexpr (C::CORR)
+                        corr = (corr_flags[4 * s] | corr_flags[4 * s + 1] | corr_flags[4 * s + 2] |
+                                corr_flags[4 * s + 3]) != 0;
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = gb % kAccSlots;
+                        if (!mbar_wait(&bars.acc_empty[slot], ((gb / kAccSlots) & 1) ^ 1, err, ERR_GEMM_ACC_EMPTY,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem + (uint32_t)(slot * BN);
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t koff = (uint32_t)((2 * h + kk) * 32);
-                        const uint64_t adesc = sw128_kmajor_desc(a_base + s * kTile + koff);
-                        mma_f16(d_tmem, adesc, sw128_kmajor_desc(b_base + s * kTile + koff), idesc, kk);
-                        if (corr) mma_f16(d_tmem, adesc, sw128_kmajor_desc(bc_base + s * kTile + koff), idesc, 1);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t koff = (uint32_t)((2 * h + kk) * 32);
+                            const uint64_t adesc = sw128_kmajor_desc(a_base + s * kTile + koff);
+                            mma_f16(d_tmem, adesc, sw128_kmajor_desc(b_base + s * kTile + koff), idesc, kk);
+                            if (corr)
+                                mma_f16(d_tmem, adesc, sw128_kmajor_desc(bc_base + s * kTile + koff), idesc, 1);
+                        }
+                        mma_commit(&bars.acc_full[slot]);
+                        ++gb;
                     }
-                    mma_commit(&bars.acc_full[slot]);
-                    ++gb;
+                    mma_commit(&bars.ab_empty[s]);
                 }
-                mma_commit(&bars.ab_empty[s]);
+                if constexpr (C::MIN) {
+                    // min term of this super-block, summed over the whole K in its own TMEM region:
+                    // MIN (+)= (d_a S) x (-dmin m_j), both operands tf32 (hi, lo) pairs, three MMAs of K = 8
+                    if (!ok) break;
+                    const uint32_t ph = (sb >> 1) & 1;
+                    if (!mbar_wait(&bars.amin_full[sb & 1], ph, err, ERR_GEMM_MIN, abort_flag) ||
+                        !mbar_wait(&bars.info_full[sb & 1], ph, err, ERR_GEMM_INFO_FULL, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t at = amin_base + (sb & 1) * C::MIN_TILE, bt = bmin_base + (sb & 1) * C::MIN_TILE;
+                    // (hi + lo)(d_a S) x (hi + lo)(-dmin m): hi*hi + lo*hi + hi*lo (lo*lo is below 2^-22)
+                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt), idesc_min, sb > 0 ? 1u : 0u);
+                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at + 32), sw64_kmajor_desc(bt), idesc_min, 1u);
+                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt + 32), idesc_min, 1u);
+                    mma_commit(&bars.amin_empty[sb & 1]);
+                    mma_commit(&bars.info_empty[sb & 1]);
+                }
+            }
+            if constexpr (C::MIN) {
+                if (ok) mma_commit(bars.min_final);
             }
         }
+      }   // warps 2-3 of the control warpgroup are idle
     } else if (warp < kWarpEpi0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsUnpack));
         // ------------------------------------------------------------ unpackers
         const int r = threadIdx.x - 32 * kWarpUnpack0;     // weight row in the tile
         const int64_t n = n0 + r;
@@ -224,26 +337,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *wrow = w + (valid ? n : 0) * row_bytes;
         uint8_t *raw_row0 = sm + C::OFF_RAW + r * C::RAW_ROW;
         const uint32_t b_tile0 = smem_u32(sm + C::OFF_B), bc_tile0 = smem_u32(sm + C::OFF_BC);
+        const uint32_t bmin_tile0 = smem_u32(sm + C::OFF_BMIN);
         float *info0 = reinterpret_cast<float *>(sm + C::OFF_INFO);
 
+        // Q6_K: this row's block (210 B, 2-byte aligned) as the 16-byte aligned superset, fetched by
+        // 16-byte cp.async (too small and too many for the bulk-copy engine: 128 rows per super-block)
         auto issue_raw = [&](int sb) {
             const int slot = sb % R;
             if (valid) {
                 const uint8_t *src = wrow + (int64_t)sb * C::BB;
-                const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15);
-                const uintptr_t a1 = (reinterpret_cast<uintptr_t>(src) + C::BB + 15) & ~uintptr_t(15);
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars.raw_full[slot], (uint32_t)(a1 - a0));
-                bulk_copy_g2s(raw_row0 + slot * BN * C::RAW_ROW, reinterpret_cast<const void *>(a0),
-                              (uint32_t)(a1 - a0), &bars.raw_full[slot]);
+                const uint8_t *a0 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15));
+                const int nchunk = (int)(((reinterpret_cast<uintptr_t>(src) + C::BB + 15) & ~uintptr_t(15)) -
+                                         reinterpret_cast<uintptr_t>(a0)) / 16;
+                const uint32_t dst = smem_u32(raw_row0 + slot * BN * C::RAW_ROW);
+                for (int i = 0; i < nchunk; ++i) cp_async16(dst + 16 * i, a0 + 16 * i);
+                cp_async_arrive_noinc(&bars.raw_full[slot]);
             } else {
                 mbar_arrive(&bars.raw_full[slot]);
             }
         };
-        for (int sb = 0; sb < R && sb < nsb; ++sb) issue_raw(sb);
+        if constexpr (FMT == FMT_Q6K) {
+            for (int sb = 0; sb < R && sb < nsb; ++sb) issue_raw(sb);
+        }
 
         uint32_t dirty = (1u << S) - 1;      // Q6_K correction rows that may hold non-zero data
-        int issued = R < nsb ? R : nsb;
+        int issued = (FMT == FMT_Q6K) ? (R < nsb ? R : nsb) : 0;
         int sb = 0;
         for (; sb < nsb; ++sb) {
             const int slot = sb % R;
@@ -284,20 +402,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) sc[i] = (int)(int8_t)((tail[i >> 2] >> (8 * (i & 3))) & 0xff);
                 d = __half2float(__ushort_as_half((unsigned short)(tail[4] & 0xffff)));
             }
-            // ---- per-row factors for the epilogue
+            // ---- per-row factors of this super-block: d for the epilogue, -dmin m_j for the min MMA
             if (!mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY, abort_flag)) break;
-            float *info = info0 + (sb & 1) * BN * C::INFO + r * C::INFO;
-            if constexpr (FMT == FMT_Q4K) {
-                reinterpret_cast<float4 *>(info)[0] = make_float4(d, dmin, (float)mn[0], (float)mn[1]);
-                reinterpret_cast<float4 *>(info)[1] = make_float4((float)mn[2], (float)mn[3], (float)mn[4], (float)mn[5]);
-                reinterpret_cast<float4 *>(info)[2] = make_float4((float)mn[6], (float)mn[7], 0.0f, 0.0f);
-            } else {
-                info[0] = d;
+            info0[(sb & 1) * BN + r] = d;
+            if constexpr (C::MIN) {
+                // -dmin*m_j has at most 17 significant bits (exact in f32); it splits exactly into
+                // a tf32 pair: row = [hi_0..hi_7 | lo_0..lo_7]
+                uint32_t wh[8], wl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float v = -(dmin * (float)mn[j]);
+                    const float vh = tf32_rn(v);
+                    wh[j] = __float_as_uint(vh);
+                    wl[j] = __float_as_uint(v - vh);
+                }
+                const uint32_t bt = bmin_tile0 + (sb & 1) * C::MIN_TILE;
+                sts128(sw64_chunk(bt, r, 0), make_uint4(wh[0], wh[1], wh[2], wh[3]));
+                sts128(sw64_chunk(bt, r, 1), make_uint4(wh[4], wh[5], wh[6], wh[7]));
+                sts128(sw64_chunk(bt, r, 2), make_uint4(wl[0], wl[1], wl[2], wl[3]));
+                sts128(sw64_chunk(bt, r, 3), make_uint4(wl[4], wl[5], wl[6], wl[7]));
+                fence_proxy_async_smem();
             }
             mbar_arrive(&bars.info_full[sb & 1]);
 
-            // ---- four 64-value stages of this super-block
+            // ---- four 64-value stages of this super-block (unrolled: sc[] stays in registers)
             bool ok = true;
+#pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int st = sb * 4 + q, s = st % S;
                 if (!mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) {
@@ -344,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) ql[i] = 0;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) qh[i] = 0x0a0a0a0au;   // q = 32 - 32 = 0 (unused: scale 0)
+                        for (int i = 0; i < 8; ++i) qh[i] = 0;
                     }
                     const int nsh = (g0 >= 2) ? 4 : 0;
                     bool need_corr = false;
@@ -386,7 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars.b_full[s]);
             }
             if (!ok) break;
-            if (sb + R < nsb) {
+            if constexpr (FMT == FMT_Q4K) {
+                __syncwarp();                               // the warp's 32 rows of this slot are read
+                if (lane == 0) mbar_arrive(&bars.raw_empty[slot]);
+            } else if (sb + R < nsb) {
                 issue_raw(sb + R);
                 ++issued;
             }
@@ -396,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars.raw_full[i % R], (i / R) & 1, err, ERR_GEMM_RAW_FULL, nullptr);
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ------------------------------------------------------------ epilogue
         const int e = warp - kWarpEpi0, qd = warp & 3, hf = e >> 2;
         const int64_t m = m0 + 32 * qd + lane;
@@ -404,30 +538,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = hf * 64;
         const int64_t nblk32 = K / kQ8;
         const float *info0 = reinterpret_cast<const float *>(sm + C::OFF_INFO);
-        float acc[64];
+        // acc: the running sum over super-blocks; part: sum_j d_a[j] I_j of the current super-block
+        float2 acc[32], part[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            acc[i] = make_float2(0.0f, 0.0f);
+            part[i] = make_float2(0.0f, 0.0f);
+        }
+        // activation scales of the current and the next super-block (prefetched a super-block ahead)
+        float da_cur[8], da_nxt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) da_cur[j] = valid_m ? __ldg(p.d + (int64_t)j * M + m) : 0.0f;
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
-            float dS[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                da_nxt[j] = (valid_m && sb + 1 < nsb) ? __ldg(p.d + (int64_t)(8 * (sb + 1) + j) * M + m) : 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int gb = sb * 8 + j;
-                const float da = valid_m ? __ldg(p.d + (int64_t)gb * M + m) : 0.0f;
-                if constexpr (FMT == FMT_Q4K) dS[j] = valid_m ? da * (float)__ldg(p.s + (int64_t)gb * M + m) : 0.0f;
                 const int slot = gb % kAccSlots;
                 if (!mbar_wait(&bars.acc_full[slot], (gb / kAccSlots) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const float2 da2 = make_float2(da_cur[j], da_cur[j]);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t v[32];
                     tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32 * hh), v);
                     tmem_ld_wait();
+                    if (hh == 1) {       // both halves are in registers: hand the slot back to the MMA
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
+                    }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(__uint_as_float(v[i]), da, acc[32 * hh + i]);
+                    for (int i = 0; i < 16; ++i)
+                        part[16 * hh + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                                       da2, part[16 * hh + i]);
                     if constexpr (DUMP) {
                         if (valid_m && m >= dump.m0 && m < dump.m0 + dump.m_cnt) {
 #pragma unroll
@@ -440,72 +590,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
             }
             if (!ok) break;
-            // ---- super-block end: fold d (and the Q4_K min term) into the running sum
+            // ---- super-block end: acc += d * part (d: fp16 factor of each weight row)
             if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
-            const float *info = info0 + (sb & 1) * BN * C::INFO;
+            const float *info = info0 + (sb & 1) * BN + col0;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                if (sb > 0) {
-                    tmem_ld32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = col0 + 32 * hh + i;
-                    float add;
-                    if constexpr (FMT == FMT_Q4K) {
-                        const float4 f0 = reinterpret_cast<const float4 *>(info + col * C::INFO)[0];
-                        const float4 f1 = reinterpret_cast<const float4 *>(info + col * C::INFO)[1];
-                        const float4 f2 = reinterpret_cast<const float4 *>(info + col * C::INFO)[2];
-                        float t = f0.z * dS[0];
-                        t = fmaf(f0.w, dS[1], t);
-                        t = fmaf(f1.x, dS[2], t);
-                        t = fmaf(f1.y, dS[3], t);
-                        t = fmaf(f1.z, dS[4], t);
-                        t = fmaf(f1.w, dS[5], t);
-                        t = fmaf(f2.x, dS[6], t);
-                        t = fmaf(f2.y, dS[7], t);
-                        add = fmaf(f0.x, acc[32 * hh + i], -f0.y * t);
-                    } else {
-                        add = info[col] * acc[32 * hh + i];
-                    }
-                    v[i] = __float_as_uint(__uint_as_float(v[i]) + add);
-                    acc[32 * hh + i] = 0.0f;
-                }
-                tmem_st32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
+            for (int i = 0; i < 32; ++i) {
+                acc[i] = __ffma2_rn(part[i], *reinterpret_cast<const float2 *>(info + 2 * i), acc[i]);
+                part[i] = make_float2(0.0f, 0.0f);
             }
-            tmem_st_wait();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.info_empty[sb & 1]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) da_cur[j] = da_nxt[j];
         }
         if (ok && !*abort_flag) {
+            if constexpr (C::MIN) {
+                // the tensor-core min term, summed over all super-blocks
+                if (mbar_wait(bars.min_final, 0, err, ERR_GEMM_MIN, abort_flag)) {
+                    tc_fence_after();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t v[32];
-                tmem_ld32(trow + kAccCol + (uint32_t)(col0 + 32 * hh), v);
-                tmem_ld_wait();
-                if (valid_m) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
+                        tmem_ld32(trow + kMinCol + (uint32_t)(col0 + 32 * hh), v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[16 * hh + i] = __fadd2_rn(acc[16 * hh + i],
+                                                          make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
+                    }
+                } else {
+                    ok = false;
+                }
+            }
+            if (ok && valid_m) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
                     const int64_t nb0 = n0 + col0 + 32 * hh;
                     float *dst = y + m * N + nb0;
                     if (nb0 + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(dst + i) =
-                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        for (int i = 0; i < 16; i += 2)
+                            *reinterpret_cast<float4 *>(dst + 2 * i) =
+                                make_float4(acc[16 * hh + i].x, acc[16 * hh + i].y, acc[16 * hh + i + 1].x,
+                                            acc[16 * hh + i + 1].y);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (nb0 + i < N) dst[i] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 16; ++i) {
+                            if (nb0 + 2 * i < N) dst[2 * i] = acc[16 * hh + i].x;
+                            if (nb0 + 2 * i + 1 < N) dst[2 * i + 1] = acc[16 * hh + i].y;
+                        }
                     }
                 }
             }
@@ -538,14 +673,15 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 template <int FMT, bool DUMP>
-int launch_fmt(const CUtensorMap &tm, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
-               const Dump &dump, unsigned int *err, cudaStream_t stream) {
+int launch_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap &tmw, const uint8_t *w, int64_t N,
+               int64_t K, const Plane &p, int64_t M, float *y, const Dump &dump, unsigned int *err,
+               cudaStream_t stream) {
     using C = GmCfg<FMT>;
     auto kern = gemm_kernel<FMT, DUMP>;
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, FMT * 2 + (DUMP ? 1 : 0));
     if (rc != MQ_OK) return rc;
     const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    kern<<<grid, kThreads, C::SMEM, stream>>>(tm, w, N, K, p, M, y, dump, err);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tm, tmds, tmw, w, N, K, p, M, y, dump, err);
     return cuda_error(cudaGetLastError(), "gemm launch");
 }
 
@@ -566,12 +702,38 @@ int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for M=%lld K=%lld", (int)r,
                                             (long long)M, (long long)K);
+    // d*S tf32 pairs: [M][2*K/32] f32, one 128-token x 16-value box per super-block, 64-byte swizzle
+    CUtensorMap tmds;
+    const cuuint64_t dims2[2] = {(cuuint64_t)(2 * (K / kQ8)), (cuuint64_t)M};
+    const cuuint64_t strides2[1] = {(cuuint64_t)(2 * (K / kQ8)) * 4};
+    const cuuint32_t box2[2] = {16, BM};
+    const CUresult r2 = enc(&tmds, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ds, dims2, strides2, box2, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r2 != CUDA_SUCCESS)
+        return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled (d*S) failed (%d) for M=%lld K=%lld", (int)r2,
+                         (long long)M, (long long)K);
+    // raw Q4_K weights: [N][K/256 * 144] bytes, one 144 B x 128-row box per super-block
+    CUtensorMap tmw;
+    memset(&tmw, 0, sizeof tmw);
+    if (fmt == FMT_Q4K) {
+        const cuuint64_t dims3[2] = {(cuuint64_t)((K / kQK) * 144), (cuuint64_t)N};
+        const cuuint64_t strides3[1] = {(cuuint64_t)((K / kQK) * 144)};
+        const cuuint32_t box3[2] = {144, BN};
+        const CUresult r3 = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims3, strides3, box3,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r3 != CUDA_SUCCESS)
+            return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d) for N=%lld K=%lld", (int)r3,
+                             (long long)N, (long long)K);
+    }
     const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
     if (fmt == FMT_Q4K)
-        return dmp ? launch_fmt<FMT_Q4K, true>(tm, w, N, K, p, M, y, dump, err, stream)
-                   : launch_fmt<FMT_Q4K, false>(tm, w, N, K, p, M, y, dump, err, stream);
-    return dmp ? launch_fmt<FMT_Q6K, true>(tm, w, N, K, p, M, y, dump, err, stream)
-               : launch_fmt<FMT_Q6K, false>(tm, w, N, K, p, M, y, dump, err, stream);
+        return dmp ? launch_fmt<FMT_Q4K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
+                   : launch_fmt<FMT_Q4K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
+    return dmp ? launch_fmt<FMT_Q6K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
+               : launch_fmt<FMT_Q6K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
 }
 
 }  // namespace mq
+

@@ -22,6 +22,7 @@ struct Plane {
     int8_t *q8;        // int8 codes [M][K]
     float *d;          // [K/32][M]
     int32_t *s;        // [K/32][M]
+    float *ds;         // [M][2*K/32]: per super-block hi[8], lo[8] of tf32(d*S)
 };
 
 // window of the integer checkpoint dump (test hook); cnt == 0 disables it

@@ -60,6 +60,13 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const P
         const int64_t b = k0 / kQ8;
         p.d[b * M + m] = d;
         p.s[b * M + m] = s;
+        // d*S as a tf32 (hi, lo) pair: operand of the tensor-core Q4_K min term
+        const float ds = __fmul_rn(d, (float)s);
+        const float hi = tf32_rn(ds);
+        const float lo = tf32_rn(__fsub_rn(ds, hi));
+        float *row = p.ds + m * (2 * (K / kQ8)) + (b >> 3) * 16 + (b & 7);
+        row[0] = hi;
+        row[8] = lo;
     }
 }
 

@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol(L):
 def test_plane_layout(L, M, K):
     lay = B.mq_q8_plane_layout(M, K)
     nb = K // 32
-    secs = [("off_q16", 2 * M * K), ("off_q8", M * K), ("off_d", 4 * nb * M), ("off_s", 4 * nb * M)]
+    secs = [("off_q16", 2 * M * K), ("off_q8", M * K), ("off_d", 4 * nb * M), ("off_s", 4 * nb * M),
+            ("off_ds", 8 * nb * M)]
     end = 0
     for name, size in secs:
         assert lay[name] % 256 == 0 and lay[name] >= end
