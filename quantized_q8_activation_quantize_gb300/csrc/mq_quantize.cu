@@ -72,12 +72,13 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const P
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int64_t M, int64_t K, Plane p) {
     const int lane = threadIdx.x & 31;
-    const int64_t nch = K / 256;
-    const int64_t items = M * nch;
+    const uint32_t nch = (uint32_t)(K / 256);
+    const int64_t items = M * (int64_t)nch;
     const int64_t stride = (int64_t)gridDim.x * 8;
     for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += stride) {
-        const int64_t m = it / nch;
-        const int64_t k0 = (it - m * nch) * 256 + lane * 8;
+        // items < 2^31 * 2^23: the quotient fits 32 bits; divide in 64 bits only when it must
+        const int64_t m = (it < 0xffffffffll) ? (int64_t)((uint32_t)it / nch) : it / (int64_t)nch;
+        const int64_t k0 = (it - m * (int64_t)nch) * 256 + lane * 8;
         const float4 *src = reinterpret_cast<const float4 *>(x + m * K + k0);
         const float4 a = __ldg(src), b = __ldg(src + 1);
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
