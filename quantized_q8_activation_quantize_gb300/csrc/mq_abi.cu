@@ -90,6 +90,27 @@ int ensure_smem_attr(const void *kernel, int bytes, int slot) {
     return MQ_OK;
 }
 
+int resident_ctas(const void *kernel, int threads, int smem_bytes, int slot, int *out) {
+    // per (device, slot): the shared-memory size last asked about and the answer
+    static int cache_smem[kMaxDevices][kAttrSlots] = {};
+    static int cache_n[kMaxDevices][kAttrSlots] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kAttrSlots)
+        return set_error(MQ_ERR_CUDA, "resident_ctas: bad device %d / slot %d", dev, slot);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (cache_n[dev][slot] == 0 || cache_smem[dev][slot] != smem_bytes) {
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes);
+        if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (n < 1) return set_error(MQ_ERR_CUDA, "kernel in slot %d cannot be resident (%d B shared memory)", slot, smem_bytes);
+        cache_n[dev][slot] = n;
+        cache_smem[dev][slot] = smem_bytes;
+    }
+    *out = cache_n[dev][slot];
+    return MQ_OK;
+}
+
 int cuda_error(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return MQ_OK;
     return set_error(MQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));

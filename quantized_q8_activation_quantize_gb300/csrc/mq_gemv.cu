@@ -4,14 +4,27 @@
 // kernels; "Roadmap > 0": the decode path streams the weights once per token.
 //
 // Design (HBM-bound): every weight byte is read from HBM exactly once per group of up
-// to 8 tokens.  Each warp owns a private 3-stage ring in shared memory and walks its
-// rows in chunks of up to 8 super-blocks; lane 0 refills a stage with one 1-D bulk
-// async copy (TMA engine) of the 16-byte-aligned superset of the chunk's bytes, so a
-// Q6_K block (210 B, only 2-byte aligned) needs no special load path from HBM.  Four
-// 8-warp CTAs per SM keep ~160 KB in flight.  The math runs from shared memory: 4 lanes
-// per super-block, each owning 64 of its 256 values (so scale decoding and the float
-// work of a block amortize over 64 values), dp4a against the int8 codes (read through
-// L1), f32 scaling per 32-value block, one warp reduction per row.
+// to 8 tokens.  The weight matrix is one flat stream of super-blocks (row-major, rows
+// contiguous).  Each CTA owns a contiguous range of whole rows and walks it in units of
+// TU super-blocks (a unit may start or end inside a row):
+//   * a producer warp refills a 4-stage shared-memory ring with ONE large 1-D bulk copy
+//     (TMA engine) per unit -- the 16-byte aligned superset of the unit's bytes, so the
+//     2-byte aligned 210-byte Q6_K block needs no special load path.  A few large copies
+//     per SM keep the copy engine streaming at full HBM rate, where many small per-warp
+//     copies stall it;
+//   * 8 consumer warps take 4 threads per super-block, each owning 64 of its 256 values
+//     (scale decoding and float work amortize over 64 values): dp4a against the int8
+//     codes, f32 scaling per 32-value block, a 4-lane reduction, and one partial per
+//     (token, super-block) into a ring of partial buffers;
+//   * a reducer warp sums each row's partials in a fixed order (a row that continues
+//     into the next unit carries its running sum), so results are deterministic, and
+//     writes Y.  Consumers wait for the reducer only when the partial ring is full.
+// The shared-memory data pipe is the scarce resource once the weights stream at full
+// rate: when the tokens' activations fit, each CTA first stages them in shared memory
+// (codes in an XOR-swizzled layout that makes every lane pattern below conflict-free,
+// plus a per-block table of (d_a, d_a * S) pairs -- for Q6_K per 16-value half block,
+// with the -32 code offset folded in), so the inner loop reads 4 wavefronts per 512
+// bytes instead of one scattered L1 line per lane.
 #include <cuda_fp16.h>
 
 #include "mq_device.cuh"
@@ -20,18 +33,34 @@
 namespace mq {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kStages = 3;
-constexpr int kChunkBlocks = 8;        // super-blocks per staged chunk: 32 lanes x 64 values
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // + producer warp + reducer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kReducerWarp = kConsumerWarps + 1;
+constexpr int kStages = 4;
+constexpr int kPartBufs = 4;
+constexpr int kSbPerPass = kConsumerWarps * 8;         // 4 threads per super-block
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int FMT>
 struct GvCfg {
     static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
-    // superset of an 8-block chunk + up to 15 leading bytes + 16 bytes of over-read slack
-    static constexpr int STAGE = ((kChunkBlocks * BB + 15 + 15) / 16) * 16 + 16;
-    static constexpr int SMEM = kWarps * kStages * STAGE;
+    static constexpr int PASSES = FMT == FMT_Q4K ? 2 : 1;
+    static constexpr int TU = kSbPerPass * PASSES;     // super-blocks per unit
+    static constexpr int STAGES = FMT == FMT_Q4K ? 3 : 4;
+    // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
+    static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
+    static constexpr int OFF_PART = STAGES * STAGE;
+    static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
+    // staged activations: int8 codes [MT][K] + float2 table, per half block (Q6_K) or block (Q4_K)
+    static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K + (FMT == FMT_Q6K ? K / 2 : K / 4)); }
+    // 16-byte chunk c of a token's codes lives at chunk swz(c) (XOR of bits 0-2 only)
+    __device__ static __forceinline__ uint32_t swz(uint32_t c) {
+        return FMT == FMT_Q6K ? c ^ (((c >> 3) & 1u) << 1) ^ (((c >> 4) & 1u) << 2)
+                              : c ^ (((c >> 3) & 1u) << 1) ^ ((c >> 4) & 1u);
+    }
 };
+constexpr int kActSmemMax = 48 * 1024;               // stage activations when they fit in this
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -46,6 +75,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void sts64(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
 }
 // 16 bytes at a 2-byte aligned shared address (five aligned words, funnel-shifted)
@@ -66,258 +107,416 @@ __device__ __forceinline__ int dot16(const uint4 &w, const uint4 &a) {
     return __dp4a((int)w.w, (int)a.w, __dp4a((int)w.z, (int)a.z, __dp4a((int)w.y, (int)a.y, __dp4a((int)w.x, (int)a.x, 0))));
 }
 
-// Each warp owns a kStages ring in shared memory and walks its rows in chunks of up to 8
-// super-blocks (one bulk copy of the chunk's 16-byte aligned superset per stage).  Lane l
-// takes super-block l/4 of the chunk and a 64-value quarter u = l%4 of it.
-template <int FMT, int MT, bool DUMP>
-__global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t *__restrict__ w, int64_t N, int64_t K,
-                                                           Plane p, int64_t M, int64_t t0, int mt,
-                                                           float *__restrict__ y, Dump dump, unsigned int *err) {
-    using C = GvCfg<FMT>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+// x / d (and x % d in rem) for 0 <= x < 2^24 through a float reciprocal (inv_d = 1/d rounded):
+// the estimate is within one of the quotient, and one correction each way makes it exact.
+__device__ __forceinline__ uint32_t divmod_small(uint32_t x, uint32_t d, float inv_d, uint32_t &rem) {
+    uint32_t q = __float2uint_rz(__uint2float_rz(x) * inv_d);
+    int r = (int)x - (int)(q * d);
+    if (r < 0) { --q; r += (int)d; }
+    if (r >= (int)d) { ++q; r -= (int)d; }
+    rem = (uint32_t)r;
+    return q;
+}
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t *ring = smem + warp * kStages * C::STAGE;
-    const uint32_t ring_s = smem_u32(ring);
-    uint64_t *bar = bars[warp];
+struct GvArgs {
+    const uint8_t *w;
+    int64_t N, K;
+    Plane p;
+    int64_t M, t0;
+    int mt;
+    float *y;
+    Dump dump;
+    unsigned int *err;
+};
 
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
-        mbar_init_fence();
+// shared-memory addresses of the staged activations (ACT kernels): codes [MT][K], table
+struct GvAct {
+    uint32_t codes, tab;
+    uint32_t nb;
+};
+
+// Q4_K: quarter u of the super-block at shared address `blk` (row n, super-block sbi of the
+// row): qs bytes [32u, 32u+32), whose low nibbles are sub-block 2u and high nibbles 2u+1.
+template <int MT, bool ACT, bool DUMP>
+__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n, int64_t sbi,
+                                            int u, bool valid, float (&part)[MT]) {
+    using C = GvCfg<FMT_Q4K>;
+    uint4 hd = make_uint4(0, 0, 0, 0), q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+    if (valid) {
+        hd = lds128(blk);
+        q0 = lds128(blk + 16 + 32 * u);
+        q1 = lds128(blk + 32 + 32 * u);
     }
-    __syncwarp();
-
-    const int nb = (int)(K / kQK);                      // super-blocks per row
-    const int nch = (nb + kChunkBlocks - 1) / kChunkBlocks;
-    const int64_t row_bytes = (int64_t)nb * C::BB;
-    const int64_t nblk32 = K / kQ8;
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp, GW = (int64_t)gridDim.x * kWarps;
-    const int nrows = gw < N ? (int)((N - gw + GW - 1) / GW) : 0;
-    const int items = nrows * nch;
-
-    // items run row-major over (row r of this warp, chunk c); positions advance incrementally
-    auto chunk_bytes = [&](int r, int c, int64_t &start, int &nblk) {
-        const int64_t n = gw + (int64_t)r * GW;
-        start = n * row_bytes + (int64_t)c * (kChunkBlocks * C::BB);
-        nblk = min(kChunkBlocks, nb - c * kChunkBlocks);
-    };
-    int ri = 0, ci = 0, si = 0;                         // next item to issue, and its stage
-    auto issue = [&]() {
-        int64_t start;
-        int nblk;
-        chunk_bytes(ri, ci, start, nblk);
-        const int64_t a0 = start & ~(int64_t)15, a1 = (start + nblk * C::BB + 15) & ~(int64_t)15;
-        mbar_arrive_expect_tx(&bar[si], (uint32_t)(a1 - a0));
-        bulk_copy_g2s(ring + si * C::STAGE, w + a0, (uint32_t)(a1 - a0), &bar[si]);
-        if (++ci == nch) { ci = 0; ++ri; }
-        if (++si == kStages) si = 0;
-    };
-
-    if (lane == 0)
-        for (int i = 0; i < items && i < kStages; ++i) issue();
-
-    float acc[MT];
+    const float d = half_bits_to_float(hd.x & 0xffff), dmin = half_bits_to_float(hd.x >> 16);
+    // the 12 scale bytes: s[0..3] = hd.y, s[4..7] = hd.z, s[8..11] = hd.w; sub-blocks 2u, 2u+1
+    int sc0, m0, sc1, m1;
+    if (u < 2) {
+        const uint32_t x = hd.y >> (16 * u), z = hd.z >> (16 * u);
+        sc0 = x & 63; sc1 = (x >> 8) & 63; m0 = z & 63; m1 = (z >> 8) & 63;
+    } else {
+        const uint32_t lo = hd.w >> (16 * (u - 2));                                 // s[j+4], j = 2u, 2u+1
+        const uint32_t ts = hd.y >> (16 * (u - 2)), tm = hd.z >> (16 * (u - 2));   // s[j-4], s[j]
+        sc0 = (lo & 15) | (((ts >> 6) & 3) << 4);
+        sc1 = ((lo >> 8) & 15) | (((ts >> 14) & 3) << 4);
+        m0 = ((lo >> 4) & 15) | (((tm >> 6) & 3) << 4);
+        m1 = ((lo >> 12) & 15) | (((tm >> 14) & 3) << 4);
+    }
+    const uint4 lo0 = make_uint4(q0.x & 0x0f0f0f0fu, q0.y & 0x0f0f0f0fu, q0.z & 0x0f0f0f0fu, q0.w & 0x0f0f0f0fu);
+    const uint4 lo1 = make_uint4(q1.x & 0x0f0f0f0fu, q1.y & 0x0f0f0f0fu, q1.z & 0x0f0f0f0fu, q1.w & 0x0f0f0f0fu);
+    const uint4 hi0 = make_uint4((q0.x >> 4) & 0x0f0f0f0fu, (q0.y >> 4) & 0x0f0f0f0fu, (q0.z >> 4) & 0x0f0f0f0fu,
+                                 (q0.w >> 4) & 0x0f0f0f0fu);
+    const uint4 hi1 = make_uint4((q1.x >> 4) & 0x0f0f0f0fu, (q1.y >> 4) & 0x0f0f0f0fu, (q1.z >> 4) & 0x0f0f0f0fu,
+                                 (q1.w >> 4) & 0x0f0f0f0fu);
+    const int64_t k0 = sbi * kQK + 64 * u;             // values 64u .. 64u+63 of the super-block
+    const int64_t b0 = sbi * 8 + 2 * u, b1 = b0 + 1;   // their two Q8 blocks
+    const float dsc0 = d * (float)sc0, dsc1 = d * (float)sc1, dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
 #pragma unroll
-    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
-
-    const int u = lane & 3;          // the 64-value quarter of the super-block this lane owns
-    const int lb = lane >> 2;        // the super-block of the chunk this lane owns
-    bool ok = true;
-    int item = 0, r = 0, c = 0, s = 0;
-    uint32_t phase = 0;
-    for (; item < items; ++item) {
-        const bool got = mbar_wait(&bar[s], phase, err, ERR_GEMV_FULL, nullptr);
-        if (!__all_sync(kFull, got)) {   // leave the loop together (shuffles below need every lane)
-            ok = false;
-            break;
-        }
-        int64_t start;
-        int nblk_c;
-        chunk_bytes(r, c, start, nblk_c);
-        const int64_t n = gw + (int64_t)r * GW;
-        const bool valid = lb < nblk_c;                  // uniform over the 4 lanes of a block
-        const int64_t sbi = c * kChunkBlocks + lb;       // super-block index in the row
-        const uint32_t blk = ring_s + s * C::STAGE + (uint32_t)(start & 15) + (uint32_t)(lb * C::BB);
-        if constexpr (FMT == FMT_Q4K) {
-            // quarter u: qs bytes [32u, 32u+32): low nibbles -> sub-block j0 = 2u, high -> j1 = 2u+1
-            uint4 hd = make_uint4(0, 0, 0, 0), q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                hd = lds128(blk);
-                q0 = lds128(blk + 16 + 32 * u);
-                q1 = lds128(blk + 32 + 32 * u);
-            }
-            const float d = half_bits_to_float(hd.x & 0xffff), dmin = half_bits_to_float(hd.x >> 16);
-            // the 12 scale bytes: s[0..3] = hd.y, s[4..7] = hd.z, s[8..11] = hd.w; sub-blocks 2u, 2u+1
-            int sc0, m0, sc1, m1;
-            if (u < 2) {
-                const uint32_t a = hd.y >> (16 * u), b = hd.z >> (16 * u);
-                sc0 = a & 63; sc1 = (a >> 8) & 63; m0 = b & 63; m1 = (b >> 8) & 63;
+    for (int t = 0; t < MT; ++t) {
+        const int64_t m = a.t0 + t;
+        const bool act = t < a.mt && valid;
+        int D0 = 0, D1 = 0;
+        part[t] = 0.0f;
+        if (act) {
+            if constexpr (ACT) {
+                // codes: chunks 16*sbi + 4u + i of token t; table: (d, d*S) of blocks 2u, 2u+1
+                const uint32_t cb = at.codes + (uint32_t)t * (uint32_t)a.K + 256u * (uint32_t)sbi;
+                const uint32_t c0 = 4u * (uint32_t)u + 16u * ((uint32_t)sbi & 1u);   // swizzle input bits 0-4
+                const uint4 x0 = lds128(cb + 16u * (C::swz(c0) & 15u));
+                const uint4 x1 = lds128(cb + 16u * (C::swz(c0 + 1) & 15u));
+                const uint4 x2 = lds128(cb + 16u * (C::swz(c0 + 2) & 15u));
+                const uint4 x3 = lds128(cb + 16u * (C::swz(c0 + 3) & 15u));
+                D0 = dot16(lo0, x0) + dot16(lo1, x1);
+                D1 = dot16(hi0, x2) + dot16(hi1, x3);
+                const float4 tb = lds128f(at.tab + ((uint32_t)t * at.nb + (uint32_t)sbi) * 64u + 16u * (uint32_t)u);
+                part[t] = fmaf(dsc0, tb.x * (float)D0, -dm0 * tb.y) + fmaf(dsc1, tb.z * (float)D1, -dm1 * tb.w);
             } else {
-                const uint32_t lo = hd.w >> (16 * (u - 2));                  // s[j+4] for j = 2u, 2u+1
-                const uint32_t ts = hd.y >> (16 * (u - 2)), tm = hd.z >> (16 * (u - 2));   // s[j-4], s[j]
-                sc0 = (lo & 15) | (((ts >> 6) & 3) << 4);
-                sc1 = ((lo >> 8) & 15) | (((ts >> 14) & 3) << 4);
-                m0 = ((lo >> 4) & 15) | (((tm >> 6) & 3) << 4);
-                m1 = ((lo >> 12) & 15) | (((tm >> 14) & 3) << 4);
-            }
-            const uint4 lo0 = make_uint4(q0.x & 0x0f0f0f0fu, q0.y & 0x0f0f0f0fu, q0.z & 0x0f0f0f0fu, q0.w & 0x0f0f0f0fu);
-            const uint4 lo1 = make_uint4(q1.x & 0x0f0f0f0fu, q1.y & 0x0f0f0f0fu, q1.z & 0x0f0f0f0fu, q1.w & 0x0f0f0f0fu);
-            const uint4 hi0 = make_uint4((q0.x >> 4) & 0x0f0f0f0fu, (q0.y >> 4) & 0x0f0f0f0fu, (q0.z >> 4) & 0x0f0f0f0fu,
-                                         (q0.w >> 4) & 0x0f0f0f0fu);
-            const uint4 hi1 = make_uint4((q1.x >> 4) & 0x0f0f0f0fu, (q1.y >> 4) & 0x0f0f0f0fu, (q1.z >> 4) & 0x0f0f0f0fu,
-                                         (q1.w >> 4) & 0x0f0f0f0fu);
-            const int64_t k0 = sbi * kQK + 64 * u;             // values 64u .. 64u+63 of the super-block
-            const int64_t b0 = sbi * 8 + 2 * u, b1 = b0 + 1;   // their two Q8 blocks
-            const float dsc0 = d * (float)sc0, dsc1 = d * (float)sc1, dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                const int64_t m = t0 + t;
-                const bool act = t < mt && valid;
-                int D0 = 0, D1 = 0;
-                if (act) {
-                    const uint4 *a = reinterpret_cast<const uint4 *>(p.q8 + m * K + k0);
-                    D0 = dot16(lo0, __ldg(a)) + dot16(lo1, __ldg(a + 1));
-                    D1 = dot16(hi0, __ldg(a + 2)) + dot16(hi1, __ldg(a + 3));
-                    const float da0 = __ldg(p.d + b0 * M + m), da1 = __ldg(p.d + b1 * M + m);
-                    const float s0 = (float)__ldg(p.s + b0 * M + m), s1 = (float)__ldg(p.s + b1 * M + m);
-                    acc[t] += da0 * (dsc0 * (float)D0 - dm0 * s0) + da1 * (dsc1 * (float)D1 - dm1 * s1);
-                }
-                if constexpr (DUMP) {
-                    if (act && m >= dump.m0 && m < dump.m0 + dump.m_cnt && n >= dump.n0 && n < dump.n0 + dump.n_cnt) {
-                        int32_t *o = dump.out + ((m - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32;
-                        o[b0] = sc0 * D0;
-                        o[b1] = sc1 * D1;
-                    }
-                }
-            }
-        } else {
-            // quarter u: half h = u/2, l0 = 16*(u%2); values 128h + 32g + l0 + i (g = 0..3, i = 0..15).
-            // group g: low (g < 2) / high (g >= 2) nibble of ql[64h + 32(g&1) + l0 + i], high bits
-            // (qh[32h + l0 + i] >> 2g) & 3; each group is one 16-value sub-block 8h + 2g + u%2.
-            const int h = u >> 1, l0 = 16 * (u & 1);
-            uint4 ql0 = make_uint4(0, 0, 0, 0), ql1 = make_uint4(0, 0, 0, 0), qh = make_uint4(0, 0, 0, 0);
-            float d = 0.0f;
-            uint32_t scw = 0, scw2 = 0;
-            if (valid) {
-                ql0 = lds128_a2(blk + 64 * h + l0);
-                ql1 = lds128_a2(blk + 64 * h + 32 + l0);
-                qh = lds128_a2(blk + 128 + 32 * h + l0);
-                d = half_bits_to_float(lds16(blk + 208));
-                // scales 8h + (u&1) + {0, 2, 4, 6}: the 8 bytes at 192 + 8h, even or odd ones
-                const uint32_t sa = (lds16(blk + 192 + 8 * h) | (lds16(blk + 194 + 8 * h) << 16));
-                const uint32_t sb2 = (lds16(blk + 196 + 8 * h) | (lds16(blk + 198 + 8 * h) << 16));
-                const uint32_t sel = (u & 1) ? 0x7531u : 0x6420u;
-                scw = __byte_perm(sa, sb2, sel);                // 4 int8 scales of groups 0..3
-                scw2 = 0;
-            }
-            (void)scw2;
-            // 6-bit codes (q + 32) of the four groups
-            uint4 v[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint32_t *L = reinterpret_cast<const uint32_t *>((g & 1) ? &ql1 : &ql0);
-                const uint32_t *H = reinterpret_cast<const uint32_t *>(&qh);
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t lo = (g < 2) ? L[e] : (L[e] >> 4);
-                    const uint32_t hb = (g == 0) ? (H[e] << 4) : (g == 1) ? (H[e] << 2) : (g == 2) ? H[e] : (H[e] >> 2);
-                    o[e] = lop3_and_or(lo, 0x0f0f0f0fu, hb, 0x30303030u);
-                }
-                v[g] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            const int64_t kb = sbi * kQK + 128 * h + l0;
-            const int64_t bq = sbi * 8 + 4 * h;                // Q8 block of group 0
-            float dsc[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) dsc[g] = d * (float)(int8_t)((scw >> (8 * g)) & 0xff);
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                const int64_t m = t0 + t;
-                const bool act = t < mt && valid;
-                int Dg[4] = {0, 0, 0, 0};
-                if (act) {
-                    const int8_t *a = p.q8 + m * K + kb;
-                    float vsum = 0.0f;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint4 av = __ldg(reinterpret_cast<const uint4 *>(a + 32 * g));
-                        // sum (code - 32) a = sum code*a - 32 sum a
-                        Dg[g] = dot16(v[g], av) - dot16(make_uint4(0x20202020u, 0x20202020u, 0x20202020u, 0x20202020u), av);
-                        vsum += dsc[g] * (float)Dg[g] * __ldg(p.d + (bq + g) * M + m);
-                    }
-                    acc[t] += vsum;
-                }
-                if constexpr (DUMP) {
-                    int I[4];
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        I[g] = (int)(int8_t)((scw >> (8 * g)) & 0xff) * Dg[g];
-                        I[g] += __shfl_xor_sync(kFull, I[g], 1);       // the two 16-value halves of the Q8 block
-                    }
-                    if (act && (u & 1) == 0 && m >= dump.m0 && m < dump.m0 + dump.m_cnt && n >= dump.n0 &&
-                        n < dump.n0 + dump.n_cnt) {
-                        int32_t *o = dump.out + ((m - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) o[bq + g] = I[g];
-                    }
-                }
+                const uint4 *q = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K + k0);
+                D0 = dot16(lo0, __ldg(q)) + dot16(lo1, __ldg(q + 1));
+                D1 = dot16(hi0, __ldg(q + 2)) + dot16(hi1, __ldg(q + 3));
+                const float da0 = __ldg(a.p.d + b0 * a.M + m), da1 = __ldg(a.p.d + b1 * a.M + m);
+                const float s0 = (float)__ldg(a.p.s + b0 * a.M + m), s1 = (float)__ldg(a.p.s + b1 * a.M + m);
+                part[t] = da0 * (dsc0 * (float)D0 - dm0 * s0) + da1 * (dsc1 * (float)D1 - dm1 * s1);
             }
         }
-
-        if (c == nch - 1) {
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                float v = acc[t];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-                if (lane == 0 && t < mt) y[(t0 + t) * N + n] = v;
-                acc[t] = 0.0f;
+        if constexpr (DUMP) {
+            const Dump &dp = a.dump;
+            if (act && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt) {
+                int32_t *o = dp.out + ((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8);
+                o[b0] = sc0 * D0;
+                o[b1] = sc1 * D1;
             }
         }
-        __syncwarp();
-        if (lane == 0 && item + kStages < items) issue();
-        if (++c == nch) { c = 0; ++r; }
-        if (++s == kStages) { s = 0; phase ^= 1u; }
-    }
-
-    if (!ok && lane == 0) {
-        // a copy never arrived: wait (bounded) for the ones still in flight before leaving
-        for (int i = item + 1; i < items && i < item + kStages; ++i)
-            mbar_wait(&bar[i % kStages], (uint32_t)((i / kStages) & 1), err, ERR_GEMV_DRAIN, nullptr);
     }
 }
 
-template <int FMT, int MT, bool DUMP>
-int launch_one(const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, int64_t t0, int mt, float *y,
-               const Dump &dump, unsigned int *err, int nsm, cudaStream_t stream) {
+// Q6_K: quarter u -> half h = u/2, l0 = 16*(u%2); values 128h + 32g + l0 + i (g = 0..3, i < 16).
+// Group g takes the low (g < 2) / high (g >= 2) nibble of ql[64h + 32(g&1) + l0 + i] and the
+// high bits (qh[32h + l0 + i] >> 2g) & 3; each group is the 16-value sub-block 8h + 2g + u%2.
+template <int MT, bool ACT, bool DUMP>
+__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n, int64_t sbi,
+                                            int u, bool valid, float (&part)[MT]) {
+    using C = GvCfg<FMT_Q6K>;
+    const int h = u >> 1, l0 = 16 * (u & 1);
+    uint4 ql0 = make_uint4(0, 0, 0, 0), ql1 = make_uint4(0, 0, 0, 0), qh = make_uint4(0, 0, 0, 0);
+    float d = 0.0f;
+    uint32_t scw = 0;
+    if (valid) {
+        ql0 = lds128_a2(blk + 64 * h + l0);
+        ql1 = lds128_a2(blk + 64 * h + 32 + l0);
+        qh = lds128_a2(blk + 128 + 32 * h + l0);
+        d = half_bits_to_float(lds16(blk + 208));
+        // scales 8h + (u&1) + {0, 2, 4, 6}: the 8 bytes at 192 + 8h, even or odd ones
+        const uint32_t sa = lds16(blk + 192 + 8 * h) | (lds16(blk + 194 + 8 * h) << 16);
+        const uint32_t sb = lds16(blk + 196 + 8 * h) | (lds16(blk + 198 + 8 * h) << 16);
+        scw = __byte_perm(sa, sb, (u & 1) ? 0x7531u : 0x6420u);     // 4 int8 scales of groups 0..3
+    }
+    // 6-bit codes (q + 32) of the four groups
+    uint4 v[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t *L = reinterpret_cast<const uint32_t *>((g & 1) ? &ql1 : &ql0);
+        const uint32_t *H = reinterpret_cast<const uint32_t *>(&qh);
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t lo = (g < 2) ? L[e] : (L[e] >> 4);
+            const uint32_t hb = (g == 0) ? (H[e] << 4) : (g == 1) ? (H[e] << 2) : (g == 2) ? H[e] : (H[e] >> 2);
+            o[e] = lop3_and_or(lo, 0x0f0f0f0fu, hb, 0x30303030u);
+        }
+        v[g] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const int64_t kb = sbi * kQK + 128 * h + l0;
+    const int64_t bq = sbi * 8 + 4 * h;                // Q8 block of group 0
+    float dsc[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) dsc[g] = d * (float)(int8_t)((scw >> (8 * g)) & 0xff);
+    const uint4 c32 = make_uint4(0x20202020u, 0x20202020u, 0x20202020u, 0x20202020u);
+    const uint4 c01 = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const int64_t m = a.t0 + t;
+        const bool act = t < a.mt && valid;
+        int Dg[4] = {0, 0, 0, 0};
+        part[t] = 0.0f;
+        if (act) {
+            float vsum = 0.0f;
+            if constexpr (ACT) {
+                // codes: chunks 16*sbi + 8h + 2g + (u&1) of token t; table: (d_a, 32 * d_a * S16) of
+                // the four 16-value half blocks, two per 16-byte load (halves swapped on odd sbi)
+                const uint32_t cb = at.codes + (uint32_t)t * (uint32_t)a.K + 256u * (uint32_t)sbi;
+                const uint32_t tb = at.tab + ((uint32_t)t * at.nb + (uint32_t)sbi) * 128u + 32u * (uint32_t)u;
+                const uint32_t odd = (uint32_t)sbi & 1u;
+                const float4 e01 = lds128f(tb + 16u * odd), e23 = lds128f(tb + 16u * (odd ^ 1u));
+                const float de[8] = {e01.x, e01.y, e01.z, e01.w, e23.x, e23.y, e23.z, e23.w};
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t c = 8u * (uint32_t)h + 2u * (uint32_t)g + ((uint32_t)u & 1u) + 16u * odd;
+                    const uint4 av = lds128(cb + 16u * (C::swz(c) & 15u));
+                    const int Dc = dot16(v[g], av);                       // sum code * a
+                    if constexpr (DUMP) Dg[g] = Dc - 32 * dot16(c01, av);  // exact sum (code - 32) * a
+                    // d_a * (sum code * a) - 32 * d_a * S16, scaled by d * sc
+                    vsum = fmaf(dsc[g], fmaf(de[2 * g], (float)Dc, -de[2 * g + 1]), vsum);
+                }
+            } else {
+                const int8_t *q = a.p.q8 + m * a.K + kb;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 av = __ldg(reinterpret_cast<const uint4 *>(q + 32 * g));
+                    // sum (code - 32) * a = sum code * a - sum 32 * a
+                    Dg[g] = dot16(v[g], av) - dot16(c32, av);
+                    vsum += dsc[g] * (float)Dg[g] * __ldg(a.p.d + (bq + g) * a.M + m);
+                }
+            }
+            part[t] = vsum;
+        }
+        if constexpr (DUMP) {
+            int I[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                I[g] = (int)(int8_t)((scw >> (8 * g)) & 0xff) * Dg[g];
+                I[g] += __shfl_xor_sync(kFull, I[g], 1);       // the two 16-value halves of the Q8 block
+            }
+            const Dump &dp = a.dump;
+            if (act && (u & 1) == 0 && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt) {
+                int32_t *o = dp.out + ((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) o[bq + g] = I[g];
+            }
+        }
+    }
+}
+
+template <int FMT, int MT, bool ACT, bool DUMP>
+__global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs a) {
     using C = GvCfg<FMT>;
-    auto kern = gemv_kernel<FMT, MT, DUMP>;
-    constexpr int slot = 16 + FMT * 8 + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
-    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, slot);
+    constexpr int S = C::STAGES;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[S], empty[S], pfull[kPartBufs], pempty[kPartBufs];
+    __shared__ float carry[2][MT];
+    __shared__ int abort_flag;
+    float *partbuf = reinterpret_cast<float *>(smem + C::OFF_PART);   // [kPartBufs][MT][TU]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kConsumerWarps); }
+        for (int i = 0; i < kPartBufs; ++i) { mbar_init(&pfull[i], kConsumerWarps); mbar_init(&pempty[i], 1); }
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    // this CTA's rows [row_begin, row_end) and their flat super-block range
+    const uint32_t nb = (uint32_t)(a.K / kQK);
+    const int64_t row_begin = a.N * blockIdx.x / gridDim.x, row_end = a.N * (blockIdx.x + 1) / gridDim.x;
+    const int64_t sb_begin = row_begin * nb, sb_total = (row_end - row_begin) * nb;
+    const int units = (int)((sb_total + C::TU - 1) / C::TU);
+    const float inv_nb = 1.0f / (float)nb;
+    volatile int *abort = &abort_flag;
+
+    if (warp == kProducerWarp) {
+        if (lane != 0) return;
+        int s = 0, issued = 0;
+        uint32_t ph = 0;
+        for (int j = 0; j < units; ++j) {
+            if (j >= S && !mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_GEMV_FULL, abort)) break;
+            const int64_t sb0 = sb_begin + (int64_t)j * C::TU;
+            const int64_t nsb = min((int64_t)C::TU, sb_begin + sb_total - sb0);
+            const int64_t start = sb0 * C::BB;
+            const int64_t a0 = start & ~(int64_t)15, a1 = (start + nsb * C::BB + 15) & ~(int64_t)15;
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(a1 - a0));
+            bulk_copy_g2s(smem + s * C::STAGE, a.w + a0, (uint32_t)(a1 - a0), &full[s]);
+            ++issued;
+            if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        // after a failed wait: wait (bounded) for the copies still in flight before leaving
+        if (*abort)
+            for (int j = max(0, issued - S); j < issued; ++j)
+                mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), a.err, ERR_GEMV_DRAIN, nullptr);
+        return;
+    }
+
+    if (warp == kReducerWarp) {
+        // unit j covers flat super-blocks [sb0, sb0 + nsb); its first row is r_row0 and the
+        // unit starts r_sbi0 super-blocks into it
+        uint32_t r_sbi0 = 0;
+        int64_t r_row0 = row_begin;
+        int pb = 0;
+        uint32_t pph = 0;
+        for (int j = 0; j < units; ++j) {
+            if (!mbar_wait(&pfull[pb], pph, a.err, ERR_GEMV_FULL, abort)) break;
+            const int nsb = (int)min((int64_t)C::TU, sb_total - (int64_t)j * C::TU);
+            const float *pbuf = partbuf + pb * MT * C::TU;
+            const uint32_t nrows_u = (r_sbi0 + (uint32_t)nsb + nb - 1) / nb;   // rows touching this unit
+            for (int t = 0; t < a.mt; ++t) {
+                for (uint32_t rr = lane; rr < nrows_u; rr += 32) {
+                    const int i0 = max(0, (int)(rr * nb) - (int)r_sbi0);
+                    const int i1 = min(nsb, (int)((rr + 1) * nb) - (int)r_sbi0);
+                    float sum = (rr == 0 && r_sbi0 > 0) ? carry[(j + 1) & 1][t] : 0.0f;
+                    for (int i = i0; i < i1; ++i) sum += pbuf[t * C::TU + i];
+                    if ((int)((rr + 1) * nb) - (int)r_sbi0 > nsb)
+                        carry[j & 1][t] = sum;                                  // the row continues
+                    else
+                        a.y[(a.t0 + t) * a.N + r_row0 + rr] = sum;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[pb]);
+            uint32_t adv;
+            r_row0 += divmod_small(r_sbi0 + (uint32_t)nsb, nb, inv_nb, adv);
+            r_sbi0 = adv;
+            if (++pb == kPartBufs) { pb = 0; pph ^= 1u; }
+        }
+        return;
+    }
+
+    // consumer warps
+    GvAct at{0, 0, nb};
+    if constexpr (ACT) {
+        // stage the tokens' codes (swizzled 16-byte chunks) and the scale table
+        at.codes = smem_u32(smem + C::OFF_PART + C::part_bytes(MT));
+        at.tab = at.codes + (uint32_t)(MT * a.K);
+        const uint32_t nch = (uint32_t)(a.K / 16);
+        for (int t = 0; t < a.mt; ++t) {
+            const int64_t m = a.t0 + t;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);
+            const uint32_t cbase = at.codes + (uint32_t)t * (uint32_t)a.K;
+            for (uint32_t c = tid; c < nch; c += kConsumerWarps * 32) {
+                const uint4 v = __ldg(src + c);
+                sts128(cbase + 16u * ((c & ~15u) | C::swz(c & 31u) & 15u), v);
+                if constexpr (FMT == FMT_Q6K) {
+                    // half block c: entry (d_a, 32 * d_a * S16) at [sbi][u][g], the two 16-byte
+                    // halves of each u swapped on odd sbi
+                    const int s16 = dot16(v, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u));
+                    const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
+                    const uint32_t sbi = c >> 4, r = c & 15u, g = (r >> 1) & 3u;
+                    const uint32_t uu = 2u * (r >> 3) + (r & 1u);
+                    const uint32_t off = ((uint32_t)t * nb + sbi) * 128u + 32u * uu + 16u * ((g >> 1) ^ (sbi & 1u)) +
+                                         8u * (g & 1u);
+                    sts64(at.tab + off, da, da * (float)(32 * s16));
+                }
+            }
+            if constexpr (FMT == FMT_Q4K) {
+                for (uint32_t b = tid; b < nch / 2; b += kConsumerWarps * 32) {
+                    const float da = __ldg(a.p.d + (int64_t)b * a.M + m);
+                    const float sa = (float)__ldg(a.p.s + (int64_t)b * a.M + m);
+                    sts64(at.tab + ((uint32_t)t * nb * 8u + b) * 8u, da, da * sa);
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    }
+
+    const int u = tid & 3, slot = tid >> 2;          // quarter, and super-block slot within a pass
+    int s = 0, pb = 0;
+    uint32_t ph = 0, pph = 0;
+    uint32_t c_sbi0 = 0;                             // offset of the unit's first super-block in its row
+    int64_t c_row0 = row_begin;
+    for (int j = 0; j < units; ++j) {
+        const bool got = mbar_wait(&full[s], ph, a.err, ERR_GEMV_FULL, abort);
+        if (!__all_sync(kFull, got)) break;           // leave together: the shuffles below need every lane
+        const int nsb = (int)min((int64_t)C::TU, sb_total - (int64_t)j * C::TU);
+        const int64_t start = (sb_begin + (int64_t)j * C::TU) * C::BB;
+        const uint32_t sbase = smem_u32(smem + s * C::STAGE) + (uint32_t)(start & 15);
+        float part[C::PASSES][MT];
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            const int idx = ps * kSbPerPass + slot;
+            const bool valid = idx < nsb;
+            uint32_t sbi;
+            const int64_t n = c_row0 + divmod_small(c_sbi0 + (uint32_t)idx, nb, inv_nb, sbi);
+            const uint32_t blk = sbase + (uint32_t)(idx * C::BB);
+            if constexpr (FMT == FMT_Q4K)
+                q4k_quarter<MT, ACT, DUMP>(a, at, blk, n, (int64_t)sbi, u, valid, part[ps]);
+            else
+                q6k_quarter<MT, ACT, DUMP>(a, at, blk, n, (int64_t)sbi, u, valid, part[ps]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);       // stage fully read: the producer may refill it
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                part[ps][t] += __shfl_xor_sync(kFull, part[ps][t], 1);
+                part[ps][t] += __shfl_xor_sync(kFull, part[ps][t], 2);
+            }
+        const bool pgot = j < kPartBufs || mbar_wait(&pempty[pb], pph ^ 1u, a.err, ERR_GEMV_FULL, abort);
+        if (!__all_sync(kFull, pgot)) break;
+        if (u == 0) {
+            float *pbuf = partbuf + pb * MT * C::TU;
+#pragma unroll
+            for (int ps = 0; ps < C::PASSES; ++ps)
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    if (t < a.mt) pbuf[t * C::TU + ps * kSbPerPass + slot] = part[ps][t];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[pb]);
+        uint32_t adv;
+        c_row0 += divmod_small(c_sbi0 + (uint32_t)nsb, nb, inv_nb, adv);
+        c_sbi0 = adv;
+        if (++s == S) { s = 0; ph ^= 1u; }
+        if (++pb == kPartBufs) { pb = 0; pph ^= 1u; }
+    }
+}
+
+template <int FMT, int MT, bool ACT, bool DUMP>
+int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
+    using C = GvCfg<FMT>;
+    auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
+    const int smem = C::OFF_PART + C::part_bytes(MT) + (ACT ? (int)C::act_bytes(MT, a.K) : 0);
+    constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
+    constexpr int smem_max = C::OFF_PART + C::part_bytes(MT) + (ACT ? kActSmemMax : 0);
+    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_max, slot);
     if (rc != MQ_OK) return rc;
-    int64_t ctas = (N + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)nsm * 4;    // four 8-warp CTAs per SM (registers; 41.5 KB of stages each)
-    if (ctas > cap) ctas = cap;
-    kern<<<(unsigned)ctas, kWarps * 32, C::SMEM, stream>>>(w, N, K, p, M, t0, mt, y, dump, err);
+    int per_sm = 0;
+    rc = resident_ctas(reinterpret_cast<const void *>(kern), kThreads, smem, slot, &per_sm);
+    if (rc != MQ_OK) return rc;
+    int64_t ctas = (int64_t)nsm * per_sm;
+    if (ctas > a.N) ctas = a.N;                      // every CTA owns at least one row
+    kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a);
     return cuda_error(cudaGetLastError(), "gemv launch");
 }
 
+template <int FMT, int MT, bool DUMP>
+int launch_mt(const GvArgs &a, int nsm, cudaStream_t stream) {
+    if (GvCfg<FMT>::act_bytes(MT, a.K) <= kActSmemMax) return launch_one<FMT, MT, true, DUMP>(a, nsm, stream);
+    return launch_one<FMT, MT, false, DUMP>(a, nsm, stream);
+}
+
 template <int FMT, bool DUMP>
-int launch_fmt(const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y, const Dump &dump,
-               unsigned int *err, int nsm, cudaStream_t stream) {
-    for (int64_t t0 = 0; t0 < M; t0 += 8) {
-        const int mt = (int)((M - t0) < 8 ? (M - t0) : 8);
+int launch_fmt(GvArgs a, int nsm, cudaStream_t stream) {
+    for (int64_t t0 = 0; t0 < a.M; t0 += 8) {
+        a.t0 = t0;
+        a.mt = (int)((a.M - t0) < 8 ? (a.M - t0) : 8);
         int rc;
-        if (mt == 1)
-            rc = launch_one<FMT, 1, DUMP>(w, N, K, p, M, t0, mt, y, dump, err, nsm, stream);
-        else if (mt == 2)
-            rc = launch_one<FMT, 2, DUMP>(w, N, K, p, M, t0, mt, y, dump, err, nsm, stream);
-        else if (mt <= 4)
-            rc = launch_one<FMT, 4, DUMP>(w, N, K, p, M, t0, mt, y, dump, err, nsm, stream);
+        if (a.mt == 1)
+            rc = launch_mt<FMT, 1, DUMP>(a, nsm, stream);
+        else if (a.mt == 2)
+            rc = launch_mt<FMT, 2, DUMP>(a, nsm, stream);
+        else if (a.mt <= 4)
+            rc = launch_mt<FMT, 4, DUMP>(a, nsm, stream);
         else
-            rc = launch_one<FMT, 8, DUMP>(w, N, K, p, M, t0, mt, y, dump, err, nsm, stream);
+            rc = launch_mt<FMT, 8, DUMP>(a, nsm, stream);
         if (rc != MQ_OK) return rc;
     }
     return MQ_OK;
@@ -329,11 +528,10 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
                 const Dump &dump, unsigned int *err, cudaStream_t stream) {
     const int nsm = sm_count();
     const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
+    GvArgs a{w, N, K, p, M, 0, 0, y, dump, err};
     if (fmt == FMT_Q4K)
-        return dmp ? launch_fmt<FMT_Q4K, true>(w, N, K, p, M, y, dump, err, nsm, stream)
-                   : launch_fmt<FMT_Q4K, false>(w, N, K, p, M, y, dump, err, nsm, stream);
-    return dmp ? launch_fmt<FMT_Q6K, true>(w, N, K, p, M, y, dump, err, nsm, stream)
-               : launch_fmt<FMT_Q6K, false>(w, N, K, p, M, y, dump, err, nsm, stream);
+        return dmp ? launch_fmt<FMT_Q4K, true>(a, nsm, stream) : launch_fmt<FMT_Q4K, false>(a, nsm, stream);
+    return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
 }
 
 }  // namespace mq

@@ -39,6 +39,9 @@ int sm_count();
 // Sets the dynamic shared-memory limit of `kernel` once per device; returns MQ_OK or MQ_ERR_CUDA.
 int ensure_smem_attr(const void *kernel, int bytes, int slot);
 int cuda_error(cudaError_t e, const char *what);
+// CTAs of `kernel` resident per SM at this block size and dynamic shared memory (cached per
+// device and slot); returns MQ_OK or MQ_ERR_CUDA.
+int resident_ctas(const void *kernel, int threads, int smem_bytes, int slot, int *out);
 
 // launchers (arguments already validated); return MQ_OK or MQ_ERR_CUDA
 int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,

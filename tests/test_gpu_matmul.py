@@ -52,6 +52,17 @@ def test_small_shapes(path, fmt, M, N, K):
     _full_check(path, fmt, M, N, K, seed=M * 7919 + N * 31 + K)
 
 
+# rows longer than one GEMV unit (rows straddle several units), many short rows per unit,
+# and row counts that do not divide among the CTAs
+GEMV_SHAPES = [(1, 3, 65536), (3, 5, 33280), (1, 1000, 256), (2, 997, 3584), (9, 77, 18944)]
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", GEMV_SHAPES)
+def test_gemv_row_layouts(fmt, M, N, K):
+    _full_check("gemv", fmt, M, N, K, seed=M * 104729 + N * 17 + K)
+
+
 @pytest.mark.parametrize("path", ["gemv", "gemm"])
 def test_q6k_full_scale_range(path):
     # real GGML Q6_K files use scales up to +-128; odd |sc| > 64 takes the correction tile
