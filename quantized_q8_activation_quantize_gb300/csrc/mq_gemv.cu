@@ -52,15 +52,16 @@ struct GvCfg {
     static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
     static constexpr int OFF_PART = STAGES * STAGE;
     static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
-    // staged activations: int8 codes [MT][K] + float2 table, per half block (Q6_K) or block (Q4_K)
-    static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K + (FMT == FMT_Q6K ? K / 2 : K / 4)); }
-    // 16-byte chunk c of a token's codes lives at chunk swz(c) (XOR of bits 0-2 only)
-    __device__ static __forceinline__ uint32_t swz(uint32_t c) {
-        return FMT == FMT_Q6K ? c ^ (((c >> 3) & 1u) << 1) ^ (((c >> 4) & 1u) << 2)
-                              : c ^ (((c >> 3) & 1u) << 1) ^ ((c >> 4) & 1u);
-    }
+    // Staged activations, per token: int8 codes with each super-block's two 128-value halves
+    // padded apart (half stride 160 B = 10 bank groups of 16 B, super-block stride SB_STRIDE:
+    // 20 groups for Q6_K, 19 for Q4_K) so that the 8 lanes of every quarter-warp -- two
+    // consecutive super-blocks x four quarters -- read 8 distinct 16-byte bank groups; then
+    // a float2 table per half block (Q6_K: TAB_SB = 128 B per super-block) or block (Q4_K: 64 B).
+    static constexpr uint32_t SB_STRIDE = FMT == FMT_Q6K ? 320 : 304;
+    static constexpr uint32_t TAB_SB = FMT == FMT_Q6K ? 128 : 64;
+    static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * (SB_STRIDE + TAB_SB); }
 };
-constexpr int kActSmemMax = 48 * 1024;               // stage activations when they fit in this
+constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -131,15 +132,15 @@ struct GvArgs {
 
 // shared-memory addresses of the staged activations (ACT kernels): codes [MT][K], table
 struct GvAct {
-    uint32_t codes, tab;
-    uint32_t nb;
+    uint32_t codes, tab;         // token 0's codes and table
+    uint32_t ck, tk;             // per-token strides of codes and table
 };
 
 // Q4_K: quarter u of the super-block at shared address `blk` (row n, super-block sbi of the
 // row): qs bytes [32u, 32u+32), whose low nibbles are sub-block 2u and high nibbles 2u+1.
 template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n, int64_t sbi,
-                                            int u, bool valid, float (&part)[MT]) {
+__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n,
+                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
     using C = GvCfg<FMT_Q4K>;
     uint4 hd = make_uint4(0, 0, 0, 0), q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
     if (valid) {
@@ -167,8 +168,8 @@ __device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, ui
                                  (q0.w >> 4) & 0x0f0f0f0fu);
     const uint4 hi1 = make_uint4((q1.x >> 4) & 0x0f0f0f0fu, (q1.y >> 4) & 0x0f0f0f0fu, (q1.z >> 4) & 0x0f0f0f0fu,
                                  (q1.w >> 4) & 0x0f0f0f0fu);
-    const int64_t k0 = sbi * kQK + 64 * u;             // values 64u .. 64u+63 of the super-block
-    const int64_t b0 = sbi * 8 + 2 * u, b1 = b0 + 1;   // their two Q8 blocks
+    const int64_t k0 = (int64_t)sbi * kQK + 64 * u;    // values 64u .. 64u+63 of the super-block
+    const int64_t b0 = (int64_t)sbi * 8 + 2 * u, b1 = b0 + 1;   // their two Q8 blocks
     const float dsc0 = d * (float)sc0, dsc1 = d * (float)sc1, dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
@@ -178,16 +179,14 @@ __device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, ui
         part[t] = 0.0f;
         if (act) {
             if constexpr (ACT) {
-                // codes: chunks 16*sbi + 4u + i of token t; table: (d, d*S) of blocks 2u, 2u+1
-                const uint32_t cb = at.codes + (uint32_t)t * (uint32_t)a.K + 256u * (uint32_t)sbi;
-                const uint32_t c0 = 4u * (uint32_t)u + 16u * ((uint32_t)sbi & 1u);   // swizzle input bits 0-4
-                const uint4 x0 = lds128(cb + 16u * (C::swz(c0) & 15u));
-                const uint4 x1 = lds128(cb + 16u * (C::swz(c0 + 1) & 15u));
-                const uint4 x2 = lds128(cb + 16u * (C::swz(c0 + 2) & 15u));
-                const uint4 x3 = lds128(cb + 16u * (C::swz(c0 + 3) & 15u));
+                // codes 64u .. 64u+63 of the super-block (half u/2, offset 64 (u&1) in it);
+                // table: (d, d*S) of blocks 2u, 2u+1
+                const uint32_t cb = at.codes + (uint32_t)t * at.ck + sbi * C::SB_STRIDE +
+                                    160u * ((uint32_t)u >> 1) + 64u * ((uint32_t)u & 1u);
+                const uint4 x0 = lds128(cb), x1 = lds128(cb + 16), x2 = lds128(cb + 32), x3 = lds128(cb + 48);
                 D0 = dot16(lo0, x0) + dot16(lo1, x1);
                 D1 = dot16(hi0, x2) + dot16(hi1, x3);
-                const float4 tb = lds128f(at.tab + ((uint32_t)t * at.nb + (uint32_t)sbi) * 64u + 16u * (uint32_t)u);
+                const float4 tb = lds128f(at.tab + (uint32_t)t * at.tk + sbi * C::TAB_SB + 16u * (uint32_t)u);
                 part[t] = fmaf(dsc0, tb.x * (float)D0, -dm0 * tb.y) + fmaf(dsc1, tb.z * (float)D1, -dm1 * tb.w);
             } else {
                 const uint4 *q = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K + k0);
@@ -213,8 +212,8 @@ __device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, ui
 // Group g takes the low (g < 2) / high (g >= 2) nibble of ql[64h + 32(g&1) + l0 + i] and the
 // high bits (qh[32h + l0 + i] >> 2g) & 3; each group is the 16-value sub-block 8h + 2g + u%2.
 template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n, int64_t sbi,
-                                            int u, bool valid, float (&part)[MT]) {
+__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n,
+                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
     using C = GvCfg<FMT_Q6K>;
     const int h = u >> 1, l0 = 16 * (u & 1);
     uint4 ql0 = make_uint4(0, 0, 0, 0), ql1 = make_uint4(0, 0, 0, 0), qh = make_uint4(0, 0, 0, 0);
@@ -245,8 +244,8 @@ __device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, ui
         }
         v[g] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    const int64_t kb = sbi * kQK + 128 * h + l0;
-    const int64_t bq = sbi * 8 + 4 * h;                // Q8 block of group 0
+    const int64_t kb = (int64_t)sbi * kQK + 128 * h + l0;
+    const int64_t bq = (int64_t)sbi * 8 + 4 * h;       // Q8 block of group 0
     float dsc[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) dsc[g] = d * (float)(int8_t)((scw >> (8 * g)) & 0xff);
@@ -261,17 +260,17 @@ __device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, ui
         if (act) {
             float vsum = 0.0f;
             if constexpr (ACT) {
-                // codes: chunks 16*sbi + 8h + 2g + (u&1) of token t; table: (d_a, 32 * d_a * S16) of
-                // the four 16-value half blocks, two per 16-byte load (halves swapped on odd sbi)
-                const uint32_t cb = at.codes + (uint32_t)t * (uint32_t)a.K + 256u * (uint32_t)sbi;
-                const uint32_t tb = at.tab + ((uint32_t)t * at.nb + (uint32_t)sbi) * 128u + 32u * (uint32_t)u;
-                const uint32_t odd = (uint32_t)sbi & 1u;
+                // codes 128h + 32g + l0 .. +15 of the super-block; table: (d_a, 32 * d_a * S16) of the
+                // four 16-value half blocks, two per 16-byte load (the loads swap on odd sbi)
+                const uint32_t cb = at.codes + (uint32_t)t * at.ck + sbi * C::SB_STRIDE + 160u * (uint32_t)h +
+                                    16u * ((uint32_t)u & 1u);
+                const uint32_t tb = at.tab + (uint32_t)t * at.tk + sbi * C::TAB_SB + 32u * (uint32_t)u;
+                const uint32_t odd = sbi & 1u;
                 const float4 e01 = lds128f(tb + 16u * odd), e23 = lds128f(tb + 16u * (odd ^ 1u));
                 const float de[8] = {e01.x, e01.y, e01.z, e01.w, e23.x, e23.y, e23.z, e23.w};
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    const uint32_t c = 8u * (uint32_t)h + 2u * (uint32_t)g + ((uint32_t)u & 1u) + 16u * odd;
-                    const uint4 av = lds128(cb + 16u * (C::swz(c) & 15u));
+                    const uint4 av = lds128(cb + 32u * g);
                     const int Dc = dot16(v[g], av);                       // sum code * a
                     if constexpr (DUMP) Dg[g] = Dc - 32 * dot16(c01, av);  // exact sum (code - 32) * a
                     // d_a * (sum code * a) - 32 * d_a * S16, scaled by d * sc
@@ -390,36 +389,38 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     }
 
     // consumer warps
-    GvAct at{0, 0, nb};
+    GvAct at{0, 0, 0, 0};
     if constexpr (ACT) {
-        // stage the tokens' codes (swizzled 16-byte chunks) and the scale table
+        // stage the tokens' codes (padded layout) and the scale table
         at.codes = smem_u32(smem + C::OFF_PART + C::part_bytes(MT));
-        at.tab = at.codes + (uint32_t)(MT * a.K);
-        const uint32_t nch = (uint32_t)(a.K / 16);
+        at.ck = nb * C::SB_STRIDE;
+        at.tab = at.codes + MT * at.ck;
+        at.tk = nb * C::TAB_SB;
+        const uint32_t nch = nb * 16u;                // 16-byte chunks of codes per token
         for (int t = 0; t < a.mt; ++t) {
             const int64_t m = a.t0 + t;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);
-            const uint32_t cbase = at.codes + (uint32_t)t * (uint32_t)a.K;
+            const uint32_t cbase = at.codes + (uint32_t)t * at.ck, tbase = at.tab + (uint32_t)t * at.tk;
             for (uint32_t c = tid; c < nch; c += kConsumerWarps * 32) {
                 const uint4 v = __ldg(src + c);
-                sts128(cbase + 16u * ((c & ~15u) | C::swz(c & 31u) & 15u), v);
+                const uint32_t sbi = c >> 4, r = c & 15u;     // chunk r of super-block sbi
+                sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
                 if constexpr (FMT == FMT_Q6K) {
-                    // half block c: entry (d_a, 32 * d_a * S16) at [sbi][u][g], the two 16-byte
-                    // halves of each u swapped on odd sbi
+                    // half block c: (d_a, 32 * d_a * S16) at [sbi][u][g], where chunk r is
+                    // group g = (r >> 1) & 3 of quarter u = 2 (r >> 3) + (r & 1); the two
+                    // 16-byte halves of each quarter's entries swap on odd sbi
                     const int s16 = dot16(v, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u));
                     const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
-                    const uint32_t sbi = c >> 4, r = c & 15u, g = (r >> 1) & 3u;
-                    const uint32_t uu = 2u * (r >> 3) + (r & 1u);
-                    const uint32_t off = ((uint32_t)t * nb + sbi) * 128u + 32u * uu + 16u * ((g >> 1) ^ (sbi & 1u)) +
-                                         8u * (g & 1u);
-                    sts64(at.tab + off, da, da * (float)(32 * s16));
+                    const uint32_t g = (r >> 1) & 3u, uu = 2u * (r >> 3) + (r & 1u);
+                    sts64(tbase + sbi * C::TAB_SB + 32u * uu + 16u * ((g >> 1) ^ (sbi & 1u)) + 8u * (g & 1u), da,
+                          da * (float)(32 * s16));
                 }
             }
             if constexpr (FMT == FMT_Q4K) {
-                for (uint32_t b = tid; b < nch / 2; b += kConsumerWarps * 32) {
+                for (uint32_t b = tid; b < nb * 8u; b += kConsumerWarps * 32) {   // (d_a, d_a * S) per block
                     const float da = __ldg(a.p.d + (int64_t)b * a.M + m);
                     const float sa = (float)__ldg(a.p.s + (int64_t)b * a.M + m);
-                    sts64(at.tab + ((uint32_t)t * nb * 8u + b) * 8u, da, da * sa);
+                    sts64(tbase + 8u * b, da, da * sa);
                 }
             }
         }
@@ -427,28 +428,38 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     }
 
     const int u = tid & 3, slot = tid >> 2;          // quarter, and super-block slot within a pass
+    // this thread's super-block of each pass: offset in its row (and the row, for the dump);
+    // both advance by TU super-blocks per unit
+    const uint32_t tu_mod = (uint32_t)C::TU % nb, tu_div = (uint32_t)C::TU / nb;
+    uint32_t t_sbi[C::PASSES];
+    int64_t t_row[C::PASSES];
+#pragma unroll
+    for (int ps = 0; ps < C::PASSES; ++ps) {
+        uint32_t r;
+        t_row[ps] = row_begin + divmod_small((uint32_t)(ps * kSbPerPass + slot), nb, inv_nb, r);
+        t_sbi[ps] = r;
+    }
+    const uint32_t off15 = (uint32_t)((sb_begin * C::BB) & 15);   // units start 16-byte aligned after that
+    const int last = units - 1;
+    const int nsb_last = (int)(sb_total - (int64_t)last * C::TU);
+    const uint32_t ring = smem_u32(smem) + off15;
     int s = 0, pb = 0;
     uint32_t ph = 0, pph = 0;
-    uint32_t c_sbi0 = 0;                             // offset of the unit's first super-block in its row
-    int64_t c_row0 = row_begin;
     for (int j = 0; j < units; ++j) {
         const bool got = mbar_wait(&full[s], ph, a.err, ERR_GEMV_FULL, abort);
         if (!__all_sync(kFull, got)) break;           // leave together: the shuffles below need every lane
-        const int nsb = (int)min((int64_t)C::TU, sb_total - (int64_t)j * C::TU);
-        const int64_t start = (sb_begin + (int64_t)j * C::TU) * C::BB;
-        const uint32_t sbase = smem_u32(smem + s * C::STAGE) + (uint32_t)(start & 15);
+        const int nsb = j == last ? nsb_last : C::TU;
+        const uint32_t sbase = ring + (uint32_t)(s * C::STAGE);
         float part[C::PASSES][MT];
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps) {
             const int idx = ps * kSbPerPass + slot;
             const bool valid = idx < nsb;
-            uint32_t sbi;
-            const int64_t n = c_row0 + divmod_small(c_sbi0 + (uint32_t)idx, nb, inv_nb, sbi);
             const uint32_t blk = sbase + (uint32_t)(idx * C::BB);
             if constexpr (FMT == FMT_Q4K)
-                q4k_quarter<MT, ACT, DUMP>(a, at, blk, n, (int64_t)sbi, u, valid, part[ps]);
+                q4k_quarter<MT, ACT, DUMP>(a, at, blk, t_row[ps], t_sbi[ps], u, valid, part[ps]);
             else
-                q6k_quarter<MT, ACT, DUMP>(a, at, blk, n, (int64_t)sbi, u, valid, part[ps]);
+                q6k_quarter<MT, ACT, DUMP>(a, at, blk, t_row[ps], t_sbi[ps], u, valid, part[ps]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);       // stage fully read: the producer may refill it
@@ -471,9 +482,12 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[pb]);
-        uint32_t adv;
-        c_row0 += divmod_small(c_sbi0 + (uint32_t)nsb, nb, inv_nb, adv);
-        c_sbi0 = adv;
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            t_sbi[ps] += tu_mod;
+            t_row[ps] += tu_div;
+            if (t_sbi[ps] >= nb) { t_sbi[ps] -= nb; ++t_row[ps]; }
+        }
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++pb == kPartBufs) { pb = 0; pph ^= 1u; }
     }
@@ -485,8 +499,7 @@ int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
     auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
     const int smem = C::OFF_PART + C::part_bytes(MT) + (ACT ? (int)C::act_bytes(MT, a.K) : 0);
     constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
-    constexpr int smem_max = C::OFF_PART + C::part_bytes(MT) + (ACT ? kActSmemMax : 0);
-    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_max, slot);
+    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);
     if (rc != MQ_OK) return rc;
     int per_sm = 0;
     rc = resident_ctas(reinterpret_cast<const void *>(kern), kThreads, smem, slot, &per_sm);
@@ -499,7 +512,9 @@ int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
 
 template <int FMT, int MT, bool DUMP>
 int launch_mt(const GvArgs &a, int nsm, cudaStream_t stream) {
-    if (GvCfg<FMT>::act_bytes(MT, a.K) <= kActSmemMax) return launch_one<FMT, MT, true, DUMP>(a, nsm, stream);
+    using C = GvCfg<FMT>;
+    if (C::OFF_PART + C::part_bytes(MT) + C::act_bytes(MT, a.K) <= kSmemMax)
+        return launch_one<FMT, MT, true, DUMP>(a, nsm, stream);
     return launch_one<FMT, MT, false, DUMP>(a, nsm, stream);
 }
 
