@@ -282,24 +282,28 @@ class DecodeSweep:
             self.bytes += w.numel() + 1.25 * k + 4 * n + 4 * k     # weights + plane + output + activation
         self.graph = None
 
-    def run(self):
+    def run(self, quantize=True):
         B = self.B
         for fmt, w, x, plane, y, n, k in self.items:
-            B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
+            if quantize:
+                B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
             B.GEMV[fmt](w, n, k, plane, 1, y)
 
-    def capture(self):
+    def capture(self, quantize=True):
+        """One CUDA graph of the sweep: Q8 quantize + GEMV per matmul, or the GEMVs alone
+        (on the planes the last quantizing run left)."""
         t = self.torch
         s = t.cuda.Stream()
         s.wait_stream(t.cuda.current_stream())
         with t.cuda.stream(s):
-            self.run()                     # warm the launch path outside the capture
+            self.run(True)                 # warm the launch path (and fill the planes) outside the capture
         t.cuda.current_stream().wait_stream(s)
         t.cuda.synchronize()
-        self.graph = t.cuda.CUDAGraph()
-        with t.cuda.graph(self.graph):
-            self.run()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g):
+            self.run(quantize)
         t.cuda.synchronize()
+        return g
 
 
 def time_events(torch, fn, steps, warmup):
@@ -467,13 +471,18 @@ def main():
         del lm_w
         torch.cuda.empty_cache()
         sw = DecodeSweep(torch, B, I)
-        sw.capture()
-        ms = time_events(torch, sw.graph.replay, max(5, K), W)
+        ms = time_events(torch, sw.capture(True).replay, max(5, K), W)
+        ms_gemv = time_events(torch, sw.capture(False).replay, max(5, K), W)
         B.mq_device_status()
+        gemv_bytes = sw.bytes - 4 * sum(k for *_, k in sw.items)          # without the f32 activations
+        lm_ms = lm["m1_gemv"]["ms"]
         line["decode"] = {"workload": "config 3: 28 layers x 7 matmuls, M=1 (Q8 quantize + GEMV each, one CUDA graph)",
                           "ms_per_token": ms, "tok_per_s": 1e3 / ms, "weight_bytes": sw.weight_bytes,
                           "GB/s": sw.bytes / (ms * 1e-3) / 1e9, "frac_of_hbm": sw.bytes / (ms * 1e-3) / 1e9 / hbm_peak,
-                          "launches_per_token": 2 * len(sw.items)}
+                          "launches_per_token": 2 * len(sw.items),
+                          "gemv_only": {"what": "the 196 GEMVs alone, one CUDA graph (planes already quantized)",
+                                        "ms_per_token": ms_gemv, "GB/s": gemv_bytes / (ms_gemv * 1e-3) / 1e9,
+                                        "tok_per_s_with_lm_head": 1e3 / (ms_gemv + lm_ms)}}
 
     # ---------------- CPU baseline (oracle on the host cores, rank 0 only)
     if dist.rank == 0 and dist.world == 1:

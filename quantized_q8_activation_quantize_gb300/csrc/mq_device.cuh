@@ -107,6 +107,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// ------------------------------------------------------ programmatic dependent launch ---
+// Kernels are launched with programmatic stream serialization: a kernel may be scheduled
+// while its predecessor on the stream is still running.  Each kernel calls grid_dep_wait()
+// before it touches memory the predecessor may write or read (the plane, activations,
+// outputs, weights); only L2 prefetch hints go ahead of it.  grid_dep_launch() lets the
+// successor be scheduled early; it is a no-op without a successor.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// hint: bring [p, p + bytes) into L2 (16-byte aligned address and size); never faults the data
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ----------------------------------------------------------------- bulk copies ---
 // 1-D bulk async copy global -> shared, completion counted on `bar` (bytes, 16-B granular).
 __device__ __forceinline__ void bulk_copy_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {

@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // set-up above overlaps the predecessor on the stream; every global access below follows it
+    grid_dep_launch();
+    grid_dep_wait();
 
     // Each warpgroup first rebalances the register file (all four of its warps execute the
     // setmaxnreg), so the code of every role is compiled under its own budget.
@@ -681,8 +684,8 @@ int launch_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, FMT * 2 + (DUMP ? 1 : 0));
     if (rc != MQ_OK) return rc;
     const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    kern<<<grid, kThreads, C::SMEM, stream>>>(tm, tmds, tmw, w, N, K, p, M, y, dump, err);
-    return cuda_error(cudaGetLastError(), "gemm launch");
+    return cuda_error(launch_pdl(kern, grid, dim3(kThreads), C::SMEM, stream, tm, tmds, tmw, w, N, K, p, M, y, dump, err),
+                      "gemm launch");
 }
 
 }  // namespace

@@ -323,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         mbar_init_fence();
     }
     __syncthreads();
+    grid_dep_launch();
 
     // this CTA's rows [row_begin, row_end) and their flat super-block range
     const uint32_t nb = (uint32_t)(a.K / kQK);
@@ -332,16 +333,30 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     const float inv_nb = 1.0f / (float)nb;
     volatile int *abort = &abort_flag;
 
+    // the 16-byte aligned superset of unit j's bytes: [a0, a1)
+    auto unit_bytes = [&](int j, int64_t &a0, int64_t &a1) {
+        const int64_t sb0 = sb_begin + (int64_t)j * C::TU;
+        const int64_t nsb = min((int64_t)C::TU, sb_begin + sb_total - sb0);
+        a0 = (sb0 * C::BB) & ~(int64_t)15;
+        a1 = ((sb0 + nsb) * C::BB + 15) & ~(int64_t)15;
+    };
+
     if (warp == kProducerWarp) {
         if (lane != 0) return;
+        // while the predecessor on the stream finishes: pull the first units into L2 (a hint,
+        // safe whatever the predecessor writes), then wait for it before the real copies
+        for (int j = 0; j < units && j < S; ++j) {
+            int64_t a0, a1;
+            unit_bytes(j, a0, a1);
+            prefetch_l2_bulk(a.w + a0, (uint32_t)(a1 - a0));
+        }
+        grid_dep_wait();
         int s = 0, issued = 0;
         uint32_t ph = 0;
         for (int j = 0; j < units; ++j) {
             if (j >= S && !mbar_wait(&empty[s], ph ^ 1u, a.err, ERR_GEMV_FULL, abort)) break;
-            const int64_t sb0 = sb_begin + (int64_t)j * C::TU;
-            const int64_t nsb = min((int64_t)C::TU, sb_begin + sb_total - sb0);
-            const int64_t start = sb0 * C::BB;
-            const int64_t a0 = start & ~(int64_t)15, a1 = (start + nsb * C::BB + 15) & ~(int64_t)15;
+            int64_t a0, a1;
+            unit_bytes(j, a0, a1);
             mbar_arrive_expect_tx(&full[s], (uint32_t)(a1 - a0));
             bulk_copy_g2s(smem + s * C::STAGE, a.w + a0, (uint32_t)(a1 - a0), &full[s]);
             ++issued;
@@ -388,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         return;
     }
 
-    // consumer warps
+    // consumer warps (the reducer writes y only after them, so after the predecessor too)
+    grid_dep_wait();
     GvAct at{0, 0, 0, 0};
     if constexpr (ACT) {
         // stage the tokens' codes (padded layout) and the scale table
@@ -506,8 +522,7 @@ int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
     if (rc != MQ_OK) return rc;
     int64_t ctas = (int64_t)nsm * per_sm;
     if (ctas > a.N) ctas = a.N;                      // every CTA owns at least one row
-    kern<<<(unsigned)ctas, kThreads, smem, stream>>>(a);
-    return cuda_error(cudaGetLastError(), "gemv launch");
+    return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), smem, stream, a), "gemv launch");
 }
 
 template <int FMT, int MT, bool DUMP>

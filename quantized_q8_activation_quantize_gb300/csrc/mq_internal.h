@@ -43,6 +43,25 @@ int cuda_error(cudaError_t e, const char *what);
 // device and slot); returns MQ_OK or MQ_ERR_CUDA.
 int resident_ctas(const void *kernel, int threads, int smem_bytes, int slot, int *out);
 
+// Launch with programmatic stream serialization (the kernel may start while its predecessor on
+// the stream finishes; every kernel of the library waits on griddepcontrol before it touches
+// dependent memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // launchers (arguments already validated); return MQ_OK or MQ_ERR_CUDA
 int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,
                     unsigned int *err, cudaStream_t stream);

@@ -71,6 +71,8 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const P
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int64_t M, int64_t K, Plane p) {
+    grid_dep_launch();
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const uint32_t nch = (uint32_t)(K / 256);
     const int64_t items = M * (int64_t)nch;
@@ -93,6 +95,8 @@ __global__ void __launch_bounds__(256) rms_quantize_kernel(const float *__restri
                                                            const float *__restrict__ w, float eps, Plane p) {
     __shared__ double red[8];
     __shared__ float r_sh;
+    grid_dep_launch();
+    grid_dep_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t nch = K / 256;
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
@@ -139,19 +143,20 @@ int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, fl
                     unsigned int *err, cudaStream_t stream) {
     (void)err;
     const int nsm = sm_count();
+    cudaError_t e;
     if (rms_w == nullptr) {
         const int64_t warps = M * (K / 256);
         int64_t ctas = (warps + 7) / 8;
         const int64_t cap = (int64_t)nsm * 8;
         if (ctas > cap) ctas = cap;
-        quantize_kernel<<<(unsigned)ctas, 256, 0, stream>>>(x, M, K, p);
+        e = launch_pdl(quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, p);
     } else {
         int64_t ctas = M;
         const int64_t cap = (int64_t)nsm * 8;
         if (ctas > cap) ctas = cap;
-        rms_quantize_kernel<<<(unsigned)ctas, 256, 0, stream>>>(x, M, K, rms_w, eps, p);
+        e = launch_pdl(rms_quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, rms_w, eps, p);
     }
-    return cuda_error(cudaGetLastError(), "quantize launch");
+    return cuda_error(e, "quantize launch");
 }
 
 }  // namespace mq
