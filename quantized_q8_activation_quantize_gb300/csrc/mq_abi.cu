@@ -91,23 +91,30 @@ int ensure_smem_attr(const void *kernel, int bytes, int slot) {
 }
 
 int resident_ctas(const void *kernel, int threads, int smem_bytes, int slot, int *out) {
-    // per (device, slot): the shared-memory size last asked about and the answer
-    static int cache_smem[kMaxDevices][kAttrSlots] = {};
-    static int cache_n[kMaxDevices][kAttrSlots] = {};
+    // per (device, slot): a few (shared-memory size, answer) pairs, replaced round-robin
+    constexpr int kWays = 4;
+    static int cache_smem[kMaxDevices][kAttrSlots][kWays] = {};
+    static int cache_n[kMaxDevices][kAttrSlots][kWays] = {};
+    static int cache_next[kMaxDevices][kAttrSlots] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kAttrSlots)
         return set_error(MQ_ERR_CUDA, "resident_ctas: bad device %d / slot %d", dev, slot);
     std::lock_guard<std::mutex> lock(g_dev_mu);
-    if (cache_n[dev][slot] == 0 || cache_smem[dev][slot] != smem_bytes) {
-        int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes);
-        if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-        if (n < 1) return set_error(MQ_ERR_CUDA, "kernel in slot %d cannot be resident (%d B shared memory)", slot, smem_bytes);
-        cache_n[dev][slot] = n;
-        cache_smem[dev][slot] = smem_bytes;
-    }
-    *out = cache_n[dev][slot];
+    for (int i = 0; i < kWays; ++i)
+        if (cache_n[dev][slot][i] > 0 && cache_smem[dev][slot][i] == smem_bytes) {
+            *out = cache_n[dev][slot][i];
+            return MQ_OK;
+        }
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes);
+    if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (n < 1) return set_error(MQ_ERR_CUDA, "kernel in slot %d cannot be resident (%d B shared memory)", slot, smem_bytes);
+    const int i = cache_next[dev][slot];
+    cache_next[dev][slot] = (i + 1) % kWays;
+    cache_smem[dev][slot][i] = smem_bytes;
+    cache_n[dev][slot][i] = n;
+    *out = n;
     return MQ_OK;
 }
 

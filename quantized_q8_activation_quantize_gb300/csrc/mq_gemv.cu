@@ -47,10 +47,9 @@ struct GvCfg {
     static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
     static constexpr int PASSES = FMT == FMT_Q4K ? 2 : 1;
     static constexpr int TU = kSbPerPass * PASSES;     // super-blocks per unit
-    static constexpr int STAGES = FMT == FMT_Q4K ? 3 : 4;
+    static constexpr int STAGES = FMT == FMT_Q4K ? 3 : 4;  // at most; a launch may use fewer (GvArgs::nst)
     // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
     static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
-    static constexpr int OFF_PART = STAGES * STAGE;
     static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
     // Staged activations, per token: int8 codes with each super-block's two 128-value halves
     // padded apart (half stride 160 B = 10 bank groups of 16 B, super-block stride SB_STRIDE:
@@ -62,6 +61,7 @@ struct GvCfg {
     static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * (SB_STRIDE + TAB_SB); }
 };
 constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
+constexpr int kThirdCta = 76 * 1024;                 // a CTA this small leaves room for three per SM
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -125,6 +125,7 @@ struct GvArgs {
     Plane p;
     int64_t M, t0;
     int mt;
+    int nst;                     // ring stages this launch uses (2 .. STAGES)
     float *y;
     Dump dump;
     unsigned int *err;
@@ -308,12 +309,12 @@ __device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, ui
 template <int FMT, int MT, bool ACT, bool DUMP>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs a) {
     using C = GvCfg<FMT>;
-    constexpr int S = C::STAGES;
+    const int S = a.nst;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full[S], empty[S], pfull[kPartBufs], pempty[kPartBufs];
+    __shared__ __align__(8) uint64_t full[C::STAGES], empty[C::STAGES], pfull[kPartBufs], pempty[kPartBufs];
     __shared__ float carry[2][MT];
     __shared__ int abort_flag;
-    float *partbuf = reinterpret_cast<float *>(smem + C::OFF_PART);   // [kPartBufs][MT][TU]
+    float *partbuf = reinterpret_cast<float *>(smem + S * C::STAGE);   // [kPartBufs][MT][TU]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     GvAct at{0, 0, 0, 0};
     if constexpr (ACT) {
         // stage the tokens' codes (padded layout) and the scale table
-        at.codes = smem_u32(smem + C::OFF_PART + C::part_bytes(MT));
+        at.codes = smem_u32(partbuf) + (uint32_t)C::part_bytes(MT);
         at.ck = nb * C::SB_STRIDE;
         at.tab = at.codes + MT * at.ck;
         at.tk = nb * C::TAB_SB;
@@ -417,26 +418,27 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
             const int64_t m = a.t0 + t;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);
             const uint32_t cbase = at.codes + (uint32_t)t * at.ck, tbase = at.tab + (uint32_t)t * at.tk;
+            // all of an iteration's global loads go out before its stores (one latency round)
             for (uint32_t c = tid; c < nch; c += kConsumerWarps * 32) {
                 const uint4 v = __ldg(src + c);
                 const uint32_t sbi = c >> 4, r = c & 15u;     // chunk r of super-block sbi
-                sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
                 if constexpr (FMT == FMT_Q6K) {
+                    const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
+                    sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
                     // half block c: (d_a, 32 * d_a * S16) at [sbi][u][g], where chunk r is
                     // group g = (r >> 1) & 3 of quarter u = 2 (r >> 3) + (r & 1); the two
                     // 16-byte halves of each quarter's entries swap on odd sbi
                     const int s16 = dot16(v, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u));
-                    const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
                     const uint32_t g = (r >> 1) & 3u, uu = 2u * (r >> 3) + (r & 1u);
                     sts64(tbase + sbi * C::TAB_SB + 32u * uu + 16u * ((g >> 1) ^ (sbi & 1u)) + 8u * (g & 1u), da,
                           da * (float)(32 * s16));
-                }
-            }
-            if constexpr (FMT == FMT_Q4K) {
-                for (uint32_t b = tid; b < nb * 8u; b += kConsumerWarps * 32) {   // (d_a, d_a * S) per block
-                    const float da = __ldg(a.p.d + (int64_t)b * a.M + m);
-                    const float sa = (float)__ldg(a.p.s + (int64_t)b * a.M + m);
-                    sts64(tbase + 8u * b, da, da * sa);
+                } else {
+                    // block c (< K/32): (d_a, d_a * S)
+                    const bool blk = c < nb * 8u;
+                    const float da = blk ? __ldg(a.p.d + (int64_t)c * a.M + m) : 0.0f;
+                    const float sa = blk ? (float)__ldg(a.p.s + (int64_t)c * a.M + m) : 0.0f;
+                    sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
+                    if (blk) sts64(tbase + 8u * c, da, da * sa);
                 }
             }
         }
@@ -509,11 +511,24 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     }
 }
 
+// shared memory of one CTA with `nst` ring stages
+template <int FMT, int MT, bool ACT>
+int64_t gemv_smem(int nst, int64_t K) {
+    using C = GvCfg<FMT>;
+    return (int64_t)nst * C::STAGE + C::part_bytes(MT) + (ACT ? C::act_bytes(MT, K) : 0);
+}
+
 template <int FMT, int MT, bool ACT, bool DUMP>
-int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
+int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     using C = GvCfg<FMT>;
     auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
-    const int smem = C::OFF_PART + C::part_bytes(MT) + (ACT ? (int)C::act_bytes(MT, a.K) : 0);
+    // the full ring if it fits, and one stage fewer when that lets a third CTA fit on an SM
+    a.nst = C::STAGES;
+    while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kSmemMax) --a.nst;
+    if (MT <= 2 && a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kThirdCta &&
+        gemv_smem<FMT, MT, ACT>(a.nst - 1, a.K) <= kThirdCta)
+        --a.nst;
+    const int smem = (int)gemv_smem<FMT, MT, ACT>(a.nst, a.K);
     constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);
     if (rc != MQ_OK) return rc;
@@ -527,9 +542,7 @@ int launch_one(const GvArgs &a, int nsm, cudaStream_t stream) {
 
 template <int FMT, int MT, bool DUMP>
 int launch_mt(const GvArgs &a, int nsm, cudaStream_t stream) {
-    using C = GvCfg<FMT>;
-    if (C::OFF_PART + C::part_bytes(MT) + C::act_bytes(MT, a.K) <= kSmemMax)
-        return launch_one<FMT, MT, true, DUMP>(a, nsm, stream);
+    if (gemv_smem<FMT, MT, true>(2, a.K) <= kSmemMax) return launch_one<FMT, MT, true, DUMP>(a, nsm, stream);
     return launch_one<FMT, MT, false, DUMP>(a, nsm, stream);
 }
 
@@ -558,7 +571,7 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
                 const Dump &dump, unsigned int *err, cudaStream_t stream) {
     const int nsm = sm_count();
     const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
-    GvArgs a{w, N, K, p, M, 0, 0, y, dump, err};
+    GvArgs a{w, N, K, p, M, 0, 0, 0, y, dump, err};
     if (fmt == FMT_Q4K)
         return dmp ? launch_fmt<FMT_Q4K, true>(a, nsm, stream) : launch_fmt<FMT_Q4K, false>(a, nsm, stream);
     return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
