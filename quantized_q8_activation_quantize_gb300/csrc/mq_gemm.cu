@@ -43,9 +43,7 @@ namespace {
 constexpr int BM = 128, BN = 128, BK = 64;
 constexpr int kThreads = 512;   // 4 warpgroups: {TMA, MMA, -, -}, unpack, epilogue x2
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpUnpack0 = 4, kWarpEpi0 = 8;
-// per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file)
-constexpr int kRegsCtl = 32, kRegsUnpack = 80, kRegsEpi = 200;
-static_assert(128 * kRegsCtl + 128 * kRegsUnpack + 256 * kRegsEpi <= 65536, "register split exceeds the launch pool");
+
 constexpr int kAccSlots = 3;
 constexpr uint32_t kTmemCols = 512, kMinCol = 384;   // 3 block slots + the Q4_K min-term sum
 constexpr int kTile = BM * BK * 2;       // one 128 x 64 f16 operand tile
@@ -76,6 +74,12 @@ struct GmCfg {
     static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
+    // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file); the
+    // control warpgroup's single-thread loops must not spill (a spill reload costs an L2 trip)
+    static constexpr int REGS_CTL = 56;
+    static constexpr int REGS_UNPACK = FMT == FMT_Q4K ? 72 : 80;
+    static constexpr int REGS_EPI = FMT == FMT_Q4K ? 192 : 184;
+    static_assert(128 * REGS_CTL + 128 * REGS_UNPACK + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 };
 
 struct Bars {
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each warpgroup first rebalances the register file (all four of its warps execute the
     // setmaxnreg), so the code of every role is compiled under its own budget.
     if (warp < kWarpUnpack0) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CTL));
       if (warp == kWarpTma) {
         // ------------------------------------------------------------ A / d*S producer
         if (lane == 0) {
@@ -265,29 +269,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_min = idesc_tf32_f32(BM, BN);
-            const uint32_t a_base = smem_u32(sm + C::OFF_A), b_base = smem_u32(sm + C::OFF_B);
-            const uint32_t bc_base = smem_u32(sm + C::OFF_BC);
+            // stage-0 descriptors; a stage adds kTile >> 4 and a K=16 step 32 B >> 4 to the
+            // start-address field (which stays below 2^14)
+            const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sm + C::OFF_A));
+            const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sm + C::OFF_B));
+            const uint64_t bc_desc0 = sw128_kmajor_desc(smem_u32(sm + C::OFF_BC));
             const uint32_t amin_base = smem_u32(sm + C::OFF_AMIN), bmin_base = smem_u32(sm + C::OFF_BMIN);
+            const uint32_t a_full0 = smem_u32(bars.a_full), b_full0 = smem_u32(bars.b_full);
+            const uint32_t acc_empty0 = smem_u32(bars.acc_empty);
             int gb = 0;
             bool ok = true;
             for (int sb = 0; sb < nsb && ok; ++sb) {
                 for (int q = 0; q < 4 && ok; ++q) {
                     const int st = sb * 4 + q, s = st % S;
                     const uint32_t ph = (st / S) & 1;
-                    if (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag) ||
-                        !mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag)) {
+                    const int slot0 = gb % kAccSlots, slot1 = (gb + 1) % kAccSlots;
+                    const uint32_t eph0 = ((gb / kAccSlots) & 1) ^ 1, eph1 = (((gb + 1) / kAccSlots) & 1) ^ 1;
+                    // All four conditions of the stage probed at once (their latencies overlap);
+                    // only a stage that is not ready yet falls back to the blocking waits.
+                    const bool ready = mbar_test_wait(a_full0 + 8u * s, ph) & mbar_test_wait(b_full0 + 8u * s, ph) &
+                                       mbar_test_wait(acc_empty0 + 8u * slot0, eph0) &
+                                       mbar_test_wait(acc_empty0 + 8u * slot1, eph1);
+                    if (!ready && (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag) ||
+                                   !mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag))) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
                     bool corr = false;
                     if constexpr (C::CORR)
                         corr = (corr_flags[4 * s] | corr_flags[4 * s + 1] | corr_flags[4 * s + 2] |
                                 corr_flags[4 * s + 3]) != 0;
+                    const uint64_t soff = (uint64_t)((s * kTile) >> 4);
                     for (int h = 0; h < 2; ++h) {
-                        const int slot = gb % kAccSlots;
-                        if (!mbar_wait(&bars.acc_empty[slot], ((gb / kAccSlots) & 1) ^ 1, err, ERR_GEMM_ACC_EMPTY,
-                                       abort_flag)) {
+                        const int slot = h ? slot1 : slot0;
+                        if (!ready && !mbar_wait(&bars.acc_empty[slot], h ? eph1 : eph0, err, ERR_GEMM_ACC_EMPTY,
+                                                 abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -295,11 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t d_tmem = tmem + (uint32_t)(slot * BN);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t koff = (uint32_t)((2 * h + kk) * 32);
-                            const uint64_t adesc = sw128_kmajor_desc(a_base + s * kTile + koff);
-                            mma_f16(d_tmem, adesc, sw128_kmajor_desc(b_base + s * kTile + koff), idesc, kk);
-                            if (corr)
-                                mma_f16(d_tmem, adesc, sw128_kmajor_desc(bc_base + s * kTile + koff), idesc, 1);
+                            const uint64_t koff = soff + (uint64_t)((2 * h + kk) * 2);
+                            mma_f16(d_tmem, a_desc0 + koff, b_desc0 + koff, idesc, kk);
+                            if (corr) mma_f16(d_tmem, a_desc0 + koff, bc_desc0 + koff, idesc, 1);
                         }
                         mma_commit(&bars.acc_full[slot]);
                         ++gb;
@@ -332,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }   // warps 2-3 of the control warpgroup are idle
     } else if (warp < kWarpEpi0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsUnpack));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_UNPACK));
         // ------------------------------------------------------------ unpackers
         const int r = threadIdx.x - 32 * kWarpUnpack0;     // weight row in the tile
         const int64_t n = n0 + r;
@@ -532,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars.raw_full[i % R], (i / R) & 1, err, ERR_GEMM_RAW_FULL, nullptr);
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_EPI));
         // ------------------------------------------------------------ epilogue
         const int e = warp - kWarpEpi0, qd = warp & 3, hf = e >> 2;
         const int64_t m = m0 + 32 * qd + lane;
@@ -567,16 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const float2 da2 = make_float2(da_cur[j], da_cur[j]);
+                // both 32-column halves in flight together, one wait, then the slot goes back
+                uint32_t vv[2][32];
+                tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
+                tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32), vv[1]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t v[32];
-                    tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32 * hh), v);
-                    tmem_ld_wait();
-                    if (hh == 1) {       // both halves are in registers: hand the slot back to the MMA
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
-                    }
+                    const uint32_t (&v)[32] = vv[hh];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         part[16 * hh + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
