@@ -300,7 +300,8 @@ int mq_device_status(mq_stream_t stream) {
     if (e != cudaSuccess) return cuda_error(e, "mq_device_status: clear error word");
     static const char *names[] = {"gemv stage", "gemm A stage", "gemm B stage", "gemm stage release",
                                   "gemm raw weights", "gemm accumulator", "gemm accumulator release",
-                                  "gemm row factors", "gemm row factor release", "gemv drain", "gemm min term"};
+                                  "gemm row factors", "gemm row factor release", "gemv drain", "gemm min term",
+                                  "gemm activation scales"};
     char buf[400] = "";
     for (int i = 0; i < 11; ++i)
         if (v & (1u << i)) {

@@ -67,11 +67,12 @@ struct GmCfg {
     static constexpr int OFF_BMIN = OFF_AMIN + (MIN ? 2 * MIN_TILE : 0);
     static constexpr int OFF_RAW = OFF_BMIN + (MIN ? 2 * MIN_TILE : 0);
     static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;   // fp16 d per weight row, 2 slots
-    static constexpr int OFF_FLAG = OFF_INFO + 2 * BN * 4;
+    static constexpr int OFF_DA = OFF_INFO + 2 * BN * 4;                    // d_a [2][8 blocks][128 tokens]
+    static constexpr int OFF_FLAG = OFF_DA + 2 * 8 * BM * 4;
     static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
     // a_full[S] b_full[S] ab_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] acc_full[3]
-    // acc_empty[3] amin_full[2] amin_empty[2] min_final[1]
-    static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5;
+    // acc_empty[3] amin_full[2] amin_empty[2] min_final[1] da_full[2] da_empty[2]
+    static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
     // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file); the
@@ -84,7 +85,7 @@ struct GmCfg {
 
 struct Bars {
     uint64_t *a_full, *b_full, *ab_empty, *raw_full, *raw_empty, *info_full, *info_empty, *acc_full, *acc_empty;
-    uint64_t *amin_full, *amin_empty, *min_final;
+    uint64_t *amin_full, *amin_empty, *min_final, *da_full, *da_empty;
 };
 
 // 16-byte async copy global -> shared (L2 only); completion tracked by cp.async groups / mbarriers
@@ -164,6 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.amin_full = bars.acc_empty + kAccSlots;
     bars.amin_empty = bars.amin_full + 2;
     bars.min_final = bars.amin_empty + 2;
+    bars.da_full = bars.min_final + 1;
+    bars.da_empty = bars.da_full + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
     volatile uint32_t *corr_flags = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_FLAG);
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&bars.a_full[s], 1);
-            mbar_init(&bars.b_full[s], 128);
+            mbar_init(&bars.b_full[s], 4);
             mbar_init(&bars.ab_empty[s], 1);
         }
         for (int r = 0; r < R; ++r) {
@@ -186,12 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (Q4_K only)
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.info_full[i], 128);
+            mbar_init(&bars.info_full[i], 4);
             mbar_init(&bars.info_empty[i], C::MIN ? 9 : 8);    // epilogue warps (+ the min MMA)
             mbar_init(&bars.amin_full[i], 1);
             mbar_init(&bars.amin_empty[i], 1);
         }
         mbar_init(bars.min_final, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.da_full[i], 2);                    // the two stager warps
+            mbar_init(&bars.da_empty[i], 8);                   // the epilogue warps
+        }
         for (int i = 0; i < kAccSlots; ++i) {
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], 8);
@@ -266,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform control flow and operands); one elected
+        // lane issues each MMA and commit.
+        {
             constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_min = idesc_tf32_f32(BM, BN);
             // stage-0 descriptors; a stage adds kTile >> 4 and a K=16 step 32 B >> 4 to the
@@ -277,6 +286,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t amin_base = smem_u32(sm + C::OFF_AMIN), bmin_base = smem_u32(sm + C::OFF_BMIN);
             const uint32_t a_full0 = smem_u32(bars.a_full), b_full0 = smem_u32(bars.b_full);
             const uint32_t acc_empty0 = smem_u32(bars.acc_empty);
+            // a blocking wait the whole warp leaves together
+            auto wait_all = [&](uint64_t *bar, uint32_t ph, uint32_t code) {
+                return __all_sync(kFull, mbar_wait(bar, ph, err, code, abort_flag));
+            };
+            // Q4_K min term of super-block x, summed over the whole K in its own TMEM region:
+            // MIN (+)= (d_a S) x (-dmin m_j), both operands tf32 (hi, lo) pairs, three MMAs of K = 8
+            auto issue_min = [&](int x) -> bool {
+                const uint32_t ph = (x >> 1) & 1;
+                const bool ready = __all_sync(kFull, mbar_test_wait(smem_u32(&bars.amin_full[x & 1]), ph) &
+                                                         mbar_test_wait(smem_u32(&bars.info_full[x & 1]), ph));
+                if (!ready && (!wait_all(&bars.amin_full[x & 1], ph, ERR_GEMM_MIN) ||
+                               !wait_all(&bars.info_full[x & 1], ph, ERR_GEMM_INFO_FULL)))
+                    return false;
+                tc_fence_after();
+                const uint32_t at = amin_base + (x & 1) * C::MIN_TILE, bt = bmin_base + (x & 1) * C::MIN_TILE;
+                // (hi + lo)(d_a S) x (hi + lo)(-dmin m): hi*hi + lo*hi + hi*lo (lo*lo is below 2^-22)
+                mma_tf32_warp(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt), idesc_min, x > 0 ? 1u : 0u);
+                mma_tf32_warp(tmem + kMinCol, sw64_kmajor_desc(at + 32), sw64_kmajor_desc(bt), idesc_min, 1u);
+                mma_tf32_warp(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt + 32), idesc_min, 1u);
+                mma_commit_warp(&bars.amin_empty[x & 1]);
+                mma_commit_warp(&bars.info_empty[x & 1]);
+                return true;
+            };
             int gb = 0;
             bool ok = true;
             for (int sb = 0; sb < nsb && ok; ++sb) {
@@ -287,11 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t eph0 = ((gb / kAccSlots) & 1) ^ 1, eph1 = (((gb + 1) / kAccSlots) & 1) ^ 1;
                     // All four conditions of the stage probed at once (their latencies overlap);
                     // only a stage that is not ready yet falls back to the blocking waits.
-                    const bool ready = mbar_test_wait(a_full0 + 8u * s, ph) & mbar_test_wait(b_full0 + 8u * s, ph) &
-                                       mbar_test_wait(acc_empty0 + 8u * slot0, eph0) &
-                                       mbar_test_wait(acc_empty0 + 8u * slot1, eph1);
-                    if (!ready && (!mbar_wait(&bars.a_full[s], ph, err, ERR_GEMM_A_FULL, abort_flag) ||
-                                   !mbar_wait(&bars.b_full[s], ph, err, ERR_GEMM_B_FULL, abort_flag))) {
+                    const bool ready = __all_sync(kFull, mbar_test_wait(a_full0 + 8u * s, ph) &
+                                                             mbar_test_wait(b_full0 + 8u * s, ph) &
+                                                             mbar_test_wait(acc_empty0 + 8u * slot0, eph0) &
+                                                             mbar_test_wait(acc_empty0 + 8u * slot1, eph1));
+                    if (!ready && (!wait_all(&bars.a_full[s], ph, ERR_GEMM_A_FULL) ||
+                                   !wait_all(&bars.b_full[s], ph, ERR_GEMM_B_FULL))) {
                         ok = false;
                         break;
                     }
@@ -300,51 +333,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                         corr = (corr_flags[4 * s] | corr_flags[4 * s + 1] | corr_flags[4 * s + 2] |
                                 corr_flags[4 * s + 3]) != 0;
                     const uint64_t soff = (uint64_t)((s * kTile) >> 4);
+                    if (ready) tc_fence_after();
                     for (int h = 0; h < 2; ++h) {
                         const int slot = h ? slot1 : slot0;
-                        if (!ready && !mbar_wait(&bars.acc_empty[slot], h ? eph1 : eph0, err, ERR_GEMM_ACC_EMPTY,
-                                                 abort_flag)) {
-                            ok = false;
-                            break;
+                        if (!ready) {
+                            if (!wait_all(&bars.acc_empty[slot], h ? eph1 : eph0, ERR_GEMM_ACC_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
                         const uint32_t d_tmem = tmem + (uint32_t)(slot * BN);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = soff + (uint64_t)((2 * h + kk) * 2);
-                            mma_f16(d_tmem, a_desc0 + koff, b_desc0 + koff, idesc, kk);
-                            if (corr) mma_f16(d_tmem, a_desc0 + koff, bc_desc0 + koff, idesc, 1);
+                            mma_f16_warp(d_tmem, a_desc0 + koff, b_desc0 + koff, idesc, kk);
+                            if (corr) mma_f16_warp(d_tmem, a_desc0 + koff, bc_desc0 + koff, idesc, 1);
                         }
-                        mma_commit(&bars.acc_full[slot]);
+                        mma_commit_warp(&bars.acc_full[slot]);
                         ++gb;
                     }
-                    mma_commit(&bars.ab_empty[s]);
-                }
-                if constexpr (C::MIN) {
-                    // min term of this super-block, summed over the whole K in its own TMEM region:
-                    // MIN (+)= (d_a S) x (-dmin m_j), both operands tf32 (hi, lo) pairs, three MMAs of K = 8
                     if (!ok) break;
-                    const uint32_t ph = (sb >> 1) & 1;
-                    if (!mbar_wait(&bars.amin_full[sb & 1], ph, err, ERR_GEMM_MIN, abort_flag) ||
-                        !mbar_wait(&bars.info_full[sb & 1], ph, err, ERR_GEMM_INFO_FULL, abort_flag)) {
-                        ok = false;
-                        break;
+                    mma_commit_warp(&bars.ab_empty[s]);
+                    if constexpr (C::MIN) {
+                        // the previous super-block's min term goes after this super-block's first
+                        // stage, so it never delays the block MMAs the epilogue is waiting for
+                        if (q == 0 && sb > 0 && !issue_min(sb - 1)) ok = false;
                     }
-                    tc_fence_after();
-                    const uint32_t at = amin_base + (sb & 1) * C::MIN_TILE, bt = bmin_base + (sb & 1) * C::MIN_TILE;
-                    // (hi + lo)(d_a S) x (hi + lo)(-dmin m): hi*hi + lo*hi + hi*lo (lo*lo is below 2^-22)
-                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt), idesc_min, sb > 0 ? 1u : 0u);
-                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at + 32), sw64_kmajor_desc(bt), idesc_min, 1u);
-                    mma_tf32(tmem + kMinCol, sw64_kmajor_desc(at), sw64_kmajor_desc(bt + 32), idesc_min, 1u);
-                    mma_commit(&bars.amin_empty[sb & 1]);
-                    mma_commit(&bars.info_empty[sb & 1]);
                 }
             }
             if constexpr (C::MIN) {
-                if (ok) mma_commit(bars.min_final);
+                if (ok && issue_min(nsb - 1)) mma_commit_warp(bars.min_final);
             }
         }
-      }   // warps 2-3 of the control warpgroup are idle
+      } else {
+        // ------------------------------------------------------------ activation-scale stager
+        // warps 2-3: d_a of the tile's 128 tokens for each super-block's 8 blocks into shared
+        // memory (two slots), so the epilogue reads them there instead of from L2
+        const int t = threadIdx.x - 64;                  // 0..63: tokens t and t + 64
+        float *da_tile0 = reinterpret_cast<float *>(sm + C::OFF_DA);
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int slot = sb & 1;
+            if (!__all_sync(kFull, mbar_wait(&bars.da_empty[slot], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_DA, abort_flag)))
+                break;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t m = m0 + t + 64 * h;
+                    v[2 * j + h] = m < M ? __ldg(p.d + (int64_t)(8 * sb + j) * M + m) : 0.0f;
+                }
+            float *dst = da_tile0 + slot * 8 * BM;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                dst[j * BM + t] = v[2 * j];
+                dst[j * BM + t + 64] = v[2 * j + 1];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.da_full[slot]);
+        }
+      }
     } else if (warp < kWarpEpi0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_UNPACK));
         // ------------------------------------------------------------ unpackers
@@ -382,7 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sb = 0;
         for (; sb < nsb; ++sb) {
             const int slot = sb % R;
-            if (!mbar_wait(&bars.raw_full[slot], (sb / R) & 1, err, ERR_GEMM_RAW_FULL, abort_flag)) break;
+            // waits are warp-uniform (all lanes leave together): the warp-level arrivals below need it
+            if (!__all_sync(kFull, mbar_wait(&bars.raw_full[slot], (sb / R) & 1, err, ERR_GEMM_RAW_FULL, abort_flag)))
+                break;
             const uint32_t blk = smem_u32(raw_row0 + slot * BN * C::RAW_ROW) +
                                  (valid ? (uint32_t)(reinterpret_cast<uintptr_t>(wrow + (int64_t)sb * C::BB) & 15) : 0u);
             // ---- super-block header
@@ -420,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d = __half2float(__ushort_as_half((unsigned short)(tail[4] & 0xffff)));
             }
             // ---- per-row factors of this super-block: d for the epilogue, -dmin m_j for the min MMA
-            if (!mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY, abort_flag)) break;
+            if (!__all_sync(kFull, mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY,
+                                             abort_flag)))
+                break;
             info0[(sb & 1) * BN + r] = d;
             if constexpr (C::MIN) {
                 // -dmin*m_j has at most 17 significant bits (exact in f32); it splits exactly into
@@ -440,14 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sts128(sw64_chunk(bt, r, 3), make_uint4(wl[4], wl[5], wl[6], wl[7]));
                 fence_proxy_async_smem();
             }
-            mbar_arrive(&bars.info_full[sb & 1]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.info_full[sb & 1]);      // one arrival per unpack warp
 
             // ---- four 64-value stages of this super-block (unrolled: sc[] stays in registers)
             bool ok = true;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int st = sb * 4 + q, s = st % S;
-                if (!mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) {
+                if (!__all_sync(kFull, mbar_wait(&bars.ab_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY,
+                                                 abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -530,7 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) corr_flags[4 * s + (warp - kWarpUnpack0)] = any ? 1u : 0u;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.b_full[s]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.b_full[s]);          // one arrival per unpack warp
             }
             if (!ok) break;
             if constexpr (FMT == FMT_Q4K) {
@@ -562,15 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[i] = make_float2(0.0f, 0.0f);
             part[i] = make_float2(0.0f, 0.0f);
         }
-        // activation scales of the current and the next super-block (prefetched a super-block ahead)
-        float da_cur[8], da_nxt[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) da_cur[j] = valid_m ? __ldg(p.d + (int64_t)j * M + m) : 0.0f;
+        // activation scales: this thread's token in the stager's shared-memory tile
+        const float *da_tok = reinterpret_cast<const float *>(sm + C::OFF_DA) + 32 * qd + lane;
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                da_nxt[j] = (valid_m && sb + 1 < nsb) ? __ldg(p.d + (int64_t)(8 * (sb + 1) + j) * M + m) : 0.0f;
+            if (!mbar_wait(&bars.da_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_DA, abort_flag)) break;
+            const float *da_sb = da_tok + (sb & 1) * 8 * BM;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int gb = sb * 8 + j;
@@ -580,18 +633,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float2 da2 = make_float2(da_cur[j], da_cur[j]);
-                // both 32-column halves in flight together, one wait, then the slot goes back
-                uint32_t vv[2][32];
-                tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
-                tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32), vv[1]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
+                const float da = da_sb[j * BM];
+                const float2 da2 = make_float2(da, da);
+                // Q4_K: both 32-column halves in flight together, one wait, then the slot goes back;
+                // Q6_K (a smaller epilogue register budget): one half at a time
+                constexpr bool kBoth = FMT == FMT_Q4K;
+                uint32_t vv[kBoth ? 2 : 1][32];
+                if constexpr (kBoth) {
+                    tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
+                    tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32), vv[kBoth ? 1 : 0]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
+                }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t (&v)[32] = vv[hh];
+                    if constexpr (!kBoth) {
+                        tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32 * hh), vv[0]);
+                        tmem_ld_wait();
+                        if (hh == 1) {       // both halves are in registers: hand the slot back to the MMA
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
+                        }
+                    }
+                    const uint32_t (&v)[32] = vv[kBoth ? hh : 0];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         part[16 * hh + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
@@ -619,9 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 part[i] = make_float2(0.0f, 0.0f);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.info_empty[sb & 1]);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) da_cur[j] = da_nxt[j];
+            if (lane == 0) {
+                mbar_arrive(&bars.info_empty[sb & 1]);
+                mbar_arrive(&bars.da_empty[sb & 1]);
+            }
         }
         if (ok && !*abort_flag) {
             if constexpr (C::MIN) {
