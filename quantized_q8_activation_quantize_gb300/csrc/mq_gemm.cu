@@ -679,11 +679,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // ---- super-block end: acc += d * part (d: fp16 factor of each weight row)
             if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
-            const float *info = info0 + (sb & 1) * BN + col0;
+            const float4 *info = reinterpret_cast<const float4 *>(info0 + (sb & 1) * BN + col0);
+            // all 16 loads of the 64 row factors first (independent, their latencies overlap), then the FMAs
+            float4 dv[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                acc[i] = __ffma2_rn(part[i], *reinterpret_cast<const float2 *>(info + 2 * i), acc[i]);
-                part[i] = make_float2(0.0f, 0.0f);
+            for (int i = 0; i < 16; ++i) dv[i] = info[i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                acc[2 * i] = __ffma2_rn(part[2 * i], make_float2(dv[i].x, dv[i].y), acc[2 * i]);
+                acc[2 * i + 1] = __ffma2_rn(part[2 * i + 1], make_float2(dv[i].z, dv[i].w), acc[2 * i + 1]);
+                part[2 * i] = make_float2(0.0f, 0.0f);
+                part[2 * i + 1] = make_float2(0.0f, 0.0f);
             }
             __syncwarp();
             if (lane == 0) {
