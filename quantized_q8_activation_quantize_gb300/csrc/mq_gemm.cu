@@ -75,11 +75,11 @@ struct GmCfg {
     static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
-    // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file); the
-    // control warpgroup's single-thread loops must not spill (a spill reload costs an L2 trip)
-    static constexpr int REGS_CTL = 56;
+    // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file), chosen
+    // per format by measurement (spill reloads in a pipeline loop cost an L2 trip each)
+    static constexpr int REGS_CTL = FMT == FMT_Q4K ? 56 : 48;
     static constexpr int REGS_UNPACK = FMT == FMT_Q4K ? 72 : 80;
-    static constexpr int REGS_EPI = FMT == FMT_Q4K ? 192 : 184;
+    static constexpr int REGS_EPI = 192;
     static_assert(128 * REGS_CTL + 128 * REGS_UNPACK + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 };
 
