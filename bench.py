@@ -57,6 +57,14 @@ def parse_args():
     return ap.parse_args()
 
 
+# DRAM bytes (read + write) of one launch of the roofline kernels, from one ncu capture of the
+# current kernels (dram__bytes_read.sum + dram__bytes_write.sum); set to None whenever a kernel
+# changes until it is captured again.
+TRAFFIC_GEMM_Q4K_GATE = 96.623616e6 + 207.959296e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
+TRAFFIC_GEMV_Q6K_LMHEAD = 447.194368e6 + 3.913984e6     # 152064x3584 Q6_K, M=1
+# the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs)
+INT8_MMA_SYNC_PEAK_TOPS = 158.1
+
 # single-kernel cases for profiler captures: name -> (config, kernel); inputs of the named config
 CASES = {
     "gemm_q4k_gate": "config 2 gate GEMM: Q4_K 18944x3584, M=3314",
@@ -329,7 +337,8 @@ def cpu_oracle_ffn(budget_s: float, threads: int):
     t_done, ops, tokens = 0.0, 0, 0
     chunk = 4
     while t_done < budget_s and tokens < c["x_hidden"].shape[0]:
-        sl = slice(tokens, tokens + chunk)
+        n = min(chunk, c["x_hidden"].shape[0] - tokens)       # the last slice may be short
+        sl = slice(tokens, tokens + n)
         t0 = time.perf_counter()
         ph = oracle.quantize_q8(c["x_hidden"][sl], c["rms_w"], float(c["eps"]))
         oracle.matmul(c["w_gate"], "q4k", ph, threads=threads)
@@ -337,8 +346,8 @@ def cpu_oracle_ffn(budget_s: float, threads: int):
         pf = oracle.quantize_q8(c["x_ffn"][sl])
         oracle.matmul(c["w_down"], "q6k", pf, threads=threads)
         t_done += time.perf_counter() - t0
-        ops += ffn_ops(chunk)
-        tokens += chunk
+        ops += ffn_ops(n)
+        tokens += n
     return ops / t_done / 1e12, tokens, t_done
 
 
@@ -444,8 +453,10 @@ def main():
         "kernels_rate": {"gemm_q4k_tops": q4k_tflops, "gemm_q6k_tops": q6k_tflops,
                          "rms_quantize_gbs": qrms_gbs, "quantize_gbs": q_gbs},
         "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,
-                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak, "traffic": None,
-                     "peak_kind": f"{peak_kind} dense bf16 (f16 MMA has the same nominal rate)"},
+                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak,
+                     "traffic": TRAFFIC_GEMM_Q4K_GATE,
+                     "peak_kind": f"{peak_kind} dense bf16 (f16 MMA has the same nominal rate)",
+                     "vs_int8_mma_sync_peak": q4k_tflops / INT8_MMA_SYNC_PEAK_TOPS},
         "e2e": e2e, "gpu_launches": pf.launches * K, "clocks": clk,
     }
 
@@ -466,7 +477,8 @@ def main():
         line["lm_head"] = lm
         g = lm["m1_gemv"]["GB/s"]
         line["roofline_decode"] = {"bound": "hbm", "kernel": "mq_gemv_q6k (152064x3584, M=1)", "achieved": g,
-                                   "peak": hbm_peak, "unit": "GB/s", "frac": g / hbm_peak, "traffic": None,
+                                   "peak": hbm_peak, "unit": "GB/s", "frac": g / hbm_peak,
+                                   "traffic": TRAFFIC_GEMV_Q6K_LMHEAD,
                                    "peak_kind": f"{peak_kind} HBM copy"}
         del lm_w
         torch.cuda.empty_cache()
