@@ -47,7 +47,7 @@ struct GvCfg {
     static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
     static constexpr int PASSES = FMT == FMT_Q4K ? 2 : 1;
     static constexpr int TU = kSbPerPass * PASSES;     // super-blocks per unit
-    static constexpr int STAGES = FMT == FMT_Q4K ? 3 : 4;  // at most; a launch may use fewer (GvArgs::nst)
+    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 5;  // at most; a launch may use fewer (GvArgs::nst)
     // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
     static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
     static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
@@ -61,7 +61,7 @@ struct GvCfg {
     static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * (SB_STRIDE + TAB_SB); }
 };
 constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
-constexpr int kThirdCta = 76 * 1024;                 // a CTA this small leaves room for three per SM
+constexpr int kThirdCta = 74 * 1024;                 // a CTA this small leaves room for three per SM
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -522,12 +522,12 @@ template <int FMT, int MT, bool ACT, bool DUMP>
 int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     using C = GvCfg<FMT>;
     auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
-    // the full ring if it fits, and one stage fewer when that lets a third CTA fit on an SM
+    // the deepest ring that fits, made shallower (down to 2 stages) when that lets a third
+    // CTA share the SM (the register budget allows three only for MT <= 2)
     a.nst = C::STAGES;
     while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kSmemMax) --a.nst;
-    if (MT <= 2 && a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kThirdCta &&
-        gemv_smem<FMT, MT, ACT>(a.nst - 1, a.K) <= kThirdCta)
-        --a.nst;
+    if (MT <= 2 && gemv_smem<FMT, MT, ACT>(2, a.K) <= kThirdCta)
+        while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kThirdCta) --a.nst;
     const int smem = (int)gemv_smem<FMT, MT, ACT>(a.nst, a.K);
     constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);
