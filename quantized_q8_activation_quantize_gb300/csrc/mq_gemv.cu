@@ -137,18 +137,34 @@ struct GvAct {
     uint32_t ck, tk;             // per-token strides of codes and table
 };
 
-// Q4_K: quarter u of the super-block at shared address `blk` (row n, super-block sbi of the
-// row): qs bytes [32u, 32u+32), whose low nibbles are sub-block 2u and high nibbles 2u+1.
+// A thread's raw weight bytes of one super-block quarter, read from the stage before the
+// stage is handed back to the producer (the math runs on these registers afterwards).
+struct Q4Raw {
+    uint4 hd, q0, q1;
+};
+struct Q6Raw {
+    uint4 ql0, ql1, qh;
+    uint32_t dbits, scw;
+};
+
+// Q4_K: quarter u of the super-block at shared address `blk`: its header and qs bytes
+// [32u, 32u+32), whose low nibbles are sub-block 2u and high nibbles 2u+1.
+__device__ __forceinline__ Q4Raw q4k_load(uint32_t blk, int u, bool valid) {
+    Q4Raw r{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (valid) {
+        r.hd = lds128(blk);
+        r.q0 = lds128(blk + 16 + 32 * u);
+        r.q1 = lds128(blk + 32 + 32 * u);
+    }
+    return r;
+}
+
+// Q4_K quarter math (row n, super-block sbi of the row) on the loaded bytes
 template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n,
+__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, const Q4Raw &raw, int64_t n,
                                             uint32_t sbi, int u, bool valid, float (&part)[MT]) {
     using C = GvCfg<FMT_Q4K>;
-    uint4 hd = make_uint4(0, 0, 0, 0), q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-    if (valid) {
-        hd = lds128(blk);
-        q0 = lds128(blk + 16 + 32 * u);
-        q1 = lds128(blk + 32 + 32 * u);
-    }
+    const uint4 hd = raw.hd, q0 = raw.q0, q1 = raw.q1;
     const float d = half_bits_to_float(hd.x & 0xffff), dmin = half_bits_to_float(hd.x >> 16);
     // the 12 scale bytes: s[0..3] = hd.y, s[4..7] = hd.z, s[8..11] = hd.w; sub-blocks 2u, 2u+1
     int sc0, m0, sc1, m1;
@@ -212,24 +228,30 @@ __device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, ui
 // Q6_K: quarter u -> half h = u/2, l0 = 16*(u%2); values 128h + 32g + l0 + i (g = 0..3, i < 16).
 // Group g takes the low (g < 2) / high (g >= 2) nibble of ql[64h + 32(g&1) + l0 + i] and the
 // high bits (qh[32h + l0 + i] >> 2g) & 3; each group is the 16-value sub-block 8h + 2g + u%2.
-template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, uint32_t blk, int64_t n,
-                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
-    using C = GvCfg<FMT_Q6K>;
+__device__ __forceinline__ Q6Raw q6k_load(uint32_t blk, int u, bool valid) {
     const int h = u >> 1, l0 = 16 * (u & 1);
-    uint4 ql0 = make_uint4(0, 0, 0, 0), ql1 = make_uint4(0, 0, 0, 0), qh = make_uint4(0, 0, 0, 0);
-    float d = 0.0f;
-    uint32_t scw = 0;
+    Q6Raw r{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0u, 0u};
     if (valid) {
-        ql0 = lds128_a2(blk + 64 * h + l0);
-        ql1 = lds128_a2(blk + 64 * h + 32 + l0);
-        qh = lds128_a2(blk + 128 + 32 * h + l0);
-        d = half_bits_to_float(lds16(blk + 208));
+        r.ql0 = lds128_a2(blk + 64 * h + l0);
+        r.ql1 = lds128_a2(blk + 64 * h + 32 + l0);
+        r.qh = lds128_a2(blk + 128 + 32 * h + l0);
+        r.dbits = lds16(blk + 208);
         // scales 8h + (u&1) + {0, 2, 4, 6}: the 8 bytes at 192 + 8h, even or odd ones
         const uint32_t sa = lds16(blk + 192 + 8 * h) | (lds16(blk + 194 + 8 * h) << 16);
         const uint32_t sb = lds16(blk + 196 + 8 * h) | (lds16(blk + 198 + 8 * h) << 16);
-        scw = __byte_perm(sa, sb, (u & 1) ? 0x7531u : 0x6420u);     // 4 int8 scales of groups 0..3
+        r.scw = __byte_perm(sa, sb, (u & 1) ? 0x7531u : 0x6420u);     // 4 int8 scales of groups 0..3
     }
+    return r;
+}
+
+template <int MT, bool ACT, bool DUMP>
+__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, const Q6Raw &raw, int64_t n,
+                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
+    using C = GvCfg<FMT_Q6K>;
+    const int h = u >> 1, l0 = 16 * (u & 1);
+    const uint4 ql0 = raw.ql0, ql1 = raw.ql1, qh = raw.qh;
+    const float d = half_bits_to_float(raw.dbits);
+    const uint32_t scw = raw.scw;
     // 6-bit codes (q + 32) of the four groups
     uint4 v[4];
 #pragma unroll
@@ -469,18 +491,26 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         const int nsb = j == last ? nsb_last : C::TU;
         const uint32_t sbase = ring + (uint32_t)(s * C::STAGE);
         float part[C::PASSES][MT];
+        if constexpr (FMT == FMT_Q6K) {
+            // one pass: read this thread's weight bytes, hand the stage back to the producer,
+            // then do the math on registers (the refill overlaps the dp4a work)
+            static_assert(C::PASSES == 1, "Q6_K takes one pass per unit");
+            const Q6Raw raw = q6k_load(sbase + (uint32_t)(slot * C::BB), u, slot < nsb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
+            q6k_quarter<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+        } else {
+            // two passes, each loading and computing in turn (fewer live registers); the stage
+            // goes back after the last one
 #pragma unroll
-        for (int ps = 0; ps < C::PASSES; ++ps) {
-            const int idx = ps * kSbPerPass + slot;
-            const bool valid = idx < nsb;
-            const uint32_t blk = sbase + (uint32_t)(idx * C::BB);
-            if constexpr (FMT == FMT_Q4K)
-                q4k_quarter<MT, ACT, DUMP>(a, at, blk, t_row[ps], t_sbi[ps], u, valid, part[ps]);
-            else
-                q6k_quarter<MT, ACT, DUMP>(a, at, blk, t_row[ps], t_sbi[ps], u, valid, part[ps]);
+            for (int ps = 0; ps < C::PASSES; ++ps) {
+                const int idx = ps * kSbPerPass + slot;
+                const Q4Raw raw = q4k_load(sbase + (uint32_t)(idx * C::BB), u, idx < nsb);
+                q4k_quarter<MT, ACT, DUMP>(a, at, raw, t_row[ps], t_sbi[ps], u, idx < nsb, part[ps]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);   // stage fully read: the producer may refill it
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);       // stage fully read: the producer may refill it
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps)
 #pragma unroll
