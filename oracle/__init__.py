@@ -42,6 +42,9 @@ def lib():
         L.oq_q6k_dequant.argtypes = [P, I64, I64, P]
         L.oq_rmsnorm.argtypes = [P, I64, I64, P, F32, P]
         L.oq_quantize_q8.argtypes = [P, I64, I64, P, P, P]
+        L.oq_exp_f32.argtypes = [F32]
+        L.oq_exp_f32.restype = F32
+        L.oq_swiglu.argtypes = [P, P, I64, I64, P]
         for f in (L.oq_q4k_blockdots, L.oq_q6k_blockdots):
             f.argtypes = [P, I64, I64, P, I64, P, I64, P, I64, P, P]
         for f in (L.oq_q4k_matmul, L.oq_q6k_matmul):
@@ -104,6 +107,25 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     y = np.empty_like(x)
     lib().oq_rmsnorm(_p(x), m, k, _p(w), float(eps), _p(y))
     return y
+
+
+def exp_f32(x: float) -> float:
+    return float(lib().oq_exp_f32(float(x)))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """y = silu(g) * u in f32 (C8)."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    assert g.shape == u.shape and g.ndim == 2
+    y = np.empty_like(g)
+    lib().oq_swiglu(_p(g), _p(u), g.shape[0], g.shape[1], _p(y))
+    return y
+
+
+def quantize_swiglu_q8(g: np.ndarray, u: np.ndarray):
+    """Q8 plane of silu(g) * u -> (q, d, S)."""
+    return quantize_q8(swiglu(g, u))
 
 
 def quantize_q8(x: np.ndarray, rms_w: np.ndarray | None = None, eps: float = 1e-6):

@@ -21,6 +21,9 @@
  *   C5  integer block dots between decoded weight quants and Q8 codes
  *   C6  float scaling of the block dots into f32 outputs (accumulated in f64)
  *   C7  the per-(token, row, 32-block) integer checkpoint I
+ *   C8  SwiGLU producer y = silu(g) * u, silu(g) = g / (1 + exp(-g)), then C3 on y
+ *       ("Features > GPU -- CUDA": the swiglu producer emits the q8 plane directly;
+ *       "Compute Graph Design > 5": Mul(Silu(X), Y) is rewritten to SwiGLU)
  *
  * The byte layouts are not printed on the pages; they are the public GGML
  * k-quant formats that the pages name.  Rounding of Q8 is half away from zero
@@ -187,6 +190,44 @@ void oq_rmsnorm(const float *x, int64_t M, int64_t K, const float *w, float eps,
  *   S = sum q (int32).
  * Outputs in the oracle's own logical layout: q[M][K], d[M][K/32], S[M][K/32].
  */
+/*
+ * C8: the pages fix no precision for SwiGLU.  The reading used on both sides: IEEE f32,
+ * every step rounded once, and exp(x) evaluated by the textbook reduction written out
+ * here -- x = k ln2 + r with k = nearest integer to x / ln2 (ties to even) and
+ * |r| <= ln2 / 2, exp(r) by its Taylor series through r^7 (truncation error below
+ * 6e-9 relative), times 2^k -- so that the f32 value of y, and with it every Q8 code,
+ * is one fixed function of (g, u).  x is clamped to [-86, 88] (exp stays a normal f32;
+ * silu(g) is unaffected in f32 beyond that range: 1 + exp(-86) == 1, and for g < -88
+ * the result is below 1e-36).
+ */
+float oq_exp_f32(float x)
+{
+    if (x > 88.0f) x = 88.0f;
+    if (x < -86.0f) x = -86.0f;
+    const float k = rintf(x * 1.44269504f);                 /* 1 / ln2 */
+    float r = fmaf(-k, 0.693145751953125f, x);               /* ln2, high part (k * hi is exact) */
+    r = fmaf(-k, 1.42860677e-06f, r);                        /* ln2, low part */
+    float p = 1.98412698e-04f;                               /* 1/7! */
+    p = fmaf(p, r, 1.38888889e-03f);                         /* 1/6! */
+    p = fmaf(p, r, 8.33333333e-03f);                         /* 1/5! */
+    p = fmaf(p, r, 4.16666667e-02f);                         /* 1/4! */
+    p = fmaf(p, r, 1.66666667e-01f);                         /* 1/3! */
+    p = fmaf(p, r, 0.5f);                                    /* 1/2! */
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return ldexpf(p, (int)k);
+}
+
+void oq_swiglu(const float *g, const float *u, int64_t M, int64_t K, float *y)
+{
+    for (int64_t i = 0; i < M * K; ++i) {
+        const float e = oq_exp_f32(-g[i]);
+        const float den = 1.0f + e;
+        const float s = g[i] / den;                          /* silu(g) */
+        y[i] = s * u[i];
+    }
+}
+
 void oq_quantize_q8(const float *x, int64_t M, int64_t K, int8_t *q, float *d, int32_t *S)
 {
     int64_t nblk = K / OQ_Q8;
