@@ -432,6 +432,10 @@ def main():
     q6k_tflops = pf.gemm_q6k_ops / (k_ms[4] * 1e-3) / 1e12
     qrms_gbs = (pf.M * pf.H * 4 + pf.H * 4 + B.mq_q8_plane_bytes(pf.M, pf.H)) / (k_ms[0] * 1e-3) / 1e9
     q_gbs = (pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (k_ms[3] * 1e-3) / 1e9
+    # the SwiGLU producer (NEXT row, not part of config 2's step): the down projection's plane
+    # from this step's gate / up outputs
+    swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f), K, W)
+    swiglu_gbs = (2 * pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (swiglu_ms * 1e-3) / 1e9
 
     # ---------------- e2e through host buffers
     pf.e2e_setup()
@@ -453,6 +457,8 @@ def main():
                        "quantize": k_ms[3], "gemm_q6k_down": k_ms[4]},
         "kernels_rate": {"gemm_q4k_tops": q4k_tflops, "gemm_q6k_tops": q6k_tflops,
                          "rms_quantize_gbs": qrms_gbs, "quantize_gbs": q_gbs},
+        "swiglu_quantize": {"what": "SwiGLU-fused Q8 producer of the down projection, 3314 x 18944 "
+                                    "(gate / up outputs of the step)", "ms": swiglu_ms, "GB/s": swiglu_gbs},
         "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak,
                      "traffic": TRAFFIC_GEMM_Q4K_GATE,

@@ -110,6 +110,23 @@ MQ_API int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms
                    void *plane, mq_stream_t stream);
 
 /*
+ * mq_quantize_swiglu_q8 -- the SwiGLU producer of the down projection: writes the Q8 plane
+ * of y = silu(gate) * up, silu(g) = g / (1 + exp(-g)), with no f32 intermediate in memory.
+ * "Features > GPU -- CUDA": the swiglu producer emits the q8 plane directly; "Compute Graph
+ * Design > 5": Mul(Silu(X), Y) is the SwiGLU pattern.
+ *
+ *   gate, up  f32 [M][K] (token-major), each 16-byte aligned, read only
+ *   plane     as for mq_quantize_q8
+ *
+ * y is computed in IEEE f32 with every step rounded once; exp is the textbook reduction
+ * x = k ln2 + r (k nearest to x / ln2, ties to even), exp(r) by its Taylor series through
+ * r^7, times 2^k, with x clamped to [-86, 88].  Then the Q8 quantization of mq_quantize_q8
+ * applies to y.  Same errors as mq_quantize_q8 (M == 0 is a no-op).
+ */
+MQ_API int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t K, void *plane,
+                                 mq_stream_t stream);
+
+/*
  * mq_gemm_q4k / mq_gemm_q6k -- prefill GEMM (MMQ) on the tensor cores.
  * "Features > GPU -- CUDA": raw-nibble GEMMs for q4_K and q6_K over the Q8
  * plane; "Support Matrix > CUDA notes": prefill (nt >= 16) takes this path.

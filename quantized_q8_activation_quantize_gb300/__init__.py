@@ -6,4 +6,4 @@ tensors into it, ``inputs`` makes the seeded synthetic workloads.
 """
 from .binding import (MQError, alloc_plane, matmul, mq_debug_blockdots, mq_debug_forced_timeout,  # noqa: F401
                       mq_device_status, mq_gemm_q4k, mq_gemm_q6k, mq_gemv_q4k, mq_gemv_q6k, mq_q8_plane_bytes,
-                      mq_q8_plane_layout, mq_quantize_q8, plane_views)
+                      mq_q8_plane_layout, mq_quantize_q8, mq_quantize_swiglu_q8, plane_views)

@@ -56,6 +56,7 @@ def lib():
         L.mq_q8_plane_bytes.restype = ctypes.c_size_t
         L.mq_q8_plane_layout.argtypes = [I64, I64, ctypes.POINTER(PlaneLayout)]
         L.mq_quantize_q8.argtypes = [P, I64, I64, P, ctypes.c_float, P, P]
+        L.mq_quantize_swiglu_q8.argtypes = [P, P, I64, I64, P, P]
         for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
         L.mq_device_status.argtypes = [P]
@@ -134,6 +135,10 @@ def plane_views(plane, M: int, K: int, with_ds: bool = False):
 
 def mq_quantize_q8(x, M: int, K: int, rms_w, eps: float, plane, stream=None):
     return _check(lib().mq_quantize_q8(_ptr(x), M, K, _ptr(rms_w), float(eps), _ptr(plane), _stream(stream)))
+
+
+def mq_quantize_swiglu_q8(gate, up, M: int, K: int, plane, stream=None):
+    return _check(lib().mq_quantize_swiglu_q8(_ptr(gate), _ptr(up), M, K, _ptr(plane), _stream(stream)))
 
 
 def _matmul(name, w, N, K, plane, M, y, stream):

@@ -262,6 +262,28 @@ int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, flo
     return launch_quantize(x, M, K, rms_w, eps, p, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t K, void *plane, mq_stream_t stream) {
+    if (M < 0) return set_error(MQ_ERR_ARG, "mq_quantize_swiglu_q8: negative M=%lld", (long long)M);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    if (M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "mq_quantize_swiglu_q8: M=%lld must be below 2^31", (long long)M);
+    if (M == 0) return MQ_OK;
+    if (!gate || !up || !plane)
+        return set_error(MQ_ERR_ARG, "mq_quantize_swiglu_q8: NULL pointer (gate=%p up=%p plane=%p)", (const void *)gate,
+                         (const void *)up, plane);
+    if (!aligned(gate, 16) || !aligned(up, 16))
+        return set_error(MQ_ERR_ALIGN, "mq_quantize_swiglu_q8: gate %p / up %p not 16-byte aligned", (const void *)gate,
+                         (const void *)up);
+    if (!aligned(plane, 256))
+        return set_error(MQ_ERR_ALIGN, "mq_quantize_swiglu_q8: plane %p not 256-byte aligned", plane);
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    Plane p;
+    plane_from(plane, M, K, &p);
+    return launch_swiglu_quantize(gate, up, M, K, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mq_gemm_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
     return run_matmul(0, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }

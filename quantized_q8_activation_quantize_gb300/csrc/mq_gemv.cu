@@ -62,6 +62,7 @@ struct GvCfg {
 };
 constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
 constexpr int kThirdCta = 74 * 1024;                 // a CTA this small leaves room for three per SM
+constexpr int kSecondCta = 112 * 1024;               // ... and this small for two
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -552,12 +553,13 @@ template <int FMT, int MT, bool ACT, bool DUMP>
 int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     using C = GvCfg<FMT>;
     auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
-    // the deepest ring that fits, made shallower (down to 2 stages) when that lets a third
-    // CTA share the SM (the register budget allows three only for MT <= 2)
+    // the deepest ring that fits, made shallower (down to 2 stages) when that lets the SM
+    // hold as many CTAs as the registers allow: three for MT <= 2, two otherwise
+    const int per_sm_smem = MT <= 2 ? kThirdCta : kSecondCta;
     a.nst = C::STAGES;
     while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kSmemMax) --a.nst;
-    if (MT <= 2 && gemv_smem<FMT, MT, ACT>(2, a.K) <= kThirdCta)
-        while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kThirdCta) --a.nst;
+    if (gemv_smem<FMT, MT, ACT>(2, a.K) <= per_sm_smem)
+        while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > per_sm_smem) --a.nst;
     const int smem = (int)gemv_smem<FMT, MT, ACT>(a.nst, a.K);
     constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);

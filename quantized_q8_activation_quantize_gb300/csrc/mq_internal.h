@@ -65,6 +65,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // launchers (arguments already validated); return MQ_OK or MQ_ERR_CUDA
 int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,
                     unsigned int *err, cudaStream_t stream);
+int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, const Plane &p, cudaStream_t stream);
 int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
 int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,

@@ -88,6 +88,56 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     }
 }
 
+// SwiGLU producer ("Features > GPU -- CUDA": the swiglu producer emits the q8 plane directly;
+// "Compute Graph Design > 5": Mul(Silu(X), Y) -> SwiGLU): y = silu(g) * u in IEEE f32, every
+// step rounded once, then the Q8 quantization of y.  exp is evaluated by the textbook
+// reduction: x = k ln2 + r, k = nearest integer to x / ln2 (ties to even), |r| <= ln2 / 2,
+// exp(r) by its Taylor series through r^7, times 2^k; x is clamped to [-86, 88] so the
+// result stays a normal f32 (in f32, silu is unaffected outside that range).  Every step is
+// an explicitly rounded operation, so y -- and every Q8 code -- is one fixed function of
+// (g, u).
+__device__ __forceinline__ float exp_f32(float x) {
+    x = x > 88.0f ? 88.0f : x;
+    x = x < -86.0f ? -86.0f : x;
+    const float k = rintf(__fmul_rn(x, 1.44269504f));         // 1 / ln2
+    float r = fmaf(-k, 0.693145751953125f, x);                  // ln2, high part (k * hi is exact)
+    r = fmaf(-k, 1.42860677e-06f, r);                           // ln2, low part
+    float p = 1.98412698e-04f;                                  // 1/7!
+    p = fmaf(p, r, 1.38888889e-03f);                            // 1/6!
+    p = fmaf(p, r, 8.33333333e-03f);                            // 1/5!
+    p = fmaf(p, r, 4.16666667e-02f);                            // 1/4!
+    p = fmaf(p, r, 1.66666667e-01f);                            // 1/3!
+    p = fmaf(p, r, 0.5f);                                       // 1/2!
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return ldexpf(p, (int)k);
+}
+
+__device__ __forceinline__ float swiglu1(float g, float u) {
+    const float den = __fadd_rn(1.0f, exp_f32(-g));
+    return __fmul_rn(__fdiv_rn(g, den), u);
+}
+
+__global__ void __launch_bounds__(256) swiglu_quantize_kernel(const float *__restrict__ g, const float *__restrict__ up,
+                                                              int64_t M, int64_t K, Plane p) {
+    grid_dep_launch();
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const uint32_t nch = (uint32_t)(K / 256);
+    const int64_t items = M * (int64_t)nch;
+    const int64_t stride = (int64_t)gridDim.x * 8;
+    for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += stride) {
+        const int64_t m = (it < 0xffffffffll) ? (int64_t)((uint32_t)it / nch) : it / (int64_t)nch;
+        const int64_t k0 = (it - m * (int64_t)nch) * 256 + lane * 8;
+        const float4 *gs = reinterpret_cast<const float4 *>(g + m * K + k0);
+        const float4 *us = reinterpret_cast<const float4 *>(up + m * K + k0);
+        const float4 ga = __ldg(gs), gb = __ldg(gs + 1), ua = __ldg(us), ub = __ldg(us + 1);
+        const float v[8] = {swiglu1(ga.x, ua.x), swiglu1(ga.y, ua.y), swiglu1(ga.z, ua.z), swiglu1(ga.w, ua.w),
+                            swiglu1(gb.x, ub.x), swiglu1(gb.y, ub.y), swiglu1(gb.z, ub.z), swiglu1(gb.w, ub.w)};
+        quantize8(v, lane, p, M, K, m, k0);
+    }
+}
+
 // RMSNorm producer: one CTA per token.  Pass 1 sums x^2 in f64 (each square is exact
 // in f64); r = (float)(1 / sqrt(sum/K + eps)) is rounded once; pass 2 re-reads the row
 // (L2-resident) and quantizes y = fl(fl(x * r) * w).
@@ -157,6 +207,16 @@ int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, fl
         e = launch_pdl(rms_quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, rms_w, eps, p);
     }
     return cuda_error(e, "quantize launch");
+}
+
+int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, const Plane &p, cudaStream_t stream) {
+    const int nsm = sm_count();
+    const int64_t warps = M * (K / 256);
+    int64_t ctas = (warps + 7) / 8;
+    const int64_t cap = (int64_t)nsm * 8;
+    if (ctas > cap) ctas = cap;
+    return cuda_error(launch_pdl(swiglu_quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, g, up, M, K, p),
+                      "swiglu quantize launch");
 }
 
 }  // namespace mq

@@ -25,6 +25,7 @@ import numpy as np
 
 SEED_BASE = 20261202
 STREAM_W, STREAM_X, STREAM_RMS_W, STREAM_OUTLIERS = 0, 1, 2, 3
+STREAM_SWIGLU = 4            # gate / up inputs of the SwiGLU producer
 
 QK_K = 256             # values per k-quant super-block
 Q8_BLOCK = 32          # values per Q8 activation block
@@ -101,6 +102,17 @@ def outlier_channels(r: np.random.Generator, k: int, fraction: float = 0.01) -> 
     return np.sort(r.permutation(k)[:n])
 
 
+def swiglu_inputs(r: np.random.Generator, m: int, k: int):
+    """Gate and up projections [m, k] f32 for the SwiGLU producer: N(0, 4^2) and N(0, 2^2)
+    (the spread of the config-2 gate / up outputs), a few gate values pushed into the
+    tails where exp saturates."""
+    g = (4.0 * r.standard_normal((m, k))).astype(np.float32)
+    u = (2.0 * r.standard_normal((m, k))).astype(np.float32)
+    idx = r.integers(0, g.size, size=max(1, g.size // 1000))
+    g.flat[idx] = r.choice(np.array([-120.0, -90.0, -87.5, -30.0, 30.0, 87.5, 90.0, 120.0], np.float32), idx.size)
+    return g, u
+
+
 def rms_weight(r: np.random.Generator, k: int) -> np.ndarray:
     """RMSNorm weight [k] drawn N(1, 0.1) in f32."""
     return (1.0 + 0.1 * r.standard_normal(k)).astype(np.float32)
@@ -175,6 +187,11 @@ def config3_matrix(layer: int, idx: int):
 def config4_weights():
     """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
     return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
+
+
+def config2_swiglu(m: int = PREFILL_TOKENS):
+    """The down projection's SwiGLU producer inputs at the config-2 size: gate, up m x 18944."""
+    return swiglu_inputs(rng(2, STREAM_SWIGLU), m, FFN)
 
 
 def config4_x(m: int):

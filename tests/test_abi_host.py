@@ -17,7 +17,8 @@ def L():
     return B.lib()
 
 
-EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quantize_q8", "mq_gemm_q4k",
+EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quantize_q8", "mq_quantize_swiglu_q8",
+            "mq_gemm_q4k",
             "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_device_status", "mq_debug_blockdots",
             "mq_debug_forced_timeout"}
 
@@ -74,6 +75,19 @@ def test_quantize_argument_errors(L):
     assert q(16, 4, 256, None, 0.0, 128, None) == B.MQ_ERR_ALIGN     # plane not 256-byte aligned
     assert q(16, 4, 256, 32, float("nan"), 256, None) == B.MQ_ERR_ARG
     assert q(16, 4, 256, 32, -1.0, 256, None) == B.MQ_ERR_ARG
+
+
+def test_swiglu_quantize_argument_errors(L):
+    q = L.mq_quantize_swiglu_q8
+    assert q(16, 32, 4, 100, 256, None) == B.MQ_ERR_SHAPE
+    assert q(16, 32, -1, 256, 256, None) == B.MQ_ERR_ARG
+    assert q(16, 32, 0, 256, 256, None) == B.MQ_OK                     # empty: nothing to do
+    assert q(None, 32, 4, 256, 256, None) == B.MQ_ERR_ARG
+    assert q(16, None, 4, 256, 256, None) == B.MQ_ERR_ARG
+    assert q(16, 32, 4, 256, None, None) == B.MQ_ERR_ARG
+    assert q(20, 32, 4, 256, 256, None) == B.MQ_ERR_ALIGN              # gate not 16-byte aligned
+    assert q(16, 36, 4, 256, 256, None) == B.MQ_ERR_ALIGN              # up not 16-byte aligned
+    assert q(16, 32, 4, 256, 128, None) == B.MQ_ERR_ALIGN              # plane not 256-byte aligned
 
 
 @pytest.mark.parametrize("name", ["mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k"])
