@@ -150,10 +150,10 @@ MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
 
 /*
  * mq_gemv_q4k / mq_gemv_q6k -- decode GEMV (MMVQ): streams every weight byte
- * once per group of up to 8 tokens and takes dp4a int8 dots per block
- * ("Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ kernels).
- * Same arguments, same result definition as the GEMMs.  Meant for M < 16
- * (any M >= 0 is accepted; each further group of 8 tokens streams W again).
+ * once per group of up to 8 (Q4_K) or 4 (Q6_K) tokens and takes dp4a int8 dots
+ * per block ("Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ
+ * kernels).  Same arguments, same result definition as the GEMMs.  Meant for
+ * M < 16 (any M >= 0 is accepted; each further token group streams W again).
  */
 MQ_API int mq_gemv_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
                 float *y, mq_stream_t stream);

@@ -4,27 +4,28 @@
 // kernels; "Roadmap > 0": the decode path streams the weights once per token.
 //
 // Design (HBM-bound): every weight byte is read from HBM exactly once per group of up
-// to 8 tokens.  The weight matrix is one flat stream of super-blocks (row-major, rows
-// contiguous).  Each CTA owns a contiguous range of whole rows and walks it in units of
-// TU super-blocks (a unit may start or end inside a row):
-//   * a producer warp refills a 4-stage shared-memory ring with ONE large 1-D bulk copy
+// to 8 (Q4_K) or 4 (Q6_K) tokens.  The weight matrix is one flat stream of super-blocks
+// (row-major, rows contiguous).  Each CTA owns a contiguous range of whole rows and walks
+// it in units of TU super-blocks (a unit may start or end inside a row):
+//   * a producer warp refills a 2-5 stage shared-memory ring with ONE large 1-D bulk copy
 //     (TMA engine) per unit -- the 16-byte aligned superset of the unit's bytes, so the
 //     2-byte aligned 210-byte Q6_K block needs no special load path.  A few large copies
 //     per SM keep the copy engine streaming at full HBM rate, where many small per-warp
 //     copies stall it;
-//   * 8 consumer warps take 4 threads per super-block, each owning 64 of its 256 values
-//     (scale decoding and float work amortize over 64 values): dp4a against the int8
-//     codes, f32 scaling per 32-value block, a 4-lane reduction, and one partial per
-//     (token, super-block) into a ring of partial buffers;
+//   * consumer warps take a super-block with 4 threads (Q4_K, 64 values each) or 2 threads
+//     (Q6_K, one 128-value half each), so the per-unit hand-offs and the scale decoding
+//     amortize over many values: dp4a against the int8 codes, f32 scaling per 32-value
+//     block, a lane reduction, and one partial per (token, super-block) into a ring of
+//     partial buffers;
 //   * a reducer warp sums each row's partials in a fixed order (a row that continues
 //     into the next unit carries its running sum), so results are deterministic, and
 //     writes Y.  Consumers wait for the reducer only when the partial ring is full.
 // The shared-memory data pipe is the scarce resource once the weights stream at full
 // rate: when the tokens' activations fit, each CTA first stages them in shared memory
-// (codes in an XOR-swizzled layout that makes every lane pattern below conflict-free,
-// plus a per-block table of (d_a, d_a * S) pairs -- for Q6_K per 16-value half block,
-// with the -32 code offset folded in), so the inner loop reads 4 wavefronts per 512
-// bytes instead of one scattered L1 line per lane.
+// (codes in a padded layout that spreads every lane pattern below over distinct bank
+// groups, plus per-block scale data: (d_a, d_a * S) for Q4_K; d_a and the -32 code
+// offset as -32 * S16 per 16-value half block for Q6_K, which seeds the dp4a chain), so
+// the inner loop reads 4 wavefronts per 512 bytes instead of one scattered L1 line per lane.
 #include <cuda_fp16.h>
 
 #include "mq_device.cuh"
@@ -33,36 +34,45 @@
 namespace mq {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 2) * 32;   // + producer warp + reducer warp
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kReducerWarp = kConsumerWarps + 1;
-constexpr int kStages = 4;
 constexpr int kPartBufs = 4;
-constexpr int kSbPerPass = kConsumerWarps * 8;         // 4 threads per super-block
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int FMT>
 struct GvCfg {
     static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
+    static constexpr int CW = FMT == FMT_Q4K ? 8 : 4;          // consumer warps
+    static constexpr int TPS = FMT == FMT_Q4K ? 4 : 2;         // consumer threads per super-block
+    static constexpr int THREADS = (CW + 2) * 32;              // + producer warp + reducer warp
+    static constexpr int PRODUCER = CW, REDUCER = CW + 1;
+    static constexpr int SB_PER_PASS = CW * 32 / TPS;          // 64
     static constexpr int PASSES = FMT == FMT_Q4K ? 2 : 1;
-    static constexpr int TU = kSbPerPass * PASSES;     // super-blocks per unit
+    static constexpr int TU = SB_PER_PASS * PASSES;            // super-blocks per unit
     static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 5;  // at most; a launch may use fewer (GvArgs::nst)
+    // tokens per pass over the weights (Q6_K: the staged activations of 8 tokens would leave
+    // room for too few CTAs per SM; two passes of 4 measure faster)
+    static constexpr int MAX_MT = FMT == FMT_Q4K ? 8 : 4;
+    // CTAs per SM the launch aims for (registers: 64K / (THREADS * this))
+    static constexpr int ctas_per_sm(int mt) { return FMT == FMT_Q4K ? (mt <= 2 ? 3 : 2) : (mt <= 2 ? 4 : 3); }
     // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
     static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
     static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
-    // Staged activations, per token: int8 codes with each super-block's two 128-value halves
-    // padded apart (half stride 160 B = 10 bank groups of 16 B, super-block stride SB_STRIDE:
-    // 20 groups for Q6_K, 19 for Q4_K) so that the 8 lanes of every quarter-warp -- two
-    // consecutive super-blocks x four quarters -- read 8 distinct 16-byte bank groups; then
-    // a float2 table per half block (Q6_K: TAB_SB = 128 B per super-block) or block (Q4_K: 64 B).
-    static constexpr uint32_t SB_STRIDE = FMT == FMT_Q6K ? 320 : 304;
-    static constexpr uint32_t TAB_SB = FMT == FMT_Q6K ? 128 : 64;
+    // Staged activations, per token.  Q4_K: int8 codes with each super-block's two 128-value
+    // halves padded apart (half stride 160 B = 10 bank groups of 16 B, super-block stride 304 B
+    // = 19 groups) so that the 8 lanes of every quarter-warp -- two consecutive super-blocks x
+    // four quarters -- read 8 distinct 16-byte bank groups; then a float2 (d_a, d_a * S) table
+    // per block (TAB_SB = 64 B per super-block).  Q6_K: one record per half super-block, the
+    // 128 codes then 4 x 16 B of scale data ((d_a, -32 S16 of the first and second 16 values),
+    // one entry per 32-value block); half stride HALF = 208 B (5 mod 8 groups), super-block
+    // stride 464 B (5 mod 8 groups): a quarter-warp's 8 lanes -- four super-blocks two apart x
+    // two halves -- then hit 8 distinct groups (away from row ends).
+    static constexpr uint32_t SB_STRIDE = FMT == FMT_Q6K ? 464 : 304;
+    static constexpr uint32_t HALF = 208;
+    static constexpr uint32_t TAB_SB = FMT == FMT_Q6K ? 0 : 64;
     static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * (SB_STRIDE + TAB_SB); }
 };
 constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
-constexpr int kThirdCta = 74 * 1024;                 // a CTA this small leaves room for three per SM
-constexpr int kSecondCta = 112 * 1024;               // ... and this small for two
+// the largest dynamic shared memory per CTA that leaves room for n CTAs per SM
+constexpr int per_cta_smem(int n) { return n >= 4 ? 55 * 1024 : n == 3 ? 74 * 1024 : 112 * 1024; }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
@@ -86,6 +96,9 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 __device__ __forceinline__ void sts64(uint32_t addr, float a, float b) {
     asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ float4 lds128f(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -105,8 +118,11 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits) {
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t ma, uint32_t b, uint32_t mb) {
     return (a & ma) | (b & mb);
 }
-__device__ __forceinline__ int dot16(const uint4 &w, const uint4 &a) {
-    return __dp4a((int)w.w, (int)a.w, __dp4a((int)w.z, (int)a.z, __dp4a((int)w.y, (int)a.y, __dp4a((int)w.x, (int)a.x, 0))));
+__device__ __forceinline__ int dot16(const uint4 &w, const uint4 &a, int c = 0) {
+    return __dp4a((int)w.w, (int)a.w, __dp4a((int)w.z, (int)a.z, __dp4a((int)w.y, (int)a.y, __dp4a((int)w.x, (int)a.x, c))));
+}
+__device__ __forceinline__ int dot16w(const uint32_t *w, const uint4 &a, int c) {
+    return __dp4a((int)w[3], (int)a.w, __dp4a((int)w[2], (int)a.z, __dp4a((int)w[1], (int)a.y, __dp4a((int)w[0], (int)a.x, c))));
 }
 
 // x / d (and x % d in rem) for 0 <= x < 2^24 through a float reciprocal (inv_d = 1/d rounded):
@@ -143,9 +159,10 @@ struct GvAct {
 struct Q4Raw {
     uint4 hd, q0, q1;
 };
-struct Q6Raw {
-    uint4 ql0, ql1, qh;
-    uint32_t dbits, scw;
+// Q6_K: half h of a super-block -- ql bytes [64h, 64h+64), qh bytes [128+32h, 128+32h+32),
+// the eight int8 scales 8h .. 8h+7 and the fp16 d.
+struct Q6Half {
+    uint32_t ql[16], qh[8], sc[2], dbits;
 };
 
 // Q4_K: quarter u of the super-block at shared address `blk`: its header and qs bytes
@@ -226,111 +243,106 @@ __device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, co
     }
 }
 
-// Q6_K: quarter u -> half h = u/2, l0 = 16*(u%2); values 128h + 32g + l0 + i (g = 0..3, i < 16).
-// Group g takes the low (g < 2) / high (g >= 2) nibble of ql[64h + 32(g&1) + l0 + i] and the
-// high bits (qh[32h + l0 + i] >> 2g) & 3; each group is the 16-value sub-block 8h + 2g + u%2.
-__device__ __forceinline__ Q6Raw q6k_load(uint32_t blk, int u, bool valid) {
-    const int h = u >> 1, l0 = 16 * (u & 1);
-    Q6Raw r{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0u, 0u};
-    if (valid) {
-        r.ql0 = lds128_a2(blk + 64 * h + l0);
-        r.ql1 = lds128_a2(blk + 64 * h + 32 + l0);
-        r.qh = lds128_a2(blk + 128 + 32 * h + l0);
+// Q6_K: loads half h of the super-block at shared address `blk`.  A 210-byte block sits at
+// a 4-byte or a 2-byte aligned address; AL4 picks the aligned reads, else every word is
+// funnel-shifted out of two aligned neighbours (all reads stay inside the block).
+template <bool AL4>
+__device__ __forceinline__ void q6k_load_half(uint32_t blk, int h, Q6Half &r) {
+    if constexpr (AL4) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) r.ql[k] = lds32(blk + 64 * h + 4 * k);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r.qh[k] = lds32(blk + 128 + 32 * h + 4 * k);
+        r.sc[0] = lds32(blk + 192 + 8 * h);
+        r.sc[1] = lds32(blk + 196 + 8 * h);
         r.dbits = lds16(blk + 208);
-        // scales 8h + (u&1) + {0, 2, 4, 6}: the 8 bytes at 192 + 8h, even or odd ones
-        const uint32_t sa = lds16(blk + 192 + 8 * h) | (lds16(blk + 194 + 8 * h) << 16);
-        const uint32_t sb = lds16(blk + 196 + 8 * h) | (lds16(blk + 198 + 8 * h) << 16);
-        r.scw = __byte_perm(sa, sb, (u & 1) ? 0x7531u : 0x6420u);     // 4 int8 scales of groups 0..3
+    } else {
+        const uint32_t b = blk - 2;     // 4-byte aligned: byte i of the block is byte i + 2 here
+        uint32_t w0 = lds32(b + 64 * h);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t w1 = lds32(b + 64 * h + 4 * k + 4);
+            r.ql[k] = __funnelshift_r(w0, w1, 16);
+            w0 = w1;
+        }
+        w0 = lds32(b + 128 + 32 * h);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w1 = lds32(b + 128 + 32 * h + 4 * k + 4);
+            r.qh[k] = __funnelshift_r(w0, w1, 16);
+            w0 = w1;
+        }
+        const uint32_t s0 = lds32(b + 192 + 8 * h), s1 = lds32(b + 196 + 8 * h), s2 = lds32(b + 200 + 8 * h);
+        r.sc[0] = __funnelshift_r(s0, s1, 16);
+        r.sc[1] = __funnelshift_r(s1, s2, 16);
+        r.dbits = lds32(b + 208) >> 16;
     }
-    return r;
 }
 
+// Q6_K math of one half (row n, super-block sbi of the row).  Group g = 0..3 of the half is
+// the 32-value Q8 block 8 sbi + 4h + g: value 32g + l (l < 32) takes the low (g < 2) or high
+// (g >= 2) nibble of ql[32 (g & 1) + l] and the bits (qh[l] >> 2g) & 3 as its high bits; its
+// two 16-value sub-blocks have the scales 2g and 2g + 1 of the half.  The 6-bit codes are
+// q + 32, so each 16-value dot starts from -32 * S16 (S16: sum of the 16 activation codes)
+// and comes out as the exact sum (q * a); I = sc * x0 + sc' * x1 is the block's integer dot.
 template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q6k_quarter(const GvArgs &a, const GvAct &at, const Q6Raw &raw, int64_t n,
-                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
+__device__ __forceinline__ void q6k_half(const GvArgs &a, const GvAct &at, const Q6Half &r, int64_t n,
+                                         uint32_t sbi, int h, bool valid, float (&part)[MT]) {
     using C = GvCfg<FMT_Q6K>;
-    const int h = u >> 1, l0 = 16 * (u & 1);
-    const uint4 ql0 = raw.ql0, ql1 = raw.ql1, qh = raw.qh;
-    const float d = half_bits_to_float(raw.dbits);
-    const uint32_t scw = raw.scw;
-    // 6-bit codes (q + 32) of the four groups
-    uint4 v[4];
+    float acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+    const uint32_t rec = at.codes + sbi * C::SB_STRIDE + C::HALF * (uint32_t)h;   // token 0's record
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        const uint32_t *L = reinterpret_cast<const uint32_t *>((g & 1) ? &ql1 : &ql0);
-        const uint32_t *H = reinterpret_cast<const uint32_t *>(&qh);
-        uint32_t o[4];
+        const uint32_t *L = (g & 1) ? r.ql + 8 : r.ql;
+        uint32_t v[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t H = r.qh[e];
             const uint32_t lo = (g < 2) ? L[e] : (L[e] >> 4);
-            const uint32_t hb = (g == 0) ? (H[e] << 4) : (g == 1) ? (H[e] << 2) : (g == 2) ? H[e] : (H[e] >> 2);
-            o[e] = lop3_and_or(lo, 0x0f0f0f0fu, hb, 0x30303030u);
+            const uint32_t hb = (g == 0) ? (H << 4) : (g == 1) ? (H << 2) : (g == 2) ? H : (H >> 2);
+            v[e] = lop3_and_or(lo, 0x0f0f0f0fu, hb, 0x30303030u);
         }
-        v[g] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    const int64_t kb = (int64_t)sbi * kQK + 128 * h + l0;
-    const int64_t bq = (int64_t)sbi * 8 + 4 * h;       // Q8 block of group 0
-    float dsc[4];
+        const uint32_t sw = r.sc[g >> 1] >> (16 * (g & 1));
+        const int sc0 = (int)(int8_t)(sw & 0xff), sc1 = (int)(int8_t)((sw >> 8) & 0xff);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) dsc[g] = d * (float)(int8_t)((scw >> (8 * g)) & 0xff);
-    const uint4 c32 = make_uint4(0x20202020u, 0x20202020u, 0x20202020u, 0x20202020u);
-    const uint4 c01 = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        const int64_t m = a.t0 + t;
-        const bool act = t < a.mt && valid;
-        int Dg[4] = {0, 0, 0, 0};
-        part[t] = 0.0f;
-        if (act) {
-            float vsum = 0.0f;
-            if constexpr (ACT) {
-                // codes 128h + 32g + l0 .. +15 of the super-block; table: (d_a, 32 * d_a * S16) of the
-                // four 16-value half blocks, two per 16-byte load (the loads swap on odd sbi)
-                const uint32_t cb = at.codes + (uint32_t)t * at.ck + sbi * C::SB_STRIDE + 160u * (uint32_t)h +
-                                    16u * ((uint32_t)u & 1u);
-                const uint32_t tb = at.tab + (uint32_t)t * at.tk + sbi * C::TAB_SB + 32u * (uint32_t)u;
-                const uint32_t odd = sbi & 1u;
-                const float4 e01 = lds128f(tb + 16u * odd), e23 = lds128f(tb + 16u * (odd ^ 1u));
-                const float de[8] = {e01.x, e01.y, e01.z, e01.w, e23.x, e23.y, e23.z, e23.w};
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint4 av = lds128(cb + 32u * g);
-                    const int Dc = dot16(v[g], av);                       // sum code * a
-                    if constexpr (DUMP) Dg[g] = Dc - 32 * dot16(c01, av);  // exact sum (code - 32) * a
-                    // d_a * (sum code * a) - 32 * d_a * S16, scaled by d * sc
-                    vsum = fmaf(dsc[g], fmaf(de[2 * g], (float)Dc, -de[2 * g + 1]), vsum);
-                }
-            } else {
-                const int8_t *q = a.p.q8 + m * a.K + kb;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint4 av = __ldg(reinterpret_cast<const uint4 *>(q + 32 * g));
-                    // sum (code - 32) * a = sum code * a - sum 32 * a
-                    Dg[g] = dot16(v[g], av) - dot16(c32, av);
-                    vsum += dsc[g] * (float)Dg[g] * __ldg(a.p.d + (bq + g) * a.M + m);
+        for (int t = 0; t < MT; ++t) {
+            const int64_t m = a.t0 + t;
+            const bool act = t < a.mt && valid;
+            int I = 0;
+            if (act) {
+                if constexpr (ACT) {
+                    const uint32_t rt = rec + (uint32_t)t * at.ck;
+                    const uint4 a0 = lds128(rt + 32u * g), a1 = lds128(rt + 32u * g + 16u);
+                    const uint4 tb = lds128(rt + 128u + 16u * g);        // d_a, -32 S16, -32 S16'
+                    const int x0 = dot16w(v, a0, (int)tb.y), x1 = dot16w(v + 4, a1, (int)tb.z);
+                    I = sc0 * x0 + sc1 * x1;
+                    acc[t] = fmaf(__uint_as_float(tb.x), (float)I, acc[t]);
+                } else {
+                    const int8_t *q = a.p.q8 + m * a.K + (int64_t)sbi * kQK + 128 * h + 32 * g;
+                    const uint4 a0 = __ldg(reinterpret_cast<const uint4 *>(q));
+                    const uint4 a1 = __ldg(reinterpret_cast<const uint4 *>(q + 16));
+                    const uint4 c32 = make_uint4(0x20202020u, 0x20202020u, 0x20202020u, 0x20202020u);
+                    const int x0 = dot16w(v, a0, -dot16(c32, a0)), x1 = dot16w(v + 4, a1, -dot16(c32, a1));
+                    I = sc0 * x0 + sc1 * x1;
+                    acc[t] = fmaf(__ldg(a.p.d + ((int64_t)sbi * 8 + 4 * h + g) * a.M + m), (float)I, acc[t]);
                 }
             }
-            part[t] = vsum;
-        }
-        if constexpr (DUMP) {
-            int I[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                I[g] = (int)(int8_t)((scw >> (8 * g)) & 0xff) * Dg[g];
-                I[g] += __shfl_xor_sync(kFull, I[g], 1);       // the two 16-value halves of the Q8 block
-            }
-            const Dump &dp = a.dump;
-            if (act && (u & 1) == 0 && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt) {
-                int32_t *o = dp.out + ((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) o[bq + g] = I[g];
+            if constexpr (DUMP) {
+                const Dump &dp = a.dump;
+                if (act && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt)
+                    dp.out[((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8) + (int64_t)sbi * 8 + 4 * h + g] = I;
             }
         }
     }
+    const float d = half_bits_to_float(r.dbits);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) part[t] = d * acc[t];
 }
 
 template <int FMT, int MT, bool ACT, bool DUMP>
-__global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs a) {
+__global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(MT)) gemv_kernel(GvArgs a) {
     using C = GvCfg<FMT>;
     const int S = a.nst;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -341,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kConsumerWarps); }
-        for (int i = 0; i < kPartBufs; ++i) { mbar_init(&pfull[i], kConsumerWarps); mbar_init(&pempty[i], 1); }
+        for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], C::CW); }
+        for (int i = 0; i < kPartBufs; ++i) { mbar_init(&pfull[i], C::CW); mbar_init(&pempty[i], 1); }
         abort_flag = 0;
         mbar_init_fence();
     }
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         a1 = ((sb0 + nsb) * C::BB + 15) & ~(int64_t)15;
     };
 
-    if (warp == kProducerWarp) {
+    if (warp == C::PRODUCER) {
         if (lane != 0) return;
         // while the predecessor on the stream finishes: pull the first units into L2 (a hint,
         // safe whatever the predecessor writes), then wait for it before the real copies
@@ -393,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
         return;
     }
 
-    if (warp == kReducerWarp) {
+    if (warp == C::REDUCER) {
         // unit j covers flat super-blocks [sb0, sb0 + nsb); its first row is r_row0 and the
         // unit starts r_sbi0 super-blocks into it
         uint32_t r_sbi0 = 0;
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
     grid_dep_wait();
     GvAct at{0, 0, 0, 0};
     if constexpr (ACT) {
-        // stage the tokens' codes (padded layout) and the scale table
+        // stage the tokens' codes (padded layout) and their scale data
         at.codes = smem_u32(partbuf) + (uint32_t)C::part_bytes(MT);
         at.ck = nb * C::SB_STRIDE;
         at.tab = at.codes + MT * at.ck;
@@ -442,19 +454,23 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
             const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);
             const uint32_t cbase = at.codes + (uint32_t)t * at.ck, tbase = at.tab + (uint32_t)t * at.tk;
             // all of an iteration's global loads go out before its stores (one latency round)
-            for (uint32_t c = tid; c < nch; c += kConsumerWarps * 32) {
+            for (uint32_t c = tid; c < nch; c += C::CW * 32) {
                 const uint4 v = __ldg(src + c);
                 const uint32_t sbi = c >> 4, r = c & 15u;     // chunk r of super-block sbi
                 if constexpr (FMT == FMT_Q6K) {
-                    const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
-                    sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
-                    // half block c: (d_a, 32 * d_a * S16) at [sbi][u][g], where chunk r is
-                    // group g = (r >> 1) & 3 of quarter u = 2 (r >> 3) + (r & 1); the two
-                    // 16-byte halves of each quarter's entries swap on odd sbi
+                    // chunk r: half r >> 3, block g = (r >> 1) & 3 of it, its 16-value sub-block
+                    // r & 1; the block's entry holds (d_a, -32 S16, -32 S16') at 128 + 16 g
+                    const uint32_t rec = cbase + sbi * C::SB_STRIDE + C::HALF * (r >> 3);
+                    sts128(rec + 16u * (r & 7u), v);
                     const int s16 = dot16(v, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u));
-                    const uint32_t g = (r >> 1) & 3u, uu = 2u * (r >> 3) + (r & 1u);
-                    sts64(tbase + sbi * C::TAB_SB + 32u * uu + 16u * ((g >> 1) ^ (sbi & 1u)) + 8u * (g & 1u), da,
-                          da * (float)(32 * s16));
+                    const uint32_t ent = rec + 128u + 16u * ((r >> 1) & 3u);
+                    if (r & 1u) {
+                        sts32(ent + 8u, (uint32_t)(-32 * s16));
+                    } else {
+                        const float da = __ldg(a.p.d + (int64_t)(c >> 1) * a.M + m);
+                        sts32(ent, __float_as_uint(da));
+                        sts32(ent + 4u, (uint32_t)(-32 * s16));
+                    }
                 } else {
                     // block c (< K/32): (d_a, d_a * S)
                     const bool blk = c < nb * 8u;
@@ -465,10 +481,14 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
                 }
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(C::CW * 32) : "memory");
     }
 
-    const int u = tid & 3, slot = tid >> 2;          // quarter, and super-block slot within a pass
+    // super-block slot within a pass, and the thread's part of it: Q4_K quarter u = tid % 4 of
+    // slot tid / 4; Q6_K half u = lane % 2, warps alternating between even and odd slots (so a
+    // warp's blocks share one alignment mod 4): slot 2 (16 (warp / 2) + lane / 2) + warp % 2
+    const int u = FMT == FMT_Q4K ? (tid & 3) : (lane & 1);
+    const int slot = FMT == FMT_Q4K ? (tid >> 2) : 2 * (16 * (warp >> 1) + (lane >> 1)) + (warp & 1);
     // this thread's super-block of each pass: offset in its row (and the row, for the dump);
     // both advance by TU super-blocks per unit
     const uint32_t tu_mod = (uint32_t)C::TU % nb, tu_div = (uint32_t)C::TU / nb;
@@ -477,13 +497,16 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
 #pragma unroll
     for (int ps = 0; ps < C::PASSES; ++ps) {
         uint32_t r;
-        t_row[ps] = row_begin + divmod_small((uint32_t)(ps * kSbPerPass + slot), nb, inv_nb, r);
+        t_row[ps] = row_begin + divmod_small((uint32_t)(ps * C::SB_PER_PASS + slot), nb, inv_nb, r);
         t_sbi[ps] = r;
     }
     const uint32_t off15 = (uint32_t)((sb_begin * C::BB) & 15);   // units start 16-byte aligned after that
     const int last = units - 1;
     const int nsb_last = (int)(sb_total - (int64_t)last * C::TU);
     const uint32_t ring = smem_u32(smem) + off15;
+    // the stage base and 210 * (even slot) are multiples of 4, so a Q6_K warp's blocks are all
+    // 4-byte aligned or all 2 mod 4
+    const bool al4 = ((off15 + 2u * (uint32_t)(warp & 1)) & 2u) == 0;
     int s = 0, pb = 0;
     uint32_t ph = 0, pph = 0;
     for (int j = 0; j < units; ++j) {
@@ -496,16 +519,21 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
             // one pass: read this thread's weight bytes, hand the stage back to the producer,
             // then do the math on registers (the refill overlaps the dp4a work)
             static_assert(C::PASSES == 1, "Q6_K takes one pass per unit");
-            const Q6Raw raw = q6k_load(sbase + (uint32_t)(slot * C::BB), u, slot < nsb);
+            Q6Half raw;
+            const uint32_t blk = sbase + (uint32_t)(slot * C::BB);
+            if (al4)
+                q6k_load_half<true>(blk, u, raw);
+            else
+                q6k_load_half<false>(blk, u, raw);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
-            q6k_quarter<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+            q6k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
         } else {
             // two passes, each loading and computing in turn (fewer live registers); the stage
             // goes back after the last one
 #pragma unroll
             for (int ps = 0; ps < C::PASSES; ++ps) {
-                const int idx = ps * kSbPerPass + slot;
+                const int idx = ps * C::SB_PER_PASS + slot;
                 const Q4Raw raw = q4k_load(sbase + (uint32_t)(idx * C::BB), u, idx < nsb);
                 q4k_quarter<MT, ACT, DUMP>(a, at, raw, t_row[ps], t_sbi[ps], u, idx < nsb, part[ps]);
             }
@@ -517,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 part[ps][t] += __shfl_xor_sync(kFull, part[ps][t], 1);
-                part[ps][t] += __shfl_xor_sync(kFull, part[ps][t], 2);
+                if constexpr (C::TPS == 4) part[ps][t] += __shfl_xor_sync(kFull, part[ps][t], 2);
             }
         const bool pgot = j < kPartBufs || mbar_wait(&pempty[pb], pph ^ 1u, a.err, ERR_GEMV_FULL, abort);
         if (!__all_sync(kFull, pgot)) break;
@@ -527,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 2) gemv_kernel(GvArgs 
             for (int ps = 0; ps < C::PASSES; ++ps)
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
-                    if (t < a.mt) pbuf[t * C::TU + ps * kSbPerPass + slot] = part[ps][t];
+                    if (t < a.mt) pbuf[t * C::TU + ps * C::SB_PER_PASS + slot] = part[ps][t];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[pb]);
@@ -553,23 +581,23 @@ template <int FMT, int MT, bool ACT, bool DUMP>
 int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     using C = GvCfg<FMT>;
     auto kern = gemv_kernel<FMT, MT, ACT, DUMP>;
-    // the deepest ring that fits, made shallower (down to 2 stages) when that lets the SM
-    // hold as many CTAs as the registers allow: three for MT <= 2, two otherwise
-    const int per_sm_smem = MT <= 2 ? kThirdCta : kSecondCta;
+    // the most CTAs per SM (up to what the registers allow, GvCfg::ctas_per_sm) whose shared
+    // memory still fits with a 2-stage ring, then the deepest ring that keeps that many
+    int budget = kSmemMax;
+    for (int n = C::ctas_per_sm(MT); n >= 2; --n)
+        if (gemv_smem<FMT, MT, ACT>(2, a.K) <= per_cta_smem(n)) { budget = per_cta_smem(n); break; }
     a.nst = C::STAGES;
-    while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > kSmemMax) --a.nst;
-    if (gemv_smem<FMT, MT, ACT>(2, a.K) <= per_sm_smem)
-        while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > per_sm_smem) --a.nst;
+    while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > budget) --a.nst;
     const int smem = (int)gemv_smem<FMT, MT, ACT>(a.nst, a.K);
     constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2 + (DUMP ? 1 : 0);
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);
     if (rc != MQ_OK) return rc;
     int per_sm = 0;
-    rc = resident_ctas(reinterpret_cast<const void *>(kern), kThreads, smem, slot, &per_sm);
+    rc = resident_ctas(reinterpret_cast<const void *>(kern), C::THREADS, smem, slot, &per_sm);
     if (rc != MQ_OK) return rc;
     int64_t ctas = (int64_t)nsm * per_sm;
     if (ctas > a.N) ctas = a.N;                      // every CTA owns at least one row
-    return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), smem, stream, a), "gemv launch");
+    return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a), "gemv launch");
 }
 
 template <int FMT, int MT, bool DUMP>
@@ -580,9 +608,10 @@ int launch_mt(const GvArgs &a, int nsm, cudaStream_t stream) {
 
 template <int FMT, bool DUMP>
 int launch_fmt(GvArgs a, int nsm, cudaStream_t stream) {
-    for (int64_t t0 = 0; t0 < a.M; t0 += 8) {
+    constexpr int G = GvCfg<FMT>::MAX_MT;
+    for (int64_t t0 = 0; t0 < a.M; t0 += G) {
         a.t0 = t0;
-        a.mt = (int)((a.M - t0) < 8 ? (a.M - t0) : 8);
+        a.mt = (int)((a.M - t0) < G ? (a.M - t0) : G);
         int rc;
         if (a.mt == 1)
             rc = launch_mt<FMT, 1, DUMP>(a, nsm, stream);
