@@ -620,6 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // activation scales: this thread's token in the stager's shared-memory tile
         const float *da_tok = reinterpret_cast<const float *>(sm + C::OFF_DA) + 32 * qd + lane;
+        // The waits below decide the same way in every lane: the warp enters each one converged
+        // (after a .sync.aligned TMEM op) and its lanes probe the same barrier, read the same abort
+        // flag and the same timer in the same instructions, so a failure makes the whole warp leave
+        // together and no lane is left at an .aligned TMEM load alone.  (Voting on each result
+        // instead measured 10% slower.)
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             if (!mbar_wait(&bars.da_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_DA, abort_flag)) break;
