@@ -7,16 +7,15 @@
 // to 8 (Q4_K) or 4 (Q6_K) tokens.  The weight matrix is one flat stream of super-blocks
 // (row-major, rows contiguous).  Each CTA owns a contiguous range of whole rows and walks
 // it in units of TU super-blocks (a unit may start or end inside a row):
-//   * a producer warp refills a 2-5 stage shared-memory ring with ONE large 1-D bulk copy
+//   * a producer warp refills a 2-4 stage shared-memory ring with ONE large 1-D bulk copy
 //     (TMA engine) per unit -- the 16-byte aligned superset of the unit's bytes, so the
 //     2-byte aligned 210-byte Q6_K block needs no special load path.  A few large copies
 //     per SM keep the copy engine streaming at full HBM rate, where many small per-warp
 //     copies stall it;
-//   * consumer warps take a super-block with 4 threads (Q4_K, 64 values each) or 2 threads
-//     (Q6_K, one 128-value half each), so the per-unit hand-offs and the scale decoding
-//     amortize over many values: dp4a against the int8 codes, f32 scaling per 32-value
-//     block, a lane reduction, and one partial per (token, super-block) into a ring of
-//     partial buffers;
+//   * 8 consumer warps take each super-block with 2 threads, one 128-value half each, so
+//     the per-unit hand-offs and the scale decoding amortize over many values: dp4a
+//     against the int8 codes, f32 scaling per 32-value block, a lane-pair reduction, and
+//     one partial per (token, super-block) into a ring of partial buffers;
 //   * a reducer warp sums each row's partials in a fixed order (a row that continues
 //     into the next unit carries its running sum), so results are deterministic, and
 //     writes Y.  Consumers wait for the reducer only when the partial ring is full.
@@ -40,35 +39,32 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int FMT>
 struct GvCfg {
     static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
-    static constexpr int CW = FMT == FMT_Q4K ? 8 : 4;          // consumer warps
-    static constexpr int TPS = FMT == FMT_Q4K ? 4 : 2;         // consumer threads per super-block
+    static constexpr int CW = 8;                               // consumer warps
+    static constexpr int TPS = 2;                              // consumer threads per super-block
     static constexpr int THREADS = (CW + 2) * 32;              // + producer warp + reducer warp
     static constexpr int PRODUCER = CW, REDUCER = CW + 1;
-    static constexpr int SB_PER_PASS = CW * 32 / TPS;          // 64
-    static constexpr int PASSES = FMT == FMT_Q4K ? 2 : 1;
+    static constexpr int SB_PER_PASS = CW * 32 / TPS;          // 128
+    static constexpr int PASSES = 1;
     static constexpr int TU = SB_PER_PASS * PASSES;            // super-blocks per unit
-    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 5;  // at most; a launch may use fewer (GvArgs::nst)
+    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 3;  // at most; a launch may use fewer (GvArgs::nst)
     // tokens per pass over the weights (Q6_K: the staged activations of 8 tokens would leave
     // room for too few CTAs per SM; two passes of 4 measure faster)
     static constexpr int MAX_MT = FMT == FMT_Q4K ? 8 : 4;
     // CTAs per SM the launch aims for (registers: 64K / (THREADS * this))
-    static constexpr int ctas_per_sm(int mt) { return FMT == FMT_Q4K ? (mt <= 2 ? 3 : 2) : (mt <= 2 ? 4 : 3); }
+    static constexpr int ctas_per_sm(int mt) { return mt <= 2 ? 3 : 2; }
     // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
     static constexpr int STAGE = ((TU * BB + 30 + 15) / 16) * 16 + 16;
     static constexpr int part_bytes(int mt) { return kPartBufs * mt * TU * 4; }
-    // Staged activations, per token.  Q4_K: int8 codes with each super-block's two 128-value
-    // halves padded apart (half stride 160 B = 10 bank groups of 16 B, super-block stride 304 B
-    // = 19 groups) so that the 8 lanes of every quarter-warp -- two consecutive super-blocks x
-    // four quarters -- read 8 distinct 16-byte bank groups; then a float2 (d_a, d_a * S) table
-    // per block (TAB_SB = 64 B per super-block).  Q6_K: one record per half super-block, the
-    // 128 codes then 4 x 16 B of scale data ((d_a, -32 S16 of the first and second 16 values),
-    // one entry per 32-value block); half stride HALF = 208 B (5 mod 8 groups), super-block
-    // stride 464 B (5 mod 8 groups): a quarter-warp's 8 lanes -- four super-blocks two apart x
-    // two halves -- then hit 8 distinct groups (away from row ends).
-    static constexpr uint32_t SB_STRIDE = FMT == FMT_Q6K ? 464 : 304;
-    static constexpr uint32_t HALF = 208;
-    static constexpr uint32_t TAB_SB = FMT == FMT_Q6K ? 0 : 64;
-    static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * (SB_STRIDE + TAB_SB); }
+    // Staged activations, per token: one record per half super-block, its 128 int8 codes and
+    // then its four 32-value blocks' scale data.  Q4_K: (d_a, d_a * S) per block, 32 B; half
+    // stride HALF = 176 B (3 mod 8 bank groups of 16 B), super-block stride 416 B (2 mod 8), so
+    // a quarter-warp's 8 lanes -- four consecutive super-blocks x two halves -- read 8 distinct
+    // groups.  Q6_K: (d_a, -32 S16 of the first and second 16 values) per block, 64 B; half
+    // stride 208 B (5 mod 8), super-block stride 464 B (5 mod 8): distinct groups for its
+    // quarter-warps of four super-blocks two apart x two halves.  (Away from row ends.)
+    static constexpr uint32_t SB_STRIDE = FMT == FMT_Q6K ? 464 : 416;
+    static constexpr uint32_t HALF = FMT == FMT_Q6K ? 208 : 176;
+    static int64_t act_bytes(int mt, int64_t K) { return (int64_t)mt * (K / kQK) * SB_STRIDE; }
 };
 constexpr int kSmemMax = 200 * 1024;                 // stage activations while the CTA fits in this
 // the largest dynamic shared memory per CTA that leaves room for n CTAs per SM
@@ -150,14 +146,17 @@ struct GvArgs {
 
 // shared-memory addresses of the staged activations (ACT kernels): codes [MT][K], table
 struct GvAct {
-    uint32_t codes, tab;         // token 0's codes and table
-    uint32_t ck, tk;             // per-token strides of codes and table
+    uint32_t codes;              // token 0's records
+    uint32_t ck;                 // per-token stride of the records
 };
 
 // A thread's raw weight bytes of one super-block quarter, read from the stage before the
 // stage is handed back to the producer (the math runs on these registers afterwards).
-struct Q4Raw {
-    uint4 hd, q0, q1;
+// Q4_K: half h of a super-block -- the 16-byte header (d, dmin, 12 scale bytes) and the
+// qs bytes [64h, 64h+64) holding sub-blocks 4h .. 4h+3.
+struct Q4Half {
+    uint4 hd;
+    uint32_t q[16];
 };
 // Q6_K: half h of a super-block -- ql bytes [64h, 64h+64), qh bytes [128+32h, 128+32h+32),
 // the eight int8 scales 8h .. 8h+7 and the fp16 d.
@@ -165,82 +164,76 @@ struct Q6Half {
     uint32_t ql[16], qh[8], sc[2], dbits;
 };
 
-// Q4_K: quarter u of the super-block at shared address `blk`: its header and qs bytes
-// [32u, 32u+32), whose low nibbles are sub-block 2u and high nibbles 2u+1.
-__device__ __forceinline__ Q4Raw q4k_load(uint32_t blk, int u, bool valid) {
-    Q4Raw r{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (valid) {
-        r.hd = lds128(blk);
-        r.q0 = lds128(blk + 16 + 32 * u);
-        r.q1 = lds128(blk + 32 + 32 * u);
+// Q4_K: loads half h of the super-block at shared address `blk` (144-byte blocks keep every
+// block 16-byte aligned inside a unit, so these are plain 16-byte reads).
+__device__ __forceinline__ void q4k_load_half(uint32_t blk, int h, Q4Half &r) {
+    r.hd = lds128(blk);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 v = lds128(blk + 16 + 64 * h + 16 * k);
+        r.q[4 * k] = v.x;
+        r.q[4 * k + 1] = v.y;
+        r.q[4 * k + 2] = v.z;
+        r.q[4 * k + 3] = v.w;
     }
-    return r;
 }
 
-// Q4_K quarter math (row n, super-block sbi of the row) on the loaded bytes
+// Q4_K math of one half (row n, super-block sbi of the row).  Sub-block j = 4h + i (i < 4) is
+// the 32-value Q8 block 8 sbi + j: the low (i even) or high (i odd) nibbles of the qs words
+// 8 (i / 2) .. 8 (i / 2) + 7.  Its integer dot I = sc_j D_j is exact; the row's two scalings
+// are summed separately, d * sum_j d_a I_j - dmin * sum_j m_j (d_a S)_j.
 template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q4k_quarter(const GvArgs &a, const GvAct &at, const Q4Raw &raw, int64_t n,
-                                            uint32_t sbi, int u, bool valid, float (&part)[MT]) {
+__device__ __forceinline__ void q4k_half(const GvArgs &a, const GvAct &at, const Q4Half &r, int64_t n,
+                                         uint32_t sbi, int h, bool valid, float (&part)[MT]) {
     using C = GvCfg<FMT_Q4K>;
-    const uint4 hd = raw.hd, q0 = raw.q0, q1 = raw.q1;
+    const uint4 hd = r.hd;
     const float d = half_bits_to_float(hd.x & 0xffff), dmin = half_bits_to_float(hd.x >> 16);
-    // the 12 scale bytes: s[0..3] = hd.y, s[4..7] = hd.z, s[8..11] = hd.w; sub-blocks 2u, 2u+1
-    int sc0, m0, sc1, m1;
-    if (u < 2) {
-        const uint32_t x = hd.y >> (16 * u), z = hd.z >> (16 * u);
-        sc0 = x & 63; sc1 = (x >> 8) & 63; m0 = z & 63; m1 = (z >> 8) & 63;
-    } else {
-        const uint32_t lo = hd.w >> (16 * (u - 2));                                 // s[j+4], j = 2u, 2u+1
-        const uint32_t ts = hd.y >> (16 * (u - 2)), tm = hd.z >> (16 * (u - 2));   // s[j-4], s[j]
-        sc0 = (lo & 15) | (((ts >> 6) & 3) << 4);
-        sc1 = ((lo >> 8) & 15) | (((ts >> 14) & 3) << 4);
-        m0 = ((lo >> 4) & 15) | (((tm >> 6) & 3) << 4);
-        m1 = ((lo >> 12) & 15) | (((tm >> 14) & 3) << 4);
-    }
-    const uint4 lo0 = make_uint4(q0.x & 0x0f0f0f0fu, q0.y & 0x0f0f0f0fu, q0.z & 0x0f0f0f0fu, q0.w & 0x0f0f0f0fu);
-    const uint4 lo1 = make_uint4(q1.x & 0x0f0f0f0fu, q1.y & 0x0f0f0f0fu, q1.z & 0x0f0f0f0fu, q1.w & 0x0f0f0f0fu);
-    const uint4 hi0 = make_uint4((q0.x >> 4) & 0x0f0f0f0fu, (q0.y >> 4) & 0x0f0f0f0fu, (q0.z >> 4) & 0x0f0f0f0fu,
-                                 (q0.w >> 4) & 0x0f0f0f0fu);
-    const uint4 hi1 = make_uint4((q1.x >> 4) & 0x0f0f0f0fu, (q1.y >> 4) & 0x0f0f0f0fu, (q1.z >> 4) & 0x0f0f0f0fu,
-                                 (q1.w >> 4) & 0x0f0f0f0fu);
-    const int64_t k0 = (int64_t)sbi * kQK + 64 * u;    // values 64u .. 64u+63 of the super-block
-    const int64_t b0 = (int64_t)sbi * 8 + 2 * u, b1 = b0 + 1;   // their two Q8 blocks
-    const float dsc0 = d * (float)sc0, dsc1 = d * (float)sc1, dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
+    // the four 6-bit scales and mins of sub-blocks 4h .. 4h+3, one byte each
+    const uint32_t scw = h == 0 ? (hd.y & 0x3f3f3f3fu) : ((hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u));
+    const uint32_t mw = h == 0 ? (hd.z & 0x3f3f3f3fu) : (((hd.w >> 4) & 0x0f0f0f0fu) | ((hd.z >> 2) & 0x30303030u));
+    float acc1[MT], acc2[MT];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        const int64_t m = a.t0 + t;
-        const bool act = t < a.mt && valid;
-        int D0 = 0, D1 = 0;
-        part[t] = 0.0f;
-        if (act) {
-            if constexpr (ACT) {
-                // codes 64u .. 64u+63 of the super-block (half u/2, offset 64 (u&1) in it);
-                // table: (d, d*S) of blocks 2u, 2u+1
-                const uint32_t cb = at.codes + (uint32_t)t * at.ck + sbi * C::SB_STRIDE +
-                                    160u * ((uint32_t)u >> 1) + 64u * ((uint32_t)u & 1u);
-                const uint4 x0 = lds128(cb), x1 = lds128(cb + 16), x2 = lds128(cb + 32), x3 = lds128(cb + 48);
-                D0 = dot16(lo0, x0) + dot16(lo1, x1);
-                D1 = dot16(hi0, x2) + dot16(hi1, x3);
-                const float4 tb = lds128f(at.tab + (uint32_t)t * at.tk + sbi * C::TAB_SB + 16u * (uint32_t)u);
-                part[t] = fmaf(dsc0, tb.x * (float)D0, -dm0 * tb.y) + fmaf(dsc1, tb.z * (float)D1, -dm1 * tb.w);
-            } else {
-                const uint4 *q = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K + k0);
-                D0 = dot16(lo0, __ldg(q)) + dot16(lo1, __ldg(q + 1));
-                D1 = dot16(hi0, __ldg(q + 2)) + dot16(hi1, __ldg(q + 3));
-                const float da0 = __ldg(a.p.d + b0 * a.M + m), da1 = __ldg(a.p.d + b1 * a.M + m);
-                const float s0 = (float)__ldg(a.p.s + b0 * a.M + m), s1 = (float)__ldg(a.p.s + b1 * a.M + m);
-                part[t] = da0 * (dsc0 * (float)D0 - dm0 * s0) + da1 * (dsc1 * (float)D1 - dm1 * s1);
+    for (int t = 0; t < MT; ++t) { acc1[t] = 0.0f; acc2[t] = 0.0f; }
+    const uint32_t rec = at.codes + sbi * C::SB_STRIDE + C::HALF * (uint32_t)h;    // token 0's record
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = ((i & 1) ? (r.q[8 * (i >> 1) + e] >> 4) : r.q[8 * (i >> 1) + e]) & 0x0f0f0f0fu;
+        const int sc = (int)((scw >> (8 * i)) & 0xff);
+        const float mf = (float)((mw >> (8 * i)) & 0xff);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const int64_t m = a.t0 + t;
+            const bool act = t < a.mt && valid;
+            int I = 0;
+            if (act) {
+                if constexpr (ACT) {
+                    const uint32_t rt = rec + (uint32_t)t * at.ck;
+                    const uint4 a0 = lds128(rt + 32u * i), a1 = lds128(rt + 32u * i + 16u);
+                    const float4 tb = lds128f(rt + 128u + 16u * (i >> 1));    // (d_a, d_a S) of two blocks
+                    const float da = (i & 1) ? tb.z : tb.x, dS = (i & 1) ? tb.w : tb.y;
+                    I = sc * dot16w(v + 4, a1, dot16w(v, a0, 0));
+                    acc1[t] = fmaf(da, (float)I, acc1[t]);
+                    acc2[t] = fmaf(mf, dS, acc2[t]);
+                } else {
+                    const int64_t b = (int64_t)sbi * 8 + 4 * h + i;          // the Q8 block
+                    const uint4 *q = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K + 32 * b);
+                    I = sc * dot16w(v + 4, __ldg(q + 1), dot16w(v, __ldg(q), 0));
+                    const float da = __ldg(a.p.d + b * a.M + m);
+                    acc1[t] = fmaf(da, (float)I, acc1[t]);
+                    acc2[t] = fmaf(mf, da * (float)__ldg(a.p.s + b * a.M + m), acc2[t]);
+                }
             }
-        }
-        if constexpr (DUMP) {
-            const Dump &dp = a.dump;
-            if (act && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt) {
-                int32_t *o = dp.out + ((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8);
-                o[b0] = sc0 * D0;
-                o[b1] = sc1 * D1;
+            if constexpr (DUMP) {
+                const Dump &dp = a.dump;
+                if (act && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt)
+                    dp.out[((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8) + (int64_t)sbi * 8 + 4 * h + i] = I;
             }
         }
     }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) part[t] = fmaf(d, acc1[t], -dmin * acc2[t]);
 }
 
 // Q6_K: loads half h of the super-block at shared address `blk`.  A 210-byte block sits at
@@ -441,27 +434,25 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
 
     // consumer warps (the reducer writes y only after them, so after the predecessor too)
     grid_dep_wait();
-    GvAct at{0, 0, 0, 0};
+    GvAct at{0, 0};
     if constexpr (ACT) {
         // stage the tokens' codes (padded layout) and their scale data
         at.codes = smem_u32(partbuf) + (uint32_t)C::part_bytes(MT);
         at.ck = nb * C::SB_STRIDE;
-        at.tab = at.codes + MT * at.ck;
-        at.tk = nb * C::TAB_SB;
         const uint32_t nch = nb * 16u;                // 16-byte chunks of codes per token
         for (int t = 0; t < a.mt; ++t) {
             const int64_t m = a.t0 + t;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);
-            const uint32_t cbase = at.codes + (uint32_t)t * at.ck, tbase = at.tab + (uint32_t)t * at.tk;
+            const uint32_t cbase = at.codes + (uint32_t)t * at.ck;
             // all of an iteration's global loads go out before its stores (one latency round)
             for (uint32_t c = tid; c < nch; c += C::CW * 32) {
                 const uint4 v = __ldg(src + c);
                 const uint32_t sbi = c >> 4, r = c & 15u;     // chunk r of super-block sbi
+                // chunk r: half r >> 3, block g = (r >> 1) & 3 of it, 16-value piece r & 1
+                const uint32_t rec = cbase + sbi * C::SB_STRIDE + C::HALF * (r >> 3);
+                sts128(rec + 16u * (r & 7u), v);
                 if constexpr (FMT == FMT_Q6K) {
-                    // chunk r: half r >> 3, block g = (r >> 1) & 3 of it, its 16-value sub-block
-                    // r & 1; the block's entry holds (d_a, -32 S16, -32 S16') at 128 + 16 g
-                    const uint32_t rec = cbase + sbi * C::SB_STRIDE + C::HALF * (r >> 3);
-                    sts128(rec + 16u * (r & 7u), v);
+                    // the block's entry holds (d_a, -32 S16, -32 S16') at 128 + 16 g
                     const int s16 = dot16(v, make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u));
                     const uint32_t ent = rec + 128u + 16u * ((r >> 1) & 3u);
                     if (r & 1u) {
@@ -471,24 +462,22 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
                         sts32(ent, __float_as_uint(da));
                         sts32(ent + 4u, (uint32_t)(-32 * s16));
                     }
-                } else {
-                    // block c (< K/32): (d_a, d_a * S)
-                    const bool blk = c < nb * 8u;
-                    const float da = blk ? __ldg(a.p.d + (int64_t)c * a.M + m) : 0.0f;
-                    const float sa = blk ? (float)__ldg(a.p.s + (int64_t)c * a.M + m) : 0.0f;
-                    sts128(cbase + sbi * C::SB_STRIDE + 160u * (r >> 3) + 16u * (r & 7u), v);
-                    if (blk) sts64(tbase + 8u * c, da, da * sa);
+                } else if ((r & 1u) == 0) {
+                    // the block's entry holds (d_a, d_a * S) at 128 + 8 g
+                    const int64_t b = c >> 1;
+                    const float da = __ldg(a.p.d + b * a.M + m);
+                    sts64(rec + 128u + 8u * ((r >> 1) & 3u), da, da * (float)__ldg(a.p.s + b * a.M + m));
                 }
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::CW * 32) : "memory");
     }
 
-    // super-block slot within a pass, and the thread's part of it: Q4_K quarter u = tid % 4 of
-    // slot tid / 4; Q6_K half u = lane % 2, warps alternating between even and odd slots (so a
-    // warp's blocks share one alignment mod 4): slot 2 (16 (warp / 2) + lane / 2) + warp % 2
-    const int u = FMT == FMT_Q4K ? (tid & 3) : (lane & 1);
-    const int slot = FMT == FMT_Q4K ? (tid >> 2) : 2 * (16 * (warp >> 1) + (lane >> 1)) + (warp & 1);
+    // super-block slot within the unit, and the thread's half u = lane % 2 of it: Q4_K slot
+    // 16 warp + lane / 2; Q6_K warps alternate between even and odd slots (so a warp's 210-byte
+    // blocks share one alignment mod 4): slot 2 (16 (warp / 2) + lane / 2) + warp % 2
+    const int u = lane & 1;
+    const int slot = FMT == FMT_Q4K ? 16 * warp + (lane >> 1) : 2 * (16 * (warp >> 1) + (lane >> 1)) + (warp & 1);
     // this thread's super-block of each pass: offset in its row (and the row, for the dump);
     // both advance by TU super-blocks per unit
     const uint32_t tu_mod = (uint32_t)C::TU % nb, tu_div = (uint32_t)C::TU / nb;
@@ -515,10 +504,10 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
         const int nsb = j == last ? nsb_last : C::TU;
         const uint32_t sbase = ring + (uint32_t)(s * C::STAGE);
         float part[C::PASSES][MT];
+        // read this thread's weight bytes, hand the stage back to the producer, then do the
+        // math on registers (the refill overlaps the dp4a work)
+        static_assert(C::PASSES == 1, "one pass per unit");
         if constexpr (FMT == FMT_Q6K) {
-            // one pass: read this thread's weight bytes, hand the stage back to the producer,
-            // then do the math on registers (the refill overlaps the dp4a work)
-            static_assert(C::PASSES == 1, "Q6_K takes one pass per unit");
             Q6Half raw;
             const uint32_t blk = sbase + (uint32_t)(slot * C::BB);
             if (al4)
@@ -529,16 +518,11 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
             if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
             q6k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
         } else {
-            // two passes, each loading and computing in turn (fewer live registers); the stage
-            // goes back after the last one
-#pragma unroll
-            for (int ps = 0; ps < C::PASSES; ++ps) {
-                const int idx = ps * C::SB_PER_PASS + slot;
-                const Q4Raw raw = q4k_load(sbase + (uint32_t)(idx * C::BB), u, idx < nsb);
-                q4k_quarter<MT, ACT, DUMP>(a, at, raw, t_row[ps], t_sbi[ps], u, idx < nsb, part[ps]);
-            }
+            Q4Half raw;
+            q4k_load_half(sbase + (uint32_t)(slot * C::BB), u, raw);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);   // stage fully read: the producer may refill it
+            if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
+            q4k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
         }
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps)
