@@ -1,4 +1,4 @@
-"""CPU oracle for the Q4_K / Q6_K x Q8 matmul path (numpy front end over plain C).
+"""CPU oracle for the Q4_K / Q5_K / Q6_K x Q8 matmul path (numpy front end over plain C).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the bench's ``cpu_baseline`` / ``--impl reference`` legs, never by the
@@ -8,7 +8,7 @@ Every function here is a thin marshalling layer over ``mq_oracle.c``; the
 arithmetic, and the citation of the passage each step follows, live there.
 Arrays use the oracle's own logical layouts:
 
-* weights: raw GGML block bytes, ``[N, K/256, 144]`` (Q4_K) or ``[N, K/256, 210]`` (Q6_K)
+* weights: raw GGML block bytes, ``[N, K/256, B]`` with B = 144 (Q4_K), 176 (Q5_K), 210 (Q6_K)
 * Q8 plane: ``q`` int8 ``[M, K]``, ``d`` f32 ``[M, K/32]``, ``S`` int32 ``[M, K/32]``
 * outputs: f64 ``[len(ms), len(ns)]`` for the listed (token, row) index pairs
 
@@ -37,6 +37,8 @@ def lib():
         L.oq_half_to_double.argtypes = [ctypes.c_uint16]
         L.oq_half_to_double.restype = ctypes.c_double
         L.oq_q4k_fields.argtypes = [P, P, P, P, P, P]
+        L.oq_q5k_fields.argtypes = [P, P, P, P, P, P]
+        L.oq_q5k_dequant.argtypes = [P, I64, I64, P]
         L.oq_q6k_fields.argtypes = [P, P, P, P]
         L.oq_q4k_dequant.argtypes = [P, I64, I64, P]
         L.oq_q6k_dequant.argtypes = [P, I64, I64, P]
@@ -45,9 +47,9 @@ def lib():
         L.oq_exp_f32.argtypes = [F32]
         L.oq_exp_f32.restype = F32
         L.oq_swiglu.argtypes = [P, P, I64, I64, P]
-        for f in (L.oq_q4k_blockdots, L.oq_q6k_blockdots):
+        for f in (L.oq_q4k_blockdots, L.oq_q5k_blockdots, L.oq_q6k_blockdots):
             f.argtypes = [P, I64, I64, P, I64, P, I64, P, I64, P, P]
-        for f in (L.oq_q4k_matmul, L.oq_q6k_matmul):
+        for f in (L.oq_q4k_matmul, L.oq_q5k_matmul, L.oq_q6k_matmul):
             f.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, I64, P]
         _lib = L
     return _lib
@@ -58,7 +60,7 @@ def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-BLOCK_BYTES = {"q4k": 144, "q6k": 210}
+BLOCK_BYTES = {"q4k": 144, "q5k": 176, "q6k": 210}
 
 
 def _weights(w: np.ndarray, fmt: str):
@@ -83,6 +85,15 @@ def q4k_fields(block: np.ndarray):
     return d.value, dmin.value, sc, mn, q
 
 
+def q5k_fields(block: np.ndarray):
+    """Decode one 176-byte Q5_K block -> (d, dmin, sc[8], m[8], q[256])."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8).reshape(176)
+    d, dmin = ctypes.c_double(), ctypes.c_double()
+    sc, mn, q = np.zeros(8, np.int32), np.zeros(8, np.int32), np.zeros(256, np.int32)
+    lib().oq_q5k_fields(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(mn), _p(q))
+    return d.value, dmin.value, sc, mn, q
+
+
 def q6k_fields(block: np.ndarray):
     """Decode one 210-byte Q6_K block -> (d, sc[16], q[256])."""
     blk = np.ascontiguousarray(block, dtype=np.uint8).reshape(210)
@@ -96,7 +107,7 @@ def dequantize(w: np.ndarray, fmt: str) -> np.ndarray:
     """Dequantized weights [N, K] in f64."""
     w, n, k = _weights(w, fmt)
     out = np.empty((n, k), np.float64)
-    (lib().oq_q4k_dequant if fmt == "q4k" else lib().oq_q6k_dequant)(_p(w), n, k, _p(out))
+    {"q4k": lib().oq_q4k_dequant, "q5k": lib().oq_q5k_dequant, "q6k": lib().oq_q6k_dequant}[fmt](_p(w), n, k, _p(out))
     return out
 
 
@@ -156,9 +167,10 @@ def blockdots(w: np.ndarray, fmt: str, q: np.ndarray, ms=None, ns=None):
     assert q.shape[1] == k
     ms, ns = _idx(ms, m), _idx(ns, n)
     I = np.zeros((ms.size, ns.size, k // 32), np.int32)
-    if fmt == "q4k":
+    if fmt in ("q4k", "q5k"):
         D = np.zeros_like(I)
-        lib().oq_q4k_blockdots(_p(w), n, k, _p(q), m, _p(ms), ms.size, _p(ns), ns.size, _p(I), _p(D))
+        fn = lib().oq_q4k_blockdots if fmt == "q4k" else lib().oq_q5k_blockdots
+        fn(_p(w), n, k, _p(q), m, _p(ms), ms.size, _p(ns), ns.size, _p(I), _p(D))
     else:
         D = np.zeros((ms.size, ns.size, k // 32, 2), np.int32)
         lib().oq_q6k_blockdots(_p(w), n, k, _p(q), m, _p(ms), ms.size, _p(ns), ns.size, _p(I), _p(D))
@@ -177,7 +189,7 @@ def matmul(w: np.ndarray, fmt: str, plane, ms=None, ns=None, threads: int = 1) -
     assert q.shape == (m, k) and d.shape == (m, k // 32) and S.shape == (m, k // 32)
     assert q.dtype == np.int8 and d.dtype == np.float32 and S.dtype == np.int32
     ms, ns = _idx(ms, m), _idx(ns, n)
-    fn = lib().oq_q4k_matmul if fmt == "q4k" else lib().oq_q6k_matmul
+    fn = {"q4k": lib().oq_q4k_matmul, "q5k": lib().oq_q5k_matmul, "q6k": lib().oq_q6k_matmul}[fmt]
     if threads <= 1 or ns.size < 2:
         y = np.empty((ms.size, ns.size), np.float64)
         fn(_p(w), n, k, _p(q), _p(d), _p(S), m, _p(ms), ms.size, _p(ns), ns.size, _p(y))

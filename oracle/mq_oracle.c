@@ -15,6 +15,10 @@
  * token-major); "Compute Graph Design > 3.1" (RmsNorm{eps})):
  *
  *   C1  Q4_K super-block decode (GGML layout, 144 bytes)
+ *   C1' Q5_K super-block decode (GGML layout, 176 bytes): Q4_K's scales, mins and
+ *       nibbles plus one high bit per value ("Support Matrix > CUDA notes": decode
+ *       uses the dp4a MMVQ kernels for Q4_K/Q5_K/Q6_K; "Architecture > 6" item on
+ *       block layouts: Q4_K/Q5_K/Q6_K are 256-value super-blocks)
  *   C2  Q6_K super-block decode (GGML layout, 210 bytes)
  *   C3  Q8 activation quantization, blocks of 32, round half away from zero
  *   C4  RMSNorm producer y = (x * r) * w,  r = 1/sqrt(mean(x^2) + eps)
@@ -100,6 +104,41 @@ void oq_q4k_fields(const uint8_t *blk, double *d, double *dmin,
     }
 }
 
+/* ---------------------------------------------------------------- C1' --- */
+
+/*
+ * Q5_K: bytes [0,2) d, [2,4) dmin, [4,16) scales[12] (packed exactly as Q4_K's),
+ * [16,48) qh[32], [48,176) qs[128].  Element 32j + l of sub-block j (0..7) takes the
+ * Q4_K nibble of qs (low nibble of qs[32*(j/2) + l] for even j, high for odd j) as its
+ * low four bits and bit j of qh[l] as its fifth: q = nibble + 16 * ((qh[l] >> j) & 1),
+ * q in [0, 31].  value = d * sc_j * q - dmin * m_j.
+ */
+void oq_q5k_fields(const uint8_t *blk, double *d, double *dmin,
+                   int32_t sc[8], int32_t mn[8], int32_t q[256])
+{
+    const uint8_t *s = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    *d = oq_half_to_double(rd16(blk));
+    *dmin = oq_half_to_double(rd16(blk + 2));
+    for (int j = 0; j < 8; ++j) {
+        if (j < 4) {
+            sc[j] = s[j] & 63;
+            mn[j] = s[j + 4] & 63;
+        } else {
+            sc[j] = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+            mn[j] = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+        }
+    }
+    for (int j = 0; j < 8; ++j) {
+        for (int l = 0; l < 32; ++l) {
+            uint8_t b = qs[32 * (j / 2) + l];
+            int nib = (j % 2 == 0) ? (b & 15) : (b >> 4);
+            q[32 * j + l] = nib + 16 * ((qh[l] >> j) & 1);
+        }
+    }
+}
+
 /* ----------------------------------------------------------------- C2 --- */
 
 /*
@@ -142,6 +181,19 @@ void oq_q4k_dequant(const uint8_t *w, int64_t n_rows, int64_t K, double *out)
             double d, dmin;
             int32_t sc[8], mn[8], q[256];
             oq_q4k_fields(w + (r * nb + b) * 144, &d, &dmin, sc, mn, q);
+            for (int e = 0; e < 256; ++e)
+                out[r * K + b * 256 + e] = d * sc[e / 32] * q[e] - dmin * mn[e / 32];
+        }
+}
+
+void oq_q5k_dequant(const uint8_t *w, int64_t n_rows, int64_t K, double *out)
+{
+    int64_t nb = K / OQ_QK;
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            double d, dmin;
+            int32_t sc[8], mn[8], q[256];
+            oq_q5k_fields(w + (r * nb + b) * 176, &d, &dmin, sc, mn, q);
             for (int e = 0; e < 256; ++e)
                 out[r * K + b * 256 + e] = d * sc[e / 32] * q[e] - dmin * mn[e / 32];
         }
@@ -258,17 +310,18 @@ void oq_quantize_q8(const float *x, int64_t M, int64_t K, int8_t *q, float *d, i
 
 /* -------------------------------------------------------------- C5, C7 --- */
 
+/* the decoder of a Q4_K-style super-block: d, dmin, sc[8], m[8], q[256] */
+typedef void (*oq_kfields_fn)(const uint8_t *, double *, double *, int32_t *, int32_t *, int32_t *);
+
 /*
  * Integer checkpoint for the (token, row) pairs (ms[i], ns[j]).
- * Q4_K, 32-block b of the row (sub-block j = b % 8 of super-block b / 8):
+ * Q4_K / Q5_K, 32-block b of the row (sub-block j = b % 8 of super-block b / 8):
  *   D[b] = sum_{l<32} q_w[32b + l] * q_a[32b + l],   I[b] = sc_j * D[b].
  * Output I and D as [nm][nn][K/32].
  */
-void oq_q4k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, int64_t M,
-                      const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn,
-                      int32_t *I, int32_t *D)
+static void kq_blockdots(oq_kfields_fn fields, int bytes, const uint8_t *w, int64_t K, const int8_t *qa,
+                         const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, int32_t *I, int32_t *D)
 {
-    (void)N; (void)M;
     int64_t nb = K / OQ_QK, nblk = K / OQ_Q8;
     int32_t *qw = (int32_t *)malloc(sizeof(int32_t) * K);
     int32_t *scw = (int32_t *)malloc(sizeof(int32_t) * nblk);
@@ -277,7 +330,7 @@ void oq_q4k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, 
         for (int64_t b = 0; b < nb; ++b) {
             double dd, dm;
             int32_t sc[8], mn[8];
-            oq_q4k_fields(w + (n * nb + b) * 144, &dd, &dm, sc, mn, qw + b * 256);
+            fields(w + (n * nb + b) * bytes, &dd, &dm, sc, mn, qw + b * 256);
             for (int j = 0; j < 8; ++j) scw[b * 8 + j] = sc[j];
         }
         for (int64_t im = 0; im < nm; ++im) {
@@ -292,6 +345,22 @@ void oq_q4k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, 
     }
     free(qw);
     free(scw);
+}
+
+void oq_q4k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, int64_t M,
+                      const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn,
+                      int32_t *I, int32_t *D)
+{
+    (void)N; (void)M;
+    kq_blockdots(oq_q4k_fields, 144, w, K, qa, ms, nm, ns, nn, I, D);
+}
+
+void oq_q5k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, int64_t M,
+                      const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn,
+                      int32_t *I, int32_t *D)
+{
+    (void)N; (void)M;
+    kq_blockdots(oq_q5k_fields, 176, w, K, qa, ms, nm, ns, nn, I, D);
 }
 
 /*
@@ -338,16 +407,15 @@ void oq_q6k_blockdots(const uint8_t *w, int64_t N, int64_t K, const int8_t *qa, 
 
 /*
  * Y[ms[i]][ns[j]] for the listed pairs, accumulated in f64:
- *   Q4_K: sum over super-blocks of
+ *   Q4_K / Q5_K: sum over super-blocks of
  *         d * sum_j sc_j * da[m][j] * D_j  -  dmin * sum_j m_j * da[m][j] * S[m][j]
  *   (the min term uses the integer activation sum S of the Q8 block, as Q8_K's
  *    precomputed sums do).  Output y[nm][nn] (f64).
  */
-void oq_q4k_matmul(const uint8_t *w, int64_t N, int64_t K,
-                   const int8_t *qa, const float *da, const int32_t *Sa, int64_t M,
-                   const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, double *y)
+static void kq_matmul(oq_kfields_fn fields, int bytes, const uint8_t *w, int64_t K,
+                      const int8_t *qa, const float *da, const int32_t *Sa,
+                      const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, double *y)
 {
-    (void)N; (void)M;
     int64_t nb = K / OQ_QK, nblk = K / OQ_Q8;
     int32_t *qw = (int32_t *)malloc(sizeof(int32_t) * K);
     int32_t *scw = (int32_t *)malloc(sizeof(int32_t) * nblk);
@@ -358,7 +426,7 @@ void oq_q4k_matmul(const uint8_t *w, int64_t N, int64_t K,
         int64_t n = ns[jn];
         for (int64_t b = 0; b < nb; ++b) {
             int32_t sc[8], mn[8];
-            oq_q4k_fields(w + (n * nb + b) * 144, &dw[b], &dmw[b], sc, mn, qw + b * 256);
+            fields(w + (n * nb + b) * bytes, &dw[b], &dmw[b], sc, mn, qw + b * 256);
             for (int j = 0; j < 8; ++j) { scw[b * 8 + j] = sc[j]; mnw[b * 8 + j] = mn[j]; }
         }
         for (int64_t im = 0; im < nm; ++im) {
@@ -381,6 +449,22 @@ void oq_q4k_matmul(const uint8_t *w, int64_t N, int64_t K,
         }
     }
     free(qw); free(scw); free(mnw); free(dw); free(dmw);
+}
+
+void oq_q4k_matmul(const uint8_t *w, int64_t N, int64_t K,
+                   const int8_t *qa, const float *da, const int32_t *Sa, int64_t M,
+                   const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, double *y)
+{
+    (void)N; (void)M;
+    kq_matmul(oq_q4k_fields, 144, w, K, qa, da, Sa, ms, nm, ns, nn, y);
+}
+
+void oq_q5k_matmul(const uint8_t *w, int64_t N, int64_t K,
+                   const int8_t *qa, const float *da, const int32_t *Sa, int64_t M,
+                   const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, double *y)
+{
+    (void)N; (void)M;
+    kq_matmul(oq_q5k_fields, 176, w, K, qa, da, Sa, ms, nm, ns, nn, y);
 }
 
 /*

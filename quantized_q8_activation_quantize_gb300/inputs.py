@@ -30,6 +30,7 @@ STREAM_SWIGLU = 4            # gate / up inputs of the SwiGLU producer
 QK_K = 256             # values per k-quant super-block
 Q8_BLOCK = 32          # values per Q8 activation block
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 Q6K_BYTES = 210
 
 HIDDEN = 3584
@@ -69,6 +70,22 @@ def q4k_weights(r: np.random.Generator, n_rows: int, k: int,
     assert k % QK_K == 0
     nb = k // QK_K
     w = np.frombuffer(r.bytes(n_rows * nb * Q4K_BYTES), dtype=np.uint8).reshape(n_rows, nb, Q4K_BYTES).copy()
+    w[..., 0:2] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    w[..., 2:4] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    return w
+
+
+def q5k_weights(r: np.random.Generator, n_rows: int, k: int,
+                d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Q5_K weight matrix as raw bytes, shape [n_rows, k/256, 176].
+
+    As Q4_K: d and dmin fp16 uniform in ``d_range``; the 12 packed scale/min bytes, the
+    32 high-bit bytes and the 128 low-nibble bytes are uniform random bytes (uniform
+    5-bit quants).
+    """
+    assert k % QK_K == 0
+    nb = k // QK_K
+    w = np.frombuffer(r.bytes(n_rows * nb * Q5K_BYTES), dtype=np.uint8).reshape(n_rows, nb, Q5K_BYTES).copy()
     w[..., 0:2] = _fp16_bytes(r, (n_rows, nb), *d_range)
     w[..., 2:4] = _fp16_bytes(r, (n_rows, nb), *d_range)
     return w

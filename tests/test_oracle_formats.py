@@ -1,11 +1,12 @@
-"""Pins for the oracle's block decoders (C1 Q4_K, C2 Q6_K) and its fp16 decode.
+"""Pins for the oracle's block decoders (C1 Q4_K, C1' Q5_K, C2 Q6_K) and its fp16 decode.
 
 What pins them, besides the oracle itself:
 * numpy's float16 (an independent library routine) for every fp16 bit pattern;
 * hand-built blocks whose decodes were worked out by hand (tests/golden);
 * bijectivity of the quant-position maps (every (byte, nibble/bit) slot feeds exactly
   one element, every element is fed by exactly one slot);
-* the 144 / 210 byte block sizes and the config value ranges.
+* the 144 / 176 / 210 byte block sizes and the config value ranges;
+* Q5_K's scale fields decoded against Q4_K's (the same 12 bytes, the same packing).
 """
 import numpy as np
 import pytest
@@ -27,9 +28,9 @@ def test_half_to_double_matches_numpy_for_every_bit_pattern():
 @pytest.mark.parametrize("blk", golden_blocks.load(), ids=lambda b: b["name"])
 def test_hand_built_blocks(blk):
     b = blk["bytes"]
-    if blk["fmt"] == "q4k":
-        assert b.size == 144
-        d, dmin, sc, mn, q = oracle.q4k_fields(b)
+    if blk["fmt"] in ("q4k", "q5k"):
+        assert b.size == (144 if blk["fmt"] == "q4k" else 176)
+        d, dmin, sc, mn, q = (oracle.q4k_fields if blk["fmt"] == "q4k" else oracle.q5k_fields)(b)
         assert d == blk["d"] and dmin == blk["dmin"]
         assert sc.tolist() == blk["sc"] and mn.tolist() == blk["m"]
     else:
@@ -49,10 +50,12 @@ def test_hand_built_blocks(blk):
 def test_block_sizes():
     r = np.random.default_rng(0)
     assert inputs.q4k_weights(r, 3, 512).shape == (3, 2, 144)
+    assert inputs.q5k_weights(r, 3, 512).shape == (3, 2, 176)
     assert inputs.q6k_weights(r, 3, 512).shape == (3, 2, 210)
-    assert (inputs.Q4K_BYTES, inputs.Q6K_BYTES) == (144, 210)
-    # 4.5 and 6.5625 bits per weight
-    assert inputs.Q4K_BYTES * 8 / 256 == 4.5 and inputs.Q6K_BYTES * 8 / 256 == 6.5625
+    assert (inputs.Q4K_BYTES, inputs.Q5K_BYTES, inputs.Q6K_BYTES) == (144, 176, 210)
+    # 4.5, 5.5 and 6.5625 bits per weight
+    assert inputs.Q4K_BYTES * 8 / 256 == 4.5 and inputs.Q5K_BYTES * 8 / 256 == 5.5
+    assert inputs.Q6K_BYTES * 8 / 256 == 6.5625
 
 
 def test_q4k_quant_slots_are_a_bijection():
@@ -146,3 +149,46 @@ def test_config_value_ranges():
             d, sc, q = oracle.q6k_fields(w6[n, b])
             assert 1e-3 * 0.999 <= d <= 1e-2 * 1.001
             assert sc.min() >= -64 and sc.max() <= 63 and q.min() >= -32 and q.max() <= 31
+
+
+
+def test_q5k_quant_slots_are_a_bijection():
+    # low nibbles: one qs nibble at a time (all scales 1, d 1, dmin 0) -> exactly one element
+    # decodes to 1, every element once; high bits: one qh bit at a time -> exactly one
+    # element decodes to 16, every element once
+    base = np.zeros(176, np.uint8)
+    base[0:2] = [0x00, 0x3C]
+    base[4:8] = 1
+    base[12:16] = 0x01
+    for lo, n_slots, val in ((48, 256, 1), (16, 256, 16)):
+        hit = np.zeros(256, int)
+        for slot in range(n_slots):
+            b = base.copy()
+            if lo == 48:
+                b[48 + slot // 2] = 1 << (4 * (slot % 2))
+            else:
+                b[16 + slot // 8] = 1 << (slot % 8)
+            _, _, sc, mn, q = oracle.q5k_fields(b)
+            assert sc.tolist() == [1] * 8 and mn.tolist() == [0] * 8
+            nz = np.flatnonzero(q)
+            assert nz.size == 1 and q[nz[0]] == val
+            if lo == 16:
+                # qh byte l feeds position l of every sub-block; bit j selects sub-block j
+                assert nz[0] == 32 * (slot % 8) + slot // 8
+            hit[nz[0]] += 1
+        assert (hit == 1).all()
+
+
+def test_q5k_scales_and_low_bits_match_q4k():
+    # the same d, dmin, 12 scale bytes and 128 qs bytes decode to the same sc, m and low
+    # four bits in both formats; Q5_K adds 16 * (its qh bit)
+    r = np.random.default_rng(11)
+    for _ in range(20):
+        b5 = np.frombuffer(r.bytes(176), np.uint8).copy()
+        b4 = np.concatenate([b5[0:16], b5[48:176]])
+        d4, m4, sc4, mn4, q4 = oracle.q4k_fields(b4)
+        d5, m5, sc5, mn5, q5 = oracle.q5k_fields(b5)
+        assert (d4, m4) == (d5, m5) and np.array_equal(sc4, sc5) and np.array_equal(mn4, mn5)
+        assert np.array_equal(q5 % 16, q4) and q5.max() <= 31
+        qh = np.unpackbits(b5[16:48].reshape(32, 1), axis=1, bitorder="little")   # [l][j]
+        assert np.array_equal(q5 // 16, qh.T.reshape(256))

@@ -1,7 +1,7 @@
 """Pins for the oracle's integer block dots (C5, C7) and float-scaled matmul (C6).
 
 * Brute force: f64 dequantize(W) times the f64 dequantized Q8 plane must agree with the
-  oracle's block-integer path to ~1e-12 (same sums, different order), for Q4_K and Q6_K.
+  oracle's block-integer path to ~1e-12 (same sums, different order), for Q4_K, Q5_K and Q6_K.
 * Against the unquantized f32 activations the error must stay within the Q8 error bound
   sum_k |W[n,k]| * d_a / 2 (catches a wrong activation-scale index).
 * Exact invariants: zero weights, d/dmin doubling, token permutation, activation-scale doubling.
@@ -18,6 +18,8 @@ def _case(fmt, m, n, k, seed, scale_range=(-64, 63)):
     r = np.random.default_rng(seed)
     if fmt == "q4k":
         w = inputs.q4k_weights(r, n, k)
+    elif fmt == "q5k":
+        w = inputs.q5k_weights(r, n, k)
     else:
         w = inputs.q6k_weights(r, n, k, scale_range=scale_range)
     x = inputs.activations(r, m, k)
@@ -28,8 +30,8 @@ def _dequant_plane(q, d):
     return q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
 
 
-@pytest.mark.parametrize("fmt,m,n,k", [("q4k", 8, 16, 256), ("q4k", 5, 9, 512),
-                                       ("q6k", 8, 16, 256), ("q6k", 3, 7, 512)])
+@pytest.mark.parametrize("fmt,m,n,k", [("q4k", 8, 16, 256), ("q4k", 5, 9, 512), ("q5k", 8, 16, 256),
+                                       ("q5k", 4, 11, 512), ("q6k", 8, 16, 256), ("q6k", 3, 7, 512)])
 def test_brute_force_dequantized_matmul(fmt, m, n, k):
     w, x = _case(fmt, m, n, k, seed=100 + m + n)
     plane = oracle.quantize_q8(x)
@@ -39,7 +41,7 @@ def test_brute_force_dequantized_matmul(fmt, m, n, k):
     assert np.abs(y - ref).max() <= 1e-12 * scale.max()
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
 def test_q8_error_bound_against_unquantized_activations(fmt):
     w, x = _case(fmt, 6, 12, 512, seed=5)
     q, d, S = oracle.quantize_q8(x)
@@ -113,7 +115,7 @@ def test_q6k_d_is_linear():
     assert np.array_equal(oracle.matmul(b, "q6k", plane), 2 * oracle.matmul(w, "q6k", plane))
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
 def test_token_permutation_and_index_lists(fmt):
     w, x = _case(fmt, 7, 10, 512, seed=10)
     plane = oracle.quantize_q8(x)
@@ -126,7 +128,7 @@ def test_token_permutation_and_index_lists(fmt):
     assert np.array_equal(oracle.matmul(w, fmt, plane, threads=3), y)
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
 def test_activation_scale_doubling(fmt):
     w, x = _case(fmt, 3, 5, 256, seed=11)
     q, d, S = oracle.quantize_q8(x)
@@ -156,15 +158,15 @@ def test_q6k_blockdot_extremes():
     assert (I == 127 * 31 * 127 * 16 * 2).all()
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
 def test_blockdots_recomputed_from_decoded_integers(fmt):
     w, x = _case(fmt, 3, 4, 512, seed=12, scale_range=(-128, 127))
     q, d, S = oracle.quantize_q8(x)
     I, D = oracle.blockdots(w, fmt, q)
     for n in range(4):
         for sb in range(2):
-            if fmt == "q4k":
-                _, _, sc, _, qw = oracle.q4k_fields(w[n, sb])
+            if fmt in ("q4k", "q5k"):
+                _, _, sc, _, qw = (oracle.q4k_fields if fmt == "q4k" else oracle.q5k_fields)(w[n, sb])
                 scb = sc
             else:
                 _, sc, qw = oracle.q6k_fields(w[n, sb])
@@ -172,7 +174,7 @@ def test_blockdots_recomputed_from_decoded_integers(fmt):
                 a = q[m, 256 * sb:256 * sb + 256].astype(np.int64)
                 for j in range(8):
                     seg = slice(32 * j, 32 * j + 32)
-                    if fmt == "q4k":
+                    if fmt in ("q4k", "q5k"):
                         ref = scb[j] * int((qw[seg] * a[seg]).sum())
                     else:
                         lo, hi = slice(32 * j, 32 * j + 16), slice(32 * j + 16, 32 * j + 32)
@@ -180,7 +182,7 @@ def test_blockdots_recomputed_from_decoded_integers(fmt):
                     assert I[m, n, 8 * sb + j] == ref
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
 def test_matmul_is_scaled_sum_of_blockdots(fmt):
     # ties C6 to C7: Y = sum_b d_w * da * I (minus the Q4_K min term)
     w, x = _case(fmt, 3, 5, 512, seed=13)
@@ -191,13 +193,39 @@ def test_matmul_is_scaled_sum_of_blockdots(fmt):
         for m in range(3):
             acc = 0.0
             for sb in range(2):
-                if fmt == "q4k":
-                    dw, dmw, _, mn, _ = oracle.q4k_fields(w[n, sb])
+                if fmt in ("q4k", "q5k"):
+                    dw, dmw, _, mn, _ = (oracle.q4k_fields if fmt == "q4k" else oracle.q5k_fields)(w[n, sb])
                 else:
                     dw, _, _ = oracle.q6k_fields(w[n, sb])
                 for j in range(8):
                     b = 8 * sb + j
                     acc += dw * float(d[m, b]) * I[m, n, b]
-                    if fmt == "q4k":
+                    if fmt in ("q4k", "q5k"):
                         acc -= dmw * mn[j] * float(d[m, b]) * S[m, b]
             assert abs(acc - y[m, n]) <= 1e-12 * max(1.0, abs(y[m, n]))
+
+
+def test_q5k_blockdot_extremes():
+    b = np.zeros((1, 1, 176), np.uint8)
+    b[..., 16:] = 0xFF                                # qh and qs all ones: q = 31 everywhere
+    b[..., 4:16] = 0xFF                               # every 6-bit field = 63
+    qa = np.full((1, 256), 127, np.int8)
+    I, D = oracle.blockdots(b, "q5k", qa)
+    assert (D == 31 * 127 * 32).all() and (I == 63 * 31 * 127 * 32).all()
+    assert 63 * 31 * 127 * 32 < 2 ** 24                # exact in f32 as well
+
+
+def test_q5k_d_and_dmin_are_linear():
+    w, x = _case("q5k", 4, 8, 512, seed=14)
+    plane = oracle.quantize_q8(x)
+    a = w.copy()
+    a[..., 2:4] = 0                                   # dmin = 0
+    b = a.copy()
+    b[..., 0:2] = (a[..., 0:2].copy().view("<f2") * 2).view(np.uint8)
+    assert np.array_equal(oracle.matmul(b, "q5k", plane), 2 * oracle.matmul(a, "q5k", plane))
+    a = w.copy()
+    a[..., 0:2] = 0                                   # d = 0: only the min term is left
+    b = a.copy()
+    b[..., 2:4] = (a[..., 2:4].copy().view("<f2") * 2).view(np.uint8)
+    ya = oracle.matmul(a, "q5k", plane)
+    assert np.array_equal(oracle.matmul(b, "q5k", plane), 2 * ya) and np.abs(ya).max() > 0
