@@ -72,6 +72,7 @@ CASES = {
     "gemm_q4k_qproj": "config 1 q_proj GEMM: Q4_K 3584x3584, M=512",
     "gemv_q6k_lmhead": "config 4 LM head GEMV: Q6_K 152064x3584, M=1",
     "gemv_q4k_gate": "config 3 layer-1 gate GEMV: Q4_K 18944x3584, M=1",
+    "gemv_q5k_vocab": "Q5_K GEMV of the LM-head shape: 152064x3584 synthetic Q5_K weights, M=1",
     "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
     "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
 }
@@ -98,6 +99,9 @@ def run_case(args):
         M, K, N = x.shape[0], x.shape[1], w.shape[0]
     elif name == "gemv_q6k_lmhead":
         x, w, fmt, rms = I.config4_x(1), I.config4_weights(), "q6k", None
+        M, K, N = 1, I.HIDDEN, I.VOCAB
+    elif name == "gemv_q5k_vocab":
+        x, w, fmt, rms = I.config4_x(1), I.q5k_vocab_weights(), "q5k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     else:
         c = I.config3_matrix(1, 4)
@@ -484,6 +488,17 @@ def main():
                 lm[f"m{m}_{path}"] = {"ms": ms, "GB/s": gbs, "TOPS": 2 * m * I.VOCAB * I.HIDDEN / (ms * 1e-3) / 1e12}
             del x, plane, y
         line["lm_head"] = lm
+        # the Q5_K decode GEMV on a matrix of the LM-head shape (synthetic Q5_K weights)
+        w5 = torch.from_numpy(I.q5k_vocab_weights().reshape(I.VOCAB, -1)).cuda()
+        x = torch.from_numpy(I.config4_x(1)).cuda()
+        plane = B.alloc_plane(1, I.HIDDEN)
+        B.mq_quantize_q8(x, 1, I.HIDDEN, None, 0.0, plane)
+        y = torch.empty((1, I.VOCAB), dtype=torch.float32, device="cuda")
+        ms = time_events(torch, lambda: B.GEMV["q5k"](w5, I.VOCAB, I.HIDDEN, plane, 1, y), max(5, K), min(W, 3))
+        gbs = (w5.numel() + B.mq_q8_plane_bytes(1, I.HIDDEN) + 4 * I.VOCAB) / (ms * 1e-3) / 1e9
+        line["gemv_q5k"] = {"what": "Q5_K GEMV 152064 x 3584, M = 1 (synthetic Q5_K weights, 374.7 MB)",
+                            "ms": ms, "GB/s": gbs, "frac_of_hbm": gbs / hbm_peak}
+        del w5, x, plane, y
         g = lm["m1_gemv"]["GB/s"]
         line["roofline_decode"] = {"bound": "hbm", "kernel": "mq_gemv_q6k (152064x3584, M=1)", "achieved": g,
                                    "peak": hbm_peak, "unit": "GB/s", "frac": g / hbm_peak,

@@ -38,7 +38,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 template <int FMT>
 struct GvCfg {
-    static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
+    static constexpr int BB = FMT == FMT_Q4K ? 144 : FMT == FMT_Q5K ? 176 : 210;
     static constexpr int CW = 8;                               // consumer warps
     static constexpr int TPS = 2;                              // consumer threads per super-block
     static constexpr int THREADS = (CW + 2) * 32;              // + producer warp + reducer warp
@@ -46,10 +46,10 @@ struct GvCfg {
     static constexpr int SB_PER_PASS = CW * 32 / TPS;          // 128
     static constexpr int PASSES = 1;
     static constexpr int TU = SB_PER_PASS * PASSES;            // super-blocks per unit
-    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 3;  // at most; a launch may use fewer (GvArgs::nst)
+    static constexpr int STAGES = FMT == FMT_Q6K ? 3 : 4;  // at most; a launch may use fewer (GvArgs::nst)
     // tokens per pass over the weights (Q6_K: the staged activations of 8 tokens would leave
     // room for too few CTAs per SM; two passes of 4 measure faster)
-    static constexpr int MAX_MT = FMT == FMT_Q4K ? 8 : 4;
+    static constexpr int MAX_MT = FMT == FMT_Q6K ? 4 : 8;
     // CTAs per SM the launch aims for (registers: 64K / (THREADS * this))
     static constexpr int ctas_per_sm(int mt) { return mt <= 2 ? 3 : 2; }
     // unit bytes + up to 15 leading and 15 trailing alignment bytes, + 16 bytes of slack
@@ -158,6 +158,12 @@ struct Q4Half {
     uint4 hd;
     uint32_t q[16];
 };
+// Q5_K: the same header and qs half as Q4_K (qs at byte 48 here) plus all 32 qh bytes,
+// whose bit j is the fifth bit of sub-block j.
+struct Q5Half {
+    uint4 hd;
+    uint32_t qh[8], q[16];
+};
 // Q6_K: half h of a super-block -- ql bytes [64h, 64h+64), qh bytes [128+32h, 128+32h+32),
 // the eight int8 scales 8h .. 8h+7 and the fp16 d.
 struct Q6Half {
@@ -178,15 +184,37 @@ __device__ __forceinline__ void q4k_load_half(uint32_t blk, int h, Q4Half &r) {
     }
 }
 
-// Q4_K math of one half (row n, super-block sbi of the row).  Sub-block j = 4h + i (i < 4) is
-// the 32-value Q8 block 8 sbi + j: the low (i even) or high (i odd) nibbles of the qs words
-// 8 (i / 2) .. 8 (i / 2) + 7.  Its integer dot I = sc_j D_j is exact; the row's two scalings
-// are summed separately, d * sum_j d_a I_j - dmin * sum_j m_j (d_a S)_j.
-template <int MT, bool ACT, bool DUMP>
-__device__ __forceinline__ void q4k_half(const GvArgs &a, const GvAct &at, const Q4Half &r, int64_t n,
-                                         uint32_t sbi, int h, bool valid, float (&part)[MT]) {
-    using C = GvCfg<FMT_Q4K>;
-    const uint4 hd = r.hd;
+// Q5_K: loads half h of the 176-byte super-block at `blk` (16-byte aligned, as for Q4_K).
+__device__ __forceinline__ void q5k_load_half(uint32_t blk, int h, Q5Half &r) {
+    r.hd = lds128(blk);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint4 v = lds128(blk + 16 + 16 * k);
+        r.qh[4 * k] = v.x;
+        r.qh[4 * k + 1] = v.y;
+        r.qh[4 * k + 2] = v.z;
+        r.qh[4 * k + 3] = v.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 v = lds128(blk + 48 + 64 * h + 16 * k);
+        r.q[4 * k] = v.x;
+        r.q[4 * k + 1] = v.y;
+        r.q[4 * k + 2] = v.z;
+        r.q[4 * k + 3] = v.w;
+    }
+}
+
+// Q4_K / Q5_K math of one half (row n, super-block sbi of the row).  Sub-block j = 4h + i
+// (i < 4) is the 32-value Q8 block 8 sbi + j: the low (i even) or high (i odd) nibbles of
+// the qs words 8 (i / 2) .. 8 (i / 2) + 7, and for Q5_K bit j of each qh byte on top
+// (+16).  Its integer dot I = sc_j D_j is exact; the row's two scalings are summed
+// separately, d * sum_j d_a I_j - dmin * sum_j m_j (d_a S)_j.  qh is unused for Q4_K.
+template <int FMT, int MT, bool ACT, bool DUMP>
+__device__ __forceinline__ void kq_half(const GvArgs &a, const GvAct &at, const uint4 hd, const uint32_t (&qw)[16],
+                                        const uint32_t *qh, int64_t n, uint32_t sbi, int h, bool valid,
+                                        float (&part)[MT]) {
+    using C = GvCfg<FMT>;
     const float d = half_bits_to_float(hd.x & 0xffff), dmin = half_bits_to_float(hd.x >> 16);
     // the four 6-bit scales and mins of sub-blocks 4h .. 4h+3, one byte each
     const uint32_t scw = h == 0 ? (hd.y & 0x3f3f3f3fu) : ((hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u));
@@ -199,7 +227,10 @@ __device__ __forceinline__ void q4k_half(const GvArgs &a, const GvAct &at, const
     for (int i = 0; i < 4; ++i) {
         uint32_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = ((i & 1) ? (r.q[8 * (i >> 1) + e] >> 4) : r.q[8 * (i >> 1) + e]) & 0x0f0f0f0fu;
+        for (int e = 0; e < 8; ++e) {
+            v[e] = ((i & 1) ? (qw[8 * (i >> 1) + e] >> 4) : qw[8 * (i >> 1) + e]) & 0x0f0f0f0fu;
+            if constexpr (FMT == FMT_Q5K) v[e] |= ((qh[e] >> (4 * h + i)) & 0x01010101u) << 4;
+        }
         const int sc = (int)((scw >> (8 * i)) & 0xff);
         const float mf = (float)((mw >> (8 * i)) & 0xff);
 #pragma unroll
@@ -332,6 +363,17 @@ __device__ __forceinline__ void q6k_half(const GvArgs &a, const GvAct &at, const
     const float d = half_bits_to_float(r.dbits);
 #pragma unroll
     for (int t = 0; t < MT; ++t) part[t] = d * acc[t];
+}
+
+// Hand a ring stage back to the producer once this warp's reads of it are done.  Every lane
+// first waits for its own shared-memory loads to complete (membar.cta): the loaded registers
+// are consumed only after the release, and without the fence a lane's loads could still be
+// in flight when lane 0's arrival lets the next bulk copy overwrite the stage (observed as
+// wrong partials of whole warps on the GPU).
+__device__ __forceinline__ void release_stage(uint64_t *bar, int lane) {
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 }
 
 template <int FMT, int MT, bool ACT, bool DUMP>
@@ -514,15 +556,20 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
                 q6k_load_half<true>(blk, u, raw);
             else
                 q6k_load_half<false>(blk, u, raw);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
+            release_stage(&empty[s], lane);
             q6k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
         } else {
-            Q4Half raw;
-            q4k_load_half(sbase + (uint32_t)(slot * C::BB), u, raw);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);   // stage read: the producer may refill it
-            q4k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+            if constexpr (FMT == FMT_Q4K) {
+                Q4Half raw;
+                q4k_load_half(sbase + (uint32_t)(slot * C::BB), u, raw);
+                release_stage(&empty[s], lane);
+                kq_half<FMT, MT, ACT, DUMP>(a, at, raw.hd, raw.q, nullptr, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+            } else {
+                Q5Half raw;
+                q5k_load_half(sbase + (uint32_t)(slot * C::BB), u, raw);
+                release_stage(&empty[s], lane);
+                kq_half<FMT, MT, ACT, DUMP>(a, at, raw.hd, raw.q, raw.qh, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+            }
         }
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps)
@@ -541,8 +588,7 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
                 for (int t = 0; t < MT; ++t)
                     if (t < a.mt) pbuf[t * C::TU + ps * C::SB_PER_PASS + slot] = part[ps][t];
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull[pb]);
+        release_stage(&pfull[pb], lane);              // partials written: the reducer may read them
 #pragma unroll
         for (int ps = 0; ps < C::PASSES; ++ps) {
             t_sbi[ps] += tu_mod;
@@ -619,6 +665,8 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
     GvArgs a{w, N, K, p, M, 0, 0, 0, y, dump, err};
     if (fmt == FMT_Q4K)
         return dmp ? launch_fmt<FMT_Q4K, true>(a, nsm, stream) : launch_fmt<FMT_Q4K, false>(a, nsm, stream);
+    if (fmt == FMT_Q5K)
+        return dmp ? launch_fmt<FMT_Q5K, true>(a, nsm, stream) : launch_fmt<FMT_Q5K, false>(a, nsm, stream);
     return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
 }
 

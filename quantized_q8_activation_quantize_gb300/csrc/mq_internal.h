@@ -9,12 +9,12 @@
 
 namespace mq {
 
-enum Fmt : int { FMT_Q4K = 0, FMT_Q6K = 1 };
+enum Fmt : int { FMT_Q4K = 0, FMT_Q6K = 1, FMT_Q5K = 2 };
 
 constexpr int kQK = 256;     // values per k-quant super-block
 constexpr int kQ8 = 32;      // values per Q8 activation block
 
-inline int block_bytes(Fmt f) { return f == FMT_Q4K ? 144 : 210; }
+inline int block_bytes(Fmt f) { return f == FMT_Q4K ? 144 : f == FMT_Q5K ? 176 : 210; }
 
 // device pointers to the sections of one Q8 plane
 struct Plane {

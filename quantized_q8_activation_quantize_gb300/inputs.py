@@ -201,6 +201,11 @@ def config3_matrix(layer: int, idx: int):
     return {"w": w, "x": x, "fmt": fmt, "name": name}
 
 
+def q5k_vocab_weights():
+    """Synthetic Q5_K weights of the LM-head shape (VOCAB x HIDDEN), for the Q5_K decode GEMV."""
+    return q5k_weights(rng(4, STREAM_W, 5), VOCAB, HIDDEN)
+
+
 def config4_weights():
     """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
     return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)

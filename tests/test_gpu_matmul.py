@@ -20,6 +20,8 @@ def _weights(fmt, n, k, seed, scale_range=(-64, 63)):
     r = np.random.default_rng(seed)
     if fmt == "q4k":
         return inputs.q4k_weights(r, n, k)
+    if fmt == "q5k":
+        return inputs.q5k_weights(r, n, k)
     return inputs.q6k_weights(r, n, k, scale_range=scale_range)
 
 
@@ -192,3 +194,41 @@ def test_config4_lm_head(lm_head, M, paths):
     for path in paths:
         _sampled(path, "q6k", lm_head, plane, ref_plane, M, K, N, ms, ns,
                  dump_window=(0, min(M, 8), N - 100, 100))
+
+
+# ---- Q5_K: decode GEMV only (the pages' MMQ prefill formats do not include it)
+
+@pytest.mark.parametrize("M,N,K", SHAPES + GEMV_SHAPES)
+def test_q5k_gemv_shapes(M, N, K):
+    _full_check("gemv", "q5k", M, N, K, seed=M * 6151 + N * 13 + K)
+
+
+def test_q5k_gemv_extreme_blocks():
+    # q = 31 with sc = m = 63 and every code at +-127: the int32 / f32 headroom case
+    M, N, K = 9, 16, 512
+    x = np.full((M, K), 1.0, np.float32)
+    x[1::2] = -1.0
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    w = _weights("q5k", N, K, 5)
+    w[..., 4:] = 0xFF
+    y, wd = G.run_matmul("gemv", "q5k", w, plane, M, K, N)
+    assert G.rel_err(y, oracle.matmul(w, "q5k", ref_plane)) <= G.REL_TOL
+    I, _ = G.run_dump("gemv", "q5k", wd, plane, M, K, N, 0, M, 0, N)
+    assert np.array_equal(I, oracle.blockdots(w, "q5k", ref_plane[0])[0])
+
+
+def test_q5k_gemv_ffn_size():
+    # the 7B FFN gate shape (18944 x 3584) at M = 1, every output and a block-dot window
+    M, N, K = 1, 18944, 3584
+    err = _full_check("gemv", "q5k", M, N, K, seed=31, dump=False)
+    assert err <= G.REL_TOL
+    w = _weights("q5k", N, K, 31)
+    x = inputs.activations(np.random.default_rng(32), M, K)
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    _, wd = G.run_matmul("gemv", "q5k", w, plane, M, K, N)
+    n0, nc = 18000, 300
+    I, _ = G.run_dump("gemv", "q5k", wd, plane, M, K, N, 0, 1, n0, nc)
+    Iref, _ = oracle.blockdots(w, "q5k", ref_plane[0], ns=np.arange(n0, n0 + nc))
+    assert np.array_equal(I, Iref)
