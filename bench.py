@@ -61,7 +61,7 @@ def parse_args():
 # current kernels (dram__bytes_read.sum + dram__bytes_write.sum); set to None whenever a kernel
 # changes until it is captured again.
 TRAFFIC_GEMM_Q4K_GATE = 96.623616e6 + 207.959296e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
-TRAFFIC_GEMV_Q6K_LMHEAD = 447.182848e6 + 3.665920e6   # 152064x3584 Q6_K, M=1
+TRAFFIC_GEMV_Q6K_LMHEAD = 447.182848e6 + 3.463936e6   # 152064x3584 Q6_K, M=1
 # the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs)
 INT8_MMA_SYNC_PEAK_TOPS = 158.1
 

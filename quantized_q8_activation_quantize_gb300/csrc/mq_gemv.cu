@@ -515,11 +515,11 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
         asm volatile("bar.sync 1, %0;" ::"n"(C::CW * 32) : "memory");
     }
 
-    // super-block slot within the unit, and the thread's half u = lane % 2 of it: Q4_K slot
-    // 16 warp + lane / 2; Q6_K warps alternate between even and odd slots (so a warp's 210-byte
-    // blocks share one alignment mod 4): slot 2 (16 (warp / 2) + lane / 2) + warp % 2
+    // super-block slot within the unit, and the thread's half u = lane % 2 of it: Q4_K / Q5_K
+    // slot 16 warp + lane / 2; Q6_K warps alternate between even and odd slots (so a warp's
+    // 210-byte blocks share one alignment mod 4): slot 2 (16 (warp / 2) + lane / 2) + warp % 2
     const int u = lane & 1;
-    const int slot = FMT == FMT_Q4K ? 16 * warp + (lane >> 1) : 2 * (16 * (warp >> 1) + (lane >> 1)) + (warp & 1);
+    const int slot = FMT != FMT_Q6K ? 16 * warp + (lane >> 1) : 2 * (16 * (warp >> 1) + (lane >> 1)) + (warp & 1);
     // this thread's super-block of each pass: offset in its row (and the row, for the dump);
     // both advance by TU super-blocks per unit
     const uint32_t tu_mod = (uint32_t)C::TU % nb, tu_div = (uint32_t)C::TU / nb;

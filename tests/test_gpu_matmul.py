@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+from quantized_q8_activation_quantize_gb300 import binding as B
 from quantized_q8_activation_quantize_gb300 import inputs
 from tests import gpu_util as G
 
@@ -232,3 +233,26 @@ def test_q5k_gemv_ffn_size():
     I, _ = G.run_dump("gemv", "q5k", wd, plane, M, K, N, 0, 1, n0, nc)
     Iref, _ = oracle.blockdots(w, "q5k", ref_plane[0], ns=np.arange(n0, n0 + nc))
     assert np.array_equal(I, Iref)
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
+def test_gemv_repeated_launches_agree(fmt):
+    # 18944 x 3584 at M = 1: every CTA wraps its stage ring several times, the case where a
+    # stage handed back too early showed up as wrong partials of whole warps.  The reduction
+    # order is fixed, so repeated launches must agree bit for bit, and with the oracle.
+    import torch
+    M, N, K = 1, 18944, 3584
+    w = _weights(fmt, N, K, 77)
+    x = inputs.activations(np.random.default_rng(78), M, K)
+    plane, _ = G.gpu_plane(x)
+    ref = oracle.matmul(w, fmt, G.oracle_plane(x), threads=8)
+    wd = G.dev(w.reshape(N, -1))
+    ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for _ in range(5)]
+    for y in ys:
+        B.GEMV[fmt](wd, N, K, plane, M, y)
+    torch.cuda.synchronize()
+    B.mq_device_status()
+    first = ys[0].cpu().numpy()
+    assert G.rel_err(first, ref) <= G.REL_TOL
+    for y in ys[1:]:
+        assert np.array_equal(y.cpu().numpy(), first)
