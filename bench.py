@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of the Q4_K / Q6_K x Q8 path on GB300 at 7B shapes.  Prints ONE JSON line.
+"""Benchmark of the Q4_K / Q5_K / Q6_K x Q8 path on GB300 at 7B shapes.  Prints ONE JSON line.
 
 Step (the headline `value`): one 7B FFN prefill at the pages' 3314-token prompt length
 (config 2), every row of the hot path:
@@ -15,6 +15,8 @@ Also reported, measured in the same run:
              7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph),
              weight GB/s and tok/s; 3.9 GB of weights, far larger than L2.
   "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
+  "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
+             matrix of the LM-head shape (synthetic Q5_K weights).
   "roofline": the dominant kernel (Q4_K GEMM) against the measured dense bf16 tensor peak
              (f16 MMA rate = bf16 rate); "roofline_decode": the LM-head GEMV against the
              measured HBM copy bandwidth.
@@ -440,6 +442,10 @@ def main():
     # from this step's gate / up outputs
     swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f), K, W)
     swiglu_gbs = (2 * pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (swiglu_ms * 1e-3) / 1e9
+    # the Q5_K prefill GEMM on the gate shape (synthetic Q5_K weights), from the step's plane
+    w5g = torch.from_numpy(I.q5k_weights(I.rng(2, I.STREAM_W, 5), pf.F, pf.H).reshape(pf.F, -1)).cuda()
+    q5_ms = time_events(torch, lambda: B.mq_gemm_q5k(w5g, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate), K, W)
+    del w5g
 
     # ---------------- e2e through host buffers
     pf.e2e_setup()
@@ -463,6 +469,8 @@ def main():
                          "rms_quantize_gbs": qrms_gbs, "quantize_gbs": q_gbs},
         "swiglu_quantize": {"what": "SwiGLU-fused Q8 producer of the down projection, 3314 x 18944 "
                                     "(gate / up outputs of the step)", "ms": swiglu_ms, "GB/s": swiglu_gbs},
+        "gemm_q5k": {"what": "Q5_K GEMM on the gate shape 18944 x 3584, M = 3314 (synthetic Q5_K weights)",
+                     "ms": q5_ms, "TOPS": pf.gemm_q4k_ops / (q5_ms * 1e-3) / 1e12},
         "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak,
                      "traffic": TRAFFIC_GEMM_Q4K_GATE,

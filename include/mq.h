@@ -161,16 +161,20 @@ MQ_API int mq_gemv_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
                 float *y, mq_stream_t stream);
 
 /*
- * mq_gemv_q5k -- decode GEMV over Q5_K weights ("Support Matrix > CUDA notes": decode
- * uses the dp4a MMVQ kernels for Q4_K/Q5_K/Q6_K).  Same arguments and errors as
- * mq_gemv_q4k; w is raw Q5_K bytes (176 B/block: d, dmin, 12 scale bytes packed as in
- * Q4_K, qh[32], qs[128]) [N][K/256], 16-byte aligned.  Tokens go 8 per pass over W.
+ * mq_gemv_q5k / mq_gemm_q5k -- decode GEMV and prefill GEMM over Q5_K weights ("Support
+ * Matrix > CUDA notes": decode uses the dp4a MMVQ kernels for Q4_K/Q5_K/Q6_K; the
+ * tensor-core GEMM is the Q4_K skeleton with the fifth bit unpacked).  Same arguments and
+ * errors as mq_gemv_q4k / mq_gemm_q4k; w is raw Q5_K bytes (176 B/block: d, dmin, 12 scale
+ * bytes packed as in Q4_K, qh[32], qs[128]) [N][K/256], 16-byte aligned.  The GEMV takes
+ * tokens 8 per pass over W.
  *   Y[m][n] = sum over super-blocks of
  *             d * sum_j sc_j * d_a[m][j] * D_j  -  dmin * sum_j m_j * d_a[m][j] * S[m][j]
  * with D_j the exact integer dot of the 5-bit quants q = nibble + 16 * (bit j of qh[l])
  * and the Q8 codes over the 32-value sub-block j.
  */
 MQ_API int mq_gemv_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
                 float *y, mq_stream_t stream);
 
 /*
@@ -189,7 +193,8 @@ MQ_API int mq_device_status(mq_stream_t stream);
  *   I_out int32 [m_cnt][n_cnt][K/32], per 32-value block b:
  *     Q4_K, Q5_K: I = sc_j * D_j                (j = b % 8)
  *     Q6_K: I = sc_2b * D_2b + sc_2b+1 * D_2b+1 (16-value sub-blocks)
- * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k, 4 = mq_gemv_q5k.
+ * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k, 4 = mq_gemv_q5k,
+ *     5 = mq_gemm_q5k.
  * The window must lie inside [0, M) x [0, N).  Test infrastructure: slower
  * than the plain entry points.
  */

@@ -57,7 +57,7 @@ def lib():
         L.mq_q8_plane_layout.argtypes = [I64, I64, ctypes.POINTER(PlaneLayout)]
         L.mq_quantize_q8.argtypes = [P, I64, I64, P, ctypes.c_float, P, P]
         L.mq_quantize_swiglu_q8.argtypes = [P, P, I64, I64, P, P]
-        for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k"):
+        for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
         L.mq_device_status.argtypes = [P]
         L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
@@ -165,6 +165,10 @@ def mq_gemv_q5k(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemv_q5k", w, N, K, plane, M, y, stream)
 
 
+def mq_gemm_q5k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q5k", w, N, K, plane, M, y, stream)
+
+
 def mq_device_status(stream=None):
     return _check(lib().mq_device_status(_stream(stream)))
 
@@ -181,11 +185,10 @@ def mq_debug_forced_timeout(timeout_us: int, stream=None):
 
 # ------------------------------------------------------------------------------- convenience ---
 
-GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k}
+GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k}
 GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k}
 
 
 def matmul(fmt: str, w, N: int, K: int, plane, M: int, y, stream=None):
-    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on (Q5_K has
-    only the decode GEMV here, as the pages' MMQ formats do not include it)."""
-    return (GEMV if M < 16 or fmt not in GEMM else GEMM)[fmt](w, N, K, plane, M, y, stream)
+    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on."""
+    return (GEMV if M < 16 else GEMM)[fmt](w, N, K, plane, M, y, stream)

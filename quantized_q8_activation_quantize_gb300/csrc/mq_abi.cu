@@ -195,7 +195,8 @@ static int check_matmul(const char *fn, const void *w, int64_t N, int64_t K, con
 
 static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                       const Dump &dump, mq_stream_t stream) {
-    static const char *names[5] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k"};
+    static const char *names[6] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k",
+                                   "mq_gemm_q5k"};
     int rc = check_matmul(names[op], w, N, K, plane, M, y);
     if (rc != MQ_OK || M == 0 || N == 0) return rc;
     unsigned int *err = nullptr;
@@ -203,10 +204,10 @@ static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *p
     if (rc != MQ_OK) return rc;
     Plane p;
     plane_from(const_cast<void *>(plane), M, K, &p);
-    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K : op == 4 ? FMT_Q5K : FMT_Q6K;
+    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K : (op == 4 || op == 5) ? FMT_Q5K : FMT_Q6K;
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (op < 2) return launch_gemm(fmt, wb, N, K, p, M, y, dump, err, s);
+    if (op < 2 || op == 5) return launch_gemm(fmt, wb, N, K, p, M, y, dump, err, s);
     return launch_gemv(fmt, wb, N, K, p, M, y, dump, err, s);
 }
 
@@ -301,9 +302,13 @@ int mq_gemv_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t 
     return run_matmul(4, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }
 
+int mq_gemm_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(5, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
 int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                        int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *I_out, mq_stream_t stream) {
-    if (op < 0 || op > 4) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..4", op);
+    if (op < 0 || op > 5) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..5", op);
     if (m_cnt <= 0 || n_cnt <= 0 || m0 < 0 || n0 < 0 || m0 + m_cnt > M || n0 + n_cnt > N)
         return set_error(MQ_ERR_ARG, "mq_debug_blockdots: window [%lld,+%lld) x [%lld,+%lld) outside %lld x %lld",
                          (long long)m0, (long long)m_cnt, (long long)n0, (long long)n_cnt, (long long)M, (long long)N);

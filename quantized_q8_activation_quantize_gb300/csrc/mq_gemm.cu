@@ -53,12 +53,15 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 
 template <int FMT>
 struct GmCfg {
-    static constexpr int BB = FMT == FMT_Q4K ? 144 : 210;
-    static constexpr int STAGES = FMT == FMT_Q4K ? 4 : 3;
+    // Q4_K and Q5_K share the header (d, dmin, 12 packed scale / min bytes), the min term and the
+    // raw-block TMA box; Q5_K adds 32 bytes of fifth bits
+    static constexpr bool KQ = FMT != FMT_Q6K;
+    static constexpr int BB = FMT == FMT_Q4K ? 144 : FMT == FMT_Q5K ? 176 : 210;
+    static constexpr int STAGES = KQ ? 4 : 3;
     static constexpr int RAW_STAGES = FMT == FMT_Q4K ? 3 : 2;
-    static constexpr int RAW_ROW = FMT == FMT_Q4K ? 144 : 224;   // 16-B aligned superset of one block
+    static constexpr int RAW_ROW = KQ ? BB : 224;                 // 16-B aligned superset of one block
     static constexpr bool CORR = FMT == FMT_Q6K;                  // Q6_K odd |sc| > 64 correction tile
-    static constexpr bool MIN = FMT == FMT_Q4K;                   // Q4_K min term on the tensor pipe
+    static constexpr bool MIN = KQ;                               // Q4_K / Q5_K min term on the tensor pipe
     static constexpr int MIN_TILE = BM * 64;                      // 128 rows x 16 tf32 (64 B, 64-B swizzle)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * kTile;
@@ -75,10 +78,11 @@ struct GmCfg {
     static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA exceeds the per-CTA limit");
     // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file), chosen
     // per format by measurement (spill reloads in a pipeline loop cost an L2 trip each)
-    static constexpr int REGS_CTL = FMT == FMT_Q4K ? 56 : 48;
-    static constexpr int REGS_UNPACK = FMT == FMT_Q4K ? 72 : 80;
+    static constexpr int REGS_CTL = KQ ? 56 : 48;
+    static constexpr int REGS_UNPACK = KQ ? 72 : 80;
     static constexpr int REGS_EPI = 192;
     static_assert(128 * REGS_CTL + 128 * REGS_UNPACK + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 };
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < R; ++r) {
             // Q4_K: one tensor copy per super-block (producer); Q6_K: each row's cp.async (unpackers)
-            mbar_init(&bars.raw_full[r], FMT == FMT_Q4K ? 1 : 128);
+            mbar_init(&bars.raw_full[r], C::KQ ? 1 : 128);
             mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (Q4_K only)
         }
         for (int i = 0; i < 2; ++i) {
@@ -223,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmA);
             if constexpr (C::MIN) prefetch_tmap(&tmDS);
-            if constexpr (FMT == FMT_Q4K) prefetch_tmap(&tmW);
+            if constexpr (C::KQ) prefetch_tmap(&tmW);
             int st = 0, sb_issued = 0, raw_issued = 0;
-            // raw Q4_K blocks of the tile's 128 rows for one super-block: a 144 B x 128 box
+            // raw Q4_K / Q5_K blocks of the tile's 128 rows for one super-block: a BB x 128 box
             auto issue_raw = [&](int sb) -> bool {
                 const int slot = sb % R;
                 if (!mbar_wait(&bars.raw_empty[slot], ((sb / R) & 1) ^ 1, err, ERR_GEMM_RAW_FULL, abort_flag))
@@ -236,13 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 raw_issued = sb + 1;
                 return true;
             };
-            if constexpr (FMT == FMT_Q4K) {
+            if constexpr (C::KQ) {
                 for (int sb = 0; sb < R - 1 && sb < nsb; ++sb)
                     if (!issue_raw(sb)) break;
             }
             for (; st < nstages && !*abort_flag; ++st) {
                 const int s = st % S;
-                if constexpr (FMT == FMT_Q4K) {
+                if constexpr (C::KQ) {
                     // keep raw weights R-1 super-blocks ahead of the A stages
                     if ((st & 3) == 0 && (st >> 2) + R - 1 < nsb)
                         if (!issue_raw((st >> 2) + R - 1)) break;
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float d = 0.0f, dmin = 0.0f;
             int sc[16];
             int mn[8];
-            if constexpr (FMT == FMT_Q4K) {
+            if constexpr (C::KQ) {
                 const uint4 hd = valid ? lds128(blk) : make_uint4(0, 0, 0, 0);
                 d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xffff)));
                 dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
@@ -507,14 +511,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t btile = b_tile0 + s * kTile;
-                if constexpr (FMT == FMT_Q4K) {
-                    // sub-blocks 2q (low nibbles of qs[32q..32q+32)) and 2q+1 (high nibbles)
+                if constexpr (C::KQ) {
+                    // sub-blocks 2q (low nibbles of qs[32q..32q+32)) and 2q+1 (high nibbles); Q5_K:
+                    // qs at byte 48, and bit j of qh[l] is the fifth bit of element l of sub-block j
+                    constexpr uint32_t QS = FMT == FMT_Q5K ? 48 : 16;
                     uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+                    uint4 h0v = make_uint4(0, 0, 0, 0), h1v = make_uint4(0, 0, 0, 0);
                     if (valid) {
-                        q0 = lds128(blk + 16 + 32 * q);
-                        q1 = lds128(blk + 16 + 32 * q + 16);
+                        q0 = lds128(blk + QS + 32 * q);
+                        q1 = lds128(blk + QS + 32 * q + 16);
+                        if constexpr (FMT == FMT_Q5K) {
+                            h0v = lds128(blk + 16);
+                            h1v = lds128(blk + 32);
+                        }
                     }
                     const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint32_t wh[8] = {h0v.x, h0v.y, h0v.z, h0v.w, h1v.x, h1v.y, h1v.z, h1v.w};
 #pragma unroll
                     for (int hn = 0; hn < 2; ++hn) {
                         const float scf = (float)sc[2 * q + hn];
@@ -522,13 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __half2 neg = __float2half2_rn(-1024.0f * scf);
 #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
-                            const uint32_t va = (wq[2 * cc] >> (4 * hn)) & 0x0f0f0f0fu;
-                            const uint32_t vb = (wq[2 * cc + 1] >> (4 * hn)) & 0x0f0f0f0fu;
+                            uint32_t va = (wq[2 * cc] >> (4 * hn)) & 0x0f0f0f0fu;
+                            uint32_t vb = (wq[2 * cc + 1] >> (4 * hn)) & 0x0f0f0f0fu;
+                            if constexpr (FMT == FMT_Q5K) {             // + 16 * bit (2q + hn) of qh[l]
+                                va |= ((wh[2 * cc] >> (2 * q + hn)) & 0x01010101u) << 4;
+                                vb |= ((wh[2 * cc + 1] >> (2 * q + hn)) & 0x01010101u) << 4;
+                            }
                             uint32_t h0, h1, h2, h3;
                             bytes_to_h2_biased(va, h0, h1);
                             bytes_to_h2_biased(vb, h2, h3);
                             uint4 o;
-                            o.x = h2_as_u32(__hfma2(u32_as_h2(h0), sc2, neg));   // (1024 + q) sc - 1024 sc
+                            // (1024 + q) sc - 1024 sc in one fused op: exact, sc q <= 63 * 31 < 2048
+                            o.x = h2_as_u32(__hfma2(u32_as_h2(h0), sc2, neg));
                             o.y = h2_as_u32(__hfma2(u32_as_h2(h1), sc2, neg));
                             o.z = h2_as_u32(__hfma2(u32_as_h2(h2), sc2, neg));
                             o.w = h2_as_u32(__hfma2(u32_as_h2(h3), sc2, neg));
@@ -589,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bars.b_full[s]);          // one arrival per unpack warp
             }
             if (!ok) break;
-            if constexpr (FMT == FMT_Q4K) {
+            if constexpr (C::KQ) {
                 __syncwarp();                               // the warp's 32 rows of this slot are read
                 if (lane == 0) mbar_arrive(&bars.raw_empty[slot]);
             } else if (sb + R < nsb) {
@@ -642,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 da2 = make_float2(da, da);
                 // Q4_K: both 32-column halves in flight together, one wait, then the slot goes back;
                 // Q6_K (a smaller epilogue register budget): one half at a time
-                constexpr bool kBoth = FMT == FMT_Q4K;
+                constexpr bool kBoth = C::KQ;
                 uint32_t vv[kBoth ? 2 : 1][32];
                 if constexpr (kBoth) {
                     tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
@@ -810,13 +827,15 @@ int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
     if (r2 != CUDA_SUCCESS)
         return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled (d*S) failed (%d) for M=%lld K=%lld", (int)r2,
                          (long long)M, (long long)K);
-    // raw Q4_K weights: [N][K/256 * 144] bytes, one 144 B x 128-row box per super-block
+    // raw Q4_K / Q5_K weights: [N][K/256 * bb] bytes, one bb x 128-row box per super-block
+    // (bb = 144 or 176: a multiple of 16 bytes, so every box starts 16-byte aligned)
     CUtensorMap tmw;
     memset(&tmw, 0, sizeof tmw);
-    if (fmt == FMT_Q4K) {
-        const cuuint64_t dims3[2] = {(cuuint64_t)((K / kQK) * 144), (cuuint64_t)N};
-        const cuuint64_t strides3[1] = {(cuuint64_t)((K / kQK) * 144)};
-        const cuuint32_t box3[2] = {144, BN};
+    if (fmt != FMT_Q6K) {
+        const cuuint64_t bb = (cuuint64_t)block_bytes(fmt);
+        const cuuint64_t dims3[2] = {(cuuint64_t)(K / kQK) * bb, (cuuint64_t)N};
+        const cuuint64_t strides3[1] = {(cuuint64_t)(K / kQK) * bb};
+        const cuuint32_t box3[2] = {(cuuint32_t)bb, BN};
         const CUresult r3 = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims3, strides3, box3,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -828,6 +847,9 @@ int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
     if (fmt == FMT_Q4K)
         return dmp ? launch_fmt<FMT_Q4K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
                    : launch_fmt<FMT_Q4K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
+    if (fmt == FMT_Q5K)
+        return dmp ? launch_fmt<FMT_Q5K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
+                   : launch_fmt<FMT_Q5K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
     return dmp ? launch_fmt<FMT_Q6K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
                : launch_fmt<FMT_Q6K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
 }

@@ -197,7 +197,7 @@ def test_config4_lm_head(lm_head, M, paths):
                  dump_window=(0, min(M, 8), N - 100, 100))
 
 
-# ---- Q5_K: decode GEMV only (the pages' MMQ prefill formats do not include it)
+# ---- Q5_K (NEXT row): decode GEMV and prefill GEMM on the Q4_K skeletons
 
 @pytest.mark.parametrize("M,N,K", SHAPES + GEMV_SHAPES)
 def test_q5k_gemv_shapes(M, N, K):
@@ -256,3 +256,35 @@ def test_gemv_repeated_launches_agree(fmt):
     assert G.rel_err(first, ref) <= G.REL_TOL
     for y in ys[1:]:
         assert np.array_equal(y.cpu().numpy(), first)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_q5k_gemm_shapes(M, N, K):
+    _full_check("gemm", "q5k", M, N, K, seed=M * 7411 + N * 19 + K)
+
+
+def test_q5k_gemm_extreme_blocks():
+    # q = 31 with sc = m = 63 and every code at +-127: sc * q = 1953 must stay exact in f16
+    M, N, K = 16, 16, 512
+    x = np.full((M, K), 1.0, np.float32)
+    x[1::2] = -1.0
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    w = _weights("q5k", N, K, 5)
+    w[..., 4:] = 0xFF
+    y, wd = G.run_matmul("gemm", "q5k", w, plane, M, K, N)
+    assert G.rel_err(y, oracle.matmul(w, "q5k", ref_plane)) <= G.REL_TOL
+    I, _ = G.run_dump("gemm", "q5k", wd, plane, M, K, N, 0, M, 0, N)
+    assert np.array_equal(I, oracle.blockdots(w, "q5k", ref_plane[0])[0])
+
+
+def test_q5k_gemm_ffn_size_sampled():
+    # the 7B FFN gate shape with Q5_K weights at the 3314-token prompt
+    c = inputs.config2()
+    M, K, N = c["x_hidden"].shape[0], 3584, 18944
+    w = _weights("q5k", N, K, 41)
+    plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ref_plane = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ms = _sample_idx(M, 48, 7, must=(0, 127, 128, M - 1))
+    ns = _sample_idx(N, 384, 8, must=(0, N - 1))
+    _sampled("gemm", "q5k", w, plane, ref_plane, M, K, N, ms, ns, dump_window=(M - 40, 40, N - 70, 70))
