@@ -502,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- four 64-value stages of this super-block (unrolled: sc[] stays in registers)
             bool ok = true;
+            uint32_t ql[16], qh[8];      // Q6_K: the current half's low / high bits, read once per half
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int st = sb * 4 + q, s = st % S;
@@ -555,15 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // half h = q/2, groups g = 2(q%2), 2(q%2)+1; chunk c -> g = g0 + c/4, l = 8(c%4)
                     const int h = q >> 1, g0 = 2 * (q & 1);
-                    uint32_t ql[16], qh[8];
-                    if (valid) {
-                        lds_words_a2<16>(blk + 64 * h, ql);
-                        lds_words_a2<8>(blk + 128 + 32 * h, qh);
-                    } else {
+                    if ((q & 1) == 0) {
+                        if (valid) {
+                            lds_words_a2<16>(blk + 64 * h, ql);
+                            lds_words_a2<8>(blk + 128 + 32 * h, qh);
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) ql[i] = 0;
+                            for (int i = 0; i < 16; ++i) ql[i] = 0;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) qh[i] = 0;
+                            for (int i = 0; i < 8; ++i) qh[i] = 0;
+                        }
                     }
                     const int nsh = (g0 >= 2) ? 4 : 0;
                     bool need_corr = false;
