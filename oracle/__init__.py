@@ -1,4 +1,5 @@
-"""CPU oracle for the Q4_K / Q5_K / Q6_K x Q8 matmul path (numpy front end over plain C).
+"""CPU oracle for the k-quant (Q4_K / Q5_K / Q6_K) and 32-value block (Q4_0 / Q4_1 / Q5_0 /
+Q5_1 / Q8_0) x Q8 matmul path (numpy front end over plain C).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the bench's ``cpu_baseline`` / ``--impl reference`` legs, never by the
@@ -8,7 +9,8 @@ Every function here is a thin marshalling layer over ``mq_oracle.c``; the
 arithmetic, and the citation of the passage each step follows, live there.
 Arrays use the oracle's own logical layouts:
 
-* weights: raw GGML block bytes, ``[N, K/256, B]`` with B = 144 (Q4_K), 176 (Q5_K), 210 (Q6_K)
+* weights: raw GGML block bytes, ``[N, K/256, B]`` with B = 144 (Q4_K), 176 (Q5_K), 210 (Q6_K),
+  or ``[N, K/32, b]`` with b = 18 (Q4_0), 20 (Q4_1), 22 (Q5_0), 24 (Q5_1), 34 (Q8_0)
 * Q8 plane: ``q`` int8 ``[M, K]``, ``d`` f32 ``[M, K/32]``, ``S`` int32 ``[M, K/32]``
 * outputs: f64 ``[len(ms), len(ns)]`` for the listed (token, row) index pairs
 
@@ -51,6 +53,11 @@ def lib():
             f.argtypes = [P, I64, I64, P, I64, P, I64, P, I64, P, P]
         for f in (L.oq_q4k_matmul, L.oq_q5k_matmul, L.oq_q6k_matmul):
             f.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, I64, P]
+        C = ctypes.c_int
+        L.oq_b32_fields.argtypes = [C, P, P, P, P]
+        L.oq_b32_dequant.argtypes = [C, P, I64, I64, P]
+        L.oq_b32_blockdots.argtypes = [C, P, I64, P, P, I64, P, I64, P]
+        L.oq_b32_matmul.argtypes = [C, P, I64, P, P, P, P, I64, P, I64, P]
         _lib = L
     return _lib
 
@@ -61,12 +68,18 @@ def _p(a: np.ndarray):
 
 
 BLOCK_BYTES = {"q4k": 144, "q5k": 176, "q6k": 210}
+# the 32-value block formats: bytes per block and their id in mq_oracle.c (C9)
+B32 = {"q4_0": (18, 0), "q4_1": (20, 1), "q5_0": (22, 2), "q5_1": (24, 3), "q8_0": (34, 4)}
 
 
 def _weights(w: np.ndarray, fmt: str):
     w = np.ascontiguousarray(w, dtype=np.uint8)
     n = w.shape[0]
     per_row = w.size // n
+    if fmt in B32:
+        nb = per_row // B32[fmt][0]
+        assert nb * B32[fmt][0] == per_row
+        return w, n, nb * 32
     nb = per_row // BLOCK_BYTES[fmt]
     assert nb * BLOCK_BYTES[fmt] == per_row
     return w, n, nb * 256
@@ -103,10 +116,23 @@ def q6k_fields(block: np.ndarray):
     return d.value, sc, q
 
 
+def b32_fields(block: np.ndarray, fmt: str):
+    """Decode one 32-value block -> (d, m, iq[32]) with value = d * iq + m."""
+    nbytes, fid = B32[fmt]
+    blk = np.ascontiguousarray(block, dtype=np.uint8).reshape(nbytes)
+    d, m = ctypes.c_double(), ctypes.c_double()
+    iq = np.zeros(32, np.int32)
+    lib().oq_b32_fields(fid, _p(blk), ctypes.byref(d), ctypes.byref(m), _p(iq))
+    return d.value, m.value, iq
+
+
 def dequantize(w: np.ndarray, fmt: str) -> np.ndarray:
     """Dequantized weights [N, K] in f64."""
     w, n, k = _weights(w, fmt)
     out = np.empty((n, k), np.float64)
+    if fmt in B32:
+        lib().oq_b32_dequant(B32[fmt][1], _p(w), n, k, _p(out))
+        return out
     {"q4k": lib().oq_q4k_dequant, "q5k": lib().oq_q5k_dequant, "q6k": lib().oq_q6k_dequant}[fmt](_p(w), n, k, _p(out))
     return out
 
@@ -167,6 +193,9 @@ def blockdots(w: np.ndarray, fmt: str, q: np.ndarray, ms=None, ns=None):
     assert q.shape[1] == k
     ms, ns = _idx(ms, m), _idx(ns, n)
     I = np.zeros((ms.size, ns.size, k // 32), np.int32)
+    if fmt in B32:
+        lib().oq_b32_blockdots(B32[fmt][1], _p(w), k, _p(q), _p(ms), ms.size, _p(ns), ns.size, _p(I))
+        return I, None
     if fmt in ("q4k", "q5k"):
         D = np.zeros_like(I)
         fn = lib().oq_q4k_blockdots if fmt == "q4k" else lib().oq_q5k_blockdots
@@ -189,7 +218,11 @@ def matmul(w: np.ndarray, fmt: str, plane, ms=None, ns=None, threads: int = 1) -
     assert q.shape == (m, k) and d.shape == (m, k // 32) and S.shape == (m, k // 32)
     assert q.dtype == np.int8 and d.dtype == np.float32 and S.dtype == np.int32
     ms, ns = _idx(ms, m), _idx(ns, n)
-    fn = {"q4k": lib().oq_q4k_matmul, "q5k": lib().oq_q5k_matmul, "q6k": lib().oq_q6k_matmul}[fmt]
+    if fmt in B32:
+        fid = B32[fmt][1]
+        fn = lambda *a: lib().oq_b32_matmul(fid, a[0], a[2], a[3], a[4], a[5], *a[7:])   # no N, M
+    else:
+        fn = {"q4k": lib().oq_q4k_matmul, "q5k": lib().oq_q5k_matmul, "q6k": lib().oq_q6k_matmul}[fmt]
     if threads <= 1 or ns.size < 2:
         y = np.empty((ms.size, ns.size), np.float64)
         fn(_p(w), n, k, _p(q), _p(d), _p(S), m, _p(ms), ms.size, _p(ns), ns.size, _p(y))

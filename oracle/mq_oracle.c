@@ -20,6 +20,9 @@
  *       uses the dp4a MMVQ kernels for Q4_K/Q5_K/Q6_K; "Architecture > 6" item on
  *       block layouts: Q4_K/Q5_K/Q6_K are 256-value super-blocks)
  *   C2  Q6_K super-block decode (GGML layout, 210 bytes)
+ *   C9  32-value block formats Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0 (GGML layouts, 18 / 20 /
+ *       22 / 24 / 34 bytes; "Architecture > 6. Quantization & Tensor Layout": the weight
+ *       blocks are the GGML structs, these five holding 32 values each) and their block dots
  *   C3  Q8 activation quantization, blocks of 32, round half away from zero
  *   C4  RMSNorm producer y = (x * r) * w,  r = 1/sqrt(mean(x^2) + eps)
  *   C5  integer block dots between decoded weight quants and Q8 codes
@@ -502,4 +505,121 @@ void oq_q6k_matmul(const uint8_t *w, int64_t N, int64_t K,
         }
     }
     free(qw); free(scw); free(dw);
+}
+
+/* ----------------------------------------------------------------- C9 --- */
+
+/*
+ * 32-value block formats.  fmt: 0 = Q4_0, 1 = Q4_1, 2 = Q5_0, 3 = Q5_1, 4 = Q8_0.
+ *   Q4_0 (18 B): d fp16 | qs[16]            q_l = low nibble of qs[l], q_{l+16} = high nibble;
+ *                                           value = d * (q - 8)
+ *   Q4_1 (20 B): d fp16 | m fp16 | qs[16]   nibbles as Q4_0;            value = d * q + m
+ *   Q5_0 (22 B): d fp16 | qh[4] | qs[16]    q_l = nibble + 16 * bit l of the little-endian
+ *                                           32-bit qh (l = 0..31);       value = d * (q - 16)
+ *   Q5_1 (24 B): d fp16 | m fp16 | qh[4] | qs[16]   as Q5_0;            value = d * q + m
+ *   Q8_0 (34 B): d fp16 | qs[32] int8       q_l = qs[l];                 value = d * q
+ * Outputs the integer of each value in the format's own integer domain, iq[32] = q - off
+ * (off = 8, 0, 16, 0, 0), and d, m (m = 0 where the format has none), so value = d * iq + m.
+ */
+static const int oq_b32_bytes[5] = {18, 20, 22, 24, 34};
+
+int oq_b32_block_bytes(int fmt) { return (fmt >= 0 && fmt < 5) ? oq_b32_bytes[fmt] : 0; }
+
+void oq_b32_fields(int fmt, const uint8_t *blk, double *d, double *m, int32_t iq[32])
+{
+    *d = oq_half_to_double(rd16(blk));
+    *m = (fmt == 1 || fmt == 3) ? oq_half_to_double(rd16(blk + 2)) : 0.0;
+    if (fmt == 4) {
+        for (int l = 0; l < 32; ++l) iq[l] = (int8_t)blk[2 + l];
+        return;
+    }
+    const int has_m = (fmt == 1 || fmt == 3), five = (fmt == 2 || fmt == 3);
+    const uint8_t *after = blk + (has_m ? 4 : 2);
+    uint32_t qh = 0;
+    if (five) qh = (uint32_t)after[0] | ((uint32_t)after[1] << 8) | ((uint32_t)after[2] << 16) | ((uint32_t)after[3] << 24);
+    const uint8_t *qs = after + (five ? 4 : 0);
+    const int off = fmt == 0 ? 8 : fmt == 2 ? 16 : 0;
+    for (int l = 0; l < 16; ++l) {
+        int lo = qs[l] & 15, hi = qs[l] >> 4;
+        if (five) {
+            lo += 16 * (int)((qh >> l) & 1u);
+            hi += 16 * (int)((qh >> (l + 16)) & 1u);
+        }
+        iq[l] = lo - off;
+        iq[l + 16] = hi - off;
+    }
+}
+
+/* Dequantize: out[r][k] = d * iq + m (f64, exact). */
+void oq_b32_dequant(int fmt, const uint8_t *w, int64_t n_rows, int64_t K, double *out)
+{
+    int64_t nb = K / OQ_Q8;
+    int bytes = oq_b32_bytes[fmt];
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            double d, m;
+            int32_t iq[32];
+            oq_b32_fields(fmt, w + (r * nb + b) * bytes, &d, &m, iq);
+            for (int l = 0; l < 32; ++l) out[r * K + b * 32 + l] = d * iq[l] + m;
+        }
+}
+
+/*
+ * Integer checkpoint: I[b] = sum_l iq_w[32b + l] * q_a[32b + l] (the block's dot in the
+ * weight format's integer domain), [nm][nn][K/32].
+ */
+void oq_b32_blockdots(int fmt, const uint8_t *w, int64_t K, const int8_t *qa,
+                      const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, int32_t *I)
+{
+    int64_t nb = K / OQ_Q8;
+    int bytes = oq_b32_bytes[fmt];
+    int32_t *qw = (int32_t *)malloc(sizeof(int32_t) * K);
+    for (int64_t jn = 0; jn < nn; ++jn) {
+        for (int64_t b = 0; b < nb; ++b) {
+            double d, m;
+            oq_b32_fields(fmt, w + (ns[jn] * nb + b) * bytes, &d, &m, qw + b * 32);
+        }
+        for (int64_t im = 0; im < nm; ++im) {
+            const int8_t *a = qa + ms[im] * K;
+            for (int64_t b = 0; b < nb; ++b) {
+                int32_t dot = 0;
+                for (int l = 0; l < 32; ++l) dot += qw[b * 32 + l] * (int32_t)a[b * 32 + l];
+                I[(im * nn + jn) * nb + b] = dot;
+            }
+        }
+    }
+    free(qw);
+}
+
+/*
+ * Y[m][n] = sum_b [ d_b * da[m][b] * I_b + m_b * da[m][b] * S[m][b] ]  (f64), where the
+ * second term (the block's offset m_b times the Q8 block's value sum da * S) is present for
+ * Q4_1 / Q5_1 only.
+ */
+void oq_b32_matmul(int fmt, const uint8_t *w, int64_t K,
+                   const int8_t *qa, const float *da, const int32_t *Sa,
+                   const int64_t *ms, int64_t nm, const int64_t *ns, int64_t nn, double *y)
+{
+    int64_t nb = K / OQ_Q8;
+    int bytes = oq_b32_bytes[fmt];
+    int32_t *qw = (int32_t *)malloc(sizeof(int32_t) * K);
+    double *dw = (double *)malloc(sizeof(double) * nb);
+    double *mw = (double *)malloc(sizeof(double) * nb);
+    for (int64_t jn = 0; jn < nn; ++jn) {
+        for (int64_t b = 0; b < nb; ++b)
+            oq_b32_fields(fmt, w + (ns[jn] * nb + b) * bytes, &dw[b], &mw[b], qw + b * 32);
+        for (int64_t im = 0; im < nm; ++im) {
+            int64_t mm = ms[im];
+            const int8_t *a = qa + mm * K;
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                int64_t dot = 0;
+                for (int l = 0; l < 32; ++l) dot += (int64_t)qw[b * 32 + l] * a[b * 32 + l];
+                double dab = (double)da[mm * nb + b];
+                acc += dw[b] * dab * (double)dot + mw[b] * dab * (double)Sa[mm * nb + b];
+            }
+            y[im * nn + jn] = acc;
+        }
+    }
+    free(qw); free(dw); free(mw);
 }

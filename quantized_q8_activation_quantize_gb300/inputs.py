@@ -91,6 +91,27 @@ def q5k_weights(r: np.random.Generator, n_rows: int, k: int,
     return w
 
 
+# the 32-value block formats: bytes per block
+B32_BYTES = {"q4_0": 18, "q4_1": 20, "q5_0": 22, "q5_1": 24, "q8_0": 34}
+
+
+def b32_weights(r: np.random.Generator, n_rows: int, k: int, fmt: str,
+                d_range=(1e-3, 1e-2), m_range=(-0.08, 0.0)) -> np.ndarray:
+    """Weight matrix in a 32-value block format as raw bytes, shape [n_rows, k/32, B32_BYTES[fmt]].
+
+    d is fp16 uniform in ``d_range``; Q4_1 / Q5_1 add an fp16 block offset m uniform in
+    ``m_range`` (a block minimum, so at most 0); the high-bit words, nibbles and Q8_0's int8
+    quants are uniform random bytes.
+    """
+    assert k % 32 == 0
+    nb, bs = k // 32, B32_BYTES[fmt]
+    w = np.frombuffer(r.bytes(n_rows * nb * bs), dtype=np.uint8).reshape(n_rows, nb, bs).copy()
+    w[..., 0:2] = _fp16_bytes(r, (n_rows, nb), *d_range)
+    if fmt in ("q4_1", "q5_1"):
+        w[..., 2:4] = _fp16_bytes(r, (n_rows, nb), *m_range)
+    return w
+
+
 def q6k_weights(r: np.random.Generator, n_rows: int, k: int,
                 scale_range=(-64, 63), d_range=(1e-3, 1e-2)) -> np.ndarray:
     """Q6_K weight matrix as raw bytes, shape [n_rows, k/256, 210].

@@ -28,6 +28,16 @@ def test_half_to_double_matches_numpy_for_every_bit_pattern():
 @pytest.mark.parametrize("blk", golden_blocks.load(), ids=lambda b: b["name"])
 def test_hand_built_blocks(blk):
     b = blk["bytes"]
+    if blk["fmt"] in oracle.B32:
+        assert b.size == oracle.B32[blk["fmt"]][0]
+        d, m, q = oracle.b32_fields(b, blk["fmt"])
+        assert d == blk["d"]
+        for e, v in blk["q"].items():
+            assert q[e] == v, f"q[{e}]"
+        deq = oracle.dequantize(b.reshape(1, 1, -1), blk["fmt"])[0]
+        for e, v in blk["value"].items():
+            assert deq[e] == v, f"value[{e}]"
+        return
     if blk["fmt"] in ("q4k", "q5k"):
         assert b.size == (144 if blk["fmt"] == "q4k" else 176)
         d, dmin, sc, mn, q = (oracle.q4k_fields if blk["fmt"] == "q4k" else oracle.q5k_fields)(b)
@@ -192,3 +202,44 @@ def test_q5k_scales_and_low_bits_match_q4k():
         assert np.array_equal(q5 % 16, q4) and q5.max() <= 31
         qh = np.unpackbits(b5[16:48].reshape(32, 1), axis=1, bitorder="little")   # [l][j]
         assert np.array_equal(q5 // 16, qh.T.reshape(256))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q5_0", "q5_1", "q8_0"])
+def test_b32_quant_slots_are_a_bijection(fmt):
+    # with d = 1 and m = 0, setting one quant bit-field slot at a time moves exactly one
+    # element away from the all-zero block's integer, and every element is moved once
+    nbytes = oracle.B32[fmt][0]
+    base = np.zeros(nbytes, np.uint8)
+    base[0:2] = [0x00, 0x3C]
+    _, _, q0 = oracle.b32_fields(base, fmt)
+    if fmt == "q8_0":
+        slots = [(2 + l, 1) for l in range(32)]
+    else:
+        qs = nbytes - 16
+        slots = [(qs + byte, 1 << (4 * nib)) for byte in range(16) for nib in range(2)]
+        if fmt in ("q5_0", "q5_1"):
+            qh = qs - 4
+            slots += [(qh + bit // 8, 1 << (bit % 8)) for bit in range(32)]
+    hit = np.zeros(32, int)
+    for pos, val in slots:
+        b = base.copy()
+        b[pos] |= val
+        _, _, q = oracle.b32_fields(b, fmt)
+        nz = np.flatnonzero(q != q0)
+        assert nz.size == 1, (pos, val, nz)
+        hit[nz[0]] += 1
+    assert (hit == (2 if fmt in ("q5_0", "q5_1") else 1)).all()   # Q5: a nibble slot and a bit slot each
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q5_0", "q5_1", "q8_0"])
+def test_b32_generated_ranges(fmt):
+    w = inputs.b32_weights(np.random.default_rng(3), 5, 256, fmt)
+    assert w.shape == (5, 8, inputs.B32_BYTES[fmt])
+    lo = {"q4_0": -8, "q4_1": 0, "q5_0": -16, "q5_1": 0, "q8_0": -128}[fmt]
+    hi = {"q4_0": 7, "q4_1": 15, "q5_0": 15, "q5_1": 31, "q8_0": 127}[fmt]
+    for n in range(5):
+        for b in range(8):
+            d, m, q = oracle.b32_fields(w[n, b], fmt)
+            assert 1e-3 * 0.999 <= d <= 1e-2 * 1.001
+            assert (m == 0.0) if fmt in ("q4_0", "q5_0", "q8_0") else (-0.08 * 1.001 <= m <= 0.0)
+            assert q.min() >= lo and q.max() <= hi

@@ -229,3 +229,70 @@ def test_q5k_d_and_dmin_are_linear():
     b[..., 2:4] = (a[..., 2:4].copy().view("<f2") * 2).view(np.uint8)
     ya = oracle.matmul(a, "q5k", plane)
     assert np.array_equal(oracle.matmul(b, "q5k", plane), 2 * ya) and np.abs(ya).max() > 0
+
+
+B32_FMTS = ["q4_0", "q4_1", "q5_0", "q5_1", "q8_0"]
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+@pytest.mark.parametrize("m,n,k", [(8, 16, 256), (3, 7, 512)])
+def test_b32_brute_force_dequantized_matmul(fmt, m, n, k):
+    r = np.random.default_rng(200 + m + n)
+    w = inputs.b32_weights(r, n, k, fmt)
+    x = inputs.activations(r, m, k)
+    plane = oracle.quantize_q8(x)
+    y = oracle.matmul(w, fmt, plane)
+    ref = _dequant_plane(plane[0], plane[1]) @ oracle.dequantize(w, fmt).T
+    scale = np.linalg.norm(ref, axis=1, keepdims=True)
+    assert np.abs(y - ref).max() <= 1e-12 * scale.max()
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+def test_b32_blockdots_recomputed_and_matmul_is_their_scaled_sum(fmt):
+    r = np.random.default_rng(21)
+    w = inputs.b32_weights(r, 4, 256, fmt)
+    x = inputs.activations(r, 3, 256)
+    q, d, S = oracle.quantize_q8(x)
+    I, _ = oracle.blockdots(w, fmt, q)
+    y = oracle.matmul(w, fmt, (q, d, S))
+    for n in range(4):
+        for mm in range(3):
+            acc = 0.0
+            for b in range(8):
+                dw, mw, iq = oracle.b32_fields(w[n, b], fmt)
+                a = q[mm, 32 * b:32 * b + 32].astype(np.int64)
+                assert I[mm, n, b] == int((iq * a).sum())
+                acc += dw * float(d[mm, b]) * I[mm, n, b] + mw * float(d[mm, b]) * S[mm, b]
+            assert abs(acc - y[mm, n]) <= 1e-12 * max(1.0, abs(y[mm, n]))
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+def test_b32_d_and_m_are_linear(fmt):
+    r = np.random.default_rng(22)
+    w = inputs.b32_weights(r, 5, 512, fmt)
+    plane = oracle.quantize_q8(inputs.activations(r, 4, 512))
+    a = w.copy()
+    if fmt in ("q4_1", "q5_1"):
+        a[..., 2:4] = 0                               # m = 0
+    b = a.copy()
+    b[..., 0:2] = (a[..., 0:2].copy().view("<f2") * 2).view(np.uint8)
+    assert np.array_equal(oracle.matmul(b, fmt, plane), 2 * oracle.matmul(a, fmt, plane))
+    if fmt in ("q4_1", "q5_1"):
+        a = w.copy()
+        a[..., 0:2] = 0                               # d = 0: only the offset term is left
+        b = a.copy()
+        b[..., 2:4] = (a[..., 2:4].copy().view("<f2") * 2).view(np.uint8)
+        ya = oracle.matmul(a, fmt, plane)
+        assert np.array_equal(oracle.matmul(b, fmt, plane), 2 * ya) and np.abs(ya).max() > 0
+
+
+def test_b32_blockdot_extremes():
+    qa = np.full((1, 32), -128 + 1, np.int8)          # codes at -127
+    b = np.zeros((1, 1, 34), np.uint8)
+    b[..., 2:] = 0x80                                 # Q8_0 q = -128 everywhere
+    I, _ = oracle.blockdots(b, "q8_0", qa)
+    assert (I == 128 * 127 * 32).all()
+    b = np.zeros((1, 1, 24), np.uint8)
+    b[..., 4:] = 0xFF                                 # Q5_1 q = 31 everywhere
+    I, _ = oracle.blockdots(b, "q5_1", np.full((1, 32), 127, np.int8))
+    assert (I == 31 * 127 * 32).all()
