@@ -17,6 +17,8 @@ Also reported, measured in the same run:
   "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
+  "gemv_b32": the decode GEMV of each 32-value block format (Q4_0, Q4_1, Q5_0, Q5_1, Q8_0) on
+             a matrix of the LM-head shape (synthetic weights), GB/s against the HBM copy.
   "roofline": the dominant kernel (Q4_K GEMM) against the measured dense bf16 tensor peak
              (f16 MMA rate = bf16 rate); "roofline_decode": the LM-head GEMV against the
              measured HBM copy bandwidth.
@@ -75,6 +77,8 @@ CASES = {
     "gemv_q6k_lmhead": "config 4 LM head GEMV: Q6_K 152064x3584, M=1",
     "gemv_q4k_gate": "config 3 layer-1 gate GEMV: Q4_K 18944x3584, M=1",
     "gemv_q5k_vocab": "Q5_K GEMV of the LM-head shape: 152064x3584 synthetic Q5_K weights, M=1",
+    **{f"gemv_{f}_vocab": f"{f.upper()} GEMV of the LM-head shape: 152064x3584 synthetic {f.upper()} weights, M=1"
+       for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
     "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
     "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
 }
@@ -104,6 +108,10 @@ def run_case(args):
         M, K, N = 1, I.HIDDEN, I.VOCAB
     elif name == "gemv_q5k_vocab":
         x, w, fmt, rms = I.config4_x(1), I.q5k_vocab_weights(), "q5k", None
+        M, K, N = 1, I.HIDDEN, I.VOCAB
+    elif name.startswith("gemv_q") and name[6:-6] in I.B32_BYTES:
+        fmt = name[6:-6]
+        x, w, rms = I.config4_x(1), I.b32_vocab_weights(fmt), None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     else:
         c = I.config3_matrix(1, 4)
@@ -506,6 +514,16 @@ def main():
         gbs = (w5.numel() + B.mq_q8_plane_bytes(1, I.HIDDEN) + 4 * I.VOCAB) / (ms * 1e-3) / 1e9
         line["gemv_q5k"] = {"what": "Q5_K GEMV 152064 x 3584, M = 1 (synthetic Q5_K weights, 374.7 MB)",
                             "ms": ms, "GB/s": gbs, "frac_of_hbm": gbs / hbm_peak}
+        # the 32-value block formats' decode GEMV on the same shape
+        b32 = {}
+        for fmt in I.B32_BYTES:
+            wb = torch.from_numpy(I.b32_vocab_weights(fmt).reshape(I.VOCAB, -1)).cuda()
+            ms = time_events(torch, lambda: B.GEMV[fmt](wb, I.VOCAB, I.HIDDEN, plane, 1, y), max(5, K), min(W, 3))
+            gbs = (wb.numel() + B.mq_q8_plane_bytes(1, I.HIDDEN) + 4 * I.VOCAB) / (ms * 1e-3) / 1e9
+            b32[fmt] = {"ms": ms, "GB/s": gbs, "frac_of_hbm": gbs / hbm_peak, "weight_MB": wb.numel() / 1e6}
+            del wb
+        line["gemv_b32"] = {"what": "GEMV 152064 x 3584, M = 1, per 32-value block format (synthetic weights)",
+                            **b32}
         del w5, x, plane, y
         g = lm["m1_gemv"]["GB/s"]
         line["roofline_decode"] = {"bound": "hbm", "kernel": "mq_gemv_q6k (152064x3584, M=1)", "achieved": g,

@@ -178,6 +178,33 @@ MQ_API int mq_gemm_q5k(const void *w, int64_t N, int64_t K, const void *plane, i
                 float *y, mq_stream_t stream);
 
 /*
+ * mq_gemv_q4_0 / _q4_1 / _q5_0 / _q5_1 / _q8_0 -- decode GEMV over the 32-value GGML block
+ * formats ("Architecture > 6. Quantization & Tensor Layout": the weight blocks are the GGML
+ * structs; "Support Matrix > CUDA notes": decode runs the dp4a MMVQ kernels).  Same
+ * arguments, errors and token grouping (8 per pass over W) as mq_gemv_q4k.  w is raw block
+ * bytes [N][K/32], row-major with rows contiguous, 16-byte aligned; K % 256 == 0 (as for
+ * every entry point).  Blocks, little-endian:
+ *   Q4_0 18 B: d fp16, qs[16]                 q_l = low nibble of qs[l], q_{l+16} = high;  v = d (q - 8)
+ *   Q4_1 20 B: d fp16, m fp16, qs[16]         nibbles as Q4_0;                           v = d q + m
+ *   Q5_0 22 B: d fp16, qh u32, qs[16]         q_l = nibble + 16 * bit l of qh;            v = d (q - 16)
+ *   Q5_1 24 B: d fp16, m fp16, qh u32, qs[16] as Q5_0;                                    v = d q + m
+ *   Q8_0 34 B: d fp16, qs[32] int8            q_l = qs[l];                                v = d q
+ *   Y[m][n] = sum over blocks b of  d_b * d_a[m][b] * I_b  +  m_b * d_a[m][b] * S[m][b]
+ * with I_b the exact integer dot of (q - offset) and the Q8 codes over block b (m_b = 0 for
+ * the formats without m).
+ */
+MQ_API int mq_gemv_q4_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemv_q4_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemv_q5_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemv_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemv_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+
+/*
  * mq_device_status -- synchronizes `stream`, then reads and clears this
  * device's error word.  MQ_OK if no kernel reported a failed bounded wait
  * since the last call, MQ_ERR_DEVICE_TIMEOUT (with the failing wait named in
@@ -193,8 +220,10 @@ MQ_API int mq_device_status(mq_stream_t stream);
  *   I_out int32 [m_cnt][n_cnt][K/32], per 32-value block b:
  *     Q4_K, Q5_K: I = sc_j * D_j                (j = b % 8)
  *     Q6_K: I = sc_2b * D_2b + sc_2b+1 * D_2b+1 (16-value sub-blocks)
+ *     32-value formats: I = I_b = sum (q - offset) * code
  * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k, 4 = mq_gemv_q5k,
- *     5 = mq_gemm_q5k.
+ *     5 = mq_gemm_q5k, 6 = mq_gemv_q4_0, 7 = mq_gemv_q4_1, 8 = mq_gemv_q5_0,
+ *     9 = mq_gemv_q5_1, 10 = mq_gemv_q8_0.
  * The window must lie inside [0, M) x [0, N).  Test infrastructure: slower
  * than the plain entry points.
  */

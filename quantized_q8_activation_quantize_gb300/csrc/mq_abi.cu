@@ -60,7 +60,7 @@ int set_error(int code, const char *fmt, ...) {
 
 namespace {
 int g_sm_count[kMaxDevices] = {0};
-constexpr int kAttrSlots = 64;
+constexpr int kAttrSlots = 16 + 8 * 16;     // GEMM slots below 16; GEMV 16 + 16 per format
 bool g_attr_done[kMaxDevices][kAttrSlots] = {};
 }  // namespace
 
@@ -195,8 +195,9 @@ static int check_matmul(const char *fn, const void *w, int64_t N, int64_t K, con
 
 static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                       const Dump &dump, mq_stream_t stream) {
-    static const char *names[6] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k",
-                                   "mq_gemm_q5k"};
+    static const char *names[11] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
+                                    "mq_gemv_q5k", "mq_gemm_q5k", "mq_gemv_q4_0", "mq_gemv_q4_1",
+                                    "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0"};
     int rc = check_matmul(names[op], w, N, K, plane, M, y);
     if (rc != MQ_OK || M == 0 || N == 0) return rc;
     unsigned int *err = nullptr;
@@ -204,7 +205,10 @@ static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *p
     if (rc != MQ_OK) return rc;
     Plane p;
     plane_from(const_cast<void *>(plane), M, K, &p);
-    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K : (op == 4 || op == 5) ? FMT_Q5K : FMT_Q6K;
+    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K
+                    : (op == 4 || op == 5) ? FMT_Q5K
+                    : (op == 1 || op == 3) ? FMT_Q6K
+                                           : static_cast<Fmt>(FMT_Q4_0 + (op - 6));     // ops 6 .. 10
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (op < 2 || op == 5) return launch_gemm(fmt, wb, N, K, p, M, y, dump, err, s);
@@ -306,9 +310,25 @@ int mq_gemm_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t 
     return run_matmul(5, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }
 
+int mq_gemv_q4_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(6, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q4_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(7, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q5_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(8, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(9, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemv_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(10, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
 int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                        int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *I_out, mq_stream_t stream) {
-    if (op < 0 || op > 5) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..5", op);
+    if (op < 0 || op > 10) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..10", op);
     if (m_cnt <= 0 || n_cnt <= 0 || m0 < 0 || n0 < 0 || m0 + m_cnt > M || n0 + n_cnt > N)
         return set_error(MQ_ERR_ARG, "mq_debug_blockdots: window [%lld,+%lld) x [%lld,+%lld) outside %lld x %lld",
                          (long long)m0, (long long)m_cnt, (long long)n0, (long long)n_cnt, (long long)M, (long long)N);

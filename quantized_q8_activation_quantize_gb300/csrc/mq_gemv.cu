@@ -1,10 +1,12 @@
-// mq_gemv.cu -- decode GEMV (MMVQ): raw Q4_K / Q6_K weight bytes x Q8 codes with dp4a.
+// mq_gemv.cu -- decode GEMV (MMVQ): raw Q4_K / Q5_K / Q6_K / Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0
+// weight bytes x Q8 codes with dp4a.
 //
 // minfer pages, "Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ
 // kernels; "Roadmap > 0": the decode path streams the weights once per token.
 //
 // Design (HBM-bound): every weight byte is read from HBM exactly once per group of up
-// to 8 (Q4_K) or 4 (Q6_K) tokens.  The weight matrix is one flat stream of super-blocks
+// to 8 (4 for Q6_K) tokens.  The 32-value formats enter as groups of eight blocks (256
+// values, 144 .. 272 bytes, all multiples of 16), so they share the super-block machinery.  The weight matrix is one flat stream of super-blocks
 // (row-major, rows contiguous).  Each CTA owns a contiguous range of whole rows and walks
 // it in units of TU super-blocks (a unit may start or end inside a row):
 //   * a producer warp refills a 2-4 stage shared-memory ring with ONE large 1-D bulk copy
@@ -38,7 +40,7 @@ constexpr unsigned kFull = 0xffffffffu;
 
 template <int FMT>
 struct GvCfg {
-    static constexpr int BB = FMT == FMT_Q4K ? 144 : FMT == FMT_Q5K ? 176 : 210;
+    static constexpr int BB = block_bytes(FMT);
     static constexpr int CW = 8;                               // consumer warps
     static constexpr int TPS = 2;                              // consumer threads per super-block
     static constexpr int THREADS = (CW + 2) * 32;              // + producer warp + reducer warp
@@ -89,8 +91,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
-__device__ __forceinline__ void sts64(uint32_t addr, float a, float b) {
-    asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+__device__ __forceinline__ void sts64u(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
 }
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -365,6 +372,143 @@ __device__ __forceinline__ void q6k_half(const GvArgs &a, const GvAct &at, const
     for (int t = 0; t < MT; ++t) part[t] = d * acc[t];
 }
 
+// 32-value formats: half h of a group of eight blocks is blocks 4h .. 4h+3, HB = 4 x the
+// block size bytes (72 / 80 / 88 / 96 / 136) starting at byte h * HB of the group.  Groups are
+// 16-byte aligned in a unit (sizes 144 .. 272), so a half is 8-byte aligned, and 16-byte
+// aligned where HB is a multiple of 16; it is read with the widest aligned loads.  With
+// consecutive slots, a quarter-warp's four groups x two halves hit 8 distinct bank groups for
+// all but Q5_1 (192-byte groups: 2-way).
+template <int FMT>
+struct B32Half {
+    static constexpr int HB = 4 * b32_bytes(FMT);
+    static constexpr int NW = HB / 4;
+    uint32_t w[NW];
+};
+
+template <int FMT>
+__device__ __forceinline__ void b32_load_half(uint32_t blk, int h, B32Half<FMT> &r) {
+    constexpr int HB = B32Half<FMT>::HB;
+    const uint32_t base = blk + (uint32_t)(HB * h);
+    if constexpr (HB % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < HB / 16; ++k) {
+            const uint4 v = lds128(base + 16 * k);
+            r.w[4 * k] = v.x;
+            r.w[4 * k + 1] = v.y;
+            r.w[4 * k + 2] = v.z;
+            r.w[4 * k + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < HB / 8; ++k) {
+            const uint2 v = lds64(base + 8 * k);
+            r.w[2 * k] = v.x;
+            r.w[2 * k + 1] = v.y;
+        }
+    }
+}
+
+// the 4 bytes at byte offset o (a multiple of 2, known at compile time once unrolled) of a
+// half held in registers
+__device__ __forceinline__ uint32_t word_at(const uint32_t *w, int o) {
+    return (o & 3) ? __funnelshift_r(w[o >> 2], w[(o >> 2) + 1], 16) : w[o >> 2];
+}
+__device__ __forceinline__ uint32_t half_at(const uint32_t *w, int o) {
+    return (o & 3) ? (w[o >> 2] >> 16) : (w[o >> 2] & 0xffffu);
+}
+
+// 32-value formats, math of one half (row n, group sbi of the row).  Block g = 0..3 of the
+// half is the Q8 block 8 sbi + 4h + g.  Its quants, as bytes in the order of the 32 values:
+// Q8_0 the int8 quants themselves; the others the low nibbles of qs[0..15] (values 0..15)
+// and the high nibbles (values 16..31), plus 16 x bit l of the 32-bit qh for value l in the
+// five-bit formats (four qh bits spread to bit 4 of four bytes by one multiply: the shifted
+// copies of a 4-bit field at 4, 11, 18 and 25 never overlap).  The quants' offset (8 for
+// Q4_0, 16 for Q5_0) enters as the seed -off * S of the dp4a chain, so I = sum (q - off) a
+// exactly; then y += (d d_a) I [+ m (d_a S)].
+template <int FMT, int MT, bool ACT, bool DUMP>
+__device__ __forceinline__ void b32_half(const GvArgs &a, const GvAct &at, const B32Half<FMT> &r, int64_t n,
+                                         uint32_t sbi, int h, bool valid, float (&part)[MT]) {
+    using C = GvCfg<FMT>;
+    constexpr int BS = b32_bytes(FMT), OFF = b32_off(FMT);
+    constexpr bool HAS_M = b32_has_m(FMT), FIVE = b32_five(FMT);
+    constexpr int QH = HAS_M ? 4 : 2, QS = 2 + (HAS_M ? 2 : 0) + (FIVE ? 4 : 0);
+    float acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+    const uint32_t rec = at.codes + sbi * C::SB_STRIDE + C::HALF * (uint32_t)h;    // token 0's record
+#pragma unroll
+    for (int gp = 0; gp < 2; ++gp) {                // blocks 2 gp and 2 gp + 1: one table read
+        float d[2], mw[2];
+        uint32_t v[2][8];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int o = BS * (2 * gp + k);
+            d[k] = half_bits_to_float(half_at(r.w, o));
+            mw[k] = HAS_M ? half_bits_to_float(half_at(r.w, o + 2)) : 0.0f;
+            if constexpr (FMT == FMT_Q8_0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[k][e] = word_at(r.w, o + 2 + 4 * e);
+            } else {
+                const uint32_t qh = FIVE ? word_at(r.w, o + QH) : 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t qs = word_at(r.w, o + QS + 4 * e);
+                    v[k][e] = qs & 0x0f0f0f0fu;
+                    v[k][4 + e] = (qs >> 4) & 0x0f0f0f0fu;
+                    if constexpr (FIVE) {
+                        v[k][e] |= (((qh >> (4 * e)) & 0xfu) * 0x02040810u) & 0x10101010u;
+                        v[k][4 + e] |= (((qh >> (16 + 4 * e)) & 0xfu) * 0x02040810u) & 0x10101010u;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const int64_t m = a.t0 + t;
+            const bool act = t < a.mt && valid;
+            int I[2] = {0, 0};
+            if (act) {
+                if constexpr (ACT) {
+                    const uint32_t rt = rec + (uint32_t)t * at.ck;
+                    // (d_a, -off S) per block, or (d_a, d_a S) where the format has m
+                    const uint4 tb = lds128(rt + 128u + 16u * gp);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint32_t ca = rt + 32u * (2 * gp + k);
+                        const uint4 a0 = lds128(ca), a1 = lds128(ca + 16u);
+                        const float da = __uint_as_float(k ? tb.z : tb.x);
+                        const uint32_t x = k ? tb.w : tb.y;
+                        I[k] = dot16w(v[k] + 4, a1, dot16w(v[k], a0, OFF ? (int)x : 0));
+                        acc[t] = fmaf(d[k] * da, (float)I[k], acc[t]);
+                        if constexpr (HAS_M) acc[t] = fmaf(mw[k], __uint_as_float(x), acc[t]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int64_t b = (int64_t)sbi * 8 + 4 * h + 2 * gp + k;     // the Q8 block
+                        const uint4 *q = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K + 32 * b);
+                        const float da = __ldg(a.p.d + b * a.M + m);
+                        const int S = (OFF || HAS_M) ? __ldg(a.p.s + b * a.M + m) : 0;
+                        I[k] = dot16w(v[k] + 4, __ldg(q + 1), dot16w(v[k], __ldg(q), -OFF * S));
+                        acc[t] = fmaf(d[k] * da, (float)I[k], acc[t]);
+                        if constexpr (HAS_M) acc[t] = fmaf(mw[k], da * (float)S, acc[t]);
+                    }
+                }
+            }
+            if constexpr (DUMP) {
+                const Dump &dp = a.dump;
+                if (act && m >= dp.m0 && m < dp.m0 + dp.m_cnt && n >= dp.n0 && n < dp.n0 + dp.n_cnt)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        dp.out[((m - dp.m0) * dp.n_cnt + (n - dp.n0)) * (a.K / kQ8) + (int64_t)sbi * 8 + 4 * h +
+                               2 * gp + k] = I[k];
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) part[t] = acc[t];
+}
+
 // Hand a ring stage back to the producer once this warp's reads of it are done.  Every lane
 // first waits for its own shared-memory loads to complete (membar.cta): the loaded registers
 // are consumed only after the release, and without the fence a lane's loads could still be
@@ -505,10 +649,14 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
                         sts32(ent + 4u, (uint32_t)(-32 * s16));
                     }
                 } else if ((r & 1u) == 0) {
-                    // the block's entry holds (d_a, d_a * S) at 128 + 8 g
+                    // the block's entry at 128 + 8 g: (d_a, d_a * S) for the formats with a min or
+                    // offset m; (d_a, -off * S) for Q4_0 / Q5_0, the seed of their dp4a chains
                     const int64_t b = c >> 1;
                     const float da = __ldg(a.p.d + b * a.M + m);
-                    sts64(rec + 128u + 8u * ((r >> 1) & 3u), da, da * (float)__ldg(a.p.s + b * a.M + m));
+                    const int S = __ldg(a.p.s + b * a.M + m);
+                    const uint32_t x = (is_b32(FMT) && !b32_has_m(FMT)) ? (uint32_t)(-b32_off(FMT) * S)
+                                                                        : __float_as_uint(da * (float)S);
+                    sts64u(rec + 128u + 8u * ((r >> 1) & 3u), __float_as_uint(da), x);
                 }
             }
         }
@@ -559,7 +707,12 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
             release_stage(&empty[s], lane);
             q6k_half<MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
         } else {
-            if constexpr (FMT == FMT_Q4K) {
+            if constexpr (is_b32(FMT)) {
+                B32Half<FMT> raw;
+                b32_load_half<FMT>(sbase + (uint32_t)(slot * C::BB), u, raw);
+                release_stage(&empty[s], lane);
+                b32_half<FMT, MT, ACT, DUMP>(a, at, raw, t_row[0], t_sbi[0], u, slot < nsb, part[0]);
+            } else if constexpr (FMT == FMT_Q4K) {
                 Q4Half raw;
                 q4k_load_half(sbase + (uint32_t)(slot * C::BB), u, raw);
                 release_stage(&empty[s], lane);
@@ -667,6 +820,16 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
         return dmp ? launch_fmt<FMT_Q4K, true>(a, nsm, stream) : launch_fmt<FMT_Q4K, false>(a, nsm, stream);
     if (fmt == FMT_Q5K)
         return dmp ? launch_fmt<FMT_Q5K, true>(a, nsm, stream) : launch_fmt<FMT_Q5K, false>(a, nsm, stream);
+    if (fmt == FMT_Q4_0)
+        return dmp ? launch_fmt<FMT_Q4_0, true>(a, nsm, stream) : launch_fmt<FMT_Q4_0, false>(a, nsm, stream);
+    if (fmt == FMT_Q4_1)
+        return dmp ? launch_fmt<FMT_Q4_1, true>(a, nsm, stream) : launch_fmt<FMT_Q4_1, false>(a, nsm, stream);
+    if (fmt == FMT_Q5_0)
+        return dmp ? launch_fmt<FMT_Q5_0, true>(a, nsm, stream) : launch_fmt<FMT_Q5_0, false>(a, nsm, stream);
+    if (fmt == FMT_Q5_1)
+        return dmp ? launch_fmt<FMT_Q5_1, true>(a, nsm, stream) : launch_fmt<FMT_Q5_1, false>(a, nsm, stream);
+    if (fmt == FMT_Q8_0)
+        return dmp ? launch_fmt<FMT_Q8_0, true>(a, nsm, stream) : launch_fmt<FMT_Q8_0, false>(a, nsm, stream);
     return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
 }
 

@@ -9,12 +9,24 @@
 
 namespace mq {
 
-enum Fmt : int { FMT_Q4K = 0, FMT_Q6K = 1, FMT_Q5K = 2 };
+// weight formats: the 256-value k-quants, then the 32-value block formats
+enum Fmt : int { FMT_Q4K = 0, FMT_Q6K = 1, FMT_Q5K = 2, FMT_Q4_0 = 3, FMT_Q4_1 = 4, FMT_Q5_0 = 5, FMT_Q5_1 = 6, FMT_Q8_0 = 7 };
 
 constexpr int kQK = 256;     // values per k-quant super-block
 constexpr int kQ8 = 32;      // values per Q8 activation block
 
-inline int block_bytes(Fmt f) { return f == FMT_Q4K ? 144 : f == FMT_Q5K ? 176 : 210; }
+constexpr bool is_b32(int f) { return f >= FMT_Q4_0; }
+// 32-value formats: bytes of one block (fp16 d [, fp16 m] [, 32-bit qh] then the quants),
+// whether it has the offset m, whether it has the fifth bit, and the offset its unsigned
+// quants carry (value = d * (q - off) [+ m])
+constexpr int b32_bytes(int f) { return f == FMT_Q4_0 ? 18 : f == FMT_Q4_1 ? 20 : f == FMT_Q5_0 ? 22 : f == FMT_Q5_1 ? 24 : 34; }
+constexpr bool b32_has_m(int f) { return f == FMT_Q4_1 || f == FMT_Q5_1; }
+constexpr bool b32_five(int f) { return f == FMT_Q5_0 || f == FMT_Q5_1; }
+constexpr int b32_off(int f) { return f == FMT_Q4_0 ? 8 : f == FMT_Q5_0 ? 16 : 0; }
+// bytes per 256 values of a row (one k-quant super-block, or eight 32-value blocks)
+constexpr int block_bytes(int f) {
+    return f == FMT_Q4K ? 144 : f == FMT_Q5K ? 176 : f == FMT_Q6K ? 210 : 8 * b32_bytes(f);
+}
 
 // device pointers to the sections of one Q8 plane
 struct Plane {

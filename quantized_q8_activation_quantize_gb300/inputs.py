@@ -227,6 +227,12 @@ def q5k_vocab_weights():
     return q5k_weights(rng(4, STREAM_W, 5), VOCAB, HIDDEN)
 
 
+def b32_vocab_weights(fmt: str):
+    """Synthetic weights of the LM-head shape (VOCAB x HIDDEN) in a 32-value block format, for
+    that format's decode GEMV (one seed stream per format)."""
+    return b32_weights(rng(4, STREAM_W, 6 + list(B32_BYTES).index(fmt)), VOCAB, HIDDEN, fmt)
+
+
 def config4_weights():
     """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
     return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)

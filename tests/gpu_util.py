@@ -53,7 +53,7 @@ def run_dump(path, fmt, wd, plane, M, K, N, m0, mc, n0, nc):
     import torch
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     I = torch.full((mc, nc, K // 32), -7, dtype=torch.int32, device="cuda")
-    op = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv", "q6k"): 3, ("gemv", "q5k"): 4, ("gemm", "q5k"): 5}[(path, fmt)]
+    op = B.DEBUG_OP[(path, fmt)]
     B.mq_debug_blockdots(op, wd, N, K, plane, M, y, m0, mc, n0, nc, I)
     torch.cuda.synchronize()
     B.mq_device_status()

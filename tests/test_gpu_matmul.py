@@ -23,6 +23,8 @@ def _weights(fmt, n, k, seed, scale_range=(-64, 63)):
         return inputs.q4k_weights(r, n, k)
     if fmt == "q5k":
         return inputs.q5k_weights(r, n, k)
+    if fmt in inputs.B32_BYTES:
+        return inputs.b32_weights(r, n, k, fmt)
     return inputs.q6k_weights(r, n, k, scale_range=scale_range)
 
 
@@ -235,7 +237,7 @@ def test_q5k_gemv_ffn_size():
     assert np.array_equal(I, Iref)
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k", "q4_0", "q4_1", "q5_0", "q5_1", "q8_0"])
 def test_gemv_repeated_launches_agree(fmt):
     # 18944 x 3584 at M = 1: every CTA wraps its stage ring several times, the case where a
     # stage handed back too early showed up as wrong partials of whole warps.  The reduction
@@ -288,3 +290,53 @@ def test_q5k_gemm_ffn_size_sampled():
     ms = _sample_idx(M, 48, 7, must=(0, 127, 128, M - 1))
     ns = _sample_idx(N, 384, 8, must=(0, N - 1))
     _sampled("gemm", "q5k", w, plane, ref_plane, M, K, N, ms, ns, dump_window=(M - 40, 40, N - 70, 70))
+
+
+# ---- 32-value block formats Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0 (NEXT row): decode GEMV on the
+# k-quant GEMV skeleton, eight blocks to a 256-value group
+
+B32_FMTS = ["q4_0", "q4_1", "q5_0", "q5_1", "q8_0"]
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+@pytest.mark.parametrize("M,N,K", SHAPES + GEMV_SHAPES)
+def test_b32_gemv_shapes(fmt, M, N, K):
+    _full_check("gemv", fmt, M, N, K, seed=M * 5179 + N * 17 + K + len(fmt) * 3 + ord(fmt[1]) + ord(fmt[3]))
+
+
+@pytest.mark.parametrize("fmt,fill", [("q4_0", 0xFF), ("q4_0", 0x00), ("q4_1", 0xFF), ("q5_0", 0xFF),
+                                      ("q5_0", 0x00), ("q5_1", 0xFF), ("q8_0", 0x80), ("q8_0", 0x7F)])
+def test_b32_gemv_extreme_blocks(fmt, fill):
+    # every quant at the top or bottom of its range (q - offset = 7 / -8, 15 / -16, 15, 31,
+    # -128, 127) against codes at +-127: the int32 headroom and the dp4a seed
+    M, N, K = 9, 16, 512
+    x = np.full((M, K), 1.0, np.float32)
+    x[1::2] = -1.0
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    w = _weights(fmt, N, K, 6)
+    w[..., 4 if fmt in ("q4_1", "q5_1") else 2:] = fill
+    y, wd = G.run_matmul("gemv", fmt, w, plane, M, K, N)
+    assert G.rel_err(y, oracle.matmul(w, fmt, ref_plane)) <= G.REL_TOL
+    I, _ = G.run_dump("gemv", fmt, wd, plane, M, K, N, 0, M, 0, N)
+    assert np.array_equal(I, oracle.blockdots(w, fmt, ref_plane[0])[0])
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+@pytest.mark.parametrize("M,N,K", [(1, 18944, 3584), (8, 600, 18944), (3, 3584, 18944)])
+def test_b32_gemv_model_sizes(fmt, M, N, K):
+    # the 7B FFN gate (M = 1, staged activations) and down shapes (K = 18944: at M = 8 the
+    # activations no longer fit in shared memory and the kernel reads them from global memory)
+    _full_check("gemv", fmt, M, N, K, seed=N + K + M + ord(fmt[1]) * 7 + ord(fmt[3]), dump=M > 1)
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+def test_b32_gemv_vocab_sampled(fmt):
+    # the LM-head shape (152064 x 3584) at M = 1, the launch the benchmark times
+    w = inputs.b32_vocab_weights(fmt)
+    x = inputs.config4_x(1)
+    N, K = w.shape[0], 3584
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    ns = _sample_idx(N, 2048, 9, must=(0, N - 1))
+    _sampled("gemv", fmt, w, plane, ref_plane, 1, K, N, np.array([0]), ns, dump_window=(0, 1, N - 100, 100))
