@@ -17,8 +17,9 @@ Also reported, measured in the same run:
   "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
-  "gemv_b32": the decode GEMV of each 32-value block format (Q4_0, Q4_1, Q5_0, Q5_1, Q8_0) on
-             a matrix of the LM-head shape (synthetic weights), GB/s against the HBM copy.
+  "gemv_b32", "gemm_b32": the decode GEMV of each 32-value block format (Q4_0, Q4_1, Q5_0, Q5_1,
+             Q8_0) on a matrix of the LM-head shape, and its prefill GEMM on the gate shape
+             (synthetic weights).
   "roofline": the dominant kernel (Q4_K GEMM) against the measured dense bf16 tensor peak
              (f16 MMA rate = bf16 rate); "roofline_decode": the LM-head GEMV against the
              measured HBM copy bandwidth.
@@ -454,6 +455,12 @@ def main():
     w5g = torch.from_numpy(I.q5k_weights(I.rng(2, I.STREAM_W, 5), pf.F, pf.H).reshape(pf.F, -1)).cuda()
     q5_ms = time_events(torch, lambda: B.mq_gemm_q5k(w5g, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate), K, W)
     del w5g
+    gemm_b32 = {}
+    for i, fmt in enumerate(I.B32_BYTES):
+        wb = torch.from_numpy(I.b32_weights(I.rng(2, I.STREAM_W, 6 + i), pf.F, pf.H, fmt).reshape(pf.F, -1)).cuda()
+        ms_b = time_events(torch, lambda: B.GEMM[fmt](wb, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate), K, W)
+        gemm_b32[fmt] = {"ms": ms_b, "TOPS": 2 * pf.M * pf.F * pf.H / (ms_b * 1e-3) / 1e12}
+        del wb
 
     # ---------------- e2e through host buffers
     pf.e2e_setup()
@@ -479,6 +486,8 @@ def main():
                                     "(gate / up outputs of the step)", "ms": swiglu_ms, "GB/s": swiglu_gbs},
         "gemm_q5k": {"what": "Q5_K GEMM on the gate shape 18944 x 3584, M = 3314 (synthetic Q5_K weights)",
                      "ms": q5_ms, "TOPS": pf.gemm_q4k_ops / (q5_ms * 1e-3) / 1e12},
+        "gemm_b32": {"what": "GEMM on the gate shape 18944 x 3584, M = 3314, per 32-value block format "
+                             "(synthetic weights)", **gemm_b32},
         "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak,
                      "traffic": TRAFFIC_GEMM_Q4K_GATE,

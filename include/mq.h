@@ -205,6 +205,25 @@ MQ_API int mq_gemv_q8_0(const void *w, int64_t N, int64_t K, const void *plane, 
                 float *y, mq_stream_t stream);
 
 /*
+ * mq_gemm_q4_0 / _q4_1 / _q5_0 / _q5_1 / _q8_0 -- prefill GEMM over the same 32-value formats
+ * ("Support Matrix > CUDA notes": prefill (nt >= 16) runs the tensor-core MMQ path for
+ * Q4_0/Q4_1/Q5_0/Q5_1/Q8_0 as well).  Same arguments, errors and result as the matching
+ * mq_gemv_* (w as documented there), computed on the tensor cores like mq_gemm_q4k: the
+ * exact integers q - offset of each block multiply the Q8 codes into one accumulator per
+ * block, scaled by d * d_a; the Q4_1 / Q5_1 offset term m * d_a * S runs as tf32 MMAs.
+ */
+MQ_API int mq_gemm_q4_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q4_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q5_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+MQ_API int mq_gemm_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                float *y, mq_stream_t stream);
+
+/*
  * mq_device_status -- synchronizes `stream`, then reads and clears this
  * device's error word.  MQ_OK if no kernel reported a failed bounded wait
  * since the last call, MQ_ERR_DEVICE_TIMEOUT (with the failing wait named in
@@ -223,7 +242,8 @@ MQ_API int mq_device_status(mq_stream_t stream);
  *     32-value formats: I = I_b = sum (q - offset) * code
  * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k, 4 = mq_gemv_q5k,
  *     5 = mq_gemm_q5k, 6 = mq_gemv_q4_0, 7 = mq_gemv_q4_1, 8 = mq_gemv_q5_0,
- *     9 = mq_gemv_q5_1, 10 = mq_gemv_q8_0.
+ *     9 = mq_gemv_q5_1, 10 = mq_gemv_q8_0, 11 = mq_gemm_q4_0, 12 = mq_gemm_q4_1,
+ *     13 = mq_gemm_q5_0, 14 = mq_gemm_q5_1, 15 = mq_gemm_q8_0.
  * The window must lie inside [0, M) x [0, N).  Test infrastructure: slower
  * than the plain entry points.
  */

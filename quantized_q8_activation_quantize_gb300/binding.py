@@ -58,7 +58,8 @@ def lib():
         L.mq_quantize_q8.argtypes = [P, I64, I64, P, ctypes.c_float, P, P]
         L.mq_quantize_swiglu_q8.argtypes = [P, P, I64, I64, P, P]
         for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k",
-                     "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0"):
+                     "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
+                     "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
         L.mq_device_status.argtypes = [P]
         L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
@@ -190,6 +191,26 @@ def mq_gemv_q8_0(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemv_q8_0", w, N, K, plane, M, y, stream)
 
 
+def mq_gemm_q4_0(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q4_0", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q4_1(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q4_1", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q5_0(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q5_0", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q5_1(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q5_1", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q8_0(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_q8_0", w, N, K, plane, M, y, stream)
+
+
 def mq_device_status(stream=None):
     return _check(lib().mq_device_status(_stream(stream)))
 
@@ -206,16 +227,17 @@ def mq_debug_forced_timeout(timeout_us: int, stream=None):
 
 # ------------------------------------------------------------------------------- convenience ---
 
-GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k}
+GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k, "q4_0": mq_gemm_q4_0, "q4_1": mq_gemm_q4_1,
+        "q5_0": mq_gemm_q5_0, "q5_1": mq_gemm_q5_1, "q8_0": mq_gemm_q8_0}
 GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k, "q4_0": mq_gemv_q4_0, "q4_1": mq_gemv_q4_1,
         "q5_0": mq_gemv_q5_0, "q5_1": mq_gemv_q5_1, "q8_0": mq_gemv_q8_0}
 # debug op of each (kind, format) for mq_debug_blockdots
 DEBUG_OP = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv", "q6k"): 3, ("gemv", "q5k"): 4,
             ("gemm", "q5k"): 5, ("gemv", "q4_0"): 6, ("gemv", "q4_1"): 7, ("gemv", "q5_0"): 8, ("gemv", "q5_1"): 9,
-            ("gemv", "q8_0"): 10}
+            ("gemv", "q8_0"): 10, ("gemm", "q4_0"): 11, ("gemm", "q4_1"): 12, ("gemm", "q5_0"): 13,
+            ("gemm", "q5_1"): 14, ("gemm", "q8_0"): 15}
 
 
 def matmul(fmt: str, w, N: int, K: int, plane, M: int, y, stream=None):
-    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on (the
-    32-value formats have the GEMV only, which takes any M, 8 tokens per pass over W)."""
-    return (GEMV if M < 16 or fmt not in GEMM else GEMM)[fmt](w, N, K, plane, M, y, stream)
+    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on."""
+    return (GEMV if M < 16 else GEMM)[fmt](w, N, K, plane, M, y, stream)

@@ -193,26 +193,34 @@ static int check_matmul(const char *fn, const void *w, int64_t N, int64_t K, con
     return MQ_OK;
 }
 
+constexpr int kMatmulOps = 16;
+
 static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                       const Dump &dump, mq_stream_t stream) {
-    static const char *names[11] = {"mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
-                                    "mq_gemv_q5k", "mq_gemm_q5k", "mq_gemv_q4_0", "mq_gemv_q4_1",
-                                    "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0"};
-    int rc = check_matmul(names[op], w, N, K, plane, M, y);
+    // the matmul entry points by op number (the debug hook's numbering)
+    static const struct {
+        const char *name;
+        Fmt fmt;
+        bool gemm;
+    } ops[kMatmulOps] = {{"mq_gemm_q4k", FMT_Q4K, true},   {"mq_gemm_q6k", FMT_Q6K, true},
+                         {"mq_gemv_q4k", FMT_Q4K, false},  {"mq_gemv_q6k", FMT_Q6K, false},
+                         {"mq_gemv_q5k", FMT_Q5K, false},  {"mq_gemm_q5k", FMT_Q5K, true},
+                         {"mq_gemv_q4_0", FMT_Q4_0, false}, {"mq_gemv_q4_1", FMT_Q4_1, false},
+                         {"mq_gemv_q5_0", FMT_Q5_0, false}, {"mq_gemv_q5_1", FMT_Q5_1, false},
+                         {"mq_gemv_q8_0", FMT_Q8_0, false}, {"mq_gemm_q4_0", FMT_Q4_0, true},
+                         {"mq_gemm_q4_1", FMT_Q4_1, true},  {"mq_gemm_q5_0", FMT_Q5_0, true},
+                         {"mq_gemm_q5_1", FMT_Q5_1, true},  {"mq_gemm_q8_0", FMT_Q8_0, true}};
+    int rc = check_matmul(ops[op].name, w, N, K, plane, M, y);
     if (rc != MQ_OK || M == 0 || N == 0) return rc;
     unsigned int *err = nullptr;
     rc = device_state(&err);
     if (rc != MQ_OK) return rc;
     Plane p;
     plane_from(const_cast<void *>(plane), M, K, &p);
-    const Fmt fmt = (op == 0 || op == 2) ? FMT_Q4K
-                    : (op == 4 || op == 5) ? FMT_Q5K
-                    : (op == 1 || op == 3) ? FMT_Q6K
-                                           : static_cast<Fmt>(FMT_Q4_0 + (op - 6));     // ops 6 .. 10
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (op < 2 || op == 5) return launch_gemm(fmt, wb, N, K, p, M, y, dump, err, s);
-    return launch_gemv(fmt, wb, N, K, p, M, y, dump, err, s);
+    if (ops[op].gemm) return launch_gemm(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
+    return launch_gemv(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
 }
 
 }  // namespace mq
@@ -326,9 +334,26 @@ int mq_gemv_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t
     return run_matmul(10, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }
 
+int mq_gemm_q4_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(11, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_q4_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(12, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_q5_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(13, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(14, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
+    return run_matmul(15, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
 int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                        int64_t m0, int64_t m_cnt, int64_t n0, int64_t n_cnt, int32_t *I_out, mq_stream_t stream) {
-    if (op < 0 || op > 10) return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..10", op);
+    if (op < 0 || op >= kMatmulOps)
+        return set_error(MQ_ERR_ARG, "mq_debug_blockdots: op=%d not in 0..%d", op, kMatmulOps - 1);
     if (m_cnt <= 0 || n_cnt <= 0 || m0 < 0 || n0 < 0 || m0 + m_cnt > M || n0 + n_cnt > N)
         return set_error(MQ_ERR_ARG, "mq_debug_blockdots: window [%lld,+%lld) x [%lld,+%lld) outside %lld x %lld",
                          (long long)m0, (long long)m_cnt, (long long)n0, (long long)n_cnt, (long long)M, (long long)N);

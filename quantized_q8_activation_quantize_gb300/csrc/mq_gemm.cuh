@@ -1,4 +1,5 @@
-// mq_gemm.cu -- prefill GEMM (MMQ): raw Q4_K / Q6_K weights x Q8 plane on tcgen05 tensor cores.
+// mq_gemm.cuh -- prefill GEMM (MMQ): raw Q4_K / Q5_K / Q6_K and Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0
+// weights x Q8 plane on tcgen05 tensor cores.
 //
 // minfer pages, "Features > GPU -- CUDA": raw-nibble int8 GEMMs for q4_K and q6_K
 // over the producer-written q8 plane; "Support Matrix > CUDA notes": prefill
@@ -28,6 +29,11 @@
 // (one weight row per thread), 8-15 epilogue (2 per TMEM lane quadrant, 64 columns
 // each); setmaxnreg moves registers from the first two warpgroups to the epilogue.
 // Tile: 128 tokens x 128 weight rows, K staged 64 at a time.
+//
+// Kernel and launcher templates; mq_gemm_kq.cu instantiates the k-quants (and holds the entry
+// point, which encodes the tensor maps), mq_gemm_b32.cu the 32-value formats.
+#pragma once
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -53,15 +59,21 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 
 template <int FMT>
 struct GmCfg {
-    // Q4_K and Q5_K share the header (d, dmin, 12 packed scale / min bytes), the min term and the
-    // raw-block TMA box; Q5_K adds 32 bytes of fifth bits
-    static constexpr bool KQ = FMT != FMT_Q6K;
-    static constexpr int BB = FMT == FMT_Q4K ? 144 : FMT == FMT_Q5K ? 176 : 210;
-    static constexpr int STAGES = KQ ? 4 : 3;
+    // Q4_K and Q5_K share the header (d, dmin, 12 packed scale / min bytes) and the min term;
+    // Q5_K adds 32 bytes of fifth bits.  The 32-value formats (B32) come as groups of eight
+    // blocks per 256 values, each block with its own fp16 d (and m for Q4_1 / Q5_1).  Every
+    // format but Q6_K has a 16-byte multiple per 256 values and takes its raw rows by TMA (TMW).
+    static constexpr bool KQ = FMT == FMT_Q4K || FMT == FMT_Q5K;
+    static constexpr bool B32 = is_b32(FMT);
+    static constexpr bool TMW = FMT != FMT_Q6K;
+    static constexpr int BB = block_bytes(FMT);
+    static constexpr int TMW_ELEM = B32 ? 2 : 1;                  // bytes per tensor-map element (box <= 256)
+    static constexpr int STAGES = TMW ? 4 : 3;
     static constexpr int RAW_STAGES = FMT == FMT_Q4K ? 3 : 2;
-    static constexpr int RAW_ROW = KQ ? BB : 224;                 // 16-B aligned superset of one block
+    static constexpr int RAW_ROW = TMW ? BB : 224;                // 16-B aligned superset of one block
     static constexpr bool CORR = FMT == FMT_Q6K;                  // Q6_K odd |sc| > 64 correction tile
-    static constexpr bool MIN = KQ;                               // Q4_K / Q5_K min term on the tensor pipe
+    // the min / offset term on the tensor pipe: Q4_K / Q5_K -dmin m_j, Q4_1 / Q5_1 the block offset m
+    static constexpr bool MIN = KQ || b32_has_m(FMT);
     static constexpr int MIN_TILE = BM * 64;                      // 128 rows x 16 tf32 (64 B, 64-B swizzle)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * kTile;
@@ -69,8 +81,9 @@ struct GmCfg {
     static constexpr int OFF_AMIN = OFF_BC + (CORR ? STAGES * kTile : 0);
     static constexpr int OFF_BMIN = OFF_AMIN + (MIN ? 2 * MIN_TILE : 0);
     static constexpr int OFF_RAW = OFF_BMIN + (MIN ? 2 * MIN_TILE : 0);
-    static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;   // fp16 d per weight row, 2 slots
-    static constexpr int OFF_DA = OFF_INFO + 2 * BN * 4;                    // d_a [2][8 blocks][128 tokens]
+    // row factors, 2 slots: the super-block d per weight row, or (B32) each block's d [8][128]
+    static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;
+    static constexpr int OFF_DA = OFF_INFO + 2 * BN * 4 * (B32 ? 8 : 1);    // d_a [2][8 blocks][128 tokens]
     static constexpr int OFF_FLAG = OFF_DA + 2 * 8 * BM * 4;
     static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
     // a_full[S] b_full[S] ab_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] acc_full[3]
@@ -81,8 +94,8 @@ struct GmCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA exceeds the per-CTA limit");
     // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file), chosen
     // per format by measurement (spill reloads in a pipeline loop cost an L2 trip each)
-    static constexpr int REGS_CTL = KQ ? 56 : 48;
-    static constexpr int REGS_UNPACK = KQ ? 72 : 80;
+    static constexpr int REGS_CTL = TMW ? 56 : 48;
+    static constexpr int REGS_UNPACK = TMW ? 72 : 80;
     static constexpr int REGS_EPI = 192;
     static_assert(128 * REGS_CTL + 128 * REGS_UNPACK + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 };
@@ -189,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < R; ++r) {
             // Q4_K: one tensor copy per super-block (producer); Q6_K: each row's cp.async (unpackers)
-            mbar_init(&bars.raw_full[r], C::KQ ? 1 : 128);
-            mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (Q4_K only)
+            mbar_init(&bars.raw_full[r], C::TMW ? 1 : 128);
+            mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (TMA-fed formats only)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.info_full[i], 4);
@@ -227,26 +240,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmA);
             if constexpr (C::MIN) prefetch_tmap(&tmDS);
-            if constexpr (C::KQ) prefetch_tmap(&tmW);
+            if constexpr (C::TMW) prefetch_tmap(&tmW);
             int st = 0, sb_issued = 0, raw_issued = 0;
-            // raw Q4_K / Q5_K blocks of the tile's 128 rows for one super-block: a BB x 128 box
+            // raw blocks of the tile's 128 rows for one super-block (256 values): a BB-byte x 128 box
             auto issue_raw = [&](int sb) -> bool {
                 const int slot = sb % R;
                 if (!mbar_wait(&bars.raw_empty[slot], ((sb / R) & 1) ^ 1, err, ERR_GEMM_RAW_FULL, abort_flag))
                     return false;
                 mbar_arrive_expect_tx(&bars.raw_full[slot], BN * C::RAW_ROW);
-                tma_load_2d(sm + C::OFF_RAW + slot * BN * C::RAW_ROW, &tmW, sb * C::BB, (int32_t)n0,
+                tma_load_2d(sm + C::OFF_RAW + slot * BN * C::RAW_ROW, &tmW, sb * (C::BB / C::TMW_ELEM), (int32_t)n0,
                             &bars.raw_full[slot]);
                 raw_issued = sb + 1;
                 return true;
             };
-            if constexpr (C::KQ) {
+            if constexpr (C::TMW) {
                 for (int sb = 0; sb < R - 1 && sb < nsb; ++sb)
                     if (!issue_raw(sb)) break;
             }
             for (; st < nstages && !*abort_flag; ++st) {
                 const int s = st % S;
-                if constexpr (C::KQ) {
+                if constexpr (C::TMW) {
                     // keep raw weights R-1 super-blocks ahead of the A stages
                     if ((st & 3) == 0 && (st >> 2) + R - 1 < nsb)
                         if (!issue_raw((st >> 2) + R - 1)) break;
@@ -444,7 +457,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             float d = 0.0f, dmin = 0.0f;
             int sc[16];
             int mn[8];
-            if constexpr (C::KQ) {
+            float dw[8], mw[8];          // 32-value formats: each block's d and m (m = 0 without one)
+            if constexpr (C::B32) {
+                // block j's fp16 d at byte BS j of the group (2-byte aligned), m right after it
+                constexpr int BS = b32_bytes(FMT);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t o = (uint32_t)(BS * j);
+                    const uint32_t wd = valid ? lds32(blk + (o & ~3u)) : 0u;
+                    const uint32_t dbits = (o & 2u) ? (wd >> 16) : (wd & 0xffffu);
+                    dw[j] = __half2float(__ushort_as_half((unsigned short)dbits));
+                    mw[j] = 0.0f;
+                    if constexpr (b32_has_m(FMT))      // Q4_1 / Q5_1 blocks are 4-byte aligned: d | m << 16
+                        mw[j] = __half2float(__ushort_as_half((unsigned short)(wd >> 16)));
+                }
+            } else if constexpr (C::KQ) {
                 const uint4 hd = valid ? lds128(blk) : make_uint4(0, 0, 0, 0);
                 d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xffff)));
                 dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
@@ -478,14 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(kFull, mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY,
                                              abort_flag)))
                 break;
-            info0[(sb & 1) * BN + r] = d;
+            if constexpr (C::B32) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) info0[((sb & 1) * 8 + j) * BN + r] = dw[j];
+            } else {
+                info0[(sb & 1) * BN + r] = d;
+            }
             if constexpr (C::MIN) {
                 // -dmin*m_j has at most 17 significant bits (exact in f32); it splits exactly into
-                // a tf32 pair: row = [hi_0..hi_7 | lo_0..lo_7]
+                // a tf32 pair: row = [hi_0..hi_7 | lo_0..lo_7].  The fp16 block offset m of Q4_1 /
+                // Q5_1 is exact in tf32 itself (lo = 0).
                 uint32_t wh[8], wl[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float v = -(dmin * (float)mn[j]);
+                    const float v = C::B32 ? mw[j] : -(dmin * (float)mn[j]);
                     const float vh = tf32_rn(v);
                     wh[j] = __float_as_uint(vh);
                     wl[j] = __float_as_uint(v - vh);
@@ -512,7 +545,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t btile = b_tile0 + s * kTile;
-                if constexpr (C::KQ) {
+                if constexpr (C::B32) {
+                    // blocks 2q and 2q+1 of the group: 32 values each, as the exact f16 integers
+                    // q - off (Q8_0: the int8 quant) -- 1024 + byte by a byte permute, minus 1024 + off
+                    constexpr int BS = b32_bytes(FMT), OFF = b32_off(FMT);
+                    constexpr bool HAS_M = b32_has_m(FMT), FIVE = b32_five(FMT), Q8 = FMT == FMT_Q8_0;
+                    constexpr int QH = HAS_M ? 4 : 2, QS = 2 + (HAS_M ? 2 : 0) + (FIVE ? 4 : 0);
+                    const __half2 bias = __float2half2_rn(1024.0f + (Q8 ? 128.0f : (float)OFF));
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        // the block's 16-byte aligned superset (2 or 3 reads, inside the group)
+                        const int o0 = BS * (2 * q + k), a0 = o0 & ~15, nu = (o0 + BS - a0 + 15) >> 4;
+                        uint32_t wv[12];
+#pragma unroll
+                        for (int u = 0; u < 3; ++u) {
+                            uint4 t = make_uint4(0, 0, 0, 0);
+                            if (u < nu && valid) t = lds128(blk + (uint32_t)(a0 + 16 * u));
+                            wv[4 * u] = t.x;
+                            wv[4 * u + 1] = t.y;
+                            wv[4 * u + 2] = t.z;
+                            wv[4 * u + 3] = t.w;
+                        }
+                        const int b = o0 - a0;           // the block's first byte in wv (even)
+                        auto word = [&](int o) -> uint32_t {   // 4 bytes at byte b + o of the block
+                            const int x = b + o;
+                            return (x & 3) ? __funnelshift_r(wv[x >> 2], wv[(x >> 2) + 1], 16) : wv[x >> 2];
+                        };
+                        const uint32_t qhw = FIVE ? word(QH) : 0u;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {    // values 8c .. 8c+7 of the block
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                uint32_t v;
+                                if constexpr (Q8) {
+                                    v = word(2 + 8 * c + 4 * e) ^ 0x80808080u;      // int8 -> q + 128
+                                } else {
+                                    // values 8c + 4e .. +3: nibbles of qs word 2 (c & 1) + e, low for c < 2
+                                    const int ew = 2 * (c & 1) + e;
+                                    v = (word(QS + 4 * ew) >> (4 * (c >> 1))) & 0x0f0f0f0fu;
+                                    if constexpr (FIVE)
+                                        v |= (((qhw >> (16 * (c >> 1) + 4 * ew)) & 0xfu) * 0x02040810u) & 0x10101010u;
+                                }
+                                uint32_t h0, h1;
+                                bytes_to_h2_biased(v, h0, h1);
+                                o[2 * e] = h2_as_u32(__hsub2(u32_as_h2(h0), bias));
+                                o[2 * e + 1] = h2_as_u32(__hsub2(u32_as_h2(h1), bias));
+                            }
+                            sts128(sw128_chunk(btile, r, 4 * k + c), make_uint4(o[0], o[1], o[2], o[3]));
+                        }
+                    }
+                } else if constexpr (C::KQ) {
                     // sub-blocks 2q (low nibbles of qs[32q..32q+32)) and 2q+1 (high nibbles); Q5_K:
                     // qs at byte 48, and bit j of qh[l] is the fifth bit of element l of sub-block j
                     constexpr uint32_t QS = FMT == FMT_Q5K ? 48 : 16;
@@ -608,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bars.b_full[s]);          // one arrival per unpack warp
             }
             if (!ok) break;
-            if constexpr (C::KQ) {
+            if constexpr (C::TMW) {
                 __syncwarp();                               // the warp's 32 rows of this slot are read
                 if (lane == 0) mbar_arrive(&bars.raw_empty[slot]);
             } else if (sb + R < nsb) {
@@ -648,6 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < nsb && ok; ++sb) {
             if (!mbar_wait(&bars.da_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_DA, abort_flag)) break;
             const float *da_sb = da_tok + (sb & 1) * 8 * BM;
+            // 32-value formats: every block's d per weight row is needed from the first block on
+            if constexpr (C::B32)
+                if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int gb = sb * 8 + j;
@@ -661,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 da2 = make_float2(da, da);
                 // Q4_K: both 32-column halves in flight together, one wait, then the slot goes back;
                 // Q6_K (a smaller epilogue register budget): one half at a time
-                constexpr bool kBoth = C::KQ;
+                constexpr bool kBoth = C::TMW;
                 uint32_t vv[kBoth ? 2 : 1][32];
                 if constexpr (kBoth) {
                     tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
@@ -683,10 +769,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     const uint32_t (&v)[32] = vv[kBoth ? hh : 0];
+                    if constexpr (C::B32) {
+                        // y += I (d_a d_w): d_w of the 32 weight rows from the unpackers' table
+                        const float4 *dwv =
+                            reinterpret_cast<const float4 *>(info0 + ((sb & 1) * 8 + j) * BN + col0 + 32 * hh);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        part[16 * hh + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                                       da2, part[16 * hh + i]);
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 dv = dwv[i4];
+                            const float2 c0 = __fmul2_rn(da2, make_float2(dv.x, dv.y));
+                            const float2 c1 = __fmul2_rn(da2, make_float2(dv.z, dv.w));
+                            acc[16 * hh + 2 * i4] = __ffma2_rn(
+                                make_float2(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1])), c0,
+                                acc[16 * hh + 2 * i4]);
+                            acc[16 * hh + 2 * i4 + 1] = __ffma2_rn(
+                                make_float2(__uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3])), c1,
+                                acc[16 * hh + 2 * i4 + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            part[16 * hh + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                                           da2, part[16 * hh + i]);
+                    }
                     if constexpr (DUMP) {
                         if (valid_m && m >= dump.m0 && m < dump.m0 + dump.m_cnt) {
 #pragma unroll
@@ -702,6 +806,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- super-block end: acc += d * part (d: fp16 factor of each weight row)
+            if constexpr (C::B32) {
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars.info_empty[sb & 1]);
+                    mbar_arrive(&bars.da_empty[sb & 1]);
+                }
+                continue;
+            }
             if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
             const float4 *info = reinterpret_cast<const float4 *>(info0 + (sb & 1) * BN + col0);
             // all 16 loads of the 64 row factors first (independent, their latencies overlap), then the FMAs
@@ -770,24 +882,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
 template <int FMT, bool DUMP>
 int launch_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap &tmw, const uint8_t *w, int64_t N,
                int64_t K, const Plane &p, int64_t M, float *y, const Dump &dump, unsigned int *err,
@@ -803,58 +897,9 @@ int launch_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap
 
 }  // namespace
 
-int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
-                const Dump &dump, unsigned int *err, cudaStream_t stream) {
-    EncodeTiledFn enc = encode_tiled_fn();
-    if (enc == nullptr) return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-    if ((M + BM - 1) / BM > 65535) return set_error(MQ_ERR_SHAPE, "M=%lld: more than 65535 token tiles", (long long)M);
-    CUtensorMap tm;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {BK, BM};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.q16, dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for M=%lld K=%lld", (int)r,
-                                            (long long)M, (long long)K);
-    // d*S tf32 pairs: [M][2*K/32] f32, one 128-token x 16-value box per super-block, 64-byte swizzle
-    CUtensorMap tmds;
-    const cuuint64_t dims2[2] = {(cuuint64_t)(2 * (K / kQ8)), (cuuint64_t)M};
-    const cuuint64_t strides2[1] = {(cuuint64_t)(2 * (K / kQ8)) * 4};
-    const cuuint32_t box2[2] = {16, BM};
-    const CUresult r2 = enc(&tmds, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ds, dims2, strides2, box2, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r2 != CUDA_SUCCESS)
-        return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled (d*S) failed (%d) for M=%lld K=%lld", (int)r2,
-                         (long long)M, (long long)K);
-    // raw Q4_K / Q5_K weights: [N][K/256 * bb] bytes, one bb x 128-row box per super-block
-    // (bb = 144 or 176: a multiple of 16 bytes, so every box starts 16-byte aligned)
-    CUtensorMap tmw;
-    memset(&tmw, 0, sizeof tmw);
-    if (fmt != FMT_Q6K) {
-        const cuuint64_t bb = (cuuint64_t)block_bytes(fmt);
-        const cuuint64_t dims3[2] = {(cuuint64_t)(K / kQK) * bb, (cuuint64_t)N};
-        const cuuint64_t strides3[1] = {(cuuint64_t)(K / kQK) * bb};
-        const cuuint32_t box3[2] = {(cuuint32_t)bb, BN};
-        const CUresult r3 = enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims3, strides3, box3,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r3 != CUDA_SUCCESS)
-            return set_error(MQ_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d) for N=%lld K=%lld", (int)r3,
-                             (long long)N, (long long)K);
-    }
-    const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
-    if (fmt == FMT_Q4K)
-        return dmp ? launch_fmt<FMT_Q4K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
-                   : launch_fmt<FMT_Q4K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
-    if (fmt == FMT_Q5K)
-        return dmp ? launch_fmt<FMT_Q5K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
-                   : launch_fmt<FMT_Q5K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
-    return dmp ? launch_fmt<FMT_Q6K, true>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream)
-               : launch_fmt<FMT_Q6K, false>(tm, tmds, tmw, w, N, K, p, M, y, dump, err, stream);
-}
+// the 32-value formats' launches (mq_gemm_b32.cu), with the tensor maps launch_gemm encodes
+int launch_gemm_b32(Fmt fmt, const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap &tmw,
+                    const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y, const Dump &dump,
+                    unsigned int *err, cudaStream_t stream);
 
 }  // namespace mq
-

@@ -1,4 +1,4 @@
-// mq_gemv.cu -- decode GEMV (MMVQ): raw Q4_K / Q5_K / Q6_K / Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0
+// mq_gemv.cuh -- decode GEMV (MMVQ): raw Q4_K / Q5_K / Q6_K / Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0
 // weight bytes x Q8 codes with dp4a.
 //
 // minfer pages, "Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ
@@ -27,6 +27,11 @@
 // groups, plus per-block scale data: (d_a, d_a * S) for Q4_K; d_a and the -32 code
 // offset as -32 * S16 per 16-value half block for Q6_K, which seeds the dp4a chain), so
 // the inner loop reads 4 wavefronts per 512 bytes instead of one scattered L1 line per lane.
+//
+// Kernel and launcher templates; mq_gemv_kq.cu instantiates the k-quants (and holds the entry
+// point), mq_gemv_b32.cu the 32-value formats, so the two compile in parallel.
+#pragma once
+
 #include <cuda_fp16.h>
 
 #include "mq_device.cuh"
@@ -810,27 +815,5 @@ int launch_fmt(GvArgs a, int nsm, cudaStream_t stream) {
 }
 
 }  // namespace
-
-int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
-                const Dump &dump, unsigned int *err, cudaStream_t stream) {
-    const int nsm = sm_count();
-    const bool dmp = dump.m_cnt > 0 && dump.n_cnt > 0;
-    GvArgs a{w, N, K, p, M, 0, 0, 0, y, dump, err};
-    if (fmt == FMT_Q4K)
-        return dmp ? launch_fmt<FMT_Q4K, true>(a, nsm, stream) : launch_fmt<FMT_Q4K, false>(a, nsm, stream);
-    if (fmt == FMT_Q5K)
-        return dmp ? launch_fmt<FMT_Q5K, true>(a, nsm, stream) : launch_fmt<FMT_Q5K, false>(a, nsm, stream);
-    if (fmt == FMT_Q4_0)
-        return dmp ? launch_fmt<FMT_Q4_0, true>(a, nsm, stream) : launch_fmt<FMT_Q4_0, false>(a, nsm, stream);
-    if (fmt == FMT_Q4_1)
-        return dmp ? launch_fmt<FMT_Q4_1, true>(a, nsm, stream) : launch_fmt<FMT_Q4_1, false>(a, nsm, stream);
-    if (fmt == FMT_Q5_0)
-        return dmp ? launch_fmt<FMT_Q5_0, true>(a, nsm, stream) : launch_fmt<FMT_Q5_0, false>(a, nsm, stream);
-    if (fmt == FMT_Q5_1)
-        return dmp ? launch_fmt<FMT_Q5_1, true>(a, nsm, stream) : launch_fmt<FMT_Q5_1, false>(a, nsm, stream);
-    if (fmt == FMT_Q8_0)
-        return dmp ? launch_fmt<FMT_Q8_0, true>(a, nsm, stream) : launch_fmt<FMT_Q8_0, false>(a, nsm, stream);
-    return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
-}
 
 }  // namespace mq

@@ -80,6 +80,8 @@ int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, fl
 int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, const Plane &p, cudaStream_t stream);
 int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
+int launch_gemv_b32(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+                    const Dump &dump, unsigned int *err, cudaStream_t stream);
 int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
 

@@ -20,7 +20,8 @@ def L():
 EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quantize_q8", "mq_quantize_swiglu_q8",
             "mq_gemm_q4k",
             "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k", "mq_device_status", "mq_debug_blockdots",
-            "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0"}
+            "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
+            "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"}
 
 
 def test_header_declares_the_boundary():
@@ -92,7 +93,8 @@ def test_swiglu_quantize_argument_errors(L):
 
 @pytest.mark.parametrize("name", ["mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k",
                                   "mq_gemm_q5k", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1",
-                                  "mq_gemv_q8_0"])
+                                  "mq_gemv_q8_0", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1",
+                                  "mq_gemm_q8_0"])
 def test_matmul_argument_errors(L, name):
     f = getattr(L, name)
     assert f(16, 8, 300, 256, 4, 16, None) == B.MQ_ERR_SHAPE          # K % 256
@@ -112,7 +114,7 @@ def test_matmul_argument_errors(L, name):
 
 def test_debug_window_errors(L):
     d = L.mq_debug_blockdots
-    assert d(11, 16, 8, 256, 256, 4, 16, 0, 1, 0, 1, 16, None) == B.MQ_ERR_ARG     # op
+    assert d(16, 16, 8, 256, 256, 4, 16, 0, 1, 0, 1, 16, None) == B.MQ_ERR_ARG     # op
     assert d(-1, 16, 8, 256, 256, 4, 16, 0, 1, 0, 1, 16, None) == B.MQ_ERR_ARG
     assert d(0, 16, 8, 256, 256, 4, 16, 3, 2, 0, 1, 16, None) == B.MQ_ERR_ARG      # window past M
     assert d(0, 16, 8, 256, 256, 4, 16, 0, 1, 0, 0, 16, None) == B.MQ_ERR_ARG      # empty window

@@ -340,3 +340,54 @@ def test_b32_gemv_vocab_sampled(fmt):
     ref_plane = G.oracle_plane(x)
     ns = _sample_idx(N, 2048, 9, must=(0, N - 1))
     _sampled("gemv", fmt, w, plane, ref_plane, 1, K, N, np.array([0]), ns, dump_window=(0, 1, N - 100, 100))
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_b32_gemm_shapes(fmt, M, N, K):
+    _full_check("gemm", fmt, M, N, K, seed=M * 7919 + N * 23 + K + ord(fmt[1]) * 5 + ord(fmt[3]))
+
+
+@pytest.mark.parametrize("fmt,fill", [("q4_0", 0xFF), ("q4_0", 0x00), ("q4_1", 0xFF), ("q5_0", 0xFF),
+                                      ("q5_0", 0x00), ("q5_1", 0xFF), ("q8_0", 0x80), ("q8_0", 0x7F)])
+def test_b32_gemm_extreme_blocks(fmt, fill):
+    # quants at the ends of their ranges against codes at +-127: the f16 operands (q - offset,
+    # Q8_0's -128) and the per-block f32 accumulators stay exact
+    M, N, K = 16, 16, 512
+    x = np.full((M, K), 1.0, np.float32)
+    x[1::2] = -1.0
+    plane, _ = G.gpu_plane(x)
+    ref_plane = G.oracle_plane(x)
+    w = _weights(fmt, N, K, 7)
+    w[..., 4 if fmt in ("q4_1", "q5_1") else 2:] = fill
+    y, wd = G.run_matmul("gemm", fmt, w, plane, M, K, N)
+    assert G.rel_err(y, oracle.matmul(w, fmt, ref_plane)) <= G.REL_TOL
+    I, _ = G.run_dump("gemm", fmt, wd, plane, M, K, N, 0, M, 0, N)
+    assert np.array_equal(I, oracle.blockdots(w, fmt, ref_plane[0])[0])
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+def test_b32_gemm_ffn_size_sampled(fmt):
+    # the 7B FFN gate shape at the 3314-token prompt, synthetic weights of the format
+    c = inputs.config2()
+    M, K, N = c["x_hidden"].shape[0], 3584, 18944
+    w = _weights(fmt, N, K, 43 + ord(fmt[1]) + ord(fmt[3]))
+    plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ref_plane = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
+    ms = _sample_idx(M, 32, 11, must=(0, 127, 128, M - 1))
+    ns = _sample_idx(N, 256, 12, must=(0, N - 1))
+    _sampled("gemm", fmt, w, plane, ref_plane, M, K, N, ms, ns, dump_window=(M - 30, 30, N - 50, 50))
+
+
+@pytest.mark.parametrize("fmt", B32_FMTS)
+def test_b32_size_dispatch_agrees(fmt):
+    # matmul() takes the GEMV below 16 tokens and the GEMM from 16 on; at M = 16 both paths
+    # must meet the bar against the oracle
+    M, N, K = 16, 300, 1024
+    w = _weights(fmt, N, K, 91)
+    x = inputs.activations(np.random.default_rng(92), M, K)
+    plane, _ = G.gpu_plane(x)
+    ref = oracle.matmul(w, fmt, G.oracle_plane(x))
+    for path in ("gemv", "gemm"):
+        y, _ = G.run_matmul(path, fmt, w, plane, M, K, N)
+        assert G.rel_err(y, ref) <= G.REL_TOL, path
