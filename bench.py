@@ -17,6 +17,8 @@ Also reported, measured in the same run:
   "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
+  "gate_up_swiglu": the fused gate|up GEMM with the SwiGLU epilogue writing the down
+             projection's plane, against the unfused chain, alone and inside the whole FFN.
   "gemv_b32", "gemm_b32": the decode GEMV of each 32-value block format (Q4_0, Q4_1, Q5_0, Q5_1,
              Q8_0) on a matrix of the LM-head shape, and its prefill GEMM on the gate shape
              (synthetic weights).
@@ -451,6 +453,35 @@ def main():
     # from this step's gate / up outputs
     swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f), K, W)
     swiglu_gbs = (2 * pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (swiglu_ms * 1e-3) / 1e9
+    # the fused gate|up GEMM (NEXT row): gate and up in one kernel whose epilogue writes the down
+    # projection's plane, against the unfused chain (two GEMMs, then the SwiGLU producer), and the
+    # whole SwiGLU FFN both ways (RMSNorm-Q8 -> gate|up -> down)
+    def unfused_gu():
+        B.mq_gemm_q4k(pf.w_gate, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate)
+        B.mq_gemm_q4k(pf.w_up, pf.F, pf.H, pf.p_h, pf.M, pf.y_up)
+        B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f)
+
+    def fused_gu():
+        B.mq_gemm_q4k_swiglu(pf.w_gate, pf.w_up, pf.F, pf.H, pf.p_h, pf.M, pf.p_f)
+
+    def ffn(gu):
+        def run():
+            B.mq_quantize_q8(pf.x_h, pf.M, pf.H, pf.rms_w, pf.eps, pf.p_h)
+            gu()
+            B.mq_gemm_q6k(pf.w_down, pf.H, pf.F, pf.p_f, pf.M, pf.y_down)
+        return run
+
+    gu_unfused_ms = time_events(torch, unfused_gu, K, W)
+    gu_fused_ms = time_events(torch, fused_gu, K, W)
+    ffn_unfused_ms = time_events(torch, ffn(unfused_gu), K, W)
+    ffn_fused_ms = time_events(torch, ffn(fused_gu), K, W)
+    B.mq_device_status()
+    fused = {"what": "7B SwiGLU FFN at 3314 tokens: gate|up Q4_K 2 x 18944 x 3584 -> silu(gate) * up as the "
+                     "down projection's Q8 plane; fused = one kernel, unfused = two GEMMs + the SwiGLU producer",
+             "gate_up_fused_ms": gu_fused_ms, "gate_up_unfused_ms": gu_unfused_ms,
+             "gate_up_fused_TOPS": 2 * pf.gemm_q4k_ops / (gu_fused_ms * 1e-3) / 1e12,
+             "ffn_fused_ms": ffn_fused_ms, "ffn_unfused_ms": ffn_unfused_ms,
+             "ffn_fused_TOPS": pf.ops / (ffn_fused_ms * 1e-3) / 1e12}
     # the Q5_K prefill GEMM on the gate shape (synthetic Q5_K weights), from the step's plane
     w5g = torch.from_numpy(I.q5k_weights(I.rng(2, I.STREAM_W, 5), pf.F, pf.H).reshape(pf.F, -1)).cuda()
     q5_ms = time_events(torch, lambda: B.mq_gemm_q5k(w5g, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate), K, W)
@@ -486,6 +517,7 @@ def main():
                                     "(gate / up outputs of the step)", "ms": swiglu_ms, "GB/s": swiglu_gbs},
         "gemm_q5k": {"what": "Q5_K GEMM on the gate shape 18944 x 3584, M = 3314 (synthetic Q5_K weights)",
                      "ms": q5_ms, "TOPS": pf.gemm_q4k_ops / (q5_ms * 1e-3) / 1e12},
+        "gate_up_swiglu": fused,
         "gemm_b32": {"what": "GEMM on the gate shape 18944 x 3584, M = 3314, per 32-value block format "
                              "(synthetic weights)", **gemm_b32},
         "roofline": {"bound": "tensor", "kernel": "mq_gemm_q4k (18944x3584, M=3314)", "achieved": q4k_tflops,

@@ -149,6 +149,26 @@ MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
                 float *y, mq_stream_t stream);
 
 /*
+ * mq_gemm_q4k_swiglu -- the fused gate|up GEMM of a SwiGLU FFN: both Q4_K projections of one
+ * input plane in one kernel, whose epilogue writes the Q8 plane of silu(gate) * up for the
+ * down projection ("Features > GPU -- CUDA": the FFN's gate and up matmuls share one plane and
+ * the swiglu producer emits the q8 plane; "Compute Graph Design > 5": the FusedFFN form).
+ *
+ *   w_gate, w_up  raw Q4_K bytes [F][K/256] each, 16-byte aligned
+ *   plane_in      Q8 plane of the M x K input (mq_quantize_q8)
+ *   plane_out     Q8 plane of an M x F activation (mq_q8_plane_bytes(M, F) bytes, 256-byte
+ *                 aligned), fully written
+ *   F             rows of each projection, a positive multiple of 256 (the output plane's K)
+ *
+ * G and U are what mq_gemm_q4k writes for w_gate and w_up (the same f32 values, bit for bit);
+ * the output plane is then what mq_quantize_swiglu_q8(G, U) writes, so the pair
+ * (mq_gemm_q4k x 2, mq_quantize_swiglu_q8) and this call give identical planes, without the
+ * two f32 [M][F] intermediates.  Same errors as mq_gemm_q4k plus MQ_ERR_SHAPE for F % 256.
+ */
+MQ_API int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t K, const void *plane_in,
+                              int64_t M, void *plane_out, mq_stream_t stream);
+
+/*
  * mq_gemv_q4k / mq_gemv_q6k -- decode GEMV (MMVQ): streams every weight byte
  * once per group of up to 8 (Q4_K) or 4 (Q6_K) tokens and takes dp4a int8 dots
  * per block ("Support Matrix > CUDA notes": decode (nt == 1) uses the dp4a MMVQ

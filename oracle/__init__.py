@@ -165,6 +165,17 @@ def quantize_swiglu_q8(g: np.ndarray, u: np.ndarray):
     return quantize_q8(swiglu(g, u))
 
 
+def gate_up_swiglu_q8(w_gate: np.ndarray, w_up: np.ndarray, fmt: str, plane, ms=None, threads: int = 1):
+    """Q8 plane of silu(G) * U for the FFN's gate and up projections of one plane: G and U are
+    C6 matmuls (f64), each rounded once to f32 -- the f32 [M][F] form in which the SwiGLU
+    producer (C8) takes them -- then C8.  Rows ``ms`` of the plane (all by default), all F
+    outputs -> (q, d, S).  A composition of pinned functions; no arithmetic of its own but
+    the f64 -> f32 rounding."""
+    g = matmul(w_gate, fmt, plane, ms, None, threads).astype(np.float32)
+    u = matmul(w_up, fmt, plane, ms, None, threads).astype(np.float32)
+    return quantize_swiglu_q8(g, u)
+
+
 def quantize_q8(x: np.ndarray, rms_w: np.ndarray | None = None, eps: float = 1e-6):
     """Q8 plane of x (optionally after the RMSNorm producer) -> (q, d, S)."""
     x = np.ascontiguousarray(x, dtype=np.float32)

@@ -6,7 +6,7 @@ The compute lives in libmq.so (C ABI, include/mq.h); ``binding`` marshals torch
 tensors into it, ``inputs`` makes the seeded synthetic workloads.
 """
 from .binding import (MQError, alloc_plane, matmul, mq_debug_blockdots, mq_debug_forced_timeout,  # noqa: F401
-                      mq_device_status, mq_gemm_q4_0, mq_gemm_q4_1, mq_gemm_q4k, mq_gemm_q5_0, mq_gemm_q5_1,
+                      mq_device_status, mq_gemm_q4_0, mq_gemm_q4_1, mq_gemm_q4k, mq_gemm_q4k_swiglu, mq_gemm_q5_0, mq_gemm_q5_1,
                       mq_gemm_q5k, mq_gemm_q6k, mq_gemm_q8_0, mq_gemv_q4_0, mq_gemv_q4_1,
                       mq_gemv_q4k, mq_gemv_q5_0, mq_gemv_q5_1, mq_gemv_q5k, mq_gemv_q6k, mq_gemv_q8_0,
                       mq_q8_plane_bytes,

@@ -61,6 +61,7 @@ def lib():
                      "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
                      "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
+        L.mq_gemm_q4k_swiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
         L.mq_device_status.argtypes = [P]
         L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
         L.mq_debug_forced_timeout.argtypes = [U32, P]
@@ -209,6 +210,11 @@ def mq_gemm_q5_1(w, N: int, K: int, plane, M: int, y, stream=None):
 
 def mq_gemm_q8_0(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemm_q8_0", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_q4k_swiglu(w_gate, w_up, F: int, K: int, plane_in, M: int, plane_out, stream=None):
+    return _check(lib().mq_gemm_q4k_swiglu(_ptr(w_gate), _ptr(w_up), F, K, _ptr(plane_in), M, _ptr(plane_out),
+                                           _stream(stream)))
 
 
 def mq_device_status(stream=None):

@@ -60,7 +60,7 @@ int set_error(int code, const char *fmt, ...) {
 
 namespace {
 int g_sm_count[kMaxDevices] = {0};
-constexpr int kAttrSlots = 16 + 8 * 16;     // GEMM slots below 16; GEMV 16 + 16 per format
+constexpr int kAttrSlots = kAttrSlotSwiglu + 8;     // GEMM below 16; GEMV 16 + 16 per format; fused GEMM
 bool g_attr_done[kMaxDevices][kAttrSlots] = {};
 }  // namespace
 
@@ -348,6 +348,33 @@ int mq_gemm_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t
 }
 int mq_gemm_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
     return run_matmul(15, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
+int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t K, const void *plane_in, int64_t M,
+                       void *plane_out, mq_stream_t stream) {
+    const char *fn = "mq_gemm_q4k_swiglu";
+    if (M < 0 || F < 0) return set_error(MQ_ERR_ARG, "%s: negative size M=%lld F=%lld", fn, (long long)M, (long long)F);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    if (F == 0 || F % kQK != 0 || F >= kMaxDim)
+        return set_error(MQ_ERR_SHAPE, "%s: F=%lld must be a positive multiple of 256 below 2^31", fn, (long long)F);
+    if (M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "%s: M=%lld must be below 2^31", fn, (long long)M);
+    if (M == 0) return MQ_OK;
+    if (!w_gate || !w_up || !plane_in || !plane_out)
+        return set_error(MQ_ERR_ARG, "%s: NULL pointer (w_gate=%p w_up=%p plane_in=%p plane_out=%p)", fn, w_gate, w_up,
+                         plane_in, plane_out);
+    if (!aligned(w_gate, 16) || !aligned(w_up, 16))
+        return set_error(MQ_ERR_ALIGN, "%s: weights %p / %p not 16-byte aligned", fn, w_gate, w_up);
+    if (!aligned(plane_in, 256) || !aligned(plane_out, 256))
+        return set_error(MQ_ERR_ALIGN, "%s: planes %p / %p not 256-byte aligned", fn, plane_in, plane_out);
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    Plane pi, po;
+    plane_from(const_cast<void *>(plane_in), M, K, &pi);
+    plane_from(plane_out, M, F, &po);
+    return launch_gemm_swiglu(FMT_Q4K, static_cast<const uint8_t *>(w_gate), static_cast<const uint8_t *>(w_up), F, K,
+                              pi, M, po, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mq_debug_blockdots(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,

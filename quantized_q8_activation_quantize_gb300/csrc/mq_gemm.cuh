@@ -159,11 +159,16 @@ __device__ __forceinline__ uint32_t sw64_chunk(uint32_t tile, int r, int c) {
     return tile + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
-template <int FMT, bool DUMP>
+// SWIGLU: the fused gate|up GEMM.  The tile's 128 weight rows are 64 gate rows (tmW) and the
+// same 64 rows of up (tmW2); each epilogue thread holds gate and up of 32 outputs of its token,
+// forms silu(gate) * up and writes it as one Q8 block of the output plane `po` (no Y).
+template <int FMT, bool DUMP, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmDS,
-                const __grid_constant__ CUtensorMap tmW, const uint8_t *__restrict__ w, int64_t N, int64_t K, Plane p, int64_t M, float *__restrict__ y,
-                Dump dump, unsigned int *err) {
+                const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+                const uint8_t *__restrict__ w, int64_t N, int64_t K, Plane p, int64_t M, float *__restrict__ y,
+                Plane po, Dump dump, unsigned int *err) {
+    static_assert(!SWIGLU || (GmCfg<FMT>::TMW && !DUMP), "the fused gate|up GEMM takes TMA-fed formats, no dump");
     using C = GmCfg<FMT>;
     constexpr int S = C::STAGES, R = C::RAW_STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -189,7 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *corr_flags = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_FLAG);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    // n0: the tile's first weight row (SWIGLU: of gate and of up, 64 each).  SWIGLU walks the
+    // token tiles fastest (grid x), so the CTAs in flight share a few weight tiles while the
+    // tokens' A tiles stay in L2: gate + up of the 7B FFN (76 MB) re-streamed once per token
+    // tile would not stay in L2
+    const int64_t m0 = (int64_t)(SWIGLU ? blockIdx.x : blockIdx.y) * BM;
+    const int64_t n0 = (int64_t)(SWIGLU ? blockIdx.y : blockIdx.x) * (SWIGLU ? BN / 2 : BN);
     const int nsb = (int)(K / kQK);
     const int nstages = nsb * 4;
     const int64_t row_bytes = (int64_t)(K / kQK) * C::BB;
@@ -241,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmA);
             if constexpr (C::MIN) prefetch_tmap(&tmDS);
             if constexpr (C::TMW) prefetch_tmap(&tmW);
+            if constexpr (SWIGLU) prefetch_tmap(&tmW2);
             int st = 0, sb_issued = 0, raw_issued = 0;
             // raw blocks of the tile's 128 rows for one super-block (256 values): a BB-byte x 128 box
             auto issue_raw = [&](int sb) -> bool {
@@ -250,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&bars.raw_full[slot], BN * C::RAW_ROW);
                 tma_load_2d(sm + C::OFF_RAW + slot * BN * C::RAW_ROW, &tmW, sb * (C::BB / C::TMW_ELEM), (int32_t)n0,
                             &bars.raw_full[slot]);
+                if constexpr (SWIGLU)      // up rows n0 .. n0+63 into tile rows 64 .. 127
+                    tma_load_2d(sm + C::OFF_RAW + slot * BN * C::RAW_ROW + (BN / 2) * C::RAW_ROW, &tmW2,
+                                sb * (C::BB / C::TMW_ELEM), (int32_t)n0, &bars.raw_full[slot]);
                 raw_issued = sb + 1;
                 return true;
             };
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_UNPACK));
         // ------------------------------------------------------------ unpackers
         const int r = threadIdx.x - 32 * kWarpUnpack0;     // weight row in the tile
-        const int64_t n = n0 + r;
+        const int64_t n = n0 + (SWIGLU ? (r & (BN / 2 - 1)) : r);
         const bool valid = n < N;
         const uint8_t *wrow = w + (valid ? n : 0) * row_bytes;
         uint8_t *raw_row0 = sm + C::OFF_RAW + r * C::RAW_ROW;
@@ -711,6 +725,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid_m = m < M;
         const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
         const int col0 = hf * 64;
+        // TMEM column of this thread's 32-column half hh: plain, 64 hf + 32 hh; SWIGLU, gate
+        // columns 32 hf .. (hh = 0) and the matching up columns 64 + 32 hf .. (hh = 1)
+        auto colh = [&](int hh) -> int { return SWIGLU ? 32 * hf + 64 * hh : col0 + 32 * hh; };
         const int64_t nblk32 = K / kQ8;
         const float *info0 = reinterpret_cast<const float *>(sm + C::OFF_INFO);
         // acc: the running sum over super-blocks; part: sum_j d_a[j] I_j of the current super-block
@@ -750,8 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr bool kBoth = C::TMW;
                 uint32_t vv[kBoth ? 2 : 1][32];
                 if constexpr (kBoth) {
-                    tmem_ld32(trow + (uint32_t)(slot * BN + col0), vv[0]);
-                    tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32), vv[kBoth ? 1 : 0]);
+                    tmem_ld32(trow + (uint32_t)(slot * BN + colh(0)), vv[0]);
+                    tmem_ld32(trow + (uint32_t)(slot * BN + colh(1)), vv[kBoth ? 1 : 0]);
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -760,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if constexpr (!kBoth) {
-                        tmem_ld32(trow + (uint32_t)(slot * BN + col0 + 32 * hh), vv[0]);
+                        tmem_ld32(trow + (uint32_t)(slot * BN + colh(hh)), vv[0]);
                         tmem_ld_wait();
                         if (hh == 1) {       // both halves are in registers: hand the slot back to the MMA
                             tc_fence_before();
@@ -772,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (C::B32) {
                         // y += I (d_a d_w): d_w of the 32 weight rows from the unpackers' table
                         const float4 *dwv =
-                            reinterpret_cast<const float4 *>(info0 + ((sb & 1) * 8 + j) * BN + col0 + 32 * hh);
+                            reinterpret_cast<const float4 *>(info0 + ((sb & 1) * 8 + j) * BN + colh(hh));
 #pragma unroll
                         for (int i4 = 0; i4 < 8; ++i4) {
                             const float4 dv = dwv[i4];
@@ -795,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (valid_m && m >= dump.m0 && m < dump.m0 + dump.m_cnt) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                const int64_t n = n0 + col0 + 32 * hh + i;
+                                const int64_t n = n0 + colh(hh) + i;
                                 if (n >= dump.n0 && n < dump.n0 + dump.n_cnt && n < N)
                                     dump.out[((m - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32 + gb] =
                                         __float2int_rn(__uint_as_float(v[i]));
@@ -815,11 +832,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
-            const float4 *info = reinterpret_cast<const float4 *>(info0 + (sb & 1) * BN + col0);
+            const float4 *info = reinterpret_cast<const float4 *>(info0 + (sb & 1) * BN);
             // all 16 loads of the 64 row factors first (independent, their latencies overlap), then the FMAs
             float4 dv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dv[i] = info[i];
+            for (int i = 0; i < 16; ++i) dv[i] = info[colh(i >> 3) / 4 + (i & 7)];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 acc[2 * i] = __ffma2_rn(part[2 * i], make_float2(dv[i].x, dv[i].y), acc[2 * i]);
@@ -841,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         uint32_t v[32];
-                        tmem_ld32(trow + kMinCol + (uint32_t)(col0 + 32 * hh), v);
+                        tmem_ld32(trow + kMinCol + (uint32_t)colh(hh), v);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -852,10 +869,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                 }
             }
-            if (ok && valid_m) {
+            if constexpr (SWIGLU) {
+                // outputs n0 + 32 hf .. +31 of token m: silu(gate) * up, one Q8 block of the plane
+                // (the plane's K is N, a multiple of 256, so the block is whole)
+                const int64_t nb0 = n0 + 32 * hf;
+                if (ok && valid_m && nb0 < N) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[2 * i] = swiglu1(acc[i].x, acc[16 + i].x);
+                        v[2 * i + 1] = swiglu1(acc[i].y, acc[16 + i].y);
+                    }
+                    float d, hi, lo;
+                    int sum;
+                    quantize_block32(v, po.q8 + m * N + nb0, po.q16 + m * N + nb0, d, sum, hi, lo);
+                    const int64_t b = nb0 / kQ8;
+                    po.d[b * M + m] = d;
+                    po.s[b * M + m] = sum;
+                    float *row = po.ds + m * (2 * (N / kQ8)) + (b >> 3) * 16 + (b & 7);
+                    row[0] = hi;
+                    row[8] = lo;
+                }
+            } else if (ok && valid_m) {
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int64_t nb0 = n0 + col0 + 32 * hh;
+                    const int64_t nb0 = n0 + colh(hh);
                     float *dst = y + m * N + nb0;
                     if (nb0 + 32 <= N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
@@ -887,12 +925,29 @@ int launch_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap
                int64_t K, const Plane &p, int64_t M, float *y, const Dump &dump, unsigned int *err,
                cudaStream_t stream) {
     using C = GmCfg<FMT>;
-    auto kern = gemm_kernel<FMT, DUMP>;
+    auto kern = gemm_kernel<FMT, DUMP, false>;
     int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, FMT * 2 + (DUMP ? 1 : 0));
     if (rc != MQ_OK) return rc;
     const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-    return cuda_error(launch_pdl(kern, grid, dim3(kThreads), C::SMEM, stream, tm, tmds, tmw, w, N, K, p, M, y, dump, err),
+    return cuda_error(launch_pdl(kern, grid, dim3(kThreads), C::SMEM, stream, tm, tmds, tmw, tmw, w, N, K, p, M, y,
+                                 Plane{}, dump, err),
                       "gemm launch");
+}
+
+// the fused gate|up GEMM: tmg / tmu are the gate and up weight maps with 64-row boxes; the
+// output plane po has K = F
+template <int FMT>
+int launch_swiglu_fmt(const CUtensorMap &tm, const CUtensorMap &tmds, const CUtensorMap &tmg, const CUtensorMap &tmu,
+                      const uint8_t *wg, int64_t F, int64_t K, const Plane &p, int64_t M, const Plane &po,
+                      unsigned int *err, cudaStream_t stream) {
+    using C = GmCfg<FMT>;
+    auto kern = gemm_kernel<FMT, false, true>;
+    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), C::SMEM, kAttrSlotSwiglu + FMT);
+    if (rc != MQ_OK) return rc;
+    const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((F + BN / 2 - 1) / (BN / 2)));
+    return cuda_error(launch_pdl(kern, grid, dim3(kThreads), C::SMEM, stream, tm, tmds, tmg, tmu, wg, F, K, p, M,
+                                 static_cast<float *>(nullptr), po, Dump{nullptr, 0, 0, 0, 0}, err),
+                      "gemm swiglu launch");
 }
 
 }  // namespace

@@ -82,6 +82,12 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
 int launch_gemv_b32(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                     const Dump &dump, unsigned int *err, cudaStream_t stream);
+// the fused gate|up GEMM with the SwiGLU epilogue: plane p (M x K) -> plane po (M x F)
+int launch_gemm_swiglu(Fmt fmt, const uint8_t *wg, const uint8_t *wu, int64_t F, int64_t K, const Plane &p, int64_t M,
+                       const Plane &po, unsigned int *err, cudaStream_t stream);
+// attribute slots (ensure_smem_attr / resident_ctas): GEMM 2 fmt + dump (below 16), GEMV 16 + 16 fmt + ...,
+// the fused gate|up GEMM kAttrSlotSwiglu + fmt
+constexpr int kAttrSlotSwiglu = 16 + 8 * 16;
 int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
 

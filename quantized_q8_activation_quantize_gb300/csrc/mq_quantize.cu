@@ -88,36 +88,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     }
 }
 
-// SwiGLU producer ("Features > GPU -- CUDA": the swiglu producer emits the q8 plane directly;
-// "Compute Graph Design > 5": Mul(Silu(X), Y) -> SwiGLU): y = silu(g) * u in IEEE f32, every
-// step rounded once, then the Q8 quantization of y.  exp is evaluated by the textbook
-// reduction: x = k ln2 + r, k = nearest integer to x / ln2 (ties to even), |r| <= ln2 / 2,
-// exp(r) by its Taylor series through r^7, times 2^k; x is clamped to [-86, 88] so the
-// result stays a normal f32 (in f32, silu is unaffected outside that range).  Every step is
-// an explicitly rounded operation, so y -- and every Q8 code -- is one fixed function of
-// (g, u).
-__device__ __forceinline__ float exp_f32(float x) {
-    x = x > 88.0f ? 88.0f : x;
-    x = x < -86.0f ? -86.0f : x;
-    const float k = rintf(__fmul_rn(x, 1.44269504f));         // 1 / ln2
-    float r = fmaf(-k, 0.693145751953125f, x);                  // ln2, high part (k * hi is exact)
-    r = fmaf(-k, 1.42860677e-06f, r);                           // ln2, low part
-    float p = 1.98412698e-04f;                                  // 1/7!
-    p = fmaf(p, r, 1.38888889e-03f);                            // 1/6!
-    p = fmaf(p, r, 8.33333333e-03f);                            // 1/5!
-    p = fmaf(p, r, 4.16666667e-02f);                            // 1/4!
-    p = fmaf(p, r, 1.66666667e-01f);                            // 1/3!
-    p = fmaf(p, r, 0.5f);                                       // 1/2!
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    return ldexpf(p, (int)k);
-}
-
-__device__ __forceinline__ float swiglu1(float g, float u) {
-    const float den = __fadd_rn(1.0f, exp_f32(-g));
-    return __fmul_rn(__fdiv_rn(g, den), u);
-}
-
+// SwiGLU producer: y = swiglu1(g, u) (mq_device.cuh), then the Q8 quantization of y.
 __global__ void __launch_bounds__(256) swiglu_quantize_kernel(const float *__restrict__ g, const float *__restrict__ up,
                                                               int64_t M, int64_t K, Plane p) {
     grid_dep_launch();

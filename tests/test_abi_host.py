@@ -21,7 +21,7 @@ EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quan
             "mq_gemm_q4k",
             "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k", "mq_device_status", "mq_debug_blockdots",
             "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
-            "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"}
+            "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu"}
 
 
 def test_header_declares_the_boundary():
@@ -145,3 +145,19 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         B.lib()
+
+
+def test_gate_up_swiglu_argument_errors(L):
+    f = L.mq_gemm_q4k_swiglu          # (w_gate, w_up, F, K, plane_in, M, plane_out, stream)
+    assert f(16, 16, 300, 256, 256, 4, 256, None) == B.MQ_ERR_SHAPE      # F % 256
+    assert f(16, 16, 0, 256, 256, 4, 256, None) == B.MQ_ERR_SHAPE
+    assert f(16, 16, 256, 100, 256, 4, 256, None) == B.MQ_ERR_SHAPE      # K % 256
+    assert f(16, 16, -256, 256, 256, 4, 256, None) == B.MQ_ERR_ARG
+    assert f(16, 16, 256, 256, 256, -1, 256, None) == B.MQ_ERR_ARG
+    assert f(16, 16, 256, 256, 256, 0, 256, None) == B.MQ_OK            # M == 0: nothing to do
+    assert f(None, 16, 256, 256, 256, 4, 256, None) == B.MQ_ERR_ARG
+    assert f(16, 16, 256, 256, 256, 4, None, None) == B.MQ_ERR_ARG
+    assert f(24, 16, 256, 256, 256, 4, 256, None) == B.MQ_ERR_ALIGN     # w_gate not 16-byte aligned
+    assert f(16, 24, 256, 256, 256, 4, 256, None) == B.MQ_ERR_ALIGN
+    assert f(16, 16, 256, 256, 128, 4, 256, None) == B.MQ_ERR_ALIGN     # plane_in
+    assert f(16, 16, 256, 256, 256, 4, 384, None) == B.MQ_ERR_ALIGN     # plane_out

@@ -87,3 +87,40 @@ def test_quantize_swiglu_is_quantize_of_swiglu():
     u = r.standard_normal((3, 768)).astype(np.float32)
     for a, b in zip(oracle.quantize_swiglu_q8(g, u), oracle.quantize_q8(oracle.swiglu(g, u))):
         assert np.array_equal(a, b)
+
+
+def _negate_d(w):
+    """Q4_K bytes with d and dmin negated (fp16 sign bits): the matmul output changes sign exactly."""
+    w = w.copy()
+    w[..., 1] ^= 0x80
+    w[..., 3] ^= 0x80
+    return w
+
+
+def test_gate_up_swiglu_operand_roles_and_closed_form():
+    # y(G) - y(-G) = (silu(G) - silu(-G)) U = G U, so the planes of w_gate and of -w_gate differ,
+    # after dequantization, by G U within the two quantization steps; swapping the roles of gate
+    # and up, or dropping the f32 rounding's input, breaks it.  The plane also matches the f64
+    # closed form silu(G) U within its quantization step.
+    from quantized_q8_activation_quantize_gb300 import inputs
+    r = np.random.default_rng(31)
+    M, K, F = 4, 512, 256
+    wg = inputs.q4k_weights(r, F, K)
+    wu = inputs.q4k_weights(r, F, K)
+    plane = oracle.quantize_q8(inputs.activations(r, M, K))
+    G = oracle.matmul(wg, "q4k", plane)
+    U = oracle.matmul(wu, "q4k", plane)
+    assert np.array_equal(oracle.matmul(_negate_d(wg), "q4k", plane), -G)
+
+    def deq(p):
+        q, d, _ = p
+        return q.reshape(M, -1, 32).astype(np.float64) * d[..., None].astype(np.float64), d
+
+    yp, dp = deq(oracle.gate_up_swiglu_q8(wg, wu, "q4k", plane))
+    yn, dn = deq(oracle.gate_up_swiglu_q8(_negate_d(wg), wu, "q4k", plane))
+    GU = (G * U).reshape(M, -1, 32)
+    step = (dp + dn)[..., None].astype(np.float64)
+    assert np.all(np.abs((yp - yn) - GU) <= 0.5 * step * (1 + 1e-6) + 1e-6 * np.abs(GU))
+    silu = G / (1 + np.exp(-G))
+    ref = (silu * U).reshape(M, -1, 32)
+    assert np.all(np.abs(yp - ref) <= 0.5 * dp[..., None] * (1 + 1e-6) + 1e-5 * np.abs(ref).max())
