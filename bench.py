@@ -67,8 +67,8 @@ def parse_args():
 # DRAM bytes (read + write) of one launch of the roofline kernels, from one ncu capture of the
 # current kernels (dram__bytes_read.sum + dram__bytes_write.sum); set to None whenever a kernel
 # changes until it is captured again.
-TRAFFIC_GEMM_Q4K_GATE = 96.623616e6 + 207.959296e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
-TRAFFIC_GEMV_Q6K_LMHEAD = 447.182848e6 + 3.463936e6   # 152064x3584 Q6_K, M=1
+TRAFFIC_GEMM_Q4K_GATE = 95.565824e6 + 205.278720e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
+TRAFFIC_GEMV_Q6K_LMHEAD = 447.181568e6 + 3.106560e6   # 152064x3584 Q6_K, M=1
 # the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs)
 INT8_MMA_SYNC_PEAK_TOPS = 158.1
 
@@ -82,6 +82,9 @@ CASES = {
     "gemv_q5k_vocab": "Q5_K GEMV of the LM-head shape: 152064x3584 synthetic Q5_K weights, M=1",
     **{f"gemv_{f}_vocab": f"{f.upper()} GEMV of the LM-head shape: 152064x3584 synthetic {f.upper()} weights, M=1"
        for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
+    **{f"gemm_{f}_gate": f"{f.upper()} GEMM of the gate shape: 18944x3584 synthetic {f.upper()} weights, M=3314"
+       for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
+    "gemm_swiglu_ffn": "config 2 fused gate|up GEMM: Q4_K 2 x 18944x3584, M=3314, SwiGLU epilogue -> down plane",
     "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
     "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
 }
@@ -112,8 +115,17 @@ def run_case(args):
     elif name == "gemv_q5k_vocab":
         x, w, fmt, rms = I.config4_x(1), I.q5k_vocab_weights(), "q5k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
-    elif name.startswith("gemv_q") and name[6:-6] in I.B32_BYTES:
-        fmt = name[6:-6]
+    elif name == "gemm_swiglu_ffn" or (name.startswith("gemm_q") and name[5:-5] in I.B32_BYTES):
+        c = I.config2()
+        x, rms, K, N = c["x_hidden"], c["rms_w"], I.HIDDEN, I.FFN
+        M = x.shape[0]
+        if name == "gemm_swiglu_ffn":
+            fmt, w, w2 = "q4k", c["w_gate"], c["w_up"]
+        else:
+            fmt, w2 = name[5:-5], None
+            w = I.b32_weights(I.rng(2, I.STREAM_W, 6 + list(I.B32_BYTES).index(fmt)), N, K, fmt)
+    elif name.startswith("gemv_q") and name[5:-6] in I.B32_BYTES:
+        fmt = name[5:-6]
         x, w, rms = I.config4_x(1), I.b32_vocab_weights(fmt), None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     else:
@@ -127,6 +139,9 @@ def run_case(args):
     B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
     if name.startswith("quantize"):
         fn = lambda: B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
+    elif name == "gemm_swiglu_ffn":
+        w2d, po = dev(w2.reshape(N, -1)), B.alloc_plane(M, N)
+        fn = lambda: B.mq_gemm_q4k_swiglu(wd, w2d, N, K, plane, M, po)
     else:
         f = (B.GEMM if name.startswith("gemm") else B.GEMV)[fmt]
         fn = lambda: f(wd, N, K, plane, M, y)
