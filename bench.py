@@ -86,6 +86,7 @@ CASES = {
        for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
     "gemm_swiglu_ffn": "config 2 fused gate|up GEMM: Q4_K 2 x 18944x3584, M=3314, SwiGLU epilogue -> down plane",
     "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
+    "decode_sweep": "config 3: the 196 quantize + GEMV pairs of one decode token, plain launches",
     "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
 }
 
@@ -98,6 +99,14 @@ def run_case(args):
     from quantized_q8_activation_quantize_gb300 import inputs as I
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     name = args.case
+    if name == "decode_sweep":
+        sw = DecodeSweep(torch, B, I)
+        for _ in range(1 + args.reps):
+            sw.run(True)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+        print(json.dumps({"case": name, "what": CASES[name], "launches": (1 + args.reps) * 2 * len(sw.items)}))
+        return
     if name.startswith("gemm_q4k_gate") or name.startswith("gemm_q6k_down") or name.startswith("quantize"):
         c = I.config2()
         M = c["x_hidden"].shape[0]
