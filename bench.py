@@ -12,8 +12,10 @@ than the 129 MB L2, so consecutive steps do not hit L2 for their inputs (no flus
 
 Also reported, measured in the same run:
   "decode":  config 3, one decode token through all 196 per-layer matmuls of a 28-layer
-             7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph),
-             weight GB/s and tok/s; 3.9 GB of weights, far larger than L2.
+             7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph whose
+             branches run a layer's independent matmuls -- q|k|v, gate|up -- side by side; the
+             linear chain is reported as "serial"), weight GB/s and tok/s; 3.9 GB of weights,
+             far larger than L2.
   "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
@@ -331,26 +333,55 @@ class DecodeSweep:
             self.bytes += w.numel() + 1.25 * k + 4 * n + 4 * k     # weights + plane + output + activation
         self.graph = None
 
-    def run(self, quantize=True):
-        B = self.B
-        for fmt, w, x, plane, y, n, k in self.items:
-            if quantize:
-                B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
-            B.GEMV[fmt](w, n, k, plane, 1, y)
+    def _one(self, item, quantize):
+        fmt, w, x, plane, y, n, k = item
+        if quantize:
+            self.B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
+        self.B.GEMV[fmt](w, n, k, plane, 1, y)
 
-    def capture(self, quantize=True):
+    def run(self, quantize=True, branches=False):
+        """The sweep in layer order.  branches=True: a layer's independent matmuls -- q, k, v (all
+        from the layer input) and gate, up (both from the post-attention input) -- go to parallel
+        streams, joined before o and before down, the dependency structure of a real layer."""
+        if not branches:
+            for item in self.items:
+                self._one(item, quantize)
+            return
+        t = self.torch
+        main = t.cuda.current_stream()
+        if not hasattr(self, "side"):
+            self.side = [t.cuda.Stream(), t.cuda.Stream()]
+        for layer in range(len(self.items) // 7):
+            li = self.items[7 * layer:7 * layer + 7]           # q, k, v, o, gate, up, down
+            for group in (li[0:3], li[3:4], li[4:6], li[6:7]):
+                if len(group) == 1:
+                    self._one(group[0], quantize)
+                    continue
+                fork = t.cuda.Event()
+                fork.record(main)
+                for i in range(len(group) - 1):
+                    self.side[i].wait_event(fork)
+                    with t.cuda.stream(self.side[i]):
+                        self._one(group[1 + i], quantize)
+                self._one(group[0], quantize)
+                for i in range(len(group) - 1):
+                    join = t.cuda.Event()
+                    join.record(self.side[i])
+                    main.wait_event(join)
+
+    def capture(self, quantize=True, branches=False):
         """One CUDA graph of the sweep: Q8 quantize + GEMV per matmul, or the GEMVs alone
         (on the planes the last quantizing run left)."""
         t = self.torch
         s = t.cuda.Stream()
         s.wait_stream(t.cuda.current_stream())
         with t.cuda.stream(s):
-            self.run(True)                 # warm the launch path (and fill the planes) outside the capture
+            self.run(True, branches)       # warm the launch path (and fill the planes) outside the capture
         t.cuda.current_stream().wait_stream(s)
         t.cuda.synchronize()
         g = t.cuda.CUDAGraph()
         with t.cuda.graph(g):
-            self.run(quantize)
+            self.run(quantize, branches)
         t.cuda.synchronize()
         return g
 
@@ -600,16 +631,24 @@ def main():
         sw = DecodeSweep(torch, B, I)
         ms = time_events(torch, sw.capture(True).replay, max(5, K), W)
         ms_gemv = time_events(torch, sw.capture(False).replay, max(5, K), W)
+        ms_br = time_events(torch, sw.capture(True, True).replay, max(5, K), W)
+        ms_br_gemv = time_events(torch, sw.capture(False, True).replay, max(5, K), W)
         B.mq_device_status()
         gemv_bytes = sw.bytes - 4 * sum(k for *_, k in sw.items)          # without the f32 activations
         lm_ms = lm["m1_gemv"]["ms"]
-        line["decode"] = {"workload": "config 3: 28 layers x 7 matmuls, M=1 (Q8 quantize + GEMV each, one CUDA graph)",
-                          "ms_per_token": ms, "tok_per_s": 1e3 / ms, "weight_bytes": sw.weight_bytes,
-                          "GB/s": sw.bytes / (ms * 1e-3) / 1e9, "frac_of_hbm": sw.bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        line["decode"] = {"workload": "config 3: 28 layers x 7 matmuls, M=1, Q8 quantize + GEMV each, one CUDA graph; "
+                                      "each layer's independent matmuls (q|k|v from the layer input, gate|up from the "
+                                      "post-attention input) on parallel branches, joined before o and before down",
+                          "ms_per_token": ms_br, "tok_per_s": 1e3 / ms_br, "weight_bytes": sw.weight_bytes,
+                          "GB/s": sw.bytes / (ms_br * 1e-3) / 1e9,
+                          "frac_of_hbm": sw.bytes / (ms_br * 1e-3) / 1e9 / hbm_peak,
                           "launches_per_token": 2 * len(sw.items),
-                          "gemv_only": {"what": "the 196 GEMVs alone, one CUDA graph (planes already quantized)",
-                                        "ms_per_token": ms_gemv, "GB/s": gemv_bytes / (ms_gemv * 1e-3) / 1e9,
-                                        "tok_per_s_with_lm_head": 1e3 / (ms_gemv + lm_ms)}}
+                          "serial": {"what": "the same 392 launches as one linear chain",
+                                     "ms_per_token": ms, "GB/s": sw.bytes / (ms * 1e-3) / 1e9},
+                          "gemv_only": {"what": "the 196 GEMVs alone (planes already quantized), branched graph",
+                                        "ms_per_token": ms_br_gemv, "GB/s": gemv_bytes / (ms_br_gemv * 1e-3) / 1e9,
+                                        "serial_ms_per_token": ms_gemv,
+                                        "tok_per_s_with_lm_head": 1e3 / (ms_br_gemv + lm_ms)}}
 
     # ---------------- CPU baseline (oracle on the host cores, rank 0 only)
     if dist.rank == 0 and dist.world == 1:

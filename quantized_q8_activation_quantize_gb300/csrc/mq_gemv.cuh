@@ -784,6 +784,10 @@ int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     rc = resident_ctas(reinterpret_cast<const void *>(kern), C::THREADS, smem, slot, &per_sm);
     if (rc != MQ_OK) return rc;
     int64_t ctas = (int64_t)nsm * per_sm;
+    // at least one full unit of super-blocks per CTA: a small matrix (a 512-row k_proj is 56
+    // units) then leaves most of the GPU to kernels running beside it on other streams
+    const int64_t units = (a.N * (a.K / kQK) + C::TU - 1) / C::TU;
+    if (ctas > units) ctas = units;
     if (ctas > a.N) ctas = a.N;                      // every CTA owns at least one row
     return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a), "gemv launch");
 }
