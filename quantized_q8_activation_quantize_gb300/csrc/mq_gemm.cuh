@@ -16,7 +16,8 @@
 //  * A (tokens, f16 codes) is a TMA 2-D tile with the 128-byte swizzle; B (weights)
 //    is unpacked from raw block bytes (staged by 1-D bulk copies of each row's
 //    16-byte-aligned superset) straight into the same swizzled K-major layout.
-//  * Each 32-value block's product goes to its own TMEM accumulator (3-slot ring);
+//  * Each 32-value block's product goes to its own TMEM accumulator (a ring of 3 slots, 4
+//    for Q6_K, which has no min-term region);
 //    the epilogue warps drain it and apply the activation scale per block with packed
 //    f32x2 FMAs; once per super-block they fold the fp16 d into a running sum kept
 //    in a fourth TMEM region.
@@ -50,8 +51,9 @@ constexpr int BM = 128, BN = 128, BK = 64;
 constexpr int kThreads = 512;   // 4 warpgroups: {TMA, MMA, -, -}, unpack, epilogue x2
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpUnpack0 = 4, kWarpEpi0 = 8;
 
-constexpr int kAccSlots = 3;
-constexpr uint32_t kTmemCols = 512, kMinCol = 384;   // 3 block slots + the Q4_K min-term sum
+constexpr int kMaxAccSlots = 4;
+// 3 block slots + the min-term sum at column 384, or (formats without a min term) 4 block slots
+constexpr uint32_t kTmemCols = 512, kMinCol = 384;
 constexpr int kTile = BM * BK * 2;       // one 128 x 64 f16 operand tile
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -74,6 +76,10 @@ struct GmCfg {
     static constexpr bool CORR = FMT == FMT_Q6K;                  // Q6_K odd |sc| > 64 correction tile
     // the min / offset term on the tensor pipe: Q4_K / Q5_K -dmin m_j, Q4_1 / Q5_1 the block offset m
     static constexpr bool MIN = KQ || b32_has_m(FMT);
+    // TMEM accumulator slots of 128 columns.  Q6_K has no min-term region and takes a fourth slot
+    // (measured -1 % on its GEMMs); the 32-value formats without a min term measured 4-5 %
+    // slower with four, so they keep three
+    static constexpr int ACC = FMT == FMT_Q6K ? 4 : 3;
     static constexpr int MIN_TILE = BM * 64;                      // 128 rows x 16 tf32 (64 B, 64-B swizzle)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * kTile;
@@ -88,7 +94,7 @@ struct GmCfg {
     static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
     // a_full[S] b_full[S] ab_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] acc_full[3]
     // acc_empty[3] amin_full[2] amin_empty[2] min_final[1] da_full[2] da_empty[2]
-    static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kAccSlots + 5 + 4;
+    static constexpr int NBARS = 3 * STAGES + 2 * RAW_STAGES + 4 + 2 * kMaxAccSlots + 5 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;             // + slack to align the base to 1 KiB
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA exceeds the per-CTA limit");
@@ -183,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.info_full = bars.raw_empty + R;
     bars.info_empty = bars.info_full + 2;
     bars.acc_full = bars.info_empty + 2;
-    bars.acc_empty = bars.acc_full + kAccSlots;
-    bars.amin_full = bars.acc_empty + kAccSlots;
+    bars.acc_empty = bars.acc_full + kMaxAccSlots;
+    bars.amin_full = bars.acc_empty + kMaxAccSlots;
     bars.amin_empty = bars.amin_full + 2;
     bars.min_final = bars.amin_empty + 2;
     bars.da_full = bars.min_final + 1;
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.da_full[i], 2);                    // the two stager warps
             mbar_init(&bars.da_empty[i], 8);                   // the epilogue warps
         }
-        for (int i = 0; i < kAccSlots; ++i) {
+        for (int i = 0; i < C::ACC; ++i) {
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], 8);
         }
@@ -346,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < 4 && ok; ++q) {
                     const int st = sb * 4 + q, s = st % S;
                     const uint32_t ph = (st / S) & 1;
-                    const int slot0 = gb % kAccSlots, slot1 = (gb + 1) % kAccSlots;
-                    const uint32_t eph0 = ((gb / kAccSlots) & 1) ^ 1, eph1 = (((gb + 1) / kAccSlots) & 1) ^ 1;
+                    const int slot0 = gb % C::ACC, slot1 = (gb + 1) % C::ACC;
+                    const uint32_t eph0 = ((gb / C::ACC) & 1) ^ 1, eph1 = (((gb + 1) / C::ACC) & 1) ^ 1;
                     // All four conditions of the stage probed at once (their latencies overlap);
                     // only a stage that is not ready yet falls back to the blocking waits.
                     const bool ready = __all_sync(kFull, mbar_test_wait(a_full0 + 8u * s, ph) &
@@ -754,8 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int gb = sb * 8 + j;
-                const int slot = gb % kAccSlots;
-                if (!mbar_wait(&bars.acc_full[slot], (gb / kAccSlots) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
+                const int slot = gb % C::ACC;
+                if (!mbar_wait(&bars.acc_full[slot], (gb / C::ACC) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
                     ok = false;
                     break;
                 }
