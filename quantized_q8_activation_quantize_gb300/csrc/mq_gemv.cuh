@@ -112,14 +112,6 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr) {
     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
 }
-// 16 bytes at a 2-byte aligned shared address (five aligned words, funnel-shifted)
-__device__ __forceinline__ uint4 lds128_a2(uint32_t addr) {
-    const uint32_t b = addr & ~3u, sh = (addr & 3u) * 8u;
-    const uint32_t w0 = lds32(b), w1 = lds32(b + 4), w2 = lds32(b + 8), w3 = lds32(b + 12), w4 = lds32(b + 16);
-    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh), __funnelshift_r(w2, w3, sh),
-                      __funnelshift_r(w3, w4, sh));
-}
-
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits) {
     return __half2float(__ushort_as_half((unsigned short)bits));
 }
