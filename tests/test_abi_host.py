@@ -37,6 +37,19 @@ def test_library_exports_every_declared_symbol(L):
     assert exported == EXPECTED
 
 
+def test_binding_mirrors_every_entry_point():
+    # the Python binding has one function of the same name per C entry point (the error-string
+    # accessor is read through MQError instead), and the format / op tables cover the same calls
+    for name in B.header_functions():
+        if name == "mq_last_error":
+            continue
+        assert callable(getattr(B, name, None)), name
+    assert set(B.GEMM) <= set(B.GEMV)
+    for (path, fmt), op in B.DEBUG_OP.items():
+        assert (B.GEMM if path == "gemm" else B.GEMV)[fmt].__name__ == f"mq_{path}_{fmt}", (path, fmt, op)
+    assert sorted(B.DEBUG_OP.values()) == list(range(len(B.DEBUG_OP)))
+
+
 @pytest.mark.parametrize("M,K", [(0, 256), (1, 256), (8, 512), (3314, 3584), (3314, 18944), (7, 768)])
 def test_plane_layout(L, M, K):
     lay = B.mq_q8_plane_layout(M, K)
