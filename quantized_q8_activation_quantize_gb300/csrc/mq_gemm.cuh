@@ -111,15 +111,6 @@ struct Bars {
     uint64_t *amin_full, *amin_empty, *min_final, *da_full, *da_empty;
 };
 
-// 16-byte async copy global -> shared (L2 only); completion tracked by cp.async groups / mbarriers
-__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
-// arrive on `bar` (without raising its expected count) once this thread's cp.async copies land
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -217,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.ab_empty[s], 1);
         }
         for (int r = 0; r < R; ++r) {
-            // Q4_K: one tensor copy per super-block (producer); Q6_K: each row's cp.async (unpackers)
+            // TMA-fed formats: one tensor copy per super-block (producer); Q6_K: one bulk copy per row (unpackers)
             mbar_init(&bars.raw_full[r], C::TMW ? 1 : 128);
             mbar_init(&bars.raw_empty[r], 4);                  // unpack warps (TMA-fed formats only)
         }
@@ -443,18 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bmin_tile0 = smem_u32(sm + C::OFF_BMIN);
         float *info0 = reinterpret_cast<float *>(sm + C::OFF_INFO);
 
-        // Q6_K: this row's block (210 B, 2-byte aligned) as the 16-byte aligned superset, fetched by
-        // 16-byte cp.async (too small and too many for the bulk-copy engine: 128 rows per super-block)
+        // Q6_K: this row's block (210 B, 2-byte aligned) as the 16-byte aligned superset (224 B at
+        // most), one bulk copy per row: rows of K/256 x 210 bytes fit no TMA tensor map
         auto issue_raw = [&](int sb) {
             const int slot = sb % R;
             if (valid) {
                 const uint8_t *src = wrow + (int64_t)sb * C::BB;
                 const uint8_t *a0 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15));
-                const int nchunk = (int)(((reinterpret_cast<uintptr_t>(src) + C::BB + 15) & ~uintptr_t(15)) -
-                                         reinterpret_cast<uintptr_t>(a0)) / 16;
-                const uint32_t dst = smem_u32(raw_row0 + slot * BN * C::RAW_ROW);
-                for (int i = 0; i < nchunk; ++i) cp_async16(dst + 16 * i, a0 + 16 * i);
-                cp_async_arrive_noinc(&bars.raw_full[slot]);
+                const uint32_t nbytes = (uint32_t)(((reinterpret_cast<uintptr_t>(src) + C::BB + 15) & ~uintptr_t(15)) -
+                                                   reinterpret_cast<uintptr_t>(a0));
+                // one bulk copy of the row's aligned superset (<= RAW_ROW bytes; the bytes past
+                // the block stay in the 16-byte granule of its last byte)
+                mbar_arrive_expect_tx(&bars.raw_full[slot], nbytes);
+                bulk_copy_g2s(raw_row0 + slot * BN * C::RAW_ROW, a0, nbytes, &bars.raw_full[slot]);
             } else {
                 mbar_arrive(&bars.raw_full[slot]);
             }
