@@ -2,7 +2,7 @@
 """Benchmark of the Q4_K / Q5_K / Q6_K x Q8 path on GB300 at 7B shapes.  Prints ONE JSON line.
 
 Step (the headline `value`): one 7B FFN prefill at the pages' 3314-token prompt length
-(config 2), every row of the hot path:
+(3314 tokens), every row of the hot path:
     RMSNorm-fused Q8 quantize (x_hidden 3314 x 3584)
     -> Q4_K tensor-core GEMM gate (18944 x 3584)  -> Q4_K GEMM up (18944 x 3584)
     -> plain Q8 quantize (x_ffn 3314 x 18944)      -> Q6_K GEMM down (3584 x 18944)
@@ -11,12 +11,12 @@ The step's footprint (weights 132 MB, activations 298 MB, outputs 549 MB) is far
 than the 129 MB L2, so consecutive steps do not hit L2 for their inputs (no flush).
 
 Also reported, measured in the same run:
-  "decode":  config 3, one decode token through all 196 per-layer matmuls of a 28-layer
+  "decode":  the decode sweep, one decode token through all 196 per-layer matmuls of a 28-layer
              7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph whose
              branches run a layer's independent matmuls -- q|k|v, gate|up -- side by side; the
              linear chain is reported as "serial"), weight GB/s and tok/s; 3.9 GB of weights,
              far larger than L2.
-  "lm_head": config 4 at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
+  "lm_head": the 152064 x 3584 Q6_K LM head at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
   "gate_up_swiglu": the fused gate|up GEMM with the SwiGLU epilogue writing the down
@@ -77,20 +77,20 @@ INT8_MMA_SYNC_PEAK_TOPS = 158.1
 
 # single-kernel cases for profiler captures: name -> (config, kernel); inputs of the named config
 CASES = {
-    "gemm_q4k_gate": "config 2 gate GEMM: Q4_K 18944x3584, M=3314",
-    "gemm_q6k_down": "config 2 down GEMM: Q6_K 3584x18944, M=3314",
-    "gemm_q4k_qproj": "config 1 q_proj GEMM: Q4_K 3584x3584, M=512",
-    "gemv_q6k_lmhead": "config 4 LM head GEMV: Q6_K 152064x3584, M=1",
-    "gemv_q4k_gate": "config 3 layer-1 gate GEMV: Q4_K 18944x3584, M=1",
+    "gemm_q4k_gate": "7B FFN prefill gate GEMM: Q4_K 18944x3584, M=3314",
+    "gemm_q6k_down": "7B FFN prefill down GEMM: Q6_K 3584x18944, M=3314",
+    "gemm_q4k_qproj": "7B q_proj prefill GEMM: Q4_K 3584x3584, M=512",
+    "gemv_q6k_lmhead": "LM head GEMV: Q6_K 152064x3584, M=1",
+    "gemv_q4k_gate": "decode sweep layer-1 gate GEMV: Q4_K 18944x3584, M=1",
     "gemv_q5k_vocab": "Q5_K GEMV of the LM-head shape: 152064x3584 synthetic Q5_K weights, M=1",
     **{f"gemv_{f}_vocab": f"{f.upper()} GEMV of the LM-head shape: 152064x3584 synthetic {f.upper()} weights, M=1"
        for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
     **{f"gemm_{f}_gate": f"{f.upper()} GEMM of the gate shape: 18944x3584 synthetic {f.upper()} weights, M=3314"
        for f in ("q4_0", "q4_1", "q5_0", "q5_1", "q8_0")},
-    "gemm_swiglu_ffn": "config 2 fused gate|up GEMM: Q4_K 2 x 18944x3584, M=3314, SwiGLU epilogue -> down plane",
-    "quantize_rms": "config 2 RMSNorm-fused Q8 quantize: 3314x3584",
-    "decode_sweep": "config 3: the 196 quantize + GEMV pairs of one decode token, plain launches",
-    "quantize_ffn": "config 2 plain Q8 quantize: 3314x18944",
+    "gemm_swiglu_ffn": "7B FFN prefill fused gate|up GEMM: Q4_K 2 x 18944x3584, M=3314, SwiGLU epilogue -> down plane",
+    "quantize_rms": "7B FFN prefill RMSNorm-fused Q8 quantize: 3314x3584",
+    "decode_sweep": "decode sweep: the 196 quantize + GEMV pairs of one decode token, plain launches",
+    "quantize_ffn": "7B FFN prefill plain Q8 quantize: 3314x18944",
 }
 
 
@@ -111,24 +111,24 @@ def run_case(args):
         print(json.dumps({"case": name, "what": CASES[name], "launches": (1 + args.reps) * 2 * len(sw.items)}))
         return
     if name.startswith("gemm_q4k_gate") or name.startswith("gemm_q6k_down") or name.startswith("quantize"):
-        c = I.config2()
+        c = I.ffn_prefill()
         M = c["x_hidden"].shape[0]
         if name == "gemm_q6k_down" or name == "quantize_ffn":
             x, K, N, w, fmt, rms = c["x_ffn"], I.FFN, I.HIDDEN, c["w_down"], "q6k", None
         else:
             x, K, N, w, fmt, rms = c["x_hidden"], I.HIDDEN, I.FFN, c["w_gate"], "q4k", c["rms_w"]
     elif name == "gemm_q4k_qproj":
-        c = I.config1()
+        c = I.qproj_prefill()
         x, w, fmt, rms = c["x"], c["w"], "q4k", None
         M, K, N = x.shape[0], x.shape[1], w.shape[0]
     elif name == "gemv_q6k_lmhead":
-        x, w, fmt, rms = I.config4_x(1), I.config4_weights(), "q6k", None
+        x, w, fmt, rms = I.lm_head_x(1), I.lm_head_weights(), "q6k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     elif name == "gemv_q5k_vocab":
-        x, w, fmt, rms = I.config4_x(1), I.q5k_vocab_weights(), "q5k", None
+        x, w, fmt, rms = I.lm_head_x(1), I.q5k_vocab_weights(), "q5k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     elif name == "gemm_swiglu_ffn" or (name.startswith("gemm_q") and name[5:-5] in I.B32_BYTES):
-        c = I.config2()
+        c = I.ffn_prefill()
         x, rms, K, N = c["x_hidden"], c["rms_w"], I.HIDDEN, I.FFN
         M = x.shape[0]
         if name == "gemm_swiglu_ffn":
@@ -138,10 +138,10 @@ def run_case(args):
             w = I.b32_weights(I.rng(2, I.STREAM_W, 6 + list(I.B32_BYTES).index(fmt)), N, K, fmt)
     elif name.startswith("gemv_q") and name[5:-6] in I.B32_BYTES:
         fmt = name[5:-6]
-        x, w, rms = I.config4_x(1), I.b32_vocab_weights(fmt), None
+        x, w, rms = I.lm_head_x(1), I.b32_vocab_weights(fmt), None
         M, K, N = 1, I.HIDDEN, I.VOCAB
     else:
-        c = I.config3_matrix(1, 4)
+        c = I.decode_matrix(1, 4)
         x, w, fmt, rms = c["x"], c["w"], "q4k", None
         M, K, N = 1, I.HIDDEN, I.FFN
     xd, wd = dev(x), dev(w.reshape(N, -1))
@@ -260,11 +260,11 @@ def ffn_ops(M):
 
 
 class Prefill:
-    """Config 2: the 7B FFN prefill step at M = 3314, device-resident inputs."""
+    """The 7B FFN prefill step at M = 3314, device-resident inputs."""
 
     def __init__(self, torch, B, I):
         self.torch, self.B = torch, B
-        c = I.config2()
+        c = I.ffn_prefill()
         self.M, self.H, self.F = c["x_hidden"].shape[0], I.HIDDEN, I.FFN
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
         self.w_gate = dev(c["w_gate"].reshape(self.F, -1))
@@ -341,15 +341,15 @@ class Prefill:
 
 
 class DecodeSweep:
-    """Config 3: one decode token through the 196 matmuls of a 28-layer 7B q4_K_m stack."""
+    """The decode sweep: one decode token through the 196 matmuls of a 28-layer 7B q4_K_m stack."""
 
     def __init__(self, torch, B, I):
         self.torch, self.B = torch, B
         self.items = []
         self.weight_bytes = 0
         self.bytes = 0
-        for (layer, idx, name, fmt, n, k) in I.config3_layout():
-            c = I.config3_matrix(layer, idx)
+        for (layer, idx, name, fmt, n, k) in I.decode_layout():
+            c = I.decode_matrix(layer, idx)
             w = torch.from_numpy(c["w"].reshape(n, -1)).cuda()
             x = torch.from_numpy(c["x"]).cuda()
             plane = B.alloc_plane(1, k)
@@ -428,10 +428,10 @@ def time_events(torch, fn, steps, warmup):
 # ------------------------------------------------------------------------------ CPU oracle ---
 
 def cpu_oracle_ffn(budget_s: float, threads: int):
-    """The oracle on token slices of the config-2 step until `budget_s` is spent."""
+    """The oracle on token slices of the FFN prefill step until `budget_s` is spent."""
     import oracle
     from quantized_q8_activation_quantize_gb300 import inputs as I
-    c = I.config2()
+    c = I.ffn_prefill()
     t_done, ops, tokens = 0.0, 0, 0
     chunk = 4
     while t_done < budget_s and tokens < c["x_hidden"].shape[0]:
@@ -469,7 +469,7 @@ def run_reference(args, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8 dots, f64 scaling (CPU oracle)",
             "data": "synthetic (seeded, 7B q4_K_m shapes)",
-            "config": {"workload": "7B FFN prefill, 3314 tokens (config 2): RMSNorm-Q8, gate/up Q4_K 18944x3584, "
+            "config": {"workload": "7B FFN prefill, 3314 tokens: RMSNorm-Q8, gate/up Q4_K 18944x3584, "
                                    "Q8, down Q6_K 3584x18944", "tokens_per_step_sample": tokens},
             "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
                              "sample": f"first {tokens} of 3314 tokens of the FFN step per timed step"},
@@ -530,7 +530,7 @@ def main():
     q6k_tflops = pf.gemm_q6k_ops / (k_ms[4] * 1e-3) / 1e12
     qrms_gbs = (pf.M * pf.H * 4 + pf.H * 4 + B.mq_q8_plane_bytes(pf.M, pf.H)) / (k_ms[0] * 1e-3) / 1e9
     q_gbs = (pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (k_ms[3] * 1e-3) / 1e9
-    # the SwiGLU producer (NEXT row, not part of config 2's step): the down projection's plane
+    # the SwiGLU producer (NEXT row, not part of the FFN prefill step): the down projection's plane
     # from this step's gate / up outputs
     swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f), K, W)
     swiglu_gbs = (2 * pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (swiglu_ms * 1e-3) / 1e9
@@ -593,7 +593,7 @@ def main():
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 (exact integer block dots on f16 tensor-core MMA) + f32 scaling",
         "data": "synthetic (seeded, 7B q4_K_m shapes)",
-        "config": {"workload": "7B FFN prefill, 3314 tokens (config 2): RMSNorm-Q8, gate/up Q4_K 18944x3584, "
+        "config": {"workload": "7B FFN prefill, 3314 tokens: RMSNorm-Q8, gate/up Q4_K 18944x3584, "
                                "Q8, down Q6_K 3584x18944", "tokens": pf.M, "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{dist.world}"},
         "prefill_tok_per_s": dist.world * pf.M / (ms_step * 1e-3),
@@ -618,10 +618,10 @@ def main():
 
     # ---------------- decode: LM head GEMV and the 28-layer sweep
     if not args.skip_decode:
-        lm_w = torch.from_numpy(I.config4_weights().reshape(I.VOCAB, -1)).cuda()
+        lm_w = torch.from_numpy(I.lm_head_weights().reshape(I.VOCAB, -1)).cuda()
         lm = {}
         for m, paths in ((1, ("gemv",)), (16, ("gemv", "gemm")), (I.PREFILL_TOKENS, ("gemm",))):
-            x = torch.from_numpy(I.config4_x(m)).cuda()
+            x = torch.from_numpy(I.lm_head_x(m)).cuda()
             plane = B.alloc_plane(m, I.HIDDEN)
             B.mq_quantize_q8(x, m, I.HIDDEN, None, 0.0, plane)
             y = torch.empty((m, I.VOCAB), dtype=torch.float32, device="cuda")
@@ -635,7 +635,7 @@ def main():
         line["lm_head"] = lm
         # the Q5_K decode GEMV on a matrix of the LM-head shape (synthetic Q5_K weights)
         w5 = torch.from_numpy(I.q5k_vocab_weights().reshape(I.VOCAB, -1)).cuda()
-        x = torch.from_numpy(I.config4_x(1)).cuda()
+        x = torch.from_numpy(I.lm_head_x(1)).cuda()
         plane = B.alloc_plane(1, I.HIDDEN)
         B.mq_quantize_q8(x, 1, I.HIDDEN, None, 0.0, plane)
         y = torch.empty((1, I.VOCAB), dtype=torch.float32, device="cuda")
@@ -669,7 +669,7 @@ def main():
         B.mq_device_status()
         gemv_bytes = sw.bytes - 4 * sum(k for *_, k in sw.items)          # without the f32 activations
         lm_ms = lm["m1_gemv"]["ms"]
-        line["decode"] = {"workload": "config 3: 28 layers x 7 matmuls, M=1, Q8 quantize + GEMV each, one CUDA graph; "
+        line["decode"] = {"workload": "7B decode sweep: 28 layers x 7 matmuls, M=1, Q8 quantize + GEMV each, one CUDA graph; "
                                       "each layer's independent matmuls (q|k|v from the layer input, gate|up from the "
                                       "post-attention input) on parallel branches, joined before o and before down",
                           "ms_per_token": ms_br, "tok_per_s": 1e3 / ms_br, "weight_bytes": sw.weight_bytes,

@@ -8,10 +8,12 @@ two sides always see identical bytes.
 
 Workloads follow the 7B q4_K_m shapes of the minfer pages (Qwen2.5-7B: hidden
 3584, 28 query heads and 4 KV heads of dim 128, FFN 18944, vocab 152064;
-3314-token prefill prompt).  Seeds are ``20261202 + 100 * config + stream``
-with stream 0 = weights, 1 = activations, 2 = RMSNorm weight, 3 = outlier
-channel choice; matrices of one config that need separate streams add their
-(layer, matrix) index to the numpy ``SeedSequence``.
+3314-token prefill prompt).  Seeds are ``20261202 + 100 * case + stream`` with case
+0 = the tiny Q4_K GEMM, 1 = the q_proj prefill, 2 = the FFN prefill, 3 = the decode
+sweep, 4 = the LM head (and the synthetic-format matrices of its shape), and stream
+0 = weights, 1 = activations, 2 = RMSNorm weight, 3 = outlier channel choice; matrices
+of one workload that need separate streams add their (layer, matrix) index to the numpy
+``SeedSequence``.
 
 Block sizes (GGML k-quant super-blocks of 256 values): Q4_K = 144 bytes
 (fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales/mins, 128 bytes of 4-bit
@@ -41,15 +43,15 @@ PREFILL_TOKENS = 3314
 N_LAYERS = 28
 
 
-def seed(config: int, stream: int) -> int:
-    return SEED_BASE + 100 * config + stream
+def seed(case: int, stream: int) -> int:
+    return SEED_BASE + 100 * case + stream
 
 
-def rng(config: int, stream: int, *extra: int) -> np.random.Generator:
-    """PCG64 generator for one (config, stream[, layer, matrix]) input."""
+def rng(case: int, stream: int, *extra: int) -> np.random.Generator:
+    """PCG64 generator for one (workload case, stream[, layer, matrix]) input."""
     if extra:
-        return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed(config, stream), *extra])))
-    return np.random.Generator(np.random.PCG64(seed(config, stream)))
+        return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed(case, stream), *extra])))
+    return np.random.Generator(np.random.PCG64(seed(case, stream)))
 
 
 def _fp16_bytes(r: np.random.Generator, shape, lo: float, hi: float) -> np.ndarray:
@@ -142,7 +144,7 @@ def outlier_channels(r: np.random.Generator, k: int, fraction: float = 0.01) -> 
 
 def swiglu_inputs(r: np.random.Generator, m: int, k: int):
     """Gate and up projections [m, k] f32 for the SwiGLU producer: N(0, 4^2) and N(0, 2^2)
-    (the spread of the config-2 gate / up outputs), a few gate values pushed into the
+    (the spread of the 7B FFN prefill's gate / up outputs), a few gate values pushed into the
     tails where exp saturates."""
     g = (4.0 * r.standard_normal((m, k))).astype(np.float32)
     u = (2.0 * r.standard_normal((m, k))).astype(np.float32)
@@ -160,14 +162,14 @@ def rms_weight(r: np.random.Generator, k: int) -> np.ndarray:
 # The five workloads.  Each returns plain numpy arrays; sizes are in the docstrings.
 # --------------------------------------------------------------------------------------------
 
-def config0():
+def tiny_q4k():
     """Tiny Q4_K GEMM: W 256 x 512 (Q4_K), X 8 x 512 N(0,1); Y is 8 x 256."""
     w = q4k_weights(rng(0, STREAM_W), 256, 512)
     x = activations(rng(0, STREAM_X), 8, 512)
     return {"w": w, "x": x, "fmt": "q4k"}
 
 
-def config1():
+def qproj_prefill():
     """q_proj prefill: W 3584 x 3584 (Q4_K), X 512 x 3584 N(0,1) with 36 channels x20."""
     w = q4k_weights(rng(1, STREAM_W), HIDDEN, HIDDEN)
     x = activations(rng(1, STREAM_X), 512, HIDDEN)
@@ -176,7 +178,7 @@ def config1():
     return {"w": w, "x": x, "fmt": "q4k", "outlier_channels": ch}
 
 
-def config2(m: int = PREFILL_TOKENS):
+def ffn_prefill(m: int = PREFILL_TOKENS):
     """7B FFN prefill: gate/up W 18944 x 3584 (Q4_K), down W 3584 x 18944 (Q6_K, scales [-64, 63]).
 
     x_hidden [m, 3584] N(0,1) goes through the RMSNorm producer (weight N(1, 0.1), eps 1e-6)
@@ -199,7 +201,7 @@ LAYER_MATRICES = (("q", HIDDEN, HIDDEN), ("k", KV_DIM, HIDDEN), ("v", KV_DIM, HI
                   ("down", HIDDEN, FFN))
 
 
-def config3_layout(n_layers: int = N_LAYERS):
+def decode_layout(n_layers: int = N_LAYERS):
     """The decode sweep's matmul list: (layer, index, name, fmt, N, K).
 
     q, k, o, gate, up are Q4_K.  v and down are Q6_K in even layers and Q4_K in
@@ -213,9 +215,9 @@ def config3_layout(n_layers: int = N_LAYERS):
     return out
 
 
-def config3_matrix(layer: int, idx: int):
+def decode_matrix(layer: int, idx: int):
     """Weight bytes and the 1 x K activation for one matmul of the decode sweep."""
-    _, _, name, fmt, n, k = next(e for e in config3_layout(layer + 1) if e[0] == layer and e[1] == idx)
+    _, _, name, fmt, n, k = next(e for e in decode_layout(layer + 1) if e[0] == layer and e[1] == idx)
     gen = q6k_weights if fmt == "q6k" else q4k_weights
     w = gen(rng(3, STREAM_W, layer, idx), n, k)
     x = activations(rng(3, STREAM_X, layer, idx), 1, k)
@@ -233,21 +235,21 @@ def b32_vocab_weights(fmt: str):
     return b32_weights(rng(4, STREAM_W, 6 + list(B32_BYTES).index(fmt)), VOCAB, HIDDEN, fmt)
 
 
-def config4_weights():
+def lm_head_weights():
     """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
     return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
 
 
-def config2_swiglu(m: int = PREFILL_TOKENS):
-    """The down projection's SwiGLU producer inputs at the config-2 size: gate, up m x 18944."""
+def ffn_swiglu_inputs(m: int = PREFILL_TOKENS):
+    """The down projection's SwiGLU producer inputs at the 7B FFN prefill size: gate, up m x 18944."""
     return swiglu_inputs(rng(2, STREAM_SWIGLU), m, FFN)
 
 
-def config4_x(m: int):
+def lm_head_x(m: int):
     """LM head activations: m x 3584 f32 N(0,1), m in {1, 16, 3314}."""
     return activations(rng(4, STREAM_X, m), m, HIDDEN)
 
 
-def config4(m: int):
+def lm_head_case(m: int):
     """LM head: W 152064 x 3584 (Q6_K, scales [-64, 63]), X m x 3584 N(0,1), m in {1, 16, 3314}."""
-    return {"w": config4_weights(), "x": config4_x(m), "fmt": "q6k"}
+    return {"w": lm_head_weights(), "x": lm_head_x(m), "fmt": "q6k"}

@@ -99,8 +99,8 @@ def test_extreme_blocks(path):
 
 
 @pytest.mark.parametrize("path", ["gemv", "gemm"])
-def test_config0(path):
-    c = inputs.config0()
+def test_tiny_q4k_case(path):
+    c = inputs.tiny_q4k()
     M, K = c["x"].shape
     N = c["w"].shape[0]
     plane, got = G.gpu_plane(c["x"])
@@ -111,8 +111,8 @@ def test_config0(path):
     assert np.array_equal(I, oracle.blockdots(c["w"], "q4k", ref_plane[0])[0])
 
 
-def test_config1_gemm_full():
-    c = inputs.config1()
+def test_qproj_prefill_gemm_full():
+    c = inputs.qproj_prefill()
     M, K = c["x"].shape
     N = c["w"].shape[0]
     plane, got = G.gpu_plane(c["x"])
@@ -149,8 +149,8 @@ def _sample_idx(total, count, seed, must=()):
     return np.array(sorted(i for i in idx if 0 <= i < total))
 
 
-def test_config2_full_size_sampled():
-    c = inputs.config2()
+def test_ffn_prefill_full_size_sampled():
+    c = inputs.ffn_prefill()
     M = c["x_hidden"].shape[0]
     plane_h, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
     ref_h = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
@@ -166,11 +166,11 @@ def test_config2_full_size_sampled():
     _sampled("gemm", "q6k", c["w_down"], plane_f, ref_f, M, 18944, 3584, ms, ns, dump_window=(3200, 114, 0, 40))
 
 
-def test_config3_decode_layers():
+def test_decode_sweep_layers():
     # two layers of the decode sweep: layer 0 (Q6_K v and down) and layer 1 (all Q4_K), full rows
     for layer in (0, 1):
         for idx in range(7):
-            c = inputs.config3_matrix(layer, idx)
+            c = inputs.decode_matrix(layer, idx)
             N, K = c["w"].shape[0], c["x"].shape[1]
             plane, _ = G.gpu_plane(c["x"])
             ref_plane = G.oracle_plane(c["x"])
@@ -183,12 +183,12 @@ def test_config3_decode_layers():
 
 @pytest.fixture(scope="module")
 def lm_head():
-    return inputs.config4_weights()
+    return inputs.lm_head_weights()
 
 
 @pytest.mark.parametrize("M,paths", [(1, ("gemv",)), (16, ("gemv", "gemm")), (3314, ("gemm",))])
-def test_config4_lm_head(lm_head, M, paths):
-    x = inputs.config4_x(M)
+def test_lm_head(lm_head, M, paths):
+    x = inputs.lm_head_x(M)
     N, K = lm_head.shape[0], 3584
     plane, _ = G.gpu_plane(x)
     ref_plane = G.oracle_plane(x)
@@ -282,7 +282,7 @@ def test_q5k_gemm_extreme_blocks():
 
 def test_q5k_gemm_ffn_size_sampled():
     # the 7B FFN gate shape with Q5_K weights at the 3314-token prompt
-    c = inputs.config2()
+    c = inputs.ffn_prefill()
     M, K, N = c["x_hidden"].shape[0], 3584, 18944
     w = _weights("q5k", N, K, 41)
     plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
@@ -334,7 +334,7 @@ def test_b32_gemv_model_sizes(fmt, M, N, K):
 def test_b32_gemv_vocab_sampled(fmt):
     # the LM-head shape (152064 x 3584) at M = 1, the launch the benchmark times
     w = inputs.b32_vocab_weights(fmt)
-    x = inputs.config4_x(1)
+    x = inputs.lm_head_x(1)
     N, K = w.shape[0], 3584
     plane, _ = G.gpu_plane(x)
     ref_plane = G.oracle_plane(x)
@@ -369,7 +369,7 @@ def test_b32_gemm_extreme_blocks(fmt, fill):
 @pytest.mark.parametrize("fmt", B32_FMTS)
 def test_b32_gemm_ffn_size_sampled(fmt):
     # the 7B FFN gate shape at the 3314-token prompt, synthetic weights of the format
-    c = inputs.config2()
+    c = inputs.ffn_prefill()
     M, K, N = c["x_hidden"].shape[0], 3584, 18944
     w = _weights(fmt, N, K, 43 + ord(fmt[1]) + ord(fmt[3]))
     plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))

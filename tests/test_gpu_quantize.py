@@ -16,8 +16,8 @@ def test_plain_quantize_bit_exact(M, K):
     G.assert_plane_equal(got, G.oracle_plane(x))
 
 
-def test_config0_and_config1_planes():
-    for cfg in (inputs.config0(), inputs.config1()):
+def test_tiny_and_qproj_planes():
+    for cfg in (inputs.tiny_q4k(), inputs.qproj_prefill()):
         _, got = G.gpu_plane(cfg["x"])
         G.assert_plane_equal(got, G.oracle_plane(cfg["x"]))
 
@@ -45,8 +45,8 @@ def test_rms_quantize_bit_exact_small():
         G.assert_plane_equal(got, G.oracle_plane(x, w, 1e-6))
 
 
-def test_config2_full_size_planes():
-    cfg = inputs.config2()
+def test_ffn_prefill_full_size_planes():
+    cfg = inputs.ffn_prefill()
     _, got = G.gpu_plane(cfg["x_hidden"], cfg["rms_w"], float(cfg["eps"]))
     G.assert_plane_equal(got, G.oracle_plane(cfg["x_hidden"], cfg["rms_w"], float(cfg["eps"])))
     _, got = G.gpu_plane(cfg["x_ffn"])

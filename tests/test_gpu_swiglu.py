@@ -128,7 +128,7 @@ def test_gate_up_swiglu_shapes(M, K, F):
 
 def test_gate_up_swiglu_ffn_size():
     # the 7B FFN at the 3314-token prompt: gate / up 18944 x 3584 Q4_K from the RMSNorm plane
-    c = inputs.config2()
+    c = inputs.ffn_prefill()
     M, K, F = c["x_hidden"].shape[0], inputs.HIDDEN, inputs.FFN
     plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
     ref_plane = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
