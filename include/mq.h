@@ -1,5 +1,6 @@
 /*
- * mq.h -- C ABI of the GB300 (sm_103a) quantized k-quant matmul library.
+ * mq.h -- C ABI of the GB300 (sm_103a) quantized matmul library (GGML k-quants and
+ * 32-value block formats).
  *
  * The hot path of quantized LLM inference over GGML k-quant weights, as the
  * minfer pages describe it ("minfer" book print view, "Features > GPU -- CUDA";
@@ -7,8 +8,8 @@
  *   1. f32 activations are quantized on the fly into an int8 Q8 plane
  *      (blocks of 32, one f32 scale per block), optionally straight out of an
  *      RMSNorm producer, so the normalized f32 rows are never written;
- *   2. prefill (many tokens) multiplies the plane with raw Q4_K / Q6_K
- *      super-blocks on the tensor cores (MMQ);
+ *   2. prefill (many tokens) multiplies the plane with raw Q4_K / Q5_K / Q6_K
+ *      super-blocks (or Q4_0 .. Q8_0 blocks) on the tensor cores (MMQ);
  *   3. decode (one or a few tokens) streams the raw weight bytes once and
  *      takes integer dots per block on the CUDA cores (MMVQ).
  *
@@ -24,6 +25,9 @@
  *   - Weights are raw GGML block bytes, row-major [N rows][K/256 super-blocks]
  *     (weight memory layout [out][in], "Architecture > 4.5 Core invariants",
  *     item 3), base aligned to 16 bytes.  K must be a positive multiple of 256.
+ *     Weights are copied in 16-byte aligned pieces, so a read may run up to 15
+ *     bytes past the last weight byte, never past the 16-byte granule that holds
+ *     it; those bytes do not affect any result.
  *   - Activations are token-major f32 [M][K]; outputs are token-major f32 [M][N].
  *   - M == 0 or N == 0 is a valid empty call (returns MQ_OK, launches nothing).
  *   - Kernels never wait without bound.  A device-side wait that runs out sets
