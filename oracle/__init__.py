@@ -5,8 +5,10 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the bench's ``cpu_baseline`` / ``--impl reference`` legs, never by the
 package.  It shares no code with the CUDA library.
 
-Every function here is a thin marshalling layer over ``mq_oracle.c``; the
-arithmetic, and the citation of the passage each step follows, live there.
+Every function here is a thin marshalling layer over ``mq_oracle.c`` (the
+arithmetic, and the citation of the passage each step follows, live there), or
+a composition of such functions (``gate_up_swiglu_q8``: two matmuls rounded to
+f32, then the SwiGLU producer).
 Arrays use the oracle's own logical layouts:
 
 * weights: raw GGML block bytes, ``[N, K/256, B]`` with B = 144 (Q4_K), 176 (Q5_K), 210 (Q6_K),
