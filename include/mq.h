@@ -29,6 +29,7 @@
  *     bytes past the last weight byte, never past the 16-byte granule that holds
  *     it; those bytes do not affect any result.
  *   - Activations are token-major f32 [M][K]; outputs are token-major f32 [M][N].
+ *     An output must not overlap any input of the same call.
  *   - M == 0 or N == 0 is a valid empty call (returns MQ_OK, launches nothing).
  *   - Kernels never wait without bound.  A device-side wait that runs out sets
  *     a per-device error word and the kernel returns early; mq_device_status()
@@ -167,7 +168,8 @@ MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
  * G and U are what mq_gemm_q4k writes for w_gate and w_up (the same f32 values, bit for bit);
  * the output plane is then what mq_quantize_swiglu_q8(G, U) writes, so the pair
  * (mq_gemm_q4k x 2, mq_quantize_swiglu_q8) and this call give identical planes, without the
- * two f32 [M][F] intermediates.  Same errors as mq_gemm_q4k plus MQ_ERR_SHAPE for F % 256.
+ * two f32 [M][F] intermediates.  Same errors as mq_gemm_q4k plus MQ_ERR_SHAPE for F % 256
+ * and MQ_ERR_ARG if plane_out overlaps plane_in.
  */
 MQ_API int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t K, const void *plane_in,
                               int64_t M, void *plane_out, mq_stream_t stream);

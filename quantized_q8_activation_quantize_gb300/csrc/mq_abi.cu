@@ -367,6 +367,13 @@ int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t 
         return set_error(MQ_ERR_ALIGN, "%s: weights %p / %p not 16-byte aligned", fn, w_gate, w_up);
     if (!aligned(plane_in, 256) || !aligned(plane_out, 256))
         return set_error(MQ_ERR_ALIGN, "%s: planes %p / %p not 256-byte aligned", fn, plane_in, plane_out);
+    {
+        // the output plane is written while the input plane is read: they must not overlap
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(plane_in), o0 = reinterpret_cast<uintptr_t>(plane_out);
+        const uintptr_t i1 = i0 + mq_q8_plane_bytes(M, K), o1 = o0 + mq_q8_plane_bytes(M, F);
+        if (i0 < o1 && o0 < i1)
+            return set_error(MQ_ERR_ARG, "%s: plane_out %p overlaps plane_in %p", fn, plane_out, plane_in);
+    }
     unsigned int *err = nullptr;
     rc = device_state(&err);
     if (rc != MQ_OK) return rc;

@@ -174,3 +174,7 @@ def test_gate_up_swiglu_argument_errors(L):
     assert f(16, 24, 256, 256, 256, 4, 256, None) == B.MQ_ERR_ALIGN
     assert f(16, 16, 256, 256, 128, 4, 256, None) == B.MQ_ERR_ALIGN     # plane_in
     assert f(16, 16, 256, 256, 256, 4, 384, None) == B.MQ_ERR_ALIGN     # plane_out
+    n_in = B.mq_q8_plane_bytes(4, 256)
+    assert f(16, 16, 256, 256, 1 << 20, 4, 1 << 20, None) == B.MQ_ERR_ARG           # the same plane
+    assert f(16, 16, 256, 256, 1 << 20, 4, (1 << 20) + 256, None) == B.MQ_ERR_ARG   # overlapping
+    assert n_in > 256
