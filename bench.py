@@ -72,8 +72,13 @@ def parse_args():
 # changes until it is captured again.
 TRAFFIC_GEMM_Q4K_GATE = 95.565824e6 + 205.278720e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
 TRAFFIC_GEMV_Q6K_LMHEAD = 447.181568e6 + 3.106560e6   # 152064x3584 Q6_K, M=1
-# the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs)
+# the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs): context
+# only -- the GEMM does not use that instruction
 INT8_MMA_SYNC_PEAK_TOPS = 158.1
+# the instruction the GEMM does use, tcgen05.mma kind::f16 issued back to back from shared memory on all
+# 152 SMs (a probe of this project, profiles/probes_gb300_peaks.md): the kernel's own instruction ceiling,
+# reported beside the cuBLAS bf16 denominator
+TCGEN05_F16_PROBE_TFLOPS = 2400.4
 
 # single-kernel cases for profiler captures: name -> (config, kernel); inputs of the named config
 CASES = {
@@ -612,7 +617,9 @@ def main():
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": q4k_tflops / bf16_peak,
                      "traffic": TRAFFIC_GEMM_Q4K_GATE,
                      "peak_kind": f"{peak_kind} dense bf16 (f16 MMA has the same nominal rate)",
-                     "vs_int8_mma_sync_peak": q4k_tflops / INT8_MMA_SYNC_PEAK_TOPS},
+                     "peak_probe": TCGEN05_F16_PROBE_TFLOPS, "frac_of_probe": q4k_tflops / TCGEN05_F16_PROBE_TFLOPS,
+                     "vs_int8_mma_sync_peak": q4k_tflops / INT8_MMA_SYNC_PEAK_TOPS,
+                     "vs_int8_mma_sync_note": "context only: the legacy int8 instruction is not what the kernel runs"},
         "e2e": e2e, "gpu_launches": pf.launches * K, "clocks": clk,
     }
 
@@ -687,8 +694,11 @@ def main():
     if dist.rank == 0 and dist.world == 1:
         threads = os.cpu_count() or 1
         v, tokens, secs = cpu_oracle_ffn(args.cpu_seconds, threads)
+        v1, tokens1, secs1 = cpu_oracle_ffn(max(0.5, args.cpu_seconds / 2), 1)
         line["cpu_baseline"] = {"value": v, "unit": "TOPS", "cores": threads, "kind": "oracle",
-                                "sample": f"first {tokens} of 3314 tokens of the FFN step ({secs:.1f} s)"}
+                                "sample": f"first {tokens} of 3314 tokens of the FFN step ({secs:.1f} s)",
+                                "single_core": {"value": v1, "unit": "TOPS", "cores": 1,
+                                                "sample": f"first {tokens1} of 3314 tokens ({secs1:.1f} s)"}}
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -29,7 +29,9 @@
  *     bytes past the last weight byte, never past the 16-byte granule that holds
  *     it; those bytes do not affect any result.
  *   - Activations are token-major f32 [M][K]; outputs are token-major f32 [M][N].
- *     An output must not overlap any input of the same call.
+ *     An output must not overlap any input of the same call: every entry point
+ *     compares the byte ranges of its output and its inputs on the host and
+ *     returns MQ_ERR_ARG if any two share a byte.
  *   - M == 0 or N == 0 is a valid empty call (returns MQ_OK, launches nothing).
  *   - Kernels never wait without bound.  A device-side wait that runs out sets
  *     a per-device error word and the kernel returns early; mq_device_status()
@@ -145,8 +147,9 @@ MQ_API int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, 
  *   Q6_K: d * sum_s sc_s * d_a[m][s/2] * D_s
  * with D the exact integer dot of the weight quants and the Q8 codes over a
  * 32-value (Q4_K sub-block) or 16-value (Q6_K sub-block) range.  The integer
- * dots are exact; the float scaling is f32.  Any M >= 0 (tokens are tiled by
- * 128, the tail is masked), any N >= 0.
+ * dots are exact; the float scaling is f32.  Any N >= 0 and any M from 0 to
+ * 65535 * 128 = 8388480 (tokens are tiled by 128, the tail is masked); a larger M
+ * returns MQ_ERR_SHAPE (split the tokens over several calls).
  */
 MQ_API int mq_gemm_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
                 float *y, mq_stream_t stream);
@@ -163,13 +166,14 @@ MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
  *   plane_in      Q8 plane of the M x K input (mq_quantize_q8)
  *   plane_out     Q8 plane of an M x F activation (mq_q8_plane_bytes(M, F) bytes, 256-byte
  *                 aligned), fully written
- *   F             rows of each projection, a positive multiple of 256 (the output plane's K)
+ *   F             rows of each projection, a multiple of 256 (the output plane's K) of at most
+ *                 65535 * 64 = 4194240; F == 0 (or M == 0) is a valid empty call
  *
  * G and U are what mq_gemm_q4k writes for w_gate and w_up (the same f32 values, bit for bit);
  * the output plane is then what mq_quantize_swiglu_q8(G, U) writes, so the pair
  * (mq_gemm_q4k x 2, mq_quantize_swiglu_q8) and this call give identical planes, without the
  * two f32 [M][F] intermediates.  Same errors as mq_gemm_q4k plus MQ_ERR_SHAPE for F % 256
- * and MQ_ERR_ARG if plane_out overlaps plane_in.
+ * or F beyond the limit and MQ_ERR_ARG if plane_out overlaps plane_in or either weight matrix.
  */
 MQ_API int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t K, const void *plane_in,
                               int64_t M, void *plane_out, mq_stream_t stream);

@@ -47,7 +47,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// whether the byte ranges [a, a + na) and [b, b + nb) share a byte
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return na != 0 && nb != 0 && a0 < b0 + nb && b0 < a0 + na;
+}
+
 constexpr int64_t kMaxDim = (int64_t)1 << 31;
+// the tensor-core GEMMs put their token tiles (128 tokens) in grid.y, the fused gate|up GEMM its
+// output tiles (64 rows of gate and of up) there; CUDA caps grid.y at 65535
+constexpr int64_t kMaxGemmM = (int64_t)65535 * 128;
+constexpr int64_t kMaxSwigluF = (int64_t)65535 * 64;
 }  // namespace
 
 int set_error(int code, const char *fmt, ...) {
@@ -177,19 +187,26 @@ static int check_k(int64_t K) {
     return MQ_OK;
 }
 
-// shared validation of the matmul entry points
-static int check_matmul(const char *fn, const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
-                        const float *y) {
+// shared validation of the matmul entry points (bb: weight bytes per 256 values of a row)
+static int check_matmul(const char *fn, bool gemm, int bb, const void *w, int64_t N, int64_t K, const void *plane,
+                        int64_t M, const float *y) {
     if (M < 0 || N < 0) return set_error(MQ_ERR_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
     int rc = check_k(K);
     if (rc != MQ_OK) return rc;
     if (M >= kMaxDim || N >= kMaxDim)
         return set_error(MQ_ERR_SHAPE, "%s: M=%lld N=%lld must be below 2^31", fn, (long long)M, (long long)N);
+    if (gemm && M > kMaxGemmM)
+        return set_error(MQ_ERR_SHAPE, "%s: M=%lld exceeds the GEMM limit of %lld tokens", fn, (long long)M,
+                         (long long)kMaxGemmM);
     if (M == 0 || N == 0) return MQ_OK;
     if (!w || !plane || !y) return set_error(MQ_ERR_ARG, "%s: NULL pointer (w=%p plane=%p y=%p)", fn, w, plane, (const void *)y);
     if (!aligned(w, 16)) return set_error(MQ_ERR_ALIGN, "%s: weights %p not 16-byte aligned", fn, w);
     if (!aligned(plane, 256)) return set_error(MQ_ERR_ALIGN, "%s: plane %p not 256-byte aligned", fn, plane);
     if (!aligned(y, 4)) return set_error(MQ_ERR_ALIGN, "%s: y %p not 4-byte aligned", fn, (const void *)y);
+    const size_t yb = (size_t)M * (size_t)N * 4, wb = (size_t)N * (size_t)(K / kQK) * (size_t)bb;
+    if (overlaps(y, yb, plane, mq_q8_plane_bytes(M, K)) || overlaps(y, yb, w, wb))
+        return set_error(MQ_ERR_ARG, "%s: output y %p overlaps the plane %p or the weights %p", fn, (const void *)y,
+                         plane, w);
     return MQ_OK;
 }
 
@@ -210,7 +227,7 @@ static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *p
                          {"mq_gemv_q8_0", FMT_Q8_0, false}, {"mq_gemm_q4_0", FMT_Q4_0, true},
                          {"mq_gemm_q4_1", FMT_Q4_1, true},  {"mq_gemm_q5_0", FMT_Q5_0, true},
                          {"mq_gemm_q5_1", FMT_Q5_1, true},  {"mq_gemm_q8_0", FMT_Q8_0, true}};
-    int rc = check_matmul(ops[op].name, w, N, K, plane, M, y);
+    int rc = check_matmul(ops[op].name, ops[op].gemm, block_bytes(ops[op].fmt), w, N, K, plane, M, y);
     if (rc != MQ_OK || M == 0 || N == 0) return rc;
     unsigned int *err = nullptr;
     rc = device_state(&err);
@@ -267,6 +284,10 @@ int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, flo
     if (rms_w && !aligned(rms_w, 16))
         return set_error(MQ_ERR_ALIGN, "mq_quantize_q8: rms_w %p not 16-byte aligned", (const void *)rms_w);
     if (!aligned(plane, 256)) return set_error(MQ_ERR_ALIGN, "mq_quantize_q8: plane %p not 256-byte aligned", plane);
+    const size_t pb = mq_q8_plane_bytes(M, K);
+    if (overlaps(plane, pb, x, (size_t)M * (size_t)K * 4) || (rms_w && overlaps(plane, pb, rms_w, (size_t)K * 4)))
+        return set_error(MQ_ERR_ARG, "mq_quantize_q8: plane %p overlaps x %p or rms_w %p", plane, (const void *)x,
+                         (const void *)rms_w);
     unsigned int *err = nullptr;
     rc = device_state(&err);
     if (rc != MQ_OK) return rc;
@@ -289,6 +310,12 @@ int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t
                          (const void *)up);
     if (!aligned(plane, 256))
         return set_error(MQ_ERR_ALIGN, "mq_quantize_swiglu_q8: plane %p not 256-byte aligned", plane);
+    {
+        const size_t pb = mq_q8_plane_bytes(M, K), xb = (size_t)M * (size_t)K * 4;
+        if (overlaps(plane, pb, gate, xb) || overlaps(plane, pb, up, xb))
+            return set_error(MQ_ERR_ARG, "mq_quantize_swiglu_q8: plane %p overlaps gate %p or up %p", plane,
+                             (const void *)gate, (const void *)up);
+    }
     unsigned int *err = nullptr;
     rc = device_state(&err);
     if (rc != MQ_OK) return rc;
@@ -356,10 +383,11 @@ int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t 
     if (M < 0 || F < 0) return set_error(MQ_ERR_ARG, "%s: negative size M=%lld F=%lld", fn, (long long)M, (long long)F);
     int rc = check_k(K);
     if (rc != MQ_OK) return rc;
-    if (F == 0 || F % kQK != 0 || F >= kMaxDim)
-        return set_error(MQ_ERR_SHAPE, "%s: F=%lld must be a positive multiple of 256 below 2^31", fn, (long long)F);
+    if (F % kQK != 0 || F > kMaxSwigluF)
+        return set_error(MQ_ERR_SHAPE, "%s: F=%lld must be a multiple of 256 of at most %lld", fn, (long long)F,
+                         (long long)kMaxSwigluF);
     if (M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "%s: M=%lld must be below 2^31", fn, (long long)M);
-    if (M == 0) return MQ_OK;
+    if (M == 0 || F == 0) return MQ_OK;
     if (!w_gate || !w_up || !plane_in || !plane_out)
         return set_error(MQ_ERR_ARG, "%s: NULL pointer (w_gate=%p w_up=%p plane_in=%p plane_out=%p)", fn, w_gate, w_up,
                          plane_in, plane_out);
@@ -373,6 +401,9 @@ int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t 
         const uintptr_t i1 = i0 + mq_q8_plane_bytes(M, K), o1 = o0 + mq_q8_plane_bytes(M, F);
         if (i0 < o1 && o0 < i1)
             return set_error(MQ_ERR_ARG, "%s: plane_out %p overlaps plane_in %p", fn, plane_out, plane_in);
+        const size_t wb = (size_t)F * (size_t)(K / kQK) * (size_t)block_bytes(FMT_Q4K), ob = o1 - o0;
+        if (overlaps(plane_out, ob, w_gate, wb) || overlaps(plane_out, ob, w_up, wb))
+            return set_error(MQ_ERR_ARG, "%s: plane_out %p overlaps the weights %p / %p", fn, plane_out, w_gate, w_up);
     }
     unsigned int *err = nullptr;
     rc = device_state(&err);
@@ -412,8 +443,10 @@ int mq_device_status(mq_stream_t stream) {
                                   "gemm raw weights", "gemm accumulator", "gemm accumulator release",
                                   "gemm row factors", "gemm row factor release", "gemv drain", "gemm min term",
                                   "gemm activation scales"};
+    static_assert(sizeof names / sizeof names[0] == 12 && (ERR_GEMM_DA >> 11) == 1u,
+                  "one name per device error bit ERR_GEMV_FULL .. ERR_GEMM_DA");
     char buf[400] = "";
-    for (int i = 0; i < 11; ++i)
+    for (int i = 0; i < (int)(sizeof names / sizeof names[0]); ++i)
         if (v & (1u << i)) {
             strncat(buf, " ", sizeof buf - strlen(buf) - 1);
             strncat(buf, names[i], sizeof buf - strlen(buf) - 1);

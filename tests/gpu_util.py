@@ -39,6 +39,27 @@ def assert_plane_equal(got, ref):
     assert np.array_equal(s, sr), "block sums differ"
 
 
+def _tf32_rna(a):
+    """f32 -> the nearest tf32 value (10 explicit mantissa bits), ties away from zero, kept as f32."""
+    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    return ((b + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+def assert_ds_consistent(plane, M, K):
+    """The plane's ds section holds, per block, the tf32 pair of the f32 product d * S (the
+    definition in include/mq.h): hi = tf32(d * S), lo = tf32(d * S - hi), laid out per super-block
+    of a token as hi[8] then lo[8]."""
+    _, _, d, s, ds = B.plane_views(plane, M, K, with_ds=True)
+    d = d.t().contiguous().cpu().numpy()
+    s = s.t().contiguous().cpu().numpy()
+    ds = ds.cpu().numpy().reshape(M, K // 256, 2, 8)
+    p = (d * s.astype(np.float32)).astype(np.float32)
+    hi = _tf32_rna(p)
+    lo = _tf32_rna((p - hi).astype(np.float32))
+    assert np.array_equal(ds[:, :, 0, :].reshape(M, -1).view(np.uint32), hi.view(np.uint32)), "ds hi differs"
+    assert np.array_equal(ds[:, :, 1, :].reshape(M, -1).view(np.uint32), lo.view(np.uint32)), "ds lo differs"
+
+
 def run_matmul(path, fmt, w, plane, M, K, N):
     import torch
     wd = dev(w.reshape(N, -1))

@@ -89,6 +89,8 @@ def test_quantize_argument_errors(L):
     assert q(16, 4, 256, None, 0.0, 128, None) == B.MQ_ERR_ALIGN     # plane not 256-byte aligned
     assert q(16, 4, 256, 32, float("nan"), 256, None) == B.MQ_ERR_ARG
     assert q(16, 4, 256, 32, -1.0, 256, None) == B.MQ_ERR_ARG
+    assert q(1 << 20, 4, 256, None, 0.0, (1 << 20) + 256, None) == B.MQ_ERR_ARG      # plane over x
+    assert q(1 << 20, 4, 256, 1 << 24, 1e-6, (1 << 24) - 256, None) == B.MQ_ERR_ARG  # plane over rms_w
 
 
 def test_swiglu_quantize_argument_errors(L):
@@ -102,6 +104,7 @@ def test_swiglu_quantize_argument_errors(L):
     assert q(20, 32, 4, 256, 256, None) == B.MQ_ERR_ALIGN              # gate not 16-byte aligned
     assert q(16, 36, 4, 256, 256, None) == B.MQ_ERR_ALIGN              # up not 16-byte aligned
     assert q(16, 32, 4, 256, 128, None) == B.MQ_ERR_ALIGN              # plane not 256-byte aligned
+    assert q(1 << 20, 1 << 24, 4, 256, (1 << 24) + 256, None) == B.MQ_ERR_ARG   # plane over up
 
 
 @pytest.mark.parametrize("name", ["mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k",
@@ -123,6 +126,11 @@ def test_matmul_argument_errors(L, name):
     assert f(16, 8, 256, 64, 4, 16, None) == B.MQ_ERR_ALIGN           # plane needs 256 B
     assert f(16, 8, 256, 256, 4, 18, None) == B.MQ_ERR_ALIGN          # y needs 4 B
     assert f(16, 1 << 31, 256, 256, 4, 16, None) == B.MQ_ERR_SHAPE
+    # the output may overlap neither the plane nor the weights
+    assert f(1 << 20, 8, 256, 1 << 24, 4, (1 << 24) + 64, None) == B.MQ_ERR_ARG
+    assert f(1 << 20, 8, 256, 1 << 24, 4, (1 << 20) + 64, None) == B.MQ_ERR_ARG
+    if "gemm" in name:                                                  # token tiles in grid.y
+        assert f(16, 8, 256, 256, 65535 * 128 + 1, 16, None) == B.MQ_ERR_SHAPE
 
 
 def test_debug_window_errors(L):
@@ -139,11 +147,11 @@ def test_valid_call_without_a_device_fails_loudly(L):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a device is present")
-    rc = L.mq_gemm_q4k(16, 8, 256, 256, 4, 16, None)
+    rc = L.mq_gemm_q4k(1 << 20, 8, 256, 1 << 24, 4, 1 << 28, None)
     assert rc in (B.MQ_ERR_CUDA, B.MQ_ERR_DEVICE)
     assert B.last_error()
     with pytest.raises(B.MQError):
-        B.mq_gemm_q4k(16, 8, 256, 256, 4, 16, stream=0)
+        B.mq_gemm_q4k(1 << 20, 8, 256, 1 << 24, 4, 1 << 28, stream=0)
 
 
 def test_product_package_does_not_import_the_oracle():
@@ -163,7 +171,8 @@ def test_missing_library_raises(monkeypatch, tmp_path):
 def test_gate_up_swiglu_argument_errors(L):
     f = L.mq_gemm_q4k_swiglu          # (w_gate, w_up, F, K, plane_in, M, plane_out, stream)
     assert f(16, 16, 300, 256, 256, 4, 256, None) == B.MQ_ERR_SHAPE      # F % 256
-    assert f(16, 16, 0, 256, 256, 4, 256, None) == B.MQ_ERR_SHAPE
+    assert f(16, 16, 0, 256, 256, 4, 256, None) == B.MQ_OK            # F == 0: nothing to do
+    assert f(16, 16, 65535 * 64 + 256, 256, 256, 4, 256, None) == B.MQ_ERR_SHAPE   # F past the grid limit
     assert f(16, 16, 256, 100, 256, 4, 256, None) == B.MQ_ERR_SHAPE      # K % 256
     assert f(16, 16, -256, 256, 256, 4, 256, None) == B.MQ_ERR_ARG
     assert f(16, 16, 256, 256, 256, -1, 256, None) == B.MQ_ERR_ARG
@@ -178,3 +187,5 @@ def test_gate_up_swiglu_argument_errors(L):
     assert f(16, 16, 256, 256, 1 << 20, 4, 1 << 20, None) == B.MQ_ERR_ARG           # the same plane
     assert f(16, 16, 256, 256, 1 << 20, 4, (1 << 20) + 256, None) == B.MQ_ERR_ARG   # overlapping
     assert n_in > 256
+    # plane_out over the weights
+    assert f(1 << 20, 1 << 24, 256, 256, 1 << 28, 4, (1 << 20) + 256, None) == B.MQ_ERR_ARG

@@ -12,8 +12,9 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("M,K", [(1, 256), (3, 512), (8, 512), (1, 18944), (37, 768), (130, 3584)])
 def test_plain_quantize_bit_exact(M, K):
     x = inputs.activations(np.random.default_rng(M * 1000 + K), M, K)
-    _, got = G.gpu_plane(x)
+    plane, got = G.gpu_plane(x)
     G.assert_plane_equal(got, G.oracle_plane(x))
+    G.assert_ds_consistent(plane, M, K)
 
 
 def test_tiny_and_qproj_planes():
@@ -41,16 +42,20 @@ def test_rms_quantize_bit_exact_small():
     for M, K in ((1, 3584), (5, 256), (64, 3584), (3, 18944)):
         x = inputs.activations(r, M, K)
         w = inputs.rms_weight(r, K)
-        _, got = G.gpu_plane(x, w, 1e-6)
+        plane, got = G.gpu_plane(x, w, 1e-6)
         G.assert_plane_equal(got, G.oracle_plane(x, w, 1e-6))
+        G.assert_ds_consistent(plane, M, K)
 
 
 def test_ffn_prefill_full_size_planes():
     cfg = inputs.ffn_prefill()
-    _, got = G.gpu_plane(cfg["x_hidden"], cfg["rms_w"], float(cfg["eps"]))
+    M = cfg["x_hidden"].shape[0]
+    plane, got = G.gpu_plane(cfg["x_hidden"], cfg["rms_w"], float(cfg["eps"]))
     G.assert_plane_equal(got, G.oracle_plane(cfg["x_hidden"], cfg["rms_w"], float(cfg["eps"])))
-    _, got = G.gpu_plane(cfg["x_ffn"])
+    G.assert_ds_consistent(plane, M, inputs.HIDDEN)
+    plane, got = G.gpu_plane(cfg["x_ffn"])
     G.assert_plane_equal(got, G.oracle_plane(cfg["x_ffn"]))
+    G.assert_ds_consistent(plane, M, inputs.FFN)
 
 
 def test_quantize_is_deterministic_and_reuses_plane():

@@ -18,6 +18,7 @@ def _gpu_swiglu_plane(g, u):
     B.mq_quantize_swiglu_q8(G.dev(g), G.dev(u), M, K, plane)
     torch.cuda.synchronize()
     B.mq_device_status()
+    G.assert_ds_consistent(plane, M, K)
     q16, q8, d, s = B.plane_views(plane, M, K)
     return (q16.float().cpu().numpy(), q8.cpu().numpy(), d.t().contiguous().cpu().numpy(),
             s.t().contiguous().cpu().numpy())
@@ -51,9 +52,11 @@ def test_swiglu_full_ffn_size():
 # ---- the fused gate|up GEMM with the SwiGLU epilogue (mq_gemm_q4k_swiglu)
 
 def _plane_np(plane, M, K):
-    q16, q8, d, s = B.plane_views(plane, M, K)
+    """(q16, q8, d, S) in token-major form, then the raw ds section (tf32 pairs of d * S), which the
+    fused kernel writes itself and a Q4_K / Q5_K down projection would read."""
+    q16, q8, d, s, ds = B.plane_views(plane, M, K, with_ds=True)
     return (q16.float().cpu().numpy(), q8.cpu().numpy(), d.t().contiguous().cpu().numpy(),
-            s.t().contiguous().cpu().numpy())
+            s.t().contiguous().cpu().numpy(), ds.cpu().numpy().view(np.uint32))
 
 
 def _fused(wgd, wud, plane, M, K, F):
@@ -91,7 +94,7 @@ def _assert_near_oracle(got, wg, wu, ref_plane, ms):
     ~1e-3 of the L2 norm at F = 1024) --, every scale within 1e-3 of the row's largest scale,
     codes within 1 of the oracle's (at most 0.1% of them off), and S and the f16 codes consistent
     with the int8 codes."""
-    q16, q8, d, s = (a[ms] for a in got)
+    q16, q8, d, s = (a[ms] for a in got[:4])
     qr, dr, sr = oracle.gate_up_swiglu_q8(wg, wu, "q4k", ref_plane, ms, threads=16)
     assert np.all(np.abs(d.astype(np.float64) - dr) <= 1e-3 * dr.max(axis=1, keepdims=True))
     dq = np.abs(q8.astype(np.int32) - qr.astype(np.int32))
@@ -118,11 +121,13 @@ def test_gate_up_swiglu_shapes(M, K, F):
     plane, _ = G.gpu_plane(x)
     ref_plane = G.oracle_plane(x)
     wgd, wud = G.dev(wg.reshape(F, -1)), G.dev(wu.reshape(F, -1))
-    got = _plane_np(_fused(wgd, wud, plane, M, K, F), M, F)
-    # the same arithmetic as the unfused GPU chain, bit for bit
+    fused = _fused(wgd, wud, plane, M, K, F)
+    got = _plane_np(fused, M, F)
+    # the same arithmetic as the unfused GPU chain, bit for bit (the ds section included)
     unf = _plane_np(_unfused(wgd, wud, plane, M, K, F), M, F)
     for a, b in zip(got, unf):
         assert np.array_equal(a, b)
+    G.assert_ds_consistent(fused, M, F)
     _assert_near_oracle(got, wg, wu, ref_plane, np.arange(M))
 
 
@@ -133,10 +138,12 @@ def test_gate_up_swiglu_ffn_size():
     plane, _ = G.gpu_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
     ref_plane = G.oracle_plane(c["x_hidden"], c["rms_w"], float(c["eps"]))
     wgd, wud = G.dev(c["w_gate"].reshape(F, -1)), G.dev(c["w_up"].reshape(F, -1))
-    got = _plane_np(_fused(wgd, wud, plane, M, K, F), M, F)
+    fused = _fused(wgd, wud, plane, M, K, F)
+    got = _plane_np(fused, M, F)
     unf = _plane_np(_unfused(wgd, wud, plane, M, K, F), M, F)
     for a, b in zip(got, unf):
         assert np.array_equal(a, b)
+    G.assert_ds_consistent(fused, M, F)
     ms = np.array(sorted({0, 1, 127, 128, 1000, 2047, 2048, M - 2, M - 1} |
                          set(np.random.default_rng(5).choice(M, 15, replace=False).tolist())))
     _assert_near_oracle(got, c["w_gate"], c["w_up"], ref_plane, ms)
