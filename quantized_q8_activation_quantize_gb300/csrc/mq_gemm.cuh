@@ -72,7 +72,10 @@ struct GmCfg {
     static constexpr int TMW_ELEM = B32 ? 2 : 1;                  // bytes per tensor-map element (box <= 256)
     static constexpr int STAGES = TMW ? 4 : 3;
     static constexpr int RAW_STAGES = FMT == FMT_Q4K ? 3 : 2;
-    static constexpr int RAW_ROW = TMW ? BB : 224;                // 16-B aligned superset of one block
+    // TMA-fed formats: the block itself; Q6_K: the 16-B aligned superset of one block (224 B at most)
+    // at a 240-byte row stride, so that the 16-byte loads of eight consecutive rows hit eight
+    // distinct bank groups
+    static constexpr int RAW_ROW = TMW ? BB : 240;
     static constexpr bool CORR = FMT == FMT_Q6K;                  // Q6_K odd |sc| > 64 correction tile
     // the min / offset term on the tensor pipe: Q4_K / Q5_K -dmin m_j, Q4_1 / Q5_1 the block offset m
     static constexpr bool MIN = KQ || b32_has_m(FMT);
@@ -125,17 +128,31 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
-// NW consecutive 32-bit words starting at a 2-byte aligned shared address
+// NW consecutive 32-bit words starting r bytes (r even, < 16) past the 16-byte aligned shared address
+// base: 16-byte loads of the aligned chunks, then the word offset r / 4 selected by two levels of
+// selects and the half-word offset by a funnel shift (no per-lane indexing into a register array)
 template <int NW>
-__device__ __forceinline__ void lds_words_a2(uint32_t addr, uint32_t (&out)[NW]) {
-    const uint32_t b = addr & ~3u, sh = (addr & 3u) * 8u;
-    uint32_t prev = lds32(b);
+__device__ __forceinline__ void lds_words_r(uint32_t base, uint32_t r, uint32_t (&out)[NW]) {
+    constexpr int NC = (NW + 4 + 3) / 4;             // chunks: words 0 .. NW + 3
+    uint32_t w[4 * NC];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
-        const uint32_t next = lds32(b + 4 * (i + 1));
-        out[i] = __funnelshift_r(prev, next, sh);
-        prev = next;
+    for (int c = 0; c < NC; ++c) {
+        const uint4 t = lds128(base + 16u * c);
+        w[4 * c] = t.x;
+        w[4 * c + 1] = t.y;
+        w[4 * c + 2] = t.z;
+        w[4 * c + 3] = t.w;
     }
+    const bool s1 = (r & 4u) != 0, s2 = (r & 8u) != 0;
+    const uint32_t sh = (r & 2u) * 8u;
+    uint32_t x[NW + 3];
+#pragma unroll
+    for (int i = 0; i < NW + 3; ++i) x[i] = s1 ? w[i + 1] : w[i];
+    uint32_t v[NW + 1];
+#pragma unroll
+    for (int i = 0; i < NW + 1; ++i) v[i] = s2 ? x[i + 2] : x[i];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
 }
 
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -463,8 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // waits are warp-uniform (all lanes leave together): the warp-level arrivals below need it
             if (!__all_sync(kFull, mbar_wait(&bars.raw_full[slot], (sb / R) & 1, err, ERR_GEMM_RAW_FULL, abort_flag)))
                 break;
-            const uint32_t blk = smem_u32(raw_row0 + slot * BN * C::RAW_ROW) +
-                                 (valid ? (uint32_t)(reinterpret_cast<uintptr_t>(wrow + (int64_t)sb * C::BB) & 15) : 0u);
+            // Q6_K: the block starts blk_r bytes into its row's 16-byte aligned copy at blk_a
+            const uint32_t blk_a = smem_u32(raw_row0 + slot * BN * C::RAW_ROW);
+            const uint32_t blk_r = valid ? (uint32_t)(reinterpret_cast<uintptr_t>(wrow + (int64_t)sb * C::BB) & 15) : 0u;
+            const uint32_t blk = blk_a + blk_r;
             // ---- super-block header
             float d = 0.0f, dmin = 0.0f;
             int sc[16];
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 uint32_t tail[5];                 // bytes 192..211: scales[16], d
                 if (valid) {
-                    lds_words_a2<5>(blk + 192, tail);
+                    lds_words_r<5>(blk_a + 192, blk_r, tail);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 5; ++i) tail[i] = 0;
@@ -653,8 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int h = q >> 1, g0 = 2 * (q & 1);
                     if ((q & 1) == 0) {
                         if (valid) {
-                            lds_words_a2<16>(blk + 64 * h, ql);
-                            lds_words_a2<8>(blk + 128 + 32 * h, qh);
+                            lds_words_r<16>(blk_a + 64 * h, blk_r, ql);
+                            lds_words_r<8>(blk_a + 128 + 32 * h, blk_r, qh);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) ql[i] = 0;
