@@ -155,7 +155,7 @@ def run_case(args):
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
     if name.startswith("quantize"):
-        fn = lambda: B.mq_quantize_q8(xd, M, K, rd, 1e-6, plane)
+        fn = lambda: B.mq_quantize_q8_ex(xd, M, K, rd, 1e-6, B.PLANE_FOR_GEMM, plane)
     elif name == "gemm_swiglu_ffn":
         w2d, po = dev(w2.reshape(N, -1)), B.alloc_plane(M, N)
         fn = lambda: B.mq_gemm_q4k_swiglu(wd, w2d, N, K, plane, M, po)
@@ -295,13 +295,13 @@ class Prefill:
         B, M, H, F = self.B, self.M, self.H, self.F
         rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
         rec(0)
-        B.mq_quantize_q8(self.x_h, M, H, self.rms_w, self.eps, self.p_h)
+        B.mq_quantize_q8_ex(self.x_h, M, H, self.rms_w, self.eps, B.PLANE_FOR_GEMM, self.p_h)
         rec(1)
         B.mq_gemm_q4k(self.w_gate, F, H, self.p_h, M, self.y_gate)
         rec(2)
         B.mq_gemm_q4k(self.w_up, F, H, self.p_h, M, self.y_up)
         rec(3)
-        B.mq_quantize_q8(self.x_f, M, F, None, 0.0, self.p_f)
+        B.mq_quantize_q8_ex(self.x_f, M, F, None, 0.0, B.PLANE_FOR_GEMM, self.p_f)
         rec(4)
         B.mq_gemm_q6k(self.w_down, H, F, self.p_f, M, self.y_down)
         rec(5)
@@ -327,13 +327,13 @@ class Prefill:
             self.x_f.copy_(self.host_x_f, non_blocking=True)
             e_xf = ev(self.s_in)
         cs.wait_event(e_xh)
-        B.mq_quantize_q8(self.x_h, M, H, self.rms_w, self.eps, self.p_h)
+        B.mq_quantize_q8_ex(self.x_h, M, H, self.rms_w, self.eps, B.PLANE_FOR_GEMM, self.p_h)
         B.mq_gemm_q4k(self.w_gate, F, H, self.p_h, M, self.y_gate)
         e_g = ev(cs)
         B.mq_gemm_q4k(self.w_up, F, H, self.p_h, M, self.y_up)
         e_u = ev(cs)
         cs.wait_event(e_xf)
-        B.mq_quantize_q8(self.x_f, M, F, None, 0.0, self.p_f)
+        B.mq_quantize_q8_ex(self.x_f, M, F, None, 0.0, B.PLANE_FOR_GEMM, self.p_f)
         B.mq_gemm_q6k(self.w_down, H, F, self.p_f, M, self.y_down)
         e_d = ev(cs)
         with t.cuda.stream(self.s_out):
@@ -367,7 +367,7 @@ class DecodeSweep:
     def _one(self, item, quantize):
         fmt, w, x, plane, y, n, k = item
         if quantize:
-            self.B.mq_quantize_q8(x, 1, k, None, 0.0, plane)
+            self.B.mq_quantize_q8_ex(x, 1, k, None, 0.0, self.B.PLANE_FOR_GEMV, plane)
         self.B.GEMV[fmt](w, n, k, plane, 1, y)
 
     def run(self, quantize=True, branches=False):
@@ -533,26 +533,28 @@ def main():
     gemm_q4k_ms = (k_ms[1] + k_ms[2]) / 2
     q4k_tflops = pf.gemm_q4k_ops / (gemm_q4k_ms * 1e-3) / 1e12
     q6k_tflops = pf.gemm_q6k_ops / (k_ms[4] * 1e-3) / 1e12
-    qrms_gbs = (pf.M * pf.H * 4 + pf.H * 4 + B.mq_q8_plane_bytes(pf.M, pf.H)) / (k_ms[0] * 1e-3) / 1e9
-    q_gbs = (pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (k_ms[3] * 1e-3) / 1e9
+    # algorithmic bytes of a quantizer: 4 B in and 1.25 B out per value (+ the RMSNorm weight)
+    qrms_gbs = (pf.M * pf.H * 5.25 + pf.H * 4) / (k_ms[0] * 1e-3) / 1e9
+    q_gbs = pf.M * pf.F * 5.25 / (k_ms[3] * 1e-3) / 1e9
     # the SwiGLU producer (NEXT row, not part of the FFN prefill step): the down projection's plane
     # from this step's gate / up outputs
-    swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f), K, W)
-    swiglu_gbs = (2 * pf.M * pf.F * 4 + B.mq_q8_plane_bytes(pf.M, pf.F)) / (swiglu_ms * 1e-3) / 1e9
+    swiglu_ms = time_events(torch, lambda: B.mq_quantize_swiglu_q8_ex(pf.y_gate, pf.y_up, pf.M, pf.F, B.PLANE_FOR_GEMM,
+                                                                      pf.p_f), K, W)
+    swiglu_gbs = pf.M * pf.F * 9.25 / (swiglu_ms * 1e-3) / 1e9
     # the fused gate|up GEMM (NEXT row): gate and up in one kernel whose epilogue writes the down
     # projection's plane, against the unfused chain (two GEMMs, then the SwiGLU producer), and the
     # whole SwiGLU FFN both ways (RMSNorm-Q8 -> gate|up -> down)
     def unfused_gu():
         B.mq_gemm_q4k(pf.w_gate, pf.F, pf.H, pf.p_h, pf.M, pf.y_gate)
         B.mq_gemm_q4k(pf.w_up, pf.F, pf.H, pf.p_h, pf.M, pf.y_up)
-        B.mq_quantize_swiglu_q8(pf.y_gate, pf.y_up, pf.M, pf.F, pf.p_f)
+        B.mq_quantize_swiglu_q8_ex(pf.y_gate, pf.y_up, pf.M, pf.F, B.PLANE_FOR_GEMM, pf.p_f)
 
     def fused_gu():
         B.mq_gemm_q4k_swiglu(pf.w_gate, pf.w_up, pf.F, pf.H, pf.p_h, pf.M, pf.p_f)
 
     def ffn(gu):
         def run():
-            B.mq_quantize_q8(pf.x_h, pf.M, pf.H, pf.rms_w, pf.eps, pf.p_h)
+            B.mq_quantize_q8_ex(pf.x_h, pf.M, pf.H, pf.rms_w, pf.eps, B.PLANE_FOR_GEMM, pf.p_h)
             gu()
             B.mq_gemm_q6k(pf.w_down, pf.H, pf.F, pf.p_f, pf.M, pf.y_down)
         return run

@@ -117,6 +117,34 @@ MQ_API int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms
                    void *plane, mq_stream_t stream);
 
 /*
+ * Plane sections.  d and S are always written; the other three sections are written on request,
+ * so a producer writes only what its consumers read:
+ *   mq_gemm_*            read q16, d and (Q4_K, Q5_K, Q4_1, Q5_1) ds      -> MQ_PLANE_FOR_GEMM
+ *   mq_gemv_*            read q8, d and S                                  -> MQ_PLANE_FOR_GEMV
+ *   mq_gemm_q4k_swiglu   reads q16, d and ds of its input plane            -> MQ_PLANE_FOR_GEMM
+ * A section that was not written keeps whatever the buffer held before; a consumer that reads it
+ * then computes from those bytes (no error is raised: the plane carries no record of its sections).
+ */
+enum {
+    MQ_PLANE_Q16 = 1u,                    /* f16 codes (tensor-core operand) */
+    MQ_PLANE_Q8 = 2u,                     /* int8 codes (dp4a operand) */
+    MQ_PLANE_DS = 4u,                     /* tf32 pairs of d*S (tensor-core min term) */
+    MQ_PLANE_ALL = 7u,
+    MQ_PLANE_FOR_GEMM = 5u,               /* MQ_PLANE_Q16 | MQ_PLANE_DS */
+    MQ_PLANE_FOR_GEMV = 2u                /* MQ_PLANE_Q8 */
+};
+
+/*
+ * mq_quantize_q8_ex -- mq_quantize_q8 writing only the requested sections (a non-empty
+ * MQ_PLANE_* mask; MQ_ERR_ARG otherwise) besides d and S.  Every section it writes holds exactly
+ * what mq_quantize_q8 writes there; mq_quantize_q8 is this call with MQ_PLANE_ALL.  Per value,
+ * MQ_PLANE_ALL writes 3.5 bytes, MQ_PLANE_FOR_GEMM 2.5 and MQ_PLANE_FOR_GEMV 1.25 (the int8 code
+ * plus 8 bytes of d and S per 32 values).
+ */
+MQ_API int mq_quantize_q8_ex(const float *x, int64_t M, int64_t K, const float *rms_w, float eps,
+                             unsigned sections, void *plane, mq_stream_t stream);
+
+/*
  * mq_quantize_swiglu_q8 -- the SwiGLU producer of the down projection: writes the Q8 plane
  * of y = silu(gate) * up, silu(g) = g / (1 + exp(-g)), with no f32 intermediate in memory.
  * "Features > GPU -- CUDA": the swiglu producer emits the q8 plane directly; "Compute Graph
@@ -132,6 +160,10 @@ MQ_API int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms
  */
 MQ_API int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t K, void *plane,
                                  mq_stream_t stream);
+
+/* mq_quantize_swiglu_q8_ex -- the same, writing only the requested MQ_PLANE_* sections besides d and S. */
+MQ_API int mq_quantize_swiglu_q8_ex(const float *gate, const float *up, int64_t M, int64_t K, unsigned sections,
+                                    void *plane, mq_stream_t stream);
 
 /*
  * mq_gemm_q4k / mq_gemm_q6k -- prefill GEMM (MMQ) on the tensor cores.

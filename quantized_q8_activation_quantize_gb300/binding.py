@@ -19,6 +19,8 @@ MQ_OK, MQ_ERR_ARG, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_DEVICE, MQ_ERR_CUDA, MQ_ER
 STATUS_NAMES = {0: "MQ_OK", -1: "MQ_ERR_ARG", -2: "MQ_ERR_SHAPE", -3: "MQ_ERR_ALIGN", -4: "MQ_ERR_DEVICE",
                 -5: "MQ_ERR_CUDA", -6: "MQ_ERR_DEVICE_TIMEOUT"}
 OP_GEMM_Q4K, OP_GEMM_Q6K, OP_GEMV_Q4K, OP_GEMV_Q6K = 0, 1, 2, 3
+# plane sections (include/mq.h MQ_PLANE_*)
+PLANE_Q16, PLANE_Q8, PLANE_DS, PLANE_ALL, PLANE_FOR_GEMM, PLANE_FOR_GEMV = 1, 2, 4, 7, 5, 2
 
 
 class MQError(RuntimeError):
@@ -57,6 +59,8 @@ def lib():
         L.mq_q8_plane_layout.argtypes = [I64, I64, ctypes.POINTER(PlaneLayout)]
         L.mq_quantize_q8.argtypes = [P, I64, I64, P, ctypes.c_float, P, P]
         L.mq_quantize_swiglu_q8.argtypes = [P, P, I64, I64, P, P]
+        L.mq_quantize_q8_ex.argtypes = [P, I64, I64, P, ctypes.c_float, ctypes.c_uint, P, P]
+        L.mq_quantize_swiglu_q8_ex.argtypes = [P, P, I64, I64, ctypes.c_uint, P, P]
         for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k",
                      "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
                      "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"):
@@ -142,6 +146,15 @@ def mq_quantize_q8(x, M: int, K: int, rms_w, eps: float, plane, stream=None):
 
 def mq_quantize_swiglu_q8(gate, up, M: int, K: int, plane, stream=None):
     return _check(lib().mq_quantize_swiglu_q8(_ptr(gate), _ptr(up), M, K, _ptr(plane), _stream(stream)))
+
+
+def mq_quantize_q8_ex(x, M: int, K: int, rms_w, eps: float, sections: int, plane, stream=None):
+    return _check(lib().mq_quantize_q8_ex(_ptr(x), M, K, _ptr(rms_w), float(eps), sections, _ptr(plane),
+                                          _stream(stream)))
+
+
+def mq_quantize_swiglu_q8_ex(gate, up, M: int, K: int, sections: int, plane, stream=None):
+    return _check(lib().mq_quantize_swiglu_q8_ex(_ptr(gate), _ptr(up), M, K, sections, _ptr(plane), _stream(stream)))
 
 
 def _matmul(name, w, N, K, plane, M, y, stream):

@@ -272,6 +272,13 @@ size_t mq_q8_plane_bytes(int64_t M, int64_t K) {
 
 int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, void *plane,
                    mq_stream_t stream) {
+    return mq_quantize_q8_ex(x, M, K, rms_w, eps, MQ_PLANE_ALL, plane, stream);
+}
+
+int mq_quantize_q8_ex(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, unsigned sections,
+                      void *plane, mq_stream_t stream) {
+    if (sections == 0 || sections > MQ_PLANE_ALL)
+        return set_error(MQ_ERR_ARG, "mq_quantize_q8: sections=0x%x not a non-empty MQ_PLANE_* mask", sections);
     if (M < 0) return set_error(MQ_ERR_ARG, "mq_quantize_q8: negative M=%lld", (long long)M);
     int rc = check_k(K);
     if (rc != MQ_OK) return rc;
@@ -293,10 +300,17 @@ int mq_quantize_q8(const float *x, int64_t M, int64_t K, const float *rms_w, flo
     if (rc != MQ_OK) return rc;
     Plane p;
     plane_from(plane, M, K, &p);
-    return launch_quantize(x, M, K, rms_w, eps, p, err, reinterpret_cast<cudaStream_t>(stream));
+    return launch_quantize(x, M, K, rms_w, eps, sections, p, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t K, void *plane, mq_stream_t stream) {
+    return mq_quantize_swiglu_q8_ex(gate, up, M, K, MQ_PLANE_ALL, plane, stream);
+}
+
+int mq_quantize_swiglu_q8_ex(const float *gate, const float *up, int64_t M, int64_t K, unsigned sections, void *plane,
+                             mq_stream_t stream) {
+    if (sections == 0 || sections > MQ_PLANE_ALL)
+        return set_error(MQ_ERR_ARG, "mq_quantize_swiglu_q8: sections=0x%x not a non-empty MQ_PLANE_* mask", sections);
     if (M < 0) return set_error(MQ_ERR_ARG, "mq_quantize_swiglu_q8: negative M=%lld", (long long)M);
     int rc = check_k(K);
     if (rc != MQ_OK) return rc;
@@ -321,7 +335,7 @@ int mq_quantize_swiglu_q8(const float *gate, const float *up, int64_t M, int64_t
     if (rc != MQ_OK) return rc;
     Plane p;
     plane_from(plane, M, K, &p);
-    return launch_swiglu_quantize(gate, up, M, K, p, reinterpret_cast<cudaStream_t>(stream));
+    return launch_swiglu_quantize(gate, up, M, K, sections, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mq_gemm_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {

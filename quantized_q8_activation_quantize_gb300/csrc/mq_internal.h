@@ -75,9 +75,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // launchers (arguments already validated); return MQ_OK or MQ_ERR_CUDA
-int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,
-                    unsigned int *err, cudaStream_t stream);
-int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, const Plane &p, cudaStream_t stream);
+// sections: the MQ_PLANE_* mask of the plane sections written besides d and S (1 .. 7)
+int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, unsigned sections,
+                    const Plane &p, unsigned int *err, cudaStream_t stream);
+int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, unsigned sections, const Plane &p,
+                           cudaStream_t stream);
 int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
 int launch_gemv_b32(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,

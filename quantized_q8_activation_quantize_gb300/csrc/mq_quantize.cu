@@ -20,6 +20,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// SECT: the plane sections written besides d and S (MQ_PLANE_Q16 | MQ_PLANE_Q8 | MQ_PLANE_DS)
+template <unsigned SECT>
 __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const Plane &p, int64_t M, int64_t K,
                                           int64_t m, int64_t k0) {
     float amax = 0.0f;
@@ -29,47 +31,56 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const P
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     const float d = __fdiv_rn(amax, 127.0f);
     const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-    int q[8];
-    int s = 0;
+    // the codes as floats holding integers in [-127, 127]; their sum is exact in f32 (|S| <= 4064)
+    float r[8];
+    float fs = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        float r = roundf(__fmul_rn(v[i], id));            // half away from zero
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
-        q[i] = __float2int_rz(r);
-        s += q[i];
+        // half away from zero, clamped; + 0 turns a -0 code into +0 (the f16 code of 0 is 0x0000)
+        r[i] = __fadd_rn(fminf(fmaxf(roundf(__fmul_rn(v[i], id)), -127.0f), 127.0f), 0.0f);
+        fs = __fadd_rn(fs, r[i]);
     }
-    s += __shfl_xor_sync(kFull, s, 1);
-    s += __shfl_xor_sync(kFull, s, 2);
-
+    fs = __fadd_rn(fs, __shfl_xor_sync(kFull, fs, 1));
+    fs = __fadd_rn(fs, __shfl_xor_sync(kFull, fs, 2));
+    const int s = __float2int_rn(fs);
+    // int8 bytes without conversion instructions: r + 1.5 * 2^23 holds r in the low mantissa bits,
+    // so its low byte is r in two's complement
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__fadd_rn(r[i], 12582912.0f));
     uint2 b8;
-    b8.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
-           ((uint32_t)(q[3] & 0xff) << 24);
-    b8.y = (uint32_t)(q[4] & 0xff) | ((uint32_t)(q[5] & 0xff) << 8) | ((uint32_t)(q[6] & 0xff) << 16) |
-           ((uint32_t)(q[7] & 0xff) << 24);
+    b8.x = __byte_perm(__byte_perm(w[0], w[1], 0x0040), __byte_perm(w[2], w[3], 0x0040), 0x5410);
+    b8.y = __byte_perm(__byte_perm(w[4], w[5], 0x0040), __byte_perm(w[6], w[7], 0x0040), 0x5410);
+    // f16 codes: each integer is exact in f16, so the packed conversion is exact
     uint4 h;
     __half2 t;
-    t = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1])); h.x = *reinterpret_cast<uint32_t *>(&t);
-    t = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3])); h.y = *reinterpret_cast<uint32_t *>(&t);
-    t = __halves2half2(__int2half_rn(q[4]), __int2half_rn(q[5])); h.z = *reinterpret_cast<uint32_t *>(&t);
-    t = __halves2half2(__int2half_rn(q[6]), __int2half_rn(q[7])); h.w = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2half2_rn(r[0], r[1]); h.x = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2half2_rn(r[2], r[3]); h.y = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2half2_rn(r[4], r[5]); h.z = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2half2_rn(r[6], r[7]); h.w = *reinterpret_cast<uint32_t *>(&t);
 
     const int64_t off = m * K + k0;
-    *reinterpret_cast<uint2 *>(p.q8 + off) = b8;
-    *reinterpret_cast<uint4 *>(p.q16 + off) = h;
+    if constexpr ((SECT & MQ_PLANE_Q8) != 0) *reinterpret_cast<uint2 *>(p.q8 + off) = b8;
+    if constexpr ((SECT & MQ_PLANE_Q16) != 0) *reinterpret_cast<uint4 *>(p.q16 + off) = h;
     if ((lane & 3) == 0) {
         const int64_t b = k0 / kQ8;
         p.d[b * M + m] = d;
         p.s[b * M + m] = s;
-        // d*S as a tf32 (hi, lo) pair: operand of the tensor-core Q4_K min term
-        const float ds = __fmul_rn(d, (float)s);
-        const float hi = tf32_rn(ds);
-        const float lo = tf32_rn(__fsub_rn(ds, hi));
-        float *row = p.ds + m * (2 * (K / kQ8)) + (b >> 3) * 16 + (b & 7);
-        row[0] = hi;
-        row[8] = lo;
+        if constexpr ((SECT & MQ_PLANE_DS) != 0) {
+            // d*S as a tf32 (hi, lo) pair: operand of the tensor-core Q4_K min term
+            const float ds = __fmul_rn(d, (float)s);
+            const float hi = tf32_rn(ds);
+            const float lo = tf32_rn(__fsub_rn(ds, hi));
+            float *row = p.ds + m * (2 * (K / kQ8)) + (b >> 3) * 16 + (b & 7);
+            row[0] = hi;
+            row[8] = lo;
+        }
     }
 }
 
+// Two (token, 256-value chunk) items per warp and iteration, both items' loads issued before either
+// is quantized (twice the bytes in flight per warp).
+template <unsigned SECT>
 __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int64_t M, int64_t K, Plane p) {
     grid_dep_launch();
     grid_dep_wait();
@@ -77,18 +88,33 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     const uint32_t nch = (uint32_t)(K / 256);
     const int64_t items = M * (int64_t)nch;
     const int64_t stride = (int64_t)gridDim.x * 8;
-    for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += stride) {
-        // items < 2^31 * 2^23: the quotient fits 32 bits; divide in 64 bits only when it must
-        const int64_t m = (it < 0xffffffffll) ? (int64_t)((uint32_t)it / nch) : it / (int64_t)nch;
+    // items < 2^31 * 2^23: the quotient fits 32 bits; divide in 64 bits only when it must
+    auto token = [&](int64_t it) { return (it < 0xffffffffll) ? (int64_t)((uint32_t)it / nch) : it / (int64_t)nch; };
+    for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += 2 * stride) {
+        const int64_t it2 = it + stride;
+        const bool two = it2 < items;
+        const int64_t m = token(it), m2 = two ? token(it2) : m;
         const int64_t k0 = (it - m * (int64_t)nch) * 256 + lane * 8;
+        const int64_t k02 = two ? (it2 - m2 * (int64_t)nch) * 256 + lane * 8 : k0;
         const float4 *src = reinterpret_cast<const float4 *>(x + m * K + k0);
+        const float4 *src2 = reinterpret_cast<const float4 *>(x + m2 * K + k02);
         const float4 a = __ldg(src), b = __ldg(src + 1);
+        float4 a2 = make_float4(0.f, 0.f, 0.f, 0.f), b2 = a2;
+        if (two) {
+            a2 = __ldg(src2);
+            b2 = __ldg(src2 + 1);
+        }
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        quantize8(v, lane, p, M, K, m, k0);
+        quantize8<SECT>(v, lane, p, M, K, m, k0);
+        if (two) {
+            const float v2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
+            quantize8<SECT>(v2, lane, p, M, K, m2, k02);
+        }
     }
 }
 
 // SwiGLU producer: y = swiglu1(g, u) (mq_device.cuh), then the Q8 quantization of y.
+template <unsigned SECT>
 __global__ void __launch_bounds__(256) swiglu_quantize_kernel(const float *__restrict__ g, const float *__restrict__ up,
                                                               int64_t M, int64_t K, Plane p) {
     grid_dep_launch();
@@ -105,46 +131,67 @@ __global__ void __launch_bounds__(256) swiglu_quantize_kernel(const float *__res
         const float4 ga = __ldg(gs), gb = __ldg(gs + 1), ua = __ldg(us), ub = __ldg(us + 1);
         const float v[8] = {swiglu1(ga.x, ua.x), swiglu1(ga.y, ua.y), swiglu1(ga.z, ua.z), swiglu1(ga.w, ua.w),
                             swiglu1(gb.x, ub.x), swiglu1(gb.y, ub.y), swiglu1(gb.z, ub.z), swiglu1(gb.w, ub.w)};
-        quantize8(v, lane, p, M, K, m, k0);
+        quantize8<SECT>(v, lane, p, M, K, m, k0);
     }
 }
 
-// RMSNorm producer: one CTA per token.  Pass 1 sums x^2 in f64 (each square is exact
-// in f64); r = (float)(1 / sqrt(sum/K + eps)) is rounded once; pass 2 re-reads the row
-// (L2-resident) and quantizes y = fl(fl(x * r) * w).
+// Error-free product and sum in f32 (Dekker / Knuth): x * x = p + e exactly (e from one fused
+// multiply-add), and the running pair (hi, lo) takes p with Knuth's branch-free two-sum, whose
+// rounding error goes to lo.  Every step is an explicitly rounded intrinsic, so the compiler can
+// neither contract nor reassociate it.
+__device__ __forceinline__ void add_square(float v, float &hi, float &lo) {
+    const float p = __fmul_rn(v, v);
+    const float e = __fmaf_rn(v, v, -p);
+    const float s = __fadd_rn(hi, p);
+    const float bv = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(p, bv));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+}
+
+// RMSNorm producer: one warp per token.  Pass 1 sums x^2 per lane as an f32 pair (hi, lo)
+// carrying about 48 significant bits (every square and every addition's rounding error kept),
+// then combines the lanes in f64 in a fixed order; r = (float)(1 / sqrt(sum/K + eps)) is rounded
+// once (f64 sums of the same squares in another order give the same f32 r but with probability
+// ~1e-7 per token).  The f64 pipe of this GPU issues ~1.7 ops per clock per SM, so only the 32
+// lane sums per token and one lane's square root and divide go through it.  Pass 2 re-reads the
+// row (cache-resident) and quantizes y = fl(fl(x * r) * w) with the layout of quantize_kernel
+// (lane l holds values 8l .. 8l + 7 of each 256-value chunk).
+template <unsigned SECT>
 __global__ void __launch_bounds__(256) rms_quantize_kernel(const float *__restrict__ x, int64_t M, int64_t K,
                                                            const float *__restrict__ w, float eps, Plane p) {
-    __shared__ double red[8];
-    __shared__ float r_sh;
     grid_dep_launch();
     grid_dep_wait();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
     const int64_t nch = K / 256;
-    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
-        const float *xr = x + m * K;
-        double ss = 0.0;
-        for (int64_t k = (int64_t)tid * 4; k < K; k += 1024) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(xr + k));
-            ss = fma((double)v.x, (double)v.x, ss);
-            ss = fma((double)v.y, (double)v.y, ss);
-            ss = fma((double)v.z, (double)v.z, ss);
-            ss = fma((double)v.w, (double)v.w, ss);
+    for (int64_t m = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); m < M; m += (int64_t)gridDim.x * 8) {
+        const float *xr = x + m * K + lane * 8;
+        float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
+#pragma unroll 4
+        for (int64_t c = 0; c < nch; ++c) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(xr + c * 256));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(xr + c * 256 + 4));
+            add_square(a.x, hi0, lo0);
+            add_square(a.y, hi1, lo1);
+            add_square(a.z, hi0, lo0);
+            add_square(a.w, hi1, lo1);
+            add_square(b.x, hi0, lo0);
+            add_square(b.y, hi1, lo1);
+            add_square(b.z, hi0, lo0);
+            add_square(b.w, hi1, lo1);
         }
+        double t = ((double)hi0 + (double)lo0) + ((double)hi1 + (double)lo1);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
-        if (tid == 0) {
-            double t = 0.0;
-            for (int i = 0; i < 8; ++i) t += red[i];
-            const double ms = t / (double)K;
-            r_sh = (float)(1.0 / sqrt(ms + (double)eps));
-        }
-        __syncthreads();
-        const float r = r_sh;
-        for (int64_t c = warp; c < nch; c += 8) {
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+        // every lane holds the same sum; one lane takes the f64 square root and divide (dozens of
+        // f64 operations each) and broadcasts r
+        float r = 0.0f;
+        if (lane == 0) r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
+        r = __shfl_sync(kFull, r, 0);
+#pragma unroll 2
+        for (int64_t c = 0; c < nch; ++c) {
             const int64_t k0 = c * 256 + lane * 8;
-            const float4 *src = reinterpret_cast<const float4 *>(xr + k0);
+            const float4 *src = reinterpret_cast<const float4 *>(x + m * K + k0);
             const float4 *ws = reinterpret_cast<const float4 *>(w + k0);
             const float4 a = __ldg(src), b = __ldg(src + 1);
             const float4 wa = __ldg(ws), wb = __ldg(ws + 1);
@@ -152,16 +199,27 @@ __global__ void __launch_bounds__(256) rms_quantize_kernel(const float *__restri
                                 __fmul_rn(__fmul_rn(a.z, r), wa.z), __fmul_rn(__fmul_rn(a.w, r), wa.w),
                                 __fmul_rn(__fmul_rn(b.x, r), wb.x), __fmul_rn(__fmul_rn(b.y, r), wb.y),
                                 __fmul_rn(__fmul_rn(b.z, r), wb.z), __fmul_rn(__fmul_rn(b.w, r), wb.w)};
-            quantize8(v, lane, p, M, K, m, k0);
+            quantize8<SECT>(v, lane, p, M, K, m, k0);
         }
-        __syncthreads();   // red / r_sh are reused by the next token
     }
 }
 
 }  // namespace
 
-int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, const Plane &p,
-                    unsigned int *err, cudaStream_t stream) {
+// the kernel of each section mask (1 .. 7)
+#define MQ_SECT_SWITCH(KERNEL, sections, ...)                               \
+    switch (sections) {                                                    \
+    case 1: e = launch_pdl(KERNEL<1>, __VA_ARGS__); break;                 \
+    case 2: e = launch_pdl(KERNEL<2>, __VA_ARGS__); break;                 \
+    case 3: e = launch_pdl(KERNEL<3>, __VA_ARGS__); break;                 \
+    case 4: e = launch_pdl(KERNEL<4>, __VA_ARGS__); break;                 \
+    case 5: e = launch_pdl(KERNEL<5>, __VA_ARGS__); break;                 \
+    case 6: e = launch_pdl(KERNEL<6>, __VA_ARGS__); break;                 \
+    default: e = launch_pdl(KERNEL<7>, __VA_ARGS__); break;                \
+    }
+
+int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, float eps, unsigned sections,
+                    const Plane &p, unsigned int *err, cudaStream_t stream) {
     (void)err;
     const int nsm = sm_count();
     cudaError_t e;
@@ -170,24 +228,26 @@ int launch_quantize(const float *x, int64_t M, int64_t K, const float *rms_w, fl
         int64_t ctas = (warps + 7) / 8;
         const int64_t cap = (int64_t)nsm * 8;
         if (ctas > cap) ctas = cap;
-        e = launch_pdl(quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, p);
+        MQ_SECT_SWITCH(quantize_kernel, sections, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, p)
     } else {
-        int64_t ctas = M;
+        int64_t ctas = (M + 7) / 8;                 // a warp per token, eight per CTA
         const int64_t cap = (int64_t)nsm * 8;
         if (ctas > cap) ctas = cap;
-        e = launch_pdl(rms_quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, rms_w, eps, p);
+        MQ_SECT_SWITCH(rms_quantize_kernel, sections, dim3((unsigned)ctas), dim3(256), 0, stream, x, M, K, rms_w, eps, p)
     }
     return cuda_error(e, "quantize launch");
 }
 
-int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, const Plane &p, cudaStream_t stream) {
+int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K, unsigned sections, const Plane &p,
+                           cudaStream_t stream) {
     const int nsm = sm_count();
     const int64_t warps = M * (K / 256);
     int64_t ctas = (warps + 7) / 8;
     const int64_t cap = (int64_t)nsm * 8;
     if (ctas > cap) ctas = cap;
-    return cuda_error(launch_pdl(swiglu_quantize_kernel, dim3((unsigned)ctas), dim3(256), 0, stream, g, up, M, K, p),
-                      "swiglu quantize launch");
+    cudaError_t e;
+    MQ_SECT_SWITCH(swiglu_quantize_kernel, sections, dim3((unsigned)ctas), dim3(256), 0, stream, g, up, M, K, p)
+    return cuda_error(e, "swiglu quantize launch");
 }
 
 }  // namespace mq

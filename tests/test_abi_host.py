@@ -21,7 +21,8 @@ EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quan
             "mq_gemm_q4k",
             "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k", "mq_device_status", "mq_debug_blockdots",
             "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
-            "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu"}
+            "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu",
+            "mq_quantize_q8_ex", "mq_quantize_swiglu_q8_ex"}
 
 
 def test_header_declares_the_boundary():
@@ -91,6 +92,18 @@ def test_quantize_argument_errors(L):
     assert q(16, 4, 256, 32, -1.0, 256, None) == B.MQ_ERR_ARG
     assert q(1 << 20, 4, 256, None, 0.0, (1 << 20) + 256, None) == B.MQ_ERR_ARG      # plane over x
     assert q(1 << 20, 4, 256, 1 << 24, 1e-6, (1 << 24) - 256, None) == B.MQ_ERR_ARG  # plane over rms_w
+
+
+def test_plane_sections_argument_errors(L):
+    q, g = L.mq_quantize_q8_ex, L.mq_quantize_swiglu_q8_ex
+    for bad in (0, 8, 0xffffffff):
+        assert q(16, 4, 256, None, 0.0, bad, 256, None) == B.MQ_ERR_ARG
+        assert "sections" in B.last_error()
+        assert g(16, 32, 4, 256, bad, 256, None) == B.MQ_ERR_ARG
+    assert q(16, 0, 256, None, 0.0, B.PLANE_FOR_GEMV, 256, None) == B.MQ_OK      # empty
+    assert q(16, 4, 100, None, 0.0, B.PLANE_FOR_GEMM, 256, None) == B.MQ_ERR_SHAPE
+    assert g(16, 32, 0, 256, B.PLANE_ALL, 256, None) == B.MQ_OK
+    assert (B.PLANE_FOR_GEMM, B.PLANE_FOR_GEMV) == (B.PLANE_Q16 | B.PLANE_DS, B.PLANE_Q8)
 
 
 def test_swiglu_quantize_argument_errors(L):

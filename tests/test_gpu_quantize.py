@@ -3,6 +3,7 @@ must match bit for bit (int8 codes, f16 codes, f32 scales, int32 sums)."""
 import numpy as np
 import pytest
 
+from quantized_q8_activation_quantize_gb300 import binding as B
 from quantized_q8_activation_quantize_gb300 import inputs
 from tests import gpu_util as G
 
@@ -64,3 +65,71 @@ def test_quantize_is_deterministic_and_reuses_plane():
     _, b = G.gpu_plane(x, plane=plane)
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+# ---- plane sections (mq_quantize_q8_ex / mq_quantize_swiglu_q8_ex)
+
+def _sections_of(plane, M, K):
+    import torch
+    q16, q8, d, s, ds = B.plane_views(plane, M, K, with_ds=True)
+    return {"q16": q16.view(torch.int16).cpu().numpy(), "q8": q8.cpu().numpy(), "d": d.cpu().numpy().view(np.uint32),
+            "s": s.cpu().numpy(), "ds": ds.cpu().numpy().view(np.uint32)}
+
+
+@pytest.mark.parametrize("producer", ["plain", "rms", "swiglu"])
+def test_plane_sections_write_only_what_is_asked(producer):
+    import torch
+    M, K = 37, 768
+    r = np.random.default_rng(11)
+    x = inputs.activations(r, M, K)
+    w = inputs.rms_weight(r, K)
+    g, u = inputs.swiglu_inputs(r, M, K)
+
+    def run(sections, plane):
+        if producer == "plain":
+            B.mq_quantize_q8_ex(G.dev(x), M, K, None, 0.0, sections, plane)
+        elif producer == "rms":
+            B.mq_quantize_q8_ex(G.dev(x), M, K, G.dev(w), 1e-6, sections, plane)
+        else:
+            B.mq_quantize_swiglu_q8_ex(G.dev(g), G.dev(u), M, K, sections, plane)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+
+    full = B.alloc_plane(M, K)
+    run(B.PLANE_ALL, full)
+    ref = _sections_of(full, M, K)
+    sentinel = _sections_of(torch.full_like(full, 0xA5), M, K)
+    for sections in range(1, 8):
+        plane = torch.full_like(full, 0xA5)
+        run(sections, plane)
+        got = _sections_of(plane, M, K)
+        want = {"q16": sections & B.PLANE_Q16, "q8": sections & B.PLANE_Q8, "ds": sections & B.PLANE_DS,
+                "d": True, "s": True}
+        for name, written in want.items():
+            expect = ref[name] if written else sentinel[name]
+            assert np.array_equal(got[name], expect), (producer, sections, name)
+
+
+def test_consumers_read_only_their_sections():
+    # a GEMM on a MQ_PLANE_FOR_GEMM plane and a GEMV on a MQ_PLANE_FOR_GEMV plane give the same
+    # outputs as on a full plane, bit for bit
+    import torch
+    M, K, N = 20, 512, 256
+    r = np.random.default_rng(12)
+    x = inputs.activations(r, M, K)
+    full, _ = G.gpu_plane(x)
+    for fmt in ("q4k", "q6k", "q4_1"):
+        wt = inputs.q4k_weights(r, N, K) if fmt == "q4k" else (
+            inputs.q6k_weights(r, N, K) if fmt == "q6k" else inputs.b32_weights(r, N, K, fmt))
+        wd = G.dev(wt.reshape(N, -1))
+        for path, sections in (("gemm", B.PLANE_FOR_GEMM), ("gemv", B.PLANE_FOR_GEMV)):
+            part = torch.full_like(full, 0xA5)
+            B.mq_quantize_q8_ex(G.dev(x), M, K, None, 0.0, sections, part)
+            y_full = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            y_part = torch.empty_like(y_full)
+            f = (B.GEMM if path == "gemm" else B.GEMV)[fmt]
+            f(wd, N, K, full, M, y_full)
+            f(wd, N, K, part, M, y_part)
+            torch.cuda.synchronize()
+            B.mq_device_status()
+            assert torch.equal(y_full, y_part), (fmt, path)
