@@ -189,6 +189,23 @@ MQ_API int mq_gemm_q6k(const void *w, int64_t N, int64_t K, const void *plane, i
                 float *y, mq_stream_t stream);
 
 /*
+ * mq_gemm_small_q4k / mq_gemm_small_q5k / mq_gemm_small_q6k -- the small-M band (1 <= M <= 32
+ * tokens) on the tensor cores ("Support Matrix > CUDA notes": the band between decode (nt == 1,
+ * dp4a MMVQ) and prefill (nt >= 16, MMQ); "Features > Continuous batching": several sequences
+ * decoded together).  Same arguments, layouts, errors and result as mq_gemm_q4k / mq_gemm_q5k /
+ * mq_gemm_q6k (the same exact integer block dots, f32 scaling), computed with the weights as the
+ * 128-row MMA operand and the tokens as its 16- or 32-wide side, so every weight byte is read
+ * from memory once for all M tokens.  M must be at most 32 (MQ_ERR_SHAPE otherwise); M == 0 or
+ * N == 0 is a valid empty call.  The plane needs the MQ_PLANE_FOR_GEMM sections.
+ */
+MQ_API int mq_gemm_small_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                             float *y, mq_stream_t stream);
+MQ_API int mq_gemm_small_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                             float *y, mq_stream_t stream);
+MQ_API int mq_gemm_small_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M,
+                             float *y, mq_stream_t stream);
+
+/*
  * mq_gemm_q4k_swiglu -- the fused gate|up GEMM of a SwiGLU FFN: both Q4_K projections of one
  * input plane in one kernel, whose epilogue writes the Q8 plane of silu(gate) * up for the
  * down projection ("Features > GPU -- CUDA": the FFN's gate and up matmuls share one plane and
@@ -305,7 +322,8 @@ MQ_API int mq_device_status(mq_stream_t stream);
  * op: 0 = mq_gemm_q4k, 1 = mq_gemm_q6k, 2 = mq_gemv_q4k, 3 = mq_gemv_q6k, 4 = mq_gemv_q5k,
  *     5 = mq_gemm_q5k, 6 = mq_gemv_q4_0, 7 = mq_gemv_q4_1, 8 = mq_gemv_q5_0,
  *     9 = mq_gemv_q5_1, 10 = mq_gemv_q8_0, 11 = mq_gemm_q4_0, 12 = mq_gemm_q4_1,
- *     13 = mq_gemm_q5_0, 14 = mq_gemm_q5_1, 15 = mq_gemm_q8_0.
+ *     13 = mq_gemm_q5_0, 14 = mq_gemm_q5_1, 15 = mq_gemm_q8_0, 16 = mq_gemm_small_q4k,
+ *     17 = mq_gemm_small_q6k, 18 = mq_gemm_small_q5k.
  * The window must lie inside [0, M) x [0, N).  Test infrastructure: slower
  * than the plain entry points.
  */

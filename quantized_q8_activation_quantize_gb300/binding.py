@@ -63,7 +63,8 @@ def lib():
         L.mq_quantize_swiglu_q8_ex.argtypes = [P, P, I64, I64, ctypes.c_uint, P, P]
         for name in ("mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k",
                      "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
-                     "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0"):
+                     "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0",
+                     "mq_gemm_small_q4k", "mq_gemm_small_q5k", "mq_gemm_small_q6k"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
         L.mq_gemm_q4k_swiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
         L.mq_device_status.argtypes = [P]
@@ -225,6 +226,18 @@ def mq_gemm_q8_0(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemm_q8_0", w, N, K, plane, M, y, stream)
 
 
+def mq_gemm_small_q4k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_small_q4k", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_small_q5k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_small_q5k", w, N, K, plane, M, y, stream)
+
+
+def mq_gemm_small_q6k(w, N: int, K: int, plane, M: int, y, stream=None):
+    return _matmul("mq_gemm_small_q6k", w, N, K, plane, M, y, stream)
+
+
 def mq_gemm_q4k_swiglu(w_gate, w_up, F: int, K: int, plane_in, M: int, plane_out, stream=None):
     return _check(lib().mq_gemm_q4k_swiglu(_ptr(w_gate), _ptr(w_up), F, K, _ptr(plane_in), M, _ptr(plane_out),
                                            _stream(stream)))
@@ -250,13 +263,29 @@ GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k, "q4_0": mq_g
         "q5_0": mq_gemm_q5_0, "q5_1": mq_gemm_q5_1, "q8_0": mq_gemm_q8_0}
 GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k, "q4_0": mq_gemv_q4_0, "q4_1": mq_gemv_q4_1,
         "q5_0": mq_gemv_q5_0, "q5_1": mq_gemv_q5_1, "q8_0": mq_gemv_q8_0}
+# the small-M band (1 <= M <= 32) on the tensor cores, k-quant weights
+GEMM_SMALL = {"q4k": mq_gemm_small_q4k, "q5k": mq_gemm_small_q5k, "q6k": mq_gemm_small_q6k}
+SMALL_MAX_M = 32
 # debug op of each (kind, format) for mq_debug_blockdots
 DEBUG_OP = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv", "q6k"): 3, ("gemv", "q5k"): 4,
             ("gemm", "q5k"): 5, ("gemv", "q4_0"): 6, ("gemv", "q4_1"): 7, ("gemv", "q5_0"): 8, ("gemv", "q5_1"): 9,
             ("gemv", "q8_0"): 10, ("gemm", "q4_0"): 11, ("gemm", "q4_1"): 12, ("gemm", "q5_0"): 13,
-            ("gemm", "q5_1"): 14, ("gemm", "q8_0"): 15}
+            ("gemm", "q5_1"): 14, ("gemm", "q8_0"): 15, ("small", "q4k"): 16, ("small", "q6k"): 17,
+            ("small", "q5k"): 18}
+
+
+def matmul_path(fmt: str, M: int) -> str:
+    """The entry point family the size dispatch picks: the pages' gate (MMVQ for one token, MMQ from 16),
+    with the band 2 <= M <= 32 on the small-M tensor-core kernel where the format has one."""
+    if M == 1:
+        return "gemv"
+    if M <= SMALL_MAX_M and fmt in GEMM_SMALL:
+        return "small"
+    return "gemv" if M < 16 else "gemm"
 
 
 def matmul(fmt: str, w, N: int, K: int, plane, M: int, y, stream=None):
-    """Size dispatch of the pages' MMQ gate: GEMV below 16 tokens, GEMM from 16 on."""
-    return (GEMV if M < 16 else GEMM)[fmt](w, N, K, plane, M, y, stream)
+    """Size dispatch (matmul_path): GEMV for one token, the small-M tensor-core GEMM for 2 .. 32 tokens
+    (k-quants), the GEMV below 16 tokens and the GEMM from 16 on otherwise."""
+    table = {"gemv": GEMV, "gemm": GEMM, "small": GEMM_SMALL}[matmul_path(fmt, M)]
+    return table[fmt](w, N, K, plane, M, y, stream)

@@ -70,7 +70,7 @@ int set_error(int code, const char *fmt, ...) {
 
 namespace {
 int g_sm_count[kMaxDevices] = {0};
-constexpr int kAttrSlots = kAttrSlotSwiglu + 8;     // GEMM below 16; GEMV 16 + 16 per format; fused GEMM
+constexpr int kAttrSlots = kAttrSlotSmall + 16;     // GEMM below 16; GEMV 16 + 16 per format; fused GEMM; small-M GEMM
 bool g_attr_done[kMaxDevices][kAttrSlots] = {};
 }  // namespace
 
@@ -187,17 +187,21 @@ static int check_k(int64_t K) {
     return MQ_OK;
 }
 
+enum MatmulKind { KIND_GEMV = 0, KIND_GEMM = 1, KIND_SMALL = 2 };
+
 // shared validation of the matmul entry points (bb: weight bytes per 256 values of a row)
-static int check_matmul(const char *fn, bool gemm, int bb, const void *w, int64_t N, int64_t K, const void *plane,
+static int check_matmul(const char *fn, int kind, int bb, const void *w, int64_t N, int64_t K, const void *plane,
                         int64_t M, const float *y) {
     if (M < 0 || N < 0) return set_error(MQ_ERR_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
     int rc = check_k(K);
     if (rc != MQ_OK) return rc;
     if (M >= kMaxDim || N >= kMaxDim)
         return set_error(MQ_ERR_SHAPE, "%s: M=%lld N=%lld must be below 2^31", fn, (long long)M, (long long)N);
-    if (gemm && M > kMaxGemmM)
+    if (kind == KIND_GEMM && M > kMaxGemmM)
         return set_error(MQ_ERR_SHAPE, "%s: M=%lld exceeds the GEMM limit of %lld tokens", fn, (long long)M,
                          (long long)kMaxGemmM);
+    if (kind == KIND_SMALL && M > 32)
+        return set_error(MQ_ERR_SHAPE, "%s: M=%lld exceeds the small-M limit of 32 tokens", fn, (long long)M);
     if (M == 0 || N == 0) return MQ_OK;
     if (!w || !plane || !y) return set_error(MQ_ERR_ARG, "%s: NULL pointer (w=%p plane=%p y=%p)", fn, w, plane, (const void *)y);
     if (!aligned(w, 16)) return set_error(MQ_ERR_ALIGN, "%s: weights %p not 16-byte aligned", fn, w);
@@ -210,7 +214,7 @@ static int check_matmul(const char *fn, bool gemm, int bb, const void *w, int64_
     return MQ_OK;
 }
 
-constexpr int kMatmulOps = 16;
+constexpr int kMatmulOps = 19;
 
 static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                       const Dump &dump, mq_stream_t stream) {
@@ -218,16 +222,18 @@ static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *p
     static const struct {
         const char *name;
         Fmt fmt;
-        bool gemm;
-    } ops[kMatmulOps] = {{"mq_gemm_q4k", FMT_Q4K, true},   {"mq_gemm_q6k", FMT_Q6K, true},
-                         {"mq_gemv_q4k", FMT_Q4K, false},  {"mq_gemv_q6k", FMT_Q6K, false},
-                         {"mq_gemv_q5k", FMT_Q5K, false},  {"mq_gemm_q5k", FMT_Q5K, true},
-                         {"mq_gemv_q4_0", FMT_Q4_0, false}, {"mq_gemv_q4_1", FMT_Q4_1, false},
-                         {"mq_gemv_q5_0", FMT_Q5_0, false}, {"mq_gemv_q5_1", FMT_Q5_1, false},
-                         {"mq_gemv_q8_0", FMT_Q8_0, false}, {"mq_gemm_q4_0", FMT_Q4_0, true},
-                         {"mq_gemm_q4_1", FMT_Q4_1, true},  {"mq_gemm_q5_0", FMT_Q5_0, true},
-                         {"mq_gemm_q5_1", FMT_Q5_1, true},  {"mq_gemm_q8_0", FMT_Q8_0, true}};
-    int rc = check_matmul(ops[op].name, ops[op].gemm, block_bytes(ops[op].fmt), w, N, K, plane, M, y);
+        int kind;
+    } ops[kMatmulOps] = {{"mq_gemm_q4k", FMT_Q4K, KIND_GEMM},   {"mq_gemm_q6k", FMT_Q6K, KIND_GEMM},
+                         {"mq_gemv_q4k", FMT_Q4K, KIND_GEMV},   {"mq_gemv_q6k", FMT_Q6K, KIND_GEMV},
+                         {"mq_gemv_q5k", FMT_Q5K, KIND_GEMV},   {"mq_gemm_q5k", FMT_Q5K, KIND_GEMM},
+                         {"mq_gemv_q4_0", FMT_Q4_0, KIND_GEMV}, {"mq_gemv_q4_1", FMT_Q4_1, KIND_GEMV},
+                         {"mq_gemv_q5_0", FMT_Q5_0, KIND_GEMV}, {"mq_gemv_q5_1", FMT_Q5_1, KIND_GEMV},
+                         {"mq_gemv_q8_0", FMT_Q8_0, KIND_GEMV}, {"mq_gemm_q4_0", FMT_Q4_0, KIND_GEMM},
+                         {"mq_gemm_q4_1", FMT_Q4_1, KIND_GEMM}, {"mq_gemm_q5_0", FMT_Q5_0, KIND_GEMM},
+                         {"mq_gemm_q5_1", FMT_Q5_1, KIND_GEMM}, {"mq_gemm_q8_0", FMT_Q8_0, KIND_GEMM},
+                         {"mq_gemm_small_q4k", FMT_Q4K, KIND_SMALL}, {"mq_gemm_small_q6k", FMT_Q6K, KIND_SMALL},
+                         {"mq_gemm_small_q5k", FMT_Q5K, KIND_SMALL}};
+    int rc = check_matmul(ops[op].name, ops[op].kind, block_bytes(ops[op].fmt), w, N, K, plane, M, y);
     if (rc != MQ_OK || M == 0 || N == 0) return rc;
     unsigned int *err = nullptr;
     rc = device_state(&err);
@@ -236,7 +242,8 @@ static int run_matmul(int op, const void *w, int64_t N, int64_t K, const void *p
     plane_from(const_cast<void *>(plane), M, K, &p);
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (ops[op].gemm) return launch_gemm(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
+    if (ops[op].kind == KIND_GEMM) return launch_gemm(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
+    if (ops[op].kind == KIND_SMALL) return launch_gemm_small(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
     return launch_gemv(ops[op].fmt, wb, N, K, p, M, y, dump, err, s);
 }
 
@@ -389,6 +396,19 @@ int mq_gemm_q5_1(const void *w, int64_t N, int64_t K, const void *plane, int64_t
 }
 int mq_gemm_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y, mq_stream_t stream) {
     return run_matmul(15, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+
+int mq_gemm_small_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
+                      mq_stream_t stream) {
+    return run_matmul(16, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_small_q6k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
+                      mq_stream_t stream) {
+    return run_matmul(17, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
+}
+int mq_gemm_small_q5k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
+                      mq_stream_t stream) {
+    return run_matmul(18, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }
 
 int mq_gemm_q4k_swiglu(const void *w_gate, const void *w_up, int64_t F, int64_t K, const void *plane_in, int64_t M,

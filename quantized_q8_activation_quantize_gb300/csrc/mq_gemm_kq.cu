@@ -25,6 +25,8 @@ EncodeTiledFn encode_tiled_fn() {
 
 }  // namespace
 
+void *tensor_map_encoder() { return reinterpret_cast<void *>(encode_tiled_fn()); }
+
 // the activation maps: f16 codes [M][K] in 64 x 128 boxes (128-byte swizzle) and the d*S tf32
 // pairs [M][2*K/32] f32, one 16-value x 128-token box per super-block (64-byte swizzle)
 static int encode_act_maps(EncodeTiledFn enc, const Plane &p, int64_t M, int64_t K, CUtensorMap *tm,

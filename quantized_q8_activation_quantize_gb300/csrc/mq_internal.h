@@ -92,5 +92,12 @@ int launch_gemm_swiglu(Fmt fmt, const uint8_t *wg, const uint8_t *wu, int64_t F,
 constexpr int kAttrSlotSwiglu = 16 + 8 * 16;
 int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                 const Dump &dump, unsigned int *err, cudaStream_t stream);
+// the small-M tensor-core GEMM (1 <= M <= 32 tokens; k-quant weights)
+int launch_gemm_small(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
+                      const Dump &dump, unsigned int *err, cudaStream_t stream);
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable), resolved once
+void *tensor_map_encoder();
+// attribute slots of the small-M GEMM: kAttrSlotSmall + 2 * (3 fmt + NT/32) + dump
+constexpr int kAttrSlotSmall = kAttrSlotSwiglu + 8;
 
 }  // namespace mq

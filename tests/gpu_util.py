@@ -64,7 +64,7 @@ def run_matmul(path, fmt, w, plane, M, K, N):
     import torch
     wd = dev(w.reshape(N, -1))
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    (B.GEMM if path == "gemm" else B.GEMV)[fmt](wd, N, K, plane, M, y)
+    {"gemm": B.GEMM, "gemv": B.GEMV, "small": B.GEMM_SMALL}[path][fmt](wd, N, K, plane, M, y)
     torch.cuda.synchronize()
     B.mq_device_status()
     return y.cpu().numpy(), wd

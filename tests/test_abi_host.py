@@ -22,7 +22,8 @@ EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quan
             "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k", "mq_gemm_q5k", "mq_device_status", "mq_debug_blockdots",
             "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
             "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu",
-            "mq_quantize_q8_ex", "mq_quantize_swiglu_q8_ex"}
+            "mq_quantize_q8_ex", "mq_quantize_swiglu_q8_ex", "mq_gemm_small_q4k", "mq_gemm_small_q5k",
+            "mq_gemm_small_q6k"}
 
 
 def test_header_declares_the_boundary():
@@ -46,8 +47,10 @@ def test_binding_mirrors_every_entry_point():
             continue
         assert callable(getattr(B, name, None)), name
     assert set(B.GEMM) <= set(B.GEMV)
+    tables = {"gemm": (B.GEMM, "mq_gemm_"), "gemv": (B.GEMV, "mq_gemv_"), "small": (B.GEMM_SMALL, "mq_gemm_small_")}
     for (path, fmt), op in B.DEBUG_OP.items():
-        assert (B.GEMM if path == "gemm" else B.GEMV)[fmt].__name__ == f"mq_{path}_{fmt}", (path, fmt, op)
+        table, prefix = tables[path]
+        assert table[fmt].__name__ == prefix + fmt, (path, fmt, op)
     assert sorted(B.DEBUG_OP.values()) == list(range(len(B.DEBUG_OP)))
 
 
@@ -123,7 +126,7 @@ def test_swiglu_quantize_argument_errors(L):
 @pytest.mark.parametrize("name", ["mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q5k",
                                   "mq_gemm_q5k", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1",
                                   "mq_gemv_q8_0", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1",
-                                  "mq_gemm_q8_0"])
+                                  "mq_gemm_q8_0", "mq_gemm_small_q4k", "mq_gemm_small_q5k", "mq_gemm_small_q6k"])
 def test_matmul_argument_errors(L, name):
     f = getattr(L, name)
     assert f(16, 8, 300, 256, 4, 16, None) == B.MQ_ERR_SHAPE          # K % 256
@@ -142,8 +145,20 @@ def test_matmul_argument_errors(L, name):
     # the output may overlap neither the plane nor the weights
     assert f(1 << 20, 8, 256, 1 << 24, 4, (1 << 24) + 64, None) == B.MQ_ERR_ARG
     assert f(1 << 20, 8, 256, 1 << 24, 4, (1 << 20) + 64, None) == B.MQ_ERR_ARG
-    if "gemm" in name:                                                  # token tiles in grid.y
+    if "small" in name:                                                 # the band's limit
+        assert f(16, 8, 256, 256, 33, 16, None) == B.MQ_ERR_SHAPE
+    elif "gemm" in name:                                                # token tiles in grid.y
         assert f(16, 8, 256, 256, 65535 * 128 + 1, 16, None) == B.MQ_ERR_SHAPE
+
+
+def test_size_dispatch():
+    # the pages' gate: one token -> MMVQ; the band up to 32 tokens -> the small-M tensor-core GEMM for the
+    # k-quants; otherwise MMVQ below 16 tokens and MMQ from 16
+    assert B.matmul_path("q6k", 1) == "gemv"
+    for m in (2, 5, 9, 15, 16, 17, 32):
+        assert B.matmul_path("q4k", m) == "small" and B.matmul_path("q6k", m) == "small"
+    assert B.matmul_path("q4k", 33) == "gemm"
+    assert B.matmul_path("q8_0", 8) == "gemv" and B.matmul_path("q8_0", 16) == "gemm"
 
 
 def test_debug_window_errors(L):

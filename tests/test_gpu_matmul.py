@@ -186,7 +186,8 @@ def lm_head():
     return inputs.lm_head_weights()
 
 
-@pytest.mark.parametrize("M,paths", [(1, ("gemv",)), (16, ("gemv", "gemm")), (3314, ("gemm",))])
+@pytest.mark.parametrize("M,paths", [(1, ("gemv",)), (4, ("small",)), (16, ("gemv", "gemm", "small")),
+                                     (32, ("small",)), (3314, ("gemm",))])
 def test_lm_head(lm_head, M, paths):
     x = inputs.lm_head_x(M)
     N, K = lm_head.shape[0], 3584
@@ -391,3 +392,77 @@ def test_b32_size_dispatch_agrees(fmt):
     for path in ("gemv", "gemm"):
         y, _ = G.run_matmul(path, fmt, w, plane, M, K, N)
         assert G.rel_err(y, ref) <= G.REL_TOL, path
+
+
+# ---- the small-M band on the tensor cores (mq_gemm_small_*): weights as the 128-row MMA operand,
+# tokens (padded to 16 or 32) as its N side; the same exact block dots and the same bar
+
+SMALL_SHAPES = [(1, 7, 256), (2, 65, 512), (5, 129, 768), (9, 300, 2048), (15, 33, 512), (16, 128, 256),
+                (17, 130, 512), (31, 257, 1024), (32, 1000, 3584), (4, 129, 18944)]
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q5k", "q6k"])
+@pytest.mark.parametrize("M,N,K", SMALL_SHAPES)
+def test_small_m_shapes(fmt, M, N, K):
+    _full_check("small", fmt, M, N, K, seed=M * 6007 + N * 37 + K + len(fmt))
+
+
+def test_small_m_q6k_full_scale_range():
+    # scales up to +-128: odd |sc| > 64 takes the correction tile (now an A operand)
+    for seed, (M, N, K) in enumerate([(3, 40, 512), (16, 200, 768), (32, 130, 256)]):
+        _full_check("small", "q6k", M, N, K, seed=700 + seed, scale_range=(-128, 127))
+
+
+def test_small_m_extreme_blocks():
+    # every quant at its extreme with every code at +-127: the int32 headroom cases
+    for M in (5, 32):
+        N, K = 16, 512
+        x = np.full((M, K), 1.0, np.float32)
+        x[1::2] = -1.0
+        plane, _ = G.gpu_plane(x)
+        ref_plane = G.oracle_plane(x)
+        for fmt in ("q4k", "q5k", "q6k"):
+            w = _weights(fmt, N, K, 5, (-128, 127))
+            if fmt == "q6k":
+                w[..., 0:192] = 0                  # q = -32
+                w[..., 192:208] = 0x80             # sc = -128
+            else:
+                w[..., 4:] = 0xFF                  # sc = m = 63, q = 15 (Q5_K: 31)
+            y, wd = G.run_matmul("small", fmt, w, plane, M, K, N)
+            assert G.rel_err(y, oracle.matmul(w, fmt, ref_plane)) <= G.REL_TOL
+            I, _ = G.run_dump("small", fmt, wd, plane, M, K, N, 0, M, 0, N)
+            assert np.array_equal(I, oracle.blockdots(w, fmt, ref_plane[0])[0]), (M, fmt)
+
+
+def test_small_m_decode_shapes():
+    # a layer of the 7B decode stack batched over 8 sequences: q (Q4_K), v and down (Q6_K), gate (Q4_K)
+    for idx in (0, 2, 4, 6):
+        c = inputs.decode_matrix(0, idx)
+        N, K = c["w"].shape[0], c["x"].shape[1]
+        x = inputs.activations(np.random.default_rng(300 + idx), 8, K)
+        plane, _ = G.gpu_plane(x)
+        ref_plane = G.oracle_plane(x)
+        ms, ns = np.arange(8), _sample_idx(N, 512, 301 + idx, must=(0, N - 1))
+        _sampled("small", c["fmt"], c["w"], plane, ref_plane, 8, K, N, ms, ns, dump_window=(0, 8, N - 64, 64))
+
+
+@pytest.mark.parametrize("M", [2, 5, 16, 32])
+def test_small_m_size_dispatch_agrees(M):
+    # matmul() routes 2 <= M <= 32 to the small-M kernel: same bar against the oracle, and the
+    # GEMV / GEMM on the same inputs meet it too
+    import torch
+    N, K = 300, 1024
+    for fmt in ("q4k", "q6k"):
+        w = _weights(fmt, N, K, 93)
+        x = inputs.activations(np.random.default_rng(94 + M), M, K)
+        plane, _ = G.gpu_plane(x)
+        ref = oracle.matmul(w, fmt, G.oracle_plane(x))
+        assert B.matmul_path(fmt, M) == "small"
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        B.matmul(fmt, G.dev(w.reshape(N, -1)), N, K, plane, M, y)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+        assert G.rel_err(y.cpu().numpy(), ref) <= G.REL_TOL
+        for path in ("gemv", "gemm"):
+            y2, _ = G.run_matmul(path, fmt, w, plane, M, K, N)
+            assert G.rel_err(y2, ref) <= G.REL_TOL, path
