@@ -86,6 +86,8 @@ CASES = {
     "gemm_q6k_down": "7B FFN prefill down GEMM: Q6_K 3584x18944, M=3314",
     "gemm_q4k_qproj": "7B q_proj prefill GEMM: Q4_K 3584x3584, M=512",
     "gemv_q6k_lmhead": "LM head GEMV: Q6_K 152064x3584, M=1",
+    "small_q6k_lmhead": "LM head small-M tensor-core GEMM: Q6_K 152064x3584, M=16",
+    "small_q4k_vocab": "small-M tensor-core GEMM of the LM-head shape: 152064x3584 synthetic Q4_K weights, M=16",
     "gemv_q4k_gate": "decode sweep layer-1 gate GEMV: Q4_K 18944x3584, M=1",
     "gemv_q5k_vocab": "Q5_K GEMV of the LM-head shape: 152064x3584 synthetic Q5_K weights, M=1",
     **{f"gemv_{f}_vocab": f"{f.upper()} GEMV of the LM-head shape: 152064x3584 synthetic {f.upper()} weights, M=1"
@@ -129,6 +131,12 @@ def run_case(args):
     elif name == "gemv_q6k_lmhead":
         x, w, fmt, rms = I.lm_head_x(1), I.lm_head_weights(), "q6k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
+    elif name == "small_q6k_lmhead":
+        x, w, fmt, rms = I.lm_head_x(16), I.lm_head_weights(), "q6k", None
+        M, K, N = 16, I.HIDDEN, I.VOCAB
+    elif name == "small_q4k_vocab":
+        x, w, fmt, rms = I.lm_head_x(16), I.q4k_weights(I.rng(4, I.STREAM_W, 1), I.VOCAB, I.HIDDEN), "q4k", None
+        M, K, N = 16, I.HIDDEN, I.VOCAB
     elif name == "gemv_q5k_vocab":
         x, w, fmt, rms = I.lm_head_x(1), I.q5k_vocab_weights(), "q5k", None
         M, K, N = 1, I.HIDDEN, I.VOCAB
@@ -160,7 +168,7 @@ def run_case(args):
         w2d, po = dev(w2.reshape(N, -1)), B.alloc_plane(M, N)
         fn = lambda: B.mq_gemm_q4k_swiglu(wd, w2d, N, K, plane, M, po)
     else:
-        f = (B.GEMM if name.startswith("gemm") else B.GEMV)[fmt]
+        f = (B.GEMM_SMALL if name.startswith("small") else B.GEMM if name.startswith("gemm") else B.GEMV)[fmt]
         fn = lambda: f(wd, N, K, plane, M, y)
     for _ in range(2 + args.reps):
         fn()

@@ -122,6 +122,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// The same bound and failure handling, but the thread waits in the hardware's default suspend
+// (try_wait without a time hint) rather than a long hinted sleep, so it resumes sooner after the
+// phase completes; for the one warp whose wake-up latency is on a pipeline's critical path.
+__device__ __forceinline__ bool mbar_wait_prompt(uint64_t *bar, uint32_t parity, unsigned int *err, uint32_t code,
+                                                 volatile int *abort) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                atomicOr(err, code);
+                if (abort != nullptr) *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------ programmatic dependent launch ---
 // Kernels are launched with programmatic stream serialization: a kernel may be scheduled
 // while its predecessor on the stream is still running.  Each kernel calls grid_dep_wait()

@@ -9,11 +9,13 @@
 // token, and the MMA work per weight byte is small enough that the kernel runs at the pace of the
 // weight stream and its unpacking.  The integer block dots are the exact f16-operand / f32-accumulator
 // integers of the prefill GEMM (q8 codes and sc*q are exact in f16, every 32-value sum below 2^24):
-// one TMEM accumulator of NT columns per 32-value block, in a ring of eight, so the block-dot
-// checkpoint is bit-exact.
+// one TMEM accumulator of NT columns per 32-value block, the two blocks of a 64-value stage side by
+// side in one ring entry (four entries), so the block-dot checkpoint is bit-exact.  Every barrier
+// probe costs a shared-memory round trip even when the phase is complete, so the MMA issuer probes a
+// stage's three conditions at once and the epilogue and unpackers probe one step ahead.
 //
-// CTA = 16 warps: 0 TMA producer (token code tiles, token d*S tiles, TMA-fed raw weights),
-// 1 MMA issuer (and TMEM owner), 2 activation-scale stager, 3 idle, 4-11 unpackers (two threads per
+// CTA = 16 warps: 0 TMA producer of the token code tiles, 1 MMA issuer (and TMEM owner),
+// 2 activation-scale stager, 3 TMA producer of the raw weights and token d*S tiles, 4-11 unpackers (two threads per
 // weight row, one 32-value block each per 64-value stage), 12-15 epilogue (one weight row per
 // thread, all tokens).
 #include <cuda.h>
@@ -29,8 +31,8 @@ namespace {
 
 constexpr int SW = 128, SBK = 64;              // weight rows per CTA (MMA M), K per stage
 constexpr int kSmThreads = 512;
-constexpr int kSmWarpTma = 0, kSmWarpMma = 1, kSmWarpDa = 2, kSmWarpUnpack0 = 4, kSmWarpEpi0 = 12;
-constexpr int kSlots = 8;                      // block accumulators in the TMEM ring
+constexpr int kSmWarpTma = 0, kSmWarpMma = 1, kSmWarpDa = 2, kSmWarpRaw = 3, kSmWarpUnpack0 = 4, kSmWarpEpi0 = 12;
+constexpr int kEnt = 4;                        // TMEM ring entries: one per 64-value stage (two block accumulators)
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kWTile = SW * SBK * 2;           // one 128 x 64 f16 weight tile (16 KB)
 
@@ -47,26 +49,40 @@ struct SmCfg {
     static constexpr bool TMW = FMT != FMT_Q6K;                         // raw rows by TMA
     static constexpr bool CORR = FMT == FMT_Q6K;                        // odd |sc| > 64 correction tile
     static constexpr int BB = block_bytes(FMT);
-    static constexpr int S = 4;                                          // 64-value stages in flight
-    static constexpr int R = FMT == FMT_Q6K ? 2 : 3;                     // raw super-block slots
+#ifndef SMALL_S
+#define SMALL_S 4
+#endif
+#ifndef SMALL_R6
+#define SMALL_R6 2
+#endif
+#ifndef SMALL_R4
+#define SMALL_R4 3
+#endif
+    static constexpr int S = SMALL_S;                                    // 64-value stages in flight
+    static constexpr int R = FMT == FMT_Q6K ? SMALL_R6 : SMALL_R4;       // raw super-block slots
     static constexpr int RAW_ROW = TMW ? BB : 240;                       // Q6_K: 16-B aligned superset
     static constexpr int XTILE = NT * SBK * 2;                           // token codes of one stage
+    // the token tiles have their own, deeper ring: they come from L2 with a latency of a few stages
+    static constexpr int XS = NT == 16 ? 16 : 6;
     static constexpr int MIN_W = SW * 64, MIN_X = NT * 64;               // tf32 (hi, lo) x 8 per row
-    static constexpr int TMEM_COLS = (kSlots + 1) * NT <= 256 ? 256 : 512;
-    static constexpr uint32_t MIN_COL = kSlots * NT;
+    static constexpr int TMEM_COLS = (2 * kEnt + 1) * NT <= 256 ? 256 : 512;
+    static constexpr uint32_t MIN_COL = 2 * kEnt * NT;
     static constexpr int OFF_W = 0;
     static constexpr int OFF_WC = OFF_W + S * kWTile;
     static constexpr int OFF_X = OFF_WC + (CORR ? S * kWTile : 0);
-    static constexpr int OFF_WMIN = sm_align(OFF_X + S * XTILE, 1024);
+    static constexpr int OFF_WMIN = sm_align(OFF_X + XS * XTILE, 1024);
     static constexpr int OFF_XMIN = OFF_WMIN + (MIN ? 2 * MIN_W : 0);
     static constexpr int OFF_RAW = sm_align(OFF_XMIN + (MIN ? 2 * MIN_X : 0), 1024);
     static constexpr int OFF_INFO = OFF_RAW + R * SW * RAW_ROW;          // d per weight row [2][128]
-    static constexpr int OFF_DA = OFF_INFO + 2 * SW * 4;                 // d_a [2][8 blocks][NT tokens]
-    static constexpr int OFF_FLAG = OFF_DA + 2 * 8 * NT * 4;             // Q6_K correction flags [S][8]
+    // the tokens' activation scales d_a [DAS][8 blocks][NT tokens]: a deep ring, since each slot is
+    // filled by plain global loads (the plane's d section has a row stride of M floats)
+    static constexpr int DAS = NT == 16 ? 8 : 4;
+    static constexpr int OFF_DA = OFF_INFO + 2 * SW * 4;
+    static constexpr int OFF_FLAG = OFF_DA + DAS * 8 * NT * 4;           // Q6_K correction flags [S][8]
     static constexpr int OFF_BAR = sm_align(OFF_FLAG + S * 8 * 4, 8);
-    // w_full[S] x_full[S] wx_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] xmin_full[2]
-    // xmin_empty[2] acc_full[8] acc_empty[8] da_full[2] da_empty[2] min_final
-    static constexpr int NBARS = 3 * S + 2 * R + 8 + 2 * kSlots + 4 + 1;
+    // w_full[S] w_empty[S] x_full[XS] x_empty[XS] raw_full[R] raw_empty[R] info_full[2] info_empty[2]
+    // xmin_full[2] xmin_empty[2] acc_full[4] acc_empty[4] da_full[DAS] da_empty[DAS] min_final
+    static constexpr int NBARS = 2 * S + 2 * XS + 2 * R + 8 + 2 * kEnt + 2 * DAS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA exceeds the per-CTA limit");
@@ -74,7 +90,7 @@ struct SmCfg {
 };
 
 struct SmBars {
-    uint64_t *w_full, *x_full, *wx_empty, *raw_full, *raw_empty, *info_full, *info_empty, *xmin_full, *xmin_empty;
+    uint64_t *w_full, *wx_empty, *x_full, *x_empty, *raw_full, *raw_empty, *info_full, *info_empty, *xmin_full, *xmin_empty;
     uint64_t *acc_full, *acc_empty, *da_full, *da_empty, *min_final;
 };
 
@@ -162,19 +178,20 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     uint64_t *bar0 = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
     SmBars bars;
     bars.w_full = bar0;
-    bars.x_full = bars.w_full + S;
-    bars.wx_empty = bars.x_full + S;
-    bars.raw_full = bars.wx_empty + S;
+    bars.wx_empty = bars.w_full + S;
+    bars.x_full = bars.wx_empty + S;
+    bars.x_empty = bars.x_full + C::XS;
+    bars.raw_full = bars.x_empty + C::XS;
     bars.raw_empty = bars.raw_full + R;
     bars.info_full = bars.raw_empty + R;
     bars.info_empty = bars.info_full + 2;
     bars.xmin_full = bars.info_empty + 2;
     bars.xmin_empty = bars.xmin_full + 2;
     bars.acc_full = bars.xmin_empty + 2;
-    bars.acc_empty = bars.acc_full + kSlots;
-    bars.da_full = bars.acc_empty + kSlots;
-    bars.da_empty = bars.da_full + 2;
-    bars.min_final = bars.da_empty + 2;
+    bars.acc_empty = bars.acc_full + kEnt;
+    bars.da_full = bars.acc_empty + kEnt;
+    bars.da_empty = bars.da_full + C::DAS;
+    bars.min_final = bars.da_empty + C::DAS;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
     volatile uint32_t *corr_flags = reinterpret_cast<volatile uint32_t *>(sm + C::OFF_FLAG);
@@ -188,8 +205,11 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&bars.w_full[s], 8);                   // the unpack warps
-            mbar_init(&bars.x_full[s], 1);
             mbar_init(&bars.wx_empty[s], 1);
+        }
+        for (int s = 0; s < C::XS; ++s) {
+            mbar_init(&bars.x_full[s], 1);
+            mbar_init(&bars.x_empty[s], 1);
         }
         for (int r = 0; r < R; ++r) {
             mbar_init(&bars.raw_full[r], C::TMW ? 1 : SW);  // TMA, or one bulk copy per row
@@ -200,12 +220,14 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             mbar_init(&bars.info_empty[i], C::MIN ? 5 : 4);  // epilogue warps (+ the min MMA)
             mbar_init(&bars.xmin_full[i], 1);
             mbar_init(&bars.xmin_empty[i], 1);
-            mbar_init(&bars.da_full[i], 1);
-            mbar_init(&bars.da_empty[i], 4);
         }
-        for (int i = 0; i < kSlots; ++i) {
+        for (int i = 0; i < kEnt; ++i) {
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], 4);
+        }
+        for (int i = 0; i < C::DAS; ++i) {
+            mbar_init(&bars.da_full[i], 1);
+            mbar_init(&bars.da_empty[i], 4);
         }
         mbar_init(bars.min_final, 1);
         *abort_flag = 0;
@@ -219,48 +241,46 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     grid_dep_wait();
 
     if (warp == kSmWarpTma) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer: token code tiles
         if (lane == 0) {
             prefetch_tmap(&tmX);
-            if constexpr (C::MIN) prefetch_tmap(&tmXS);
-            if constexpr (C::TMW) prefetch_tmap(&tmW);
-            int st = 0, raw_issued = 0, xs_issued = 0;
-            auto issue_raw = [&](int sb) -> bool {
-                const int slot = sb % R;
-                if (!mbar_wait(&bars.raw_empty[slot], ((sb / R) & 1) ^ 1, err, ERR_GEMM_RAW_FULL, abort_flag))
-                    return false;
-                mbar_arrive_expect_tx(&bars.raw_full[slot], SW * C::RAW_ROW);
-                tma_load_2d(sm + C::OFF_RAW + slot * SW * C::RAW_ROW, &tmW, sb * C::BB, (int32_t)n0,
-                            &bars.raw_full[slot]);
-                raw_issued = sb + 1;
-                return true;
-            };
-            if constexpr (C::TMW) {
-                for (int sb = 0; sb < R - 1 && sb < nsb; ++sb)
-                    if (!issue_raw(sb)) break;
-            }
+            int st = 0;
             for (; st < nstages && !*abort_flag; ++st) {
-                const int s = st % S;
-                if ((st & 3) == 0) {
-                    const int sb = st >> 2;
-                    if constexpr (C::TMW) {
-                        if (sb + R - 1 < nsb && !issue_raw(sb + R - 1)) break;
-                    }
-                    if constexpr (C::MIN) {
-                        if (!mbar_wait(&bars.xmin_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_MIN, abort_flag))
-                            break;
-                        mbar_arrive_expect_tx(&bars.xmin_full[sb & 1], C::MIN_X);
-                        tma_load_2d(sm + C::OFF_XMIN + (sb & 1) * C::MIN_X, &tmXS, sb * 16, 0, &bars.xmin_full[sb & 1]);
-                        xs_issued = sb + 1;
-                    }
-                }
-                if (!mbar_wait(&bars.wx_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) break;
+                const int s = st % C::XS;
+                if (!mbar_wait(&bars.x_empty[s], ((st / C::XS) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY, abort_flag)) break;
                 mbar_arrive_expect_tx(&bars.x_full[s], C::XTILE);
                 tma_load_2d(sm + C::OFF_X + s * C::XTILE, &tmX, st * SBK, 0, &bars.x_full[s]);
             }
             if (*abort_flag) {   // leave no copy in flight
-                for (int i = st - 1; i >= 0 && i >= st - S; --i)
-                    mbar_wait(&bars.x_full[i % S], (i / S) & 1, err, ERR_GEMM_A_FULL, nullptr);
+                for (int i = st - 1; i >= 0 && i >= st - C::XS; --i)
+                    mbar_wait(&bars.x_full[i % C::XS], (i / C::XS) & 1, err, ERR_GEMM_A_FULL, nullptr);
+            }
+        }
+    } else if (warp == kSmWarpRaw) {
+        // ------------------------------------------------------------ TMA producer: raw weights, token d*S tiles
+        // (its own thread, so a slot that the unpackers have not yet handed back never holds up the
+        // token tiles)
+        if (lane == 0 && (C::TMW || C::MIN)) {
+            if constexpr (C::MIN) prefetch_tmap(&tmXS);
+            if constexpr (C::TMW) prefetch_tmap(&tmW);
+            int raw_issued = 0, xs_issued = 0;
+            for (int sb = 0; sb < nsb && !*abort_flag; ++sb) {
+                if constexpr (C::TMW) {
+                    const int slot = sb % R;
+                    if (!mbar_wait(&bars.raw_empty[slot], ((sb / R) & 1) ^ 1, err, ERR_GEMM_RAW_FULL, abort_flag)) break;
+                    mbar_arrive_expect_tx(&bars.raw_full[slot], SW * C::RAW_ROW);
+                    tma_load_2d(sm + C::OFF_RAW + slot * SW * C::RAW_ROW, &tmW, sb * C::BB, (int32_t)n0,
+                                &bars.raw_full[slot]);
+                    raw_issued = sb + 1;
+                }
+                if constexpr (C::MIN) {
+                    if (!mbar_wait(&bars.xmin_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_MIN, abort_flag)) break;
+                    mbar_arrive_expect_tx(&bars.xmin_full[sb & 1], C::MIN_X);
+                    tma_load_2d(sm + C::OFF_XMIN + (sb & 1) * C::MIN_X, &tmXS, sb * 16, 0, &bars.xmin_full[sb & 1]);
+                    xs_issued = sb + 1;
+                }
+            }
+            if (*abort_flag) {
                 for (int sb = xs_issued - 1; sb >= 0 && sb >= xs_issued - 2; --sb)
                     mbar_wait(&bars.xmin_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_MIN, nullptr);
                 for (int sb = raw_issued - 1; sb >= 0 && sb >= raw_issued - R; --sb)
@@ -276,7 +296,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const uint64_t x_desc0 = sw128_kmajor_desc(smem_u32(sm + C::OFF_X));
         const uint32_t wmin_base = smem_u32(sm + C::OFF_WMIN), xmin_base = smem_u32(sm + C::OFF_XMIN);
         auto wait_all = [&](uint64_t *bar, uint32_t ph, uint32_t code) {
-            return __all_sync(kAll, mbar_wait(bar, ph, err, code, abort_flag));
+            return __all_sync(kAll, mbar_wait_prompt(bar, ph, err, code, abort_flag));
         };
         // the min term of super-block x into its own TMEM columns, summed over the whole K:
         // (-dmin m_j) x (d_a S), both operands tf32 (hi, lo) pairs: hi*hi + lo*hi + hi*lo
@@ -294,15 +314,18 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             mma_commit_warp(&bars.info_empty[x & 1]);
             return true;
         };
+        const uint32_t w_full0 = smem_u32(bars.w_full), x_full0 = smem_u32(bars.x_full);
+        const uint32_t acc_empty0 = smem_u32(bars.acc_empty);
         bool ok = true;
         for (int st = 0; st < nstages && ok; ++st) {
-            const int s = st % S, gb = 2 * st;
-            const uint32_t ph = (st / S) & 1;
-            const int slot0 = gb % kSlots, slot1 = (gb + 1) % kSlots;
-            const uint32_t eph0 = ((gb / kSlots) & 1) ^ 1, eph1 = (((gb + 1) / kSlots) & 1) ^ 1;
-            if (!wait_all(&bars.w_full[s], ph, ERR_GEMM_B_FULL) || !wait_all(&bars.x_full[s], ph, ERR_GEMM_A_FULL) ||
-                !wait_all(&bars.acc_empty[slot0], eph0, ERR_GEMM_ACC_EMPTY) ||
-                !wait_all(&bars.acc_empty[slot1], eph1, ERR_GEMM_ACC_EMPTY)) {
+            const int s = st % S, e = st % kEnt, xs = st % C::XS;
+            const uint32_t ph = (st / S) & 1, eph = ((st / kEnt) & 1) ^ 1, xph = (st / C::XS) & 1;
+            // the stage's three conditions probed at once (their round trips overlap)
+            const bool ready = __all_sync(kAll, mbar_test_wait(w_full0 + 8u * s, ph) &
+                                                     mbar_test_wait(x_full0 + 8u * xs, xph) &
+                                                     mbar_test_wait(acc_empty0 + 8u * e, eph));
+            if (!ready && (!wait_all(&bars.w_full[s], ph, ERR_GEMM_B_FULL) || !wait_all(&bars.x_full[xs], xph, ERR_GEMM_A_FULL) ||
+                           !wait_all(&bars.acc_empty[e], eph, ERR_GEMM_ACC_EMPTY))) {
                 ok = false;
                 break;
             }
@@ -314,19 +337,20 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                 for (int i = 0; i < 8; ++i) f |= corr_flags[8 * s + i];
                 corr = f != 0;
             }
-            const uint64_t woff = (uint64_t)((s * kWTile) >> 4), xoff = (uint64_t)((s * C::XTILE) >> 4);
+            const uint64_t woff = (uint64_t)((s * kWTile) >> 4), xoff = (uint64_t)((xs * C::XTILE) >> 4);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint32_t d_tmem = tmem + (uint32_t)((h ? slot1 : slot0) * NT);
+                const uint32_t d_tmem = tmem + (uint32_t)((2 * e + h) * NT);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const uint64_t koff = (uint64_t)((2 * h + kk) * 2);
                     mma_f16_warp(d_tmem, w_desc0 + woff + koff, x_desc0 + xoff + koff, idesc, kk);
                     if (corr) mma_f16_warp(d_tmem, wc_desc0 + woff + koff, x_desc0 + xoff + koff, idesc, 1);
                 }
-                mma_commit_warp(&bars.acc_full[h ? slot1 : slot0]);
             }
+            mma_commit_warp(&bars.acc_full[e]);
             mma_commit_warp(&bars.wx_empty[s]);
+            mma_commit_warp(&bars.x_empty[xs]);
             if constexpr (C::MIN) {
                 // the previous super-block's min term, after this super-block's first stage
                 if ((st & 3) == 0 && st > 0 && !issue_min((st >> 2) - 1)) ok = false;
@@ -339,16 +363,16 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         // ------------------------------------------------------------ activation-scale stager
         float *da0 = reinterpret_cast<float *>(sm + C::OFF_DA);
         for (int sb = 0; sb < nsb; ++sb) {
-            if (!__all_sync(kAll, mbar_wait(&bars.da_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_DA, abort_flag)))
+            if (!__all_sync(kAll, mbar_wait(&bars.da_empty[sb % C::DAS], ((sb / C::DAS) & 1) ^ 1, err, ERR_GEMM_DA, abort_flag)))
                 break;
-            float *dst = da0 + (sb & 1) * 8 * NT;
+            float *dst = da0 + (sb % C::DAS) * 8 * NT;
 #pragma unroll
             for (int i = 0; i < 8 * NT / 32; ++i) {
                 const int idx = i * 32 + lane, j = idx / NT, t = idx % NT;
                 dst[idx] = t < M ? __ldg(p.d + (int64_t)(8 * sb + j) * M + t) : 0.0f;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.da_full[sb & 1]);
+            if (lane == 0) mbar_arrive(&bars.da_full[sb % C::DAS]);
         }
     } else if (warp >= kSmWarpUnpack0 && warp < kSmWarpEpi0) {
         // ------------------------------------------------------------ unpackers: two threads per row
@@ -384,6 +408,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             issued = R < nsb ? R : nsb;
         }
         uint32_t dirty = (1u << S) - 1;              // Q6_K correction chunks that may hold non-zero data
+        const uint32_t wx_empty0 = smem_u32(bars.wx_empty);
+        // the next round's slots probed one round ahead (a fresh barrier's parity-1 phase counts as complete)
+        bool wpre = __all_sync(kAll, mbar_test_wait(wx_empty0, 1) & mbar_test_wait(wx_empty0 + 8u, 1));
         int sb = 0;
         for (; sb < nsb; ++sb) {
             const int slot = sb % R;
@@ -396,6 +423,8 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             float d = 0.0f, dmin = 0.0f;
             int sc[16];
             int mn[8];
+            uint32_t se2[8], bigm = 0;                // Q6_K: this thread's scales as f16 pairs, big-scale mask
+            bool wbig = false;                        // Q6_K: some row of the warp has a big scale
             if constexpr (C::KQ) {
                 const uint4 hd = valid ? sm_lds128(blk_a) : make_uint4(0, 0, 0, 0);
                 d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xffff)));
@@ -425,6 +454,23 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) sc[i] = (int)(int8_t)((tail[i >> 2] >> (8 * (i & 3))) & 0xff);
                 d = __half2float(__ushort_as_half((unsigned short)(tail[4] & 0xffff)));
+                // the eight 16-value scales this thread applies, sc[8h + 4a + 2t + b] at index 4h + 2a + b,
+                // as f16 pairs; an odd |sc| > 64 (13 bits with q) keeps sc - 1 here and marks the
+                // correction tile, which then carries q
+                bigm = 0;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int a = 0; a < 2; ++a)
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int idx = 4 * hh + 2 * a + b;
+                            const int scv = valid ? (t ? sc[8 * hh + 4 * a + 2 + b] : sc[8 * hh + 4 * a + b]) : 0;
+                            const bool big = (scv > 64 || scv < -64) && (scv & 1);
+                            se2[idx] = sm_h2u(__float2half2_rn((float)(big ? (scv & ~1) : scv)));
+                            bigm |= (uint32_t)big << idx;
+                        }
+                wbig = __any_sync(kAll, bigm != 0);
             }
             // ---- per-row factors: d for the epilogue; the min tile row (-dmin m_j as tf32 hi | lo)
             if (!__all_sync(kAll, mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY,
@@ -449,16 +495,23 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.info_full[sb & 1]);
 
-            // ---- four 64-value stages; thread t writes the stage's 32-value block t (chunks 4t .. 4t+3)
+            // ---- four 64-value stages, two per round (one wait, fence and hand-off round per two
+            // stages); thread t writes each stage's 32-value block t (chunks 4t .. 4t+3)
             bool ok = true;
             uint32_t ql[8], qh[8];                    // Q6_K: this thread's low / high bits of the half
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int st = sb * 4 + q, s = st % S;
-                if (!__all_sync(kAll, mbar_wait(&bars.wx_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY,
-                                                abort_flag))) {
-                    ok = false;
-                    break;
+                if ((q & 1) == 0) {
+                    const int s1 = (st + 1) % S;
+                    if (!wpre &&
+                        (!__all_sync(kAll, mbar_wait(&bars.wx_empty[s], ((st / S) & 1) ^ 1, err, ERR_GEMM_AB_EMPTY,
+                                                     abort_flag)) ||
+                         !__all_sync(kAll, mbar_wait(&bars.wx_empty[s1], (((st + 1) / S) & 1) ^ 1, err,
+                                                     ERR_GEMM_AB_EMPTY, abort_flag)))) {
+                        ok = false;
+                        break;
+                    }
                 }
                 const uint32_t wtile = w_tile0 + s * kWTile;
                 if constexpr (C::KQ) {
@@ -515,19 +568,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                     }
                     const int nsh = (q & 1) ? 4 : 0;
                     const uint32_t hsh = (uint32_t)(4 * (q & 1) + 2 * t);
-                    bool need_corr = false;
                     const __half2 bias = __float2half2_rn(1056.0f);
                     const uint32_t wct = wc_tile0 + s * kWTile;
+                    // the correction chunks are written while the warp has big scales in this super-block,
+                    // and once more (zeros) after it, warp-uniformly
+                    const bool corr_w = wbig || ((dirty >> s) & 1);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        // values l = 8c .. 8c+7 of the group; scale sc[8h + 2g + (l >= 16)]
-                        const int si0 = 8 * h + 4 * (q & 1) + (c >> 1);
-                        const int scv = valid ? (t ? sc[si0 + 2] : sc[si0]) : 0;
-                        const bool big = (scv > 64 || scv < -64) && (scv & 1);
-                        const int se = big ? (scv & ~1) : scv;
-                        need_corr |= big;
-                        const __half2 s2 = __float2half2_rn((float)se);
-                        uint32_t o[4], oc[4];
+                        // values l = 8c .. 8c+7 of the group; scale index 4h + 2(q % 2) + (l >= 16)
+                        const int idx = 4 * h + 2 * (q & 1) + (c >> 1);
+                        const __half2 s2 = sm_u2h(se2[idx]);
+                        uint32_t o[4], tq[4];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const uint32_t lw = ql[2 * c + e], hw = qh[2 * c + e];
@@ -538,20 +589,33 @@ __global__ void __launch_bounds__(kSmThreads, 1)
                             const __half2 t1 = __hsub2(sm_u2h(b1), bias);
                             o[2 * e] = sm_h2u(__hmul2(t0, s2));
                             o[2 * e + 1] = sm_h2u(__hmul2(t1, s2));
-                            oc[2 * e] = big ? sm_h2u(t0) : 0u;
-                            oc[2 * e + 1] = big ? sm_h2u(t1) : 0u;
+                            tq[2 * e] = sm_h2u(t0);
+                            tq[2 * e + 1] = sm_h2u(t1);
                         }
                         sm_sts128(sm_sw128(wtile, r, 4 * t + c), make_uint4(o[0], o[1], o[2], o[3]));
-                        if (need_corr || ((dirty >> s) & 1))
-                            sm_sts128(sm_sw128(wct, r, 4 * t + c), make_uint4(oc[0], oc[1], oc[2], oc[3]));
+                        if (corr_w) {
+                            const bool big = (bigm >> idx) & 1u;
+                            sm_sts128(sm_sw128(wct, r, 4 * t + c),
+                                      big ? make_uint4(tq[0], tq[1], tq[2], tq[3]) : make_uint4(0, 0, 0, 0));
+                        }
                     }
-                    if (need_corr) dirty |= 1u << s; else dirty &= ~(1u << s);
-                    const bool any = __any_sync(kAll, need_corr);
-                    if (lane == 0) corr_flags[8 * s + uw] = any ? 1u : 0u;
+                    if (wbig) dirty |= 1u << s; else dirty &= ~(1u << s);
+                    if (lane == 0) corr_flags[8 * s + uw] = wbig ? 1u : 0u;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.w_full[s]);
+                if (q & 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bars.w_full[(st - 1) % S]);
+                        mbar_arrive(&bars.w_full[s]);
+                    }
+                    // the next round's two slots, probed ahead
+                    wpre = st + 2 < nstages &&
+                           __all_sync(kAll, mbar_test_wait(wx_empty0 + 8u * (uint32_t)((st + 1) % S),
+                                                           ((uint32_t)((st + 1) / S) & 1u) ^ 1u) &
+                                                mbar_test_wait(wx_empty0 + 8u * (uint32_t)((st + 2) % S),
+                                                               ((uint32_t)((st + 2) / S) & 1u) ^ 1u));
+                }
             }
             if (!ok) break;
             // every lane's reads of this raw slot are done before it is refilled
@@ -583,45 +647,79 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             acc[i] = make_float2(0.0f, 0.0f);
             part[i] = make_float2(0.0f, 0.0f);
         }
+        const uint32_t acc_full0 = smem_u32(bars.acc_full), da_full0 = smem_u32(bars.da_full);
+        auto probe_acc = [&](int st) {
+            return mbar_test_wait(acc_full0 + 8u * (uint32_t)(st % kEnt), (uint32_t)(st / kEnt) & 1u);
+        };
         bool ok = true;
+        bool pre = probe_acc(0), da_pre = mbar_test_wait(da_full0, 0);
         for (int sb = 0; sb < nsb && ok; ++sb) {
-            if (!mbar_wait(&bars.da_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_DA, abort_flag)) break;
-            const float4 *da_sb = reinterpret_cast<const float4 *>(da0 + (sb & 1) * 8 * NT);
+            if (!da_pre && !mbar_wait(&bars.da_full[sb % C::DAS], (sb / C::DAS) & 1, err, ERR_GEMM_DA, abort_flag)) break;
+            const float4 *da_sb = reinterpret_cast<const float4 *>(da0 + (sb % C::DAS) * 8 * NT);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int gb = sb * 8 + j, slot = gb % kSlots;
-                if (!mbar_wait(&bars.acc_full[slot], (gb / kSlots) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
+            for (int q = 0; q < 4; ++q) {
+                // one ring entry per stage: blocks 2q and 2q + 1 side by side, one wait and one release
+                const int st = sb * 4 + q, e = st % kEnt;
+                if (!pre && !mbar_wait(&bars.acc_full[e], (st / kEnt) & 1, err, ERR_GEMM_ACC_FULL, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t v[NT];
-                sm_tmem_ld<NT>(trow + (uint32_t)(slot * NT), v);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.acc_empty[slot]);
-                // part[t] (+)= I[t] d_a[t]: the tokens' scales of block j (same for every lane)
-#pragma unroll
-                for (int i4 = 0; i4 < NT / 4; ++i4) {
-                    const float4 da = da_sb[(j * NT) / 4 + i4];
-                    const float2 x0 = make_float2(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]));
-                    const float2 x1 = make_float2(__uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3]));
-                    if (j == 0) {
-                        part[2 * i4] = __fmul2_rn(x0, make_float2(da.x, da.y));
-                        part[2 * i4 + 1] = __fmul2_rn(x1, make_float2(da.z, da.w));
-                    } else {
-                        part[2 * i4] = __ffma2_rn(x0, make_float2(da.x, da.y), part[2 * i4]);
-                        part[2 * i4 + 1] = __ffma2_rn(x1, make_float2(da.z, da.w), part[2 * i4 + 1]);
-                    }
+                // NT = 16: both blocks in one 32-column load; NT = 32: one block at a time (fewer
+                // live registers), the entry released after the second load
+                uint32_t v[32];
+                if constexpr (NT == 16) {
+                    tmem_ld32(trow + (uint32_t)(2 * e * NT), v);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.acc_empty[e]);
                 }
-                if constexpr (DUMP) {
-                    if (n >= dump.n0 && n < dump.n0 + dump.n_cnt && n < N) {
+                auto probe_next = [&]() {
+                    // the next probes go out ahead of the FMAs
+                    pre = st + 1 < nstages ? probe_acc(st + 1) : true;
+                    if (q == 3)
+                        da_pre = sb + 1 < nsb && mbar_test_wait(da_full0 + 8u * (uint32_t)((sb + 1) % C::DAS),
+                                                                (uint32_t)((sb + 1) / C::DAS) & 1u);
+                };
+                if constexpr (NT == 16) probe_next();
 #pragma unroll
-                        for (int tt = 0; tt < NT; ++tt) {
-                            if (tt >= dump.m0 && tt < dump.m0 + dump.m_cnt && tt < M)
-                                dump.out[((tt - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32 + gb] =
-                                    __float2int_rn(__uint_as_float(v[tt]));
+                for (int h = 0; h < 2; ++h) {
+                    const int j = 2 * q + h, gb = sb * 8 + j;
+                    if constexpr (NT == 32) {
+                        tmem_ld32(trow + (uint32_t)((2 * e + h) * NT), v);
+                        tmem_ld_wait();
+                        if (h == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars.acc_empty[e]);
+                            probe_next();
+                        }
+                    }
+                    const int vo = NT == 16 ? h * NT : 0;      // this block's first column in v
+                    // part[t] (+)= I[t] d_a[t]: the tokens' scales of block j (same for every lane)
+#pragma unroll
+                    for (int i4 = 0; i4 < NT / 4; ++i4) {
+                        const float4 da = da_sb[(j * NT) / 4 + i4];
+                        const float2 x0 = make_float2(__uint_as_float(v[vo + 4 * i4]), __uint_as_float(v[vo + 4 * i4 + 1]));
+                        const float2 x1 =
+                            make_float2(__uint_as_float(v[vo + 4 * i4 + 2]), __uint_as_float(v[vo + 4 * i4 + 3]));
+                        if (j == 0) {
+                            part[2 * i4] = __fmul2_rn(x0, make_float2(da.x, da.y));
+                            part[2 * i4 + 1] = __fmul2_rn(x1, make_float2(da.z, da.w));
+                        } else {
+                            part[2 * i4] = __ffma2_rn(x0, make_float2(da.x, da.y), part[2 * i4]);
+                            part[2 * i4 + 1] = __ffma2_rn(x1, make_float2(da.z, da.w), part[2 * i4 + 1]);
+                        }
+                    }
+                    if constexpr (DUMP) {
+                        if (n >= dump.n0 && n < dump.n0 + dump.n_cnt && n < N) {
+#pragma unroll
+                            for (int tt = 0; tt < NT; ++tt) {
+                                if (tt >= dump.m0 && tt < dump.m0 + dump.m_cnt && tt < M)
+                                    dump.out[((tt - dump.m0) * dump.n_cnt + (n - dump.n0)) * nblk32 + gb] =
+                                        __float2int_rn(__uint_as_float(v[vo + tt]));
+                            }
                         }
                     }
                 }
@@ -636,7 +734,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bars.info_empty[sb & 1]);
-                mbar_arrive(&bars.da_empty[sb & 1]);
+                mbar_arrive(&bars.da_empty[sb % C::DAS]);
             }
         }
         if (ok && !*abort_flag) {
