@@ -408,6 +408,56 @@ class DecodeSweep:
                     join.record(self.side[i])
                     main.wait_event(join)
 
+    def _gemv_group(self, group):
+        if len(group) == 1:
+            fmt, w, x, plane, y, n, k = group[0]
+            self.B.GEMV[fmt](w, n, k, plane, 1, y)
+        else:
+            self.B.GEMV_GROUPED[group[0][0]]([(w, n, plane, y) for (_, w, _, plane, y, n, _) in group], group[0][6], 1)
+
+    def run_grouped(self, quantize=True):
+        """The sweep with one launch per layer level and weight format: q|k|v from the layer input (one
+        grouped quantize; one grouped Q4_K GEMV, and in the Q6_K layers v's GEMV on a parallel branch),
+        then o, gate|up (grouped quantize and GEMV), down -- the dependency order of a real layer."""
+        t, B = self.torch, self.B
+        main = t.cuda.current_stream()
+        if not hasattr(self, "side"):
+            self.side = [t.cuda.Stream(), t.cuda.Stream()]
+        for layer in range(len(self.items) // 7):
+            li = self.items[7 * layer:7 * layer + 7]           # q, k, v, o, gate, up, down
+            for group in (li[0:3], li[3:4], li[4:6], li[6:7]):
+                if quantize:
+                    B.mq_quantize_q8_grouped([(it[2], it[3]) for it in group], 1, group[0][6], B.PLANE_FOR_GEMV)
+                by_fmt = {}
+                for it in group:
+                    by_fmt.setdefault(it[0], []).append(it)
+                if len(by_fmt) == 1:
+                    self._gemv_group(group)
+                    continue
+                fork = t.cuda.Event()
+                fork.record(main)
+                self.side[0].wait_event(fork)
+                with t.cuda.stream(self.side[0]):
+                    self._gemv_group(by_fmt["q6k"])
+                self._gemv_group(by_fmt["q4k"])
+                join = t.cuda.Event()
+                join.record(self.side[0])
+                main.wait_event(join)
+
+    def capture_grouped(self, quantize=True):
+        t = self.torch
+        s = t.cuda.Stream()
+        s.wait_stream(t.cuda.current_stream())
+        with t.cuda.stream(s):
+            self.run_grouped(True)
+        t.cuda.current_stream().wait_stream(s)
+        t.cuda.synchronize()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g):
+            self.run_grouped(quantize)
+        t.cuda.synchronize()
+        return g
+
     def capture(self, quantize=True, branches=False):
         """One CUDA graph of the sweep: Q8 quantize + GEMV per matmul, or the GEMVs alone
         (on the planes the last quantizing run left)."""
@@ -637,13 +687,14 @@ def main():
     if not args.skip_decode:
         lm_w = torch.from_numpy(I.lm_head_weights().reshape(I.VOCAB, -1)).cuda()
         lm = {}
-        for m, paths in ((1, ("gemv",)), (16, ("gemv", "gemm")), (I.PREFILL_TOKENS, ("gemm",))):
+        for m, paths in ((1, ("gemv",)), (4, ("gemv", "small")), (16, ("gemv", "gemm", "small")),
+                         (32, ("small",)), (I.PREFILL_TOKENS, ("gemm",))):
             x = torch.from_numpy(I.lm_head_x(m)).cuda()
             plane = B.alloc_plane(m, I.HIDDEN)
             B.mq_quantize_q8(x, m, I.HIDDEN, None, 0.0, plane)
             y = torch.empty((m, I.VOCAB), dtype=torch.float32, device="cuda")
             for path in paths:
-                f = (B.GEMV if path == "gemv" else B.GEMM)["q6k"]
+                f = {"gemv": B.GEMV, "gemm": B.GEMM, "small": B.GEMM_SMALL}[path]["q6k"]
                 reps = max(5, K) if m < 1000 else 3            # M = 3314 writes a 2 GB output per launch
                 ms = time_events(torch, lambda: f(lm_w, I.VOCAB, I.HIDDEN, plane, m, y), reps, min(W, 3))
                 gbs = (lm_w.numel() + B.mq_q8_plane_bytes(m, I.HIDDEN) + 4 * m * I.VOCAB) / (ms * 1e-3) / 1e9
@@ -683,22 +734,38 @@ def main():
         ms_gemv = time_events(torch, sw.capture(False).replay, max(5, K), W)
         ms_br = time_events(torch, sw.capture(True, True).replay, max(5, K), W)
         ms_br_gemv = time_events(torch, sw.capture(False, True).replay, max(5, K), W)
+        ms_gr = time_events(torch, sw.capture_grouped(True).replay, max(5, K), W)
+        ms_gr_gemv = time_events(torch, sw.capture_grouped(False).replay, max(5, K), W)
+        # the grouped sweep computes what the per-matrix one does, bit for bit
+        outs = [it[4].clone() for it in sw.items]
+        for it in sw.items:
+            it[4].fill_(float("nan"))
+        sw.run(True)
+        torch.cuda.synchronize()
+        if not all(torch.equal(a, it[4]) for a, it in zip(outs, sw.items)):
+            raise RuntimeError("grouped decode sweep differs from the per-matrix sweep")
         B.mq_device_status()
         gemv_bytes = sw.bytes - 4 * sum(k for *_, k in sw.items)          # without the f32 activations
         lm_ms = lm["m1_gemv"]["ms"]
+        n_layers = len(sw.items) // 7
+        gr_launches = 4 * n_layers + 4 * n_layers + (n_layers + 1) // 2      # quantize + GEMV per level (+ v)
         line["decode"] = {"workload": "7B decode sweep: 28 layers x 7 matmuls, M=1, Q8 quantize + GEMV each, one CUDA graph; "
-                                      "each layer's independent matmuls (q|k|v from the layer input, gate|up from the "
-                                      "post-attention input) on parallel branches, joined before o and before down",
-                          "ms_per_token": ms_br, "tok_per_s": 1e3 / ms_br, "weight_bytes": sw.weight_bytes,
-                          "GB/s": sw.bytes / (ms_br * 1e-3) / 1e9,
-                          "frac_of_hbm": sw.bytes / (ms_br * 1e-3) / 1e9 / hbm_peak,
-                          "launches_per_token": 2 * len(sw.items),
-                          "serial": {"what": "the same 392 launches as one linear chain",
-                                     "ms_per_token": ms, "GB/s": sw.bytes / (ms * 1e-3) / 1e9},
-                          "gemv_only": {"what": "the 196 GEMVs alone (planes already quantized), branched graph",
-                                        "ms_per_token": ms_br_gemv, "GB/s": gemv_bytes / (ms_br_gemv * 1e-3) / 1e9,
-                                        "serial_ms_per_token": ms_gemv,
-                                        "tok_per_s_with_lm_head": 1e3 / (ms_br_gemv + lm_ms)}}
+                                      "one grouped launch per layer level and format (q|k|v from the layer input, o, "
+                                      "gate|up from the post-attention input, down), v's Q6_K GEMV on a parallel branch",
+                          "ms_per_token": ms_gr, "tok_per_s": 1e3 / ms_gr, "weight_bytes": sw.weight_bytes,
+                          "GB/s": sw.bytes / (ms_gr * 1e-3) / 1e9,
+                          "frac_of_hbm": sw.bytes / (ms_gr * 1e-3) / 1e9 / hbm_peak,
+                          "launches_per_token": gr_launches,
+                          "gemv_only": {"what": "the grouped GEMVs alone (planes already quantized)",
+                                        "ms_per_token": ms_gr_gemv, "GB/s": gemv_bytes / (ms_gr_gemv * 1e-3) / 1e9,
+                                        "tok_per_s_with_lm_head": 1e3 / (ms_gr_gemv + lm_ms)},
+                          "per_matrix": {"what": "one quantize + one GEMV launch per matmul (392 launches), "
+                                                 "q|k|v and gate|up on parallel branches",
+                                         "ms_per_token": ms_br, "GB/s": sw.bytes / (ms_br * 1e-3) / 1e9,
+                                         "gemv_only_ms_per_token": ms_br_gemv},
+                          "serial": {"what": "the 392 per-matrix launches as one linear chain",
+                                     "ms_per_token": ms, "GB/s": sw.bytes / (ms * 1e-3) / 1e9,
+                                     "gemv_only_ms_per_token": ms_gemv}}
 
     # ---------------- CPU baseline (oracle on the host cores, rank 0 only)
     if dist.rank == 0 and dist.world == 1:

@@ -257,6 +257,53 @@ MQ_API int mq_gemm_q5k(const void *w, int64_t N, int64_t K, const void *plane, i
                 float *y, mq_stream_t stream);
 
 /*
+ * mq_gemv_grouped_q4k / _q5k / _q6k -- several independent decode GEMVs of one format in one launch:
+ * the matrices of one level of a decoder layer (q|k|v from the layer input, gate|up from the
+ * post-attention input) share the launch's fixed cost instead of paying it each ("Features >
+ * GPU -- CUDA": decode streams the weights with the MMVQ kernel; a layer's independent matmuls
+ * have no order between them).
+ *
+ *   jobs     HOST array of n_jobs descriptors {w, N, plane, y}, read during the call and not
+ *            retained: each job is exactly the arguments of one mq_gemv_q4k / _q5k / _q6k call
+ *   n_jobs   0 .. 8 (0: nothing to do)
+ *   K, M     shared by every job: the reduction length and the tokens of every plane
+ *
+ * Each job's y is what the single call would write, bit for bit.  Errors: as the single call for
+ * each job, plus MQ_ERR_ARG for n_jobs outside 0 .. 8, a NULL table, or an output that overlaps any
+ * input or other output of the call.
+ */
+typedef struct {
+    const void *w;       /* raw weight blocks [N][K/256], 16-byte aligned (device) */
+    int64_t N;           /* rows of this job's weight matrix */
+    const void *plane;   /* Q8 plane of the job's M x K activation (device, 256-byte aligned) */
+    float *y;            /* f32 [M][N] output (device) */
+} mq_gemv_job;
+
+MQ_API int mq_gemv_grouped_q4k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream);
+MQ_API int mq_gemv_grouped_q5k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream);
+MQ_API int mq_gemv_grouped_q6k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream);
+
+/*
+ * mq_quantize_q8_grouped -- the plain mq_quantize_q8_ex over several independent activations of one
+ * shape [M][K] in one launch (the inputs of one level of a decoder layer in the decode sweep).
+ *
+ *   jobs      HOST array of n_jobs descriptors {x, plane} (read during the call, not retained):
+ *             x f32 [M][K] 16-byte aligned, plane 256-byte aligned (device pointers)
+ *   n_jobs    0 .. 8; sections a non-empty MQ_PLANE_* mask as for mq_quantize_q8_ex
+ *
+ * Every plane holds exactly what mq_quantize_q8_ex writes for its x.  Errors: as mq_quantize_q8_ex,
+ * plus MQ_ERR_ARG for n_jobs outside 0 .. 8, a NULL table or pointer, or a plane overlapping any x
+ * or other plane.
+ */
+typedef struct {
+    const float *x;      /* f32 [M][K] activation (device) */
+    void *plane;         /* its Q8 plane (device) */
+} mq_quantize_job;
+
+MQ_API int mq_quantize_q8_grouped(const mq_quantize_job *jobs, int n_jobs, int64_t M, int64_t K, unsigned sections,
+                                  mq_stream_t stream);
+
+/*
  * mq_gemv_q4_0 / _q4_1 / _q5_0 / _q5_1 / _q8_0 -- decode GEMV over the 32-value GGML block
  * formats ("Architecture > 6. Quantization & Tensor Layout": the weight blocks are the GGML
  * structs; "Support Matrix > CUDA notes": decode runs the dp4a MMVQ kernels).  Same

@@ -34,6 +34,14 @@ class PlaneLayout(ctypes.Structure):
                 ("off_s", ctypes.c_size_t), ("off_ds", ctypes.c_size_t), ("total_bytes", ctypes.c_size_t)]
 
 
+class GemvJob(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("N", ctypes.c_int64), ("plane", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class QuantizeJob(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("plane", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -67,6 +75,9 @@ def lib():
                      "mq_gemm_small_q4k", "mq_gemm_small_q5k", "mq_gemm_small_q6k"):
             getattr(L, name).argtypes = [P, I64, I64, P, I64, P, P]
         L.mq_gemm_q4k_swiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
+        for name in ("mq_gemv_grouped_q4k", "mq_gemv_grouped_q5k", "mq_gemv_grouped_q6k"):
+            getattr(L, name).argtypes = [ctypes.POINTER(GemvJob), I32, I64, I64, P]
+        L.mq_quantize_q8_grouped.argtypes = [ctypes.POINTER(QuantizeJob), I32, I64, I64, ctypes.c_uint, P]
         L.mq_device_status.argtypes = [P]
         L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
         L.mq_debug_forced_timeout.argtypes = [U32, P]
@@ -226,6 +237,30 @@ def mq_gemm_q8_0(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemm_q8_0", w, N, K, plane, M, y, stream)
 
 
+def _gemv_grouped(name, jobs, K, M, stream):
+    arr = (GemvJob * max(1, len(jobs)))(*[GemvJob(_ptr(w), N, _ptr(p), _ptr(y)) for (w, N, p, y) in jobs])
+    return _check(getattr(lib(), name)(arr, len(jobs), K, M, _stream(stream)))
+
+
+def mq_gemv_grouped_q4k(jobs, K: int, M: int, stream=None):
+    """jobs: a list of (w, N, plane, y); one launch for all of them."""
+    return _gemv_grouped("mq_gemv_grouped_q4k", jobs, K, M, stream)
+
+
+def mq_gemv_grouped_q5k(jobs, K: int, M: int, stream=None):
+    return _gemv_grouped("mq_gemv_grouped_q5k", jobs, K, M, stream)
+
+
+def mq_gemv_grouped_q6k(jobs, K: int, M: int, stream=None):
+    return _gemv_grouped("mq_gemv_grouped_q6k", jobs, K, M, stream)
+
+
+def mq_quantize_q8_grouped(jobs, M: int, K: int, sections: int, stream=None):
+    """jobs: a list of (x, plane); the plain quantizer over all of them in one launch."""
+    arr = (QuantizeJob * max(1, len(jobs)))(*[QuantizeJob(_ptr(x), _ptr(p)) for (x, p) in jobs])
+    return _check(lib().mq_quantize_q8_grouped(arr, len(jobs), M, K, sections, _stream(stream)))
+
+
 def mq_gemm_small_q4k(w, N: int, K: int, plane, M: int, y, stream=None):
     return _matmul("mq_gemm_small_q4k", w, N, K, plane, M, y, stream)
 
@@ -263,6 +298,7 @@ GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k, "q4_0": mq_g
         "q5_0": mq_gemm_q5_0, "q5_1": mq_gemm_q5_1, "q8_0": mq_gemm_q8_0}
 GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k, "q4_0": mq_gemv_q4_0, "q4_1": mq_gemv_q4_1,
         "q5_0": mq_gemv_q5_0, "q5_1": mq_gemv_q5_1, "q8_0": mq_gemv_q8_0}
+GEMV_GROUPED = {"q4k": mq_gemv_grouped_q4k, "q5k": mq_gemv_grouped_q5k, "q6k": mq_gemv_grouped_q6k}
 # the small-M band (1 <= M <= 32) on the tensor cores, k-quant weights
 GEMM_SMALL = {"q4k": mq_gemm_small_q4k, "q5k": mq_gemm_small_q5k, "q6k": mq_gemm_small_q6k}
 SMALL_MAX_M = 32

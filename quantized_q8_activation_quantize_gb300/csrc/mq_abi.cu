@@ -398,6 +398,87 @@ int mq_gemm_q8_0(const void *w, int64_t N, int64_t K, const void *plane, int64_t
     return run_matmul(15, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);
 }
 
+// the grouped GEMV: every job validated as a GEMV call, and no output may overlap any input or
+// other output of the call
+static int run_gemv_grouped(const char *fn, Fmt fmt, const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M,
+                            mq_stream_t stream) {
+    if (n_jobs < 0 || n_jobs > 8) return set_error(MQ_ERR_ARG, "%s: n_jobs=%d not in 0 .. 8", fn, n_jobs);
+    if (n_jobs == 0) return MQ_OK;
+    if (jobs == nullptr) return set_error(MQ_ERR_ARG, "%s: NULL job table", fn);
+    const uint8_t *w[8];
+    int64_t N[8];
+    Plane p[8];
+    float *y[8];
+    int nj = 0;
+    const size_t pb = mq_q8_plane_bytes(M, K);
+    for (int i = 0; i < n_jobs; ++i) {
+        int rc = check_matmul(fn, KIND_GEMV, block_bytes(fmt), jobs[i].w, jobs[i].N, K, jobs[i].plane, M, jobs[i].y);
+        if (rc != MQ_OK) return rc;
+        if (M == 0) return MQ_OK;
+        const size_t yb = (size_t)M * (size_t)jobs[i].N * 4;
+        for (int k = 0; k < n_jobs; ++k) {
+            if (k == i || jobs[k].N == 0) continue;
+            const size_t wb = (size_t)jobs[k].N * (size_t)(K / kQK) * (size_t)block_bytes(fmt);
+            if (overlaps(jobs[i].y, yb, jobs[k].w, wb) || overlaps(jobs[i].y, yb, jobs[k].plane, pb) ||
+                overlaps(jobs[i].y, yb, jobs[k].y, (size_t)M * (size_t)jobs[k].N * 4))
+                return set_error(MQ_ERR_ARG, "%s: output of job %d overlaps an input or output of job %d", fn, i, k);
+        }
+        if (jobs[i].N == 0) continue;                 // an empty job launches nothing
+        w[nj] = static_cast<const uint8_t *>(jobs[i].w);
+        N[nj] = jobs[i].N;
+        plane_from(const_cast<void *>(jobs[i].plane), M, K, &p[nj]);
+        y[nj] = jobs[i].y;
+        ++nj;
+    }
+    if (nj == 0) return MQ_OK;
+    unsigned int *err = nullptr;
+    int rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    return launch_gemv_grouped(fmt, nj, w, N, p, y, K, M, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mq_gemv_grouped_q4k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream) {
+    return run_gemv_grouped("mq_gemv_grouped_q4k", FMT_Q4K, jobs, n_jobs, K, M, stream);
+}
+int mq_gemv_grouped_q5k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream) {
+    return run_gemv_grouped("mq_gemv_grouped_q5k", FMT_Q5K, jobs, n_jobs, K, M, stream);
+}
+int mq_gemv_grouped_q6k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream) {
+    return run_gemv_grouped("mq_gemv_grouped_q6k", FMT_Q6K, jobs, n_jobs, K, M, stream);
+}
+
+int mq_quantize_q8_grouped(const mq_quantize_job *jobs, int n_jobs, int64_t M, int64_t K, unsigned sections,
+                           mq_stream_t stream) {
+    const char *fn = "mq_quantize_q8_grouped";
+    if (n_jobs < 0 || n_jobs > 8) return set_error(MQ_ERR_ARG, "%s: n_jobs=%d not in 0 .. 8", fn, n_jobs);
+    if (sections == 0 || sections > MQ_PLANE_ALL)
+        return set_error(MQ_ERR_ARG, "%s: sections=0x%x not a non-empty MQ_PLANE_* mask", fn, sections);
+    if (M < 0) return set_error(MQ_ERR_ARG, "%s: negative M=%lld", fn, (long long)M);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    if (M >= kMaxDim) return set_error(MQ_ERR_SHAPE, "%s: M=%lld must be below 2^31", fn, (long long)M);
+    if (n_jobs == 0 || M == 0) return MQ_OK;
+    if (jobs == nullptr) return set_error(MQ_ERR_ARG, "%s: NULL job table", fn);
+    const size_t pb = mq_q8_plane_bytes(M, K), xb = (size_t)M * (size_t)K * 4;
+    const float *x[8];
+    Plane p[8];
+    for (int i = 0; i < n_jobs; ++i) {
+        if (!jobs[i].x || !jobs[i].plane)
+            return set_error(MQ_ERR_ARG, "%s: NULL pointer in job %d", fn, i);
+        if (!aligned(jobs[i].x, 16) || !aligned(jobs[i].plane, 256))
+            return set_error(MQ_ERR_ALIGN, "%s: job %d: x needs 16-byte, the plane 256-byte alignment", fn, i);
+        for (int k = 0; k < n_jobs; ++k)
+            if (overlaps(jobs[i].plane, pb, jobs[k].x, xb) || (k != i && overlaps(jobs[i].plane, pb, jobs[k].plane, pb)))
+                return set_error(MQ_ERR_ARG, "%s: the plane of job %d overlaps an input or plane of job %d", fn, i, k);
+        x[i] = jobs[i].x;
+        plane_from(jobs[i].plane, M, K, &p[i]);
+    }
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    return launch_quantize_grouped(n_jobs, x, p, M, K, sections, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mq_gemm_small_q4k(const void *w, int64_t N, int64_t K, const void *plane, int64_t M, float *y,
                       mq_stream_t stream) {
     return run_matmul(16, w, N, K, plane, M, y, Dump{nullptr, 0, 0, 0, 0}, stream);

@@ -148,6 +148,18 @@ struct GvArgs {
     unsigned int *err;
 };
 
+// A grouped launch: up to kMaxJobs independent matrices of the same format and K, each with its own
+// plane and output, in one grid; job j takes CTAs [cta0[j], cta0[j + 1]).  A plain launch is one job.
+constexpr int kMaxJobs = 8;
+struct GvJobs {
+    int n;
+    int cta0[kMaxJobs + 1];
+    const uint8_t *w[kMaxJobs];
+    int64_t N[kMaxJobs];
+    Plane p[kMaxJobs];
+    float *y[kMaxJobs];
+};
+
 // shared-memory addresses of the staged activations (ACT kernels): codes [MT][K], table
 struct GvAct {
     uint32_t codes;              // token 0's records
@@ -518,8 +530,25 @@ __device__ __forceinline__ void release_stage(uint64_t *bar, int lane) {
 }
 
 template <int FMT, int MT, bool ACT, bool DUMP>
-__global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(MT)) gemv_kernel(GvArgs a) {
+__global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(MT))
+    gemv_kernel(GvArgs a0, const __grid_constant__ GvJobs jobs) {
     using C = GvCfg<FMT>;
+    // this CTA's matrix: the launch's own (a0), or in a grouped launch its job's (selected with
+    // compile-time indices, so the job table stays in parameter space)
+    GvArgs a = a0;
+    int cta = blockIdx.x, ncta = gridDim.x;
+    if (jobs.n > 1) {
+#pragma unroll
+        for (int i = 0; i < kMaxJobs; ++i)
+            if (i < jobs.n && (int)blockIdx.x >= jobs.cta0[i] && (int)blockIdx.x < jobs.cta0[i + 1]) {
+                a.w = jobs.w[i];
+                a.N = jobs.N[i];
+                a.p = jobs.p[i];
+                a.y = jobs.y[i];
+                cta = blockIdx.x - jobs.cta0[i];
+                ncta = jobs.cta0[i + 1] - jobs.cta0[i];
+            }
+    }
     const int S = a.nst;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[C::STAGES], empty[C::STAGES], pfull[kPartBufs], pempty[kPartBufs];
@@ -539,7 +568,7 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
 
     // this CTA's rows [row_begin, row_end) and their flat super-block range
     const uint32_t nb = (uint32_t)(a.K / kQK);
-    const int64_t row_begin = a.N * blockIdx.x / gridDim.x, row_end = a.N * (blockIdx.x + 1) / gridDim.x;
+    const int64_t row_begin = a.N * cta / ncta, row_end = a.N * (cta + 1) / ncta;
     const int64_t sb_begin = row_begin * nb, sb_total = (row_end - row_begin) * nb;
     const int units = (int)((sb_total + C::TU - 1) / C::TU);
     const float inv_nb = 1.0f / (float)nb;
@@ -781,7 +810,45 @@ int launch_one(GvArgs a, int nsm, cudaStream_t stream) {
     const int64_t units = (a.N * (a.K / kQK) + C::TU - 1) / C::TU;
     if (ctas > units) ctas = units;
     if (ctas > a.N) ctas = a.N;                      // every CTA owns at least one row
-    return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a), "gemv launch");
+    GvJobs none;
+    none.n = 1;
+    return cuda_error(launch_pdl(kern, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a, none), "gemv launch");
+}
+
+// A grouped launch of jobs.n matrices (same format, K and tokens): one wave of CTAs, shared by the
+// jobs in proportion to their weight bytes (at least one CTA each, at most one per unit or row).
+template <int FMT, int MT, bool ACT>
+int launch_group(GvArgs a, GvJobs jobs, int nsm, cudaStream_t stream) {
+    using C = GvCfg<FMT>;
+    auto kern = gemv_kernel<FMT, MT, ACT, false>;
+    int budget = kSmemMax;
+    for (int n = C::ctas_per_sm(MT); n >= 2; --n)
+        if (gemv_smem<FMT, MT, ACT>(2, a.K) <= per_cta_smem(n)) { budget = per_cta_smem(n); break; }
+    a.nst = C::STAGES;
+    while (a.nst > 2 && gemv_smem<FMT, MT, ACT>(a.nst, a.K) > budget) --a.nst;
+    const int smem = (int)gemv_smem<FMT, MT, ACT>(a.nst, a.K);
+    constexpr int slot = 16 + FMT * 16 + (ACT ? 8 : 0) + (MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3) * 2;
+    int rc = ensure_smem_attr(reinterpret_cast<const void *>(kern), ACT ? kSmemMax : smem, slot);
+    if (rc != MQ_OK) return rc;
+    int per_sm = 0;
+    rc = resident_ctas(reinterpret_cast<const void *>(kern), C::THREADS, smem, slot, &per_sm);
+    if (rc != MQ_OK) return rc;
+    const int64_t wave = (int64_t)nsm * per_sm;
+    const int64_t nb = a.K / kQK;
+    int64_t total = 0;
+    for (int i = 0; i < jobs.n; ++i) total += jobs.N[i] * nb;
+    int c = 0;
+    for (int i = 0; i < jobs.n; ++i) {
+        jobs.cta0[i] = c;
+        int64_t n = (wave * jobs.N[i] * nb + total - 1) / total;
+        const int64_t units = (jobs.N[i] * nb + C::TU - 1) / C::TU;
+        if (n > units) n = units;
+        if (n > jobs.N[i]) n = jobs.N[i];
+        if (n < 1) n = 1;
+        c += (int)n;
+    }
+    jobs.cta0[jobs.n] = c;
+    return cuda_error(launch_pdl(kern, dim3((unsigned)c), dim3(C::THREADS), smem, stream, a, jobs), "gemv launch");
 }
 
 template <int FMT, int MT, bool DUMP>
@@ -805,6 +872,30 @@ int launch_fmt(GvArgs a, int nsm, cudaStream_t stream) {
             rc = launch_mt<FMT, 4, DUMP>(a, nsm, stream);
         else
             rc = launch_mt<FMT, 8, DUMP>(a, nsm, stream);
+        if (rc != MQ_OK) return rc;
+    }
+    return MQ_OK;
+}
+
+template <int FMT>
+int launch_group_fmt(GvArgs a, const GvJobs &jobs, int nsm, cudaStream_t stream) {
+    constexpr int G = GvCfg<FMT>::MAX_MT;
+    for (int64_t t0 = 0; t0 < a.M; t0 += G) {
+        a.t0 = t0;
+        a.mt = (int)((a.M - t0) < G ? (a.M - t0) : G);
+        int rc;
+        const bool act = gemv_smem<FMT, 8, true>(2, a.K) <= kSmemMax;
+        if (a.mt == 1)
+            rc = gemv_smem<FMT, 1, true>(2, a.K) <= kSmemMax ? launch_group<FMT, 1, true>(a, jobs, nsm, stream)
+                                                             : launch_group<FMT, 1, false>(a, jobs, nsm, stream);
+        else if (a.mt == 2)
+            rc = gemv_smem<FMT, 2, true>(2, a.K) <= kSmemMax ? launch_group<FMT, 2, true>(a, jobs, nsm, stream)
+                                                             : launch_group<FMT, 2, false>(a, jobs, nsm, stream);
+        else if (a.mt <= 4)
+            rc = gemv_smem<FMT, 4, true>(2, a.K) <= kSmemMax ? launch_group<FMT, 4, true>(a, jobs, nsm, stream)
+                                                             : launch_group<FMT, 4, false>(a, jobs, nsm, stream);
+        else
+            rc = act ? launch_group<FMT, 8, true>(a, jobs, nsm, stream) : launch_group<FMT, 8, false>(a, jobs, nsm, stream);
         if (rc != MQ_OK) return rc;
     }
     return MQ_OK;

@@ -1,5 +1,7 @@
 // mq_gemv_kq.cu -- the decode GEMV entry point and its k-quant instantiations (Q4_K, Q5_K,
 // Q6_K); the 32-value formats are instantiated in mq_gemv_b32.cu.
+#include <cstring>
+
 #include "mq_gemv.cuh"
 
 namespace mq {
@@ -15,6 +17,26 @@ int launch_gemv(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
     if (fmt == FMT_Q5K)
         return dmp ? launch_fmt<FMT_Q5K, true>(a, nsm, stream) : launch_fmt<FMT_Q5K, false>(a, nsm, stream);
     return dmp ? launch_fmt<FMT_Q6K, true>(a, nsm, stream) : launch_fmt<FMT_Q6K, false>(a, nsm, stream);
+}
+
+int launch_gemv_grouped(Fmt fmt, int nj, const uint8_t *const *w, const int64_t *N, const Plane *p, float *const *y,
+                        int64_t K, int64_t M, unsigned int *err, cudaStream_t stream) {
+    if (nj < 1 || nj > kMaxJobs) return set_error(MQ_ERR_ARG, "grouped GEMV: %d jobs (1 .. %d)", nj, kMaxJobs);
+    const int nsm = sm_count();
+    GvJobs jobs;
+    memset(&jobs, 0, sizeof jobs);
+    jobs.n = nj;
+    for (int i = 0; i < nj; ++i) {
+        jobs.w[i] = w[i];
+        jobs.N[i] = N[i];
+        jobs.p[i] = p[i];
+        jobs.y[i] = y[i];
+    }
+    GvArgs a{w[0], N[0], K, p[0], M, 0, 0, 0, y[0], Dump{nullptr, 0, 0, 0, 0}, err};
+    if (fmt == FMT_Q4K) return launch_group_fmt<FMT_Q4K>(a, jobs, nsm, stream);
+    if (fmt == FMT_Q5K) return launch_group_fmt<FMT_Q5K>(a, jobs, nsm, stream);
+    if (fmt == FMT_Q6K) return launch_group_fmt<FMT_Q6K>(a, jobs, nsm, stream);
+    return set_error(MQ_ERR_ARG, "grouped GEMV: k-quant weights (Q4_K, Q5_K, Q6_K) only");
 }
 
 }  // namespace mq

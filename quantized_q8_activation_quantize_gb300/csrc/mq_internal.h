@@ -95,6 +95,13 @@ int launch_gemm(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p,
 // the small-M tensor-core GEMM (1 <= M <= 32 tokens; k-quant weights)
 int launch_gemm_small(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Plane &p, int64_t M, float *y,
                       const Dump &dump, unsigned int *err, cudaStream_t stream);
+// one launch over nj independent matrices of one format (k-quants) and K, each with its own plane
+// (M tokens) and output
+int launch_gemv_grouped(Fmt fmt, int nj, const uint8_t *const *w, const int64_t *N, const Plane *p, float *const *y,
+                        int64_t K, int64_t M, unsigned int *err, cudaStream_t stream);
+// one launch quantizing nj activations [M][K] (plain Q8, no RMSNorm) into their own planes
+int launch_quantize_grouped(int nj, const float *const *x, const Plane *p, int64_t M, int64_t K, unsigned sections,
+                            cudaStream_t stream);
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable), resolved once
 void *tensor_map_encoder();
 // attribute slots of the small-M GEMM: kAttrSlotSmall + 2 * (3 fmt + NT/32) + dump

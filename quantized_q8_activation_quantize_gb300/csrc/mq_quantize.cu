@@ -12,6 +12,8 @@
 // intrinsics (no contraction): d = amax/127, q = round_half_away(x * (1/d)).
 #include <cuda_fp16.h>
 
+#include <cstring>
+
 #include "mq_device.cuh"
 #include "mq_internal.h"
 
@@ -110,6 +112,44 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
             const float v2[8] = {a2.x, a2.y, a2.z, a2.w, b2.x, b2.y, b2.z, b2.w};
             quantize8<SECT>(v2, lane, p, M, K, m2, k02);
         }
+    }
+}
+
+// The plain quantizer over up to 8 independent activations of the same shape [M][K] in one launch
+// (the decode sweep's inputs of one layer level); item it belongs to job it / (M * K / 256).
+constexpr int kMaxQJobs = 8;
+struct QJobs {
+    int n;
+    const float *x[kMaxQJobs];
+    Plane p[kMaxQJobs];
+};
+
+template <unsigned SECT>
+__global__ void __launch_bounds__(256) quantize_grouped_kernel(const __grid_constant__ QJobs jobs, int64_t M,
+                                                               int64_t K) {
+    grid_dep_launch();
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const uint32_t nch = (uint32_t)(K / 256);
+    const int64_t per_job = M * (int64_t)nch, items = per_job * jobs.n;
+    const int64_t stride = (int64_t)gridDim.x * 8;
+    for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += stride) {
+        const int j = (int)(it / per_job);
+        const int64_t r = it - (int64_t)j * per_job;
+        const int64_t m = r / nch;
+        const int64_t k0 = (r - m * (int64_t)nch) * 256 + lane * 8;
+        const float *x = jobs.x[0];
+        Plane p = jobs.p[0];
+#pragma unroll
+        for (int i = 1; i < kMaxQJobs; ++i)
+            if (i == j) {
+                x = jobs.x[i];
+                p = jobs.p[i];
+            }
+        const float4 *src = reinterpret_cast<const float4 *>(x + m * K + k0);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        quantize8<SECT>(v, lane, p, M, K, m, k0);
     }
 }
 
@@ -248,6 +288,26 @@ int launch_swiglu_quantize(const float *g, const float *up, int64_t M, int64_t K
     cudaError_t e;
     MQ_SECT_SWITCH(swiglu_quantize_kernel, sections, dim3((unsigned)ctas), dim3(256), 0, stream, g, up, M, K, p)
     return cuda_error(e, "swiglu quantize launch");
+}
+
+int launch_quantize_grouped(int nj, const float *const *x, const Plane *p, int64_t M, int64_t K, unsigned sections,
+                            cudaStream_t stream) {
+    if (nj < 1 || nj > kMaxQJobs) return set_error(MQ_ERR_ARG, "grouped quantize: %d jobs (1 .. %d)", nj, kMaxQJobs);
+    QJobs jobs;
+    memset(&jobs, 0, sizeof jobs);
+    jobs.n = nj;
+    for (int i = 0; i < nj; ++i) {
+        jobs.x[i] = x[i];
+        jobs.p[i] = p[i];
+    }
+    const int nsm = sm_count();
+    const int64_t warps = nj * M * (K / 256);
+    int64_t ctas = (warps + 7) / 8;
+    const int64_t cap = (int64_t)nsm * 8;
+    if (ctas > cap) ctas = cap;
+    cudaError_t e;
+    MQ_SECT_SWITCH(quantize_grouped_kernel, sections, dim3((unsigned)ctas), dim3(256), 0, stream, jobs, M, K)
+    return cuda_error(e, "grouped quantize launch");
 }
 
 }  // namespace mq

@@ -23,7 +23,8 @@ EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quan
             "mq_debug_forced_timeout", "mq_gemv_q4_0", "mq_gemv_q4_1", "mq_gemv_q5_0", "mq_gemv_q5_1", "mq_gemv_q8_0",
             "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu",
             "mq_quantize_q8_ex", "mq_quantize_swiglu_q8_ex", "mq_gemm_small_q4k", "mq_gemm_small_q5k",
-            "mq_gemm_small_q6k"}
+            "mq_gemm_small_q6k", "mq_gemv_grouped_q4k", "mq_gemv_grouped_q5k", "mq_gemv_grouped_q6k",
+            "mq_quantize_q8_grouped"}
 
 
 def test_header_declares_the_boundary():
@@ -159,6 +160,28 @@ def test_size_dispatch():
         assert B.matmul_path("q4k", m) == "small" and B.matmul_path("q6k", m) == "small"
     assert B.matmul_path("q4k", 33) == "gemm"
     assert B.matmul_path("q8_0", 8) == "gemv" and B.matmul_path("q8_0", 16) == "gemm"
+
+
+def test_grouped_argument_errors():
+    # host-side validation of the grouped calls (no device needed): job counts, NULL tables, per-job
+    # checks, and outputs overlapping another job's inputs or outputs
+    L = B.lib()
+    J = B.GemvJob
+    jobs = (J * 2)(J(1 << 20, 8, 1 << 24, 1 << 28), J(1 << 21, 8, 1 << 25, (1 << 28) + 64))
+    assert L.mq_gemv_grouped_q4k(jobs, 9, 256, 4, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_q4k(None, 2, 256, 4, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_q4k(jobs, 0, 256, 4, None) == B.MQ_OK
+    assert L.mq_gemv_grouped_q4k(jobs, 2, 300, 4, None) == B.MQ_ERR_SHAPE
+    assert L.mq_gemv_grouped_q6k(jobs, 2, 256, 4, None) == B.MQ_ERR_ARG     # job 0's y overlaps job 1's y
+    assert "overlaps" in B.last_error()
+    bad = (J * 1)(J(8, 8, 1 << 24, 1 << 28))
+    assert L.mq_gemv_grouped_q5k(bad, 1, 256, 4, None) == B.MQ_ERR_ALIGN
+    Q = B.QuantizeJob
+    q = (Q * 2)(Q(1 << 20, 1 << 24), Q(1 << 21, (1 << 24) + 256))
+    assert L.mq_quantize_q8_grouped(q, 9, 4, 256, B.PLANE_ALL, None) == B.MQ_ERR_ARG
+    assert L.mq_quantize_q8_grouped(q, 2, 4, 256, 0, None) == B.MQ_ERR_ARG
+    assert L.mq_quantize_q8_grouped(q, 2, 4, 256, B.PLANE_ALL, None) == B.MQ_ERR_ARG   # planes overlap
+    assert L.mq_quantize_q8_grouped(q, 2, 0, 256, B.PLANE_ALL, None) == B.MQ_OK
 
 
 def test_debug_window_errors(L):

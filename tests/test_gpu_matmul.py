@@ -466,3 +466,55 @@ def test_small_m_size_dispatch_agrees(M):
         for path in ("gemv", "gemm"):
             y2, _ = G.run_matmul(path, fmt, w, plane, M, K, N)
             assert G.rel_err(y2, ref) <= G.REL_TOL, path
+
+
+# ---- grouped decode GEMV and grouped quantize (one launch per layer level of the decode sweep)
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_grouped_gemv_matches_single_calls(M):
+    # the level shapes of a decoder layer: q|k|v (3584, 512, 512 rows, K = 3584), gate|up (18944 rows
+    # each), and Q6_K matrices of different heights; every job's output equals its single call bit for
+    # bit, and meets the bar against the oracle
+    import torch
+    cases = [("q4k", 3584, [3584, 512, 512]), ("q4k", 3584, [18944, 18944]), ("q6k", 18944, [3584, 1000]),
+             ("q5k", 512, [7, 300, 129])]
+    for fmt, K, Ns in cases:
+        r = np.random.default_rng(K + len(Ns) + M)
+        ws = [_weights(fmt, n, K, 500 + i + K) for i, n in enumerate(Ns)]
+        xs = [inputs.activations(r, M, K) for _ in Ns]
+        planes = [G.gpu_plane(x)[0] for x in xs]
+        wds = [G.dev(w.reshape(n, -1)) for w, n in zip(ws, Ns)]
+        ys = [torch.full((M, n), float("nan"), dtype=torch.float32, device="cuda") for n in Ns]
+        B.GEMV_GROUPED[fmt]([(wd, n, p, y) for wd, n, p, y in zip(wds, Ns, planes, ys)], K, M)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+        for i, n in enumerate(Ns):
+            y1 = torch.empty((M, n), dtype=torch.float32, device="cuda")
+            B.GEMV[fmt](wds[i], n, K, planes[i], M, y1)
+            torch.cuda.synchronize()
+            assert torch.equal(ys[i], y1), (fmt, K, n, M)
+            ref = oracle.matmul(ws[i], fmt, G.oracle_plane(xs[i]), threads=8)
+            assert G.rel_err(ys[i].cpu().numpy(), ref) <= G.REL_TOL
+
+
+def test_grouped_quantize_matches_single_calls():
+    import torch
+    for M, K, n in ((1, 3584, 3), (1, 18944, 1), (5, 512, 8)):
+        r = np.random.default_rng(M * 100 + K + n)
+        xs = [inputs.activations(r, M, K) for _ in range(n)]
+        xds = [G.dev(x) for x in xs]
+        for sections in (B.PLANE_ALL, B.PLANE_FOR_GEMV):
+            planes = [torch.full((B.mq_q8_plane_bytes(M, K),), 0x5A, dtype=torch.uint8, device="cuda") for _ in xs]
+            B.mq_quantize_q8_grouped(list(zip(xds, planes)), M, K, sections)
+            torch.cuda.synchronize()
+            B.mq_device_status()
+            for x, xd, plane in zip(xs, xds, planes):
+                single = torch.full_like(plane, 0x5A)
+                B.mq_quantize_q8_ex(xd, M, K, None, 0.0, sections, single)
+                torch.cuda.synchronize()
+                assert torch.equal(plane, single)
+                q16, q8, d, s = B.plane_views(plane, M, K)
+                G.assert_plane_equal((q16.float().cpu().numpy() if sections & B.PLANE_Q16 else
+                                      q8.cpu().numpy().astype(np.float32), q8.cpu().numpy(),
+                                      d.t().contiguous().cpu().numpy(), s.t().contiguous().cpu().numpy()),
+                                     G.oracle_plane(x))
