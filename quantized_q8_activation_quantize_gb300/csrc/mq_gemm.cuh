@@ -84,6 +84,10 @@ struct GmCfg {
     // slower with four, so they keep three
     static constexpr int ACC = FMT == FMT_Q6K ? 4 : 3;
     static constexpr int MIN_TILE = BM * 64;                      // 128 rows x 16 tf32 (64 B, 64-B swizzle)
+    // Q4_K / Q5_K: the activation scales staged token-major, so the epilogue loads a token's eight
+    // once per super-block instead of one per block (measured -3 %; Q6_K and the 32-value formats,
+    // with other register pressure in the epilogue, measured slower and keep the block-major table)
+    static constexpr bool DA_TOK = KQ;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * kTile;
     static constexpr int OFF_BC = OFF_B + STAGES * kTile;
@@ -92,7 +96,7 @@ struct GmCfg {
     static constexpr int OFF_RAW = OFF_BMIN + (MIN ? 2 * MIN_TILE : 0);
     // row factors, 2 slots: the super-block d per weight row, or (B32) each block's d [8][128]
     static constexpr int OFF_INFO = OFF_RAW + RAW_STAGES * BN * RAW_ROW;
-    static constexpr int OFF_DA = OFF_INFO + 2 * BN * 4 * (B32 ? 8 : 1);    // d_a [2][8 blocks][128 tokens]
+    static constexpr int OFF_DA = OFF_INFO + 2 * BN * 4 * (B32 ? 8 : 1);    // d_a [2][8 blocks][128 tokens] (or token-major)
     static constexpr int OFF_FLAG = OFF_DA + 2 * 8 * BM * 4;
     static constexpr int OFF_BAR = align_up(OFF_FLAG + STAGES * 4 * 4, 8);
     // a_full[S] b_full[S] ab_empty[S] raw_full[R] raw_empty[R] info_full[2] info_empty[2] acc_full[3]
@@ -430,10 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[2 * j + h] = m < M ? __ldg(p.d + (int64_t)(8 * sb + j) * M + m) : 0.0f;
                 }
             float *dst = da_tile0 + slot * 8 * BM;
+            if constexpr (C::DA_TOK) {
+                // token-major [128 tokens][8 blocks]: an epilogue thread reads its token's eight
+                // scales with two 16-byte loads per super-block
+                float4 *d4 = reinterpret_cast<float4 *>(dst);
+                d4[2 * t] = make_float4(v[0], v[2], v[4], v[6]);
+                d4[2 * t + 1] = make_float4(v[8], v[10], v[12], v[14]);
+                d4[2 * (t + 64)] = make_float4(v[1], v[3], v[5], v[7]);
+                d4[2 * (t + 64) + 1] = make_float4(v[9], v[11], v[13], v[15]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                dst[j * BM + t] = v[2 * j];
-                dst[j * BM + t + 64] = v[2 * j + 1];
+                for (int j = 0; j < 8; ++j) {
+                    dst[j * BM + t] = v[2 * j];
+                    dst[j * BM + t + 64] = v[2 * j + 1];
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.da_full[slot]);
@@ -765,6 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < nsb && ok; ++sb) {
             if (!mbar_wait(&bars.da_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_DA, abort_flag)) break;
             const float *da_sb = da_tok + (sb & 1) * 8 * BM;
+            float das[8];
+            if constexpr (C::DA_TOK) {
+                const float4 *dq = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(sm + C::OFF_DA) +
+                                                                    (sb & 1) * 8 * BM + (32 * qd + lane) * 8);
+                const float4 dq0 = dq[0], dq1 = dq[1];
+                das[0] = dq0.x; das[1] = dq0.y; das[2] = dq0.z; das[3] = dq0.w;
+                das[4] = dq1.x; das[5] = dq1.y; das[6] = dq1.z; das[7] = dq1.w;
+            }
             // 32-value formats: every block's d per weight row is needed from the first block on
             if constexpr (C::B32)
                 if (!mbar_wait(&bars.info_full[sb & 1], (sb >> 1) & 1, err, ERR_GEMM_INFO_FULL, abort_flag)) break;
@@ -777,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float da = da_sb[j * BM];
+                const float da = C::DA_TOK ? das[j] : da_sb[j * BM];
                 const float2 da2 = make_float2(da, da);
                 // Q4_K: both 32-column halves in flight together, one wait, then the slot goes back;
                 // Q6_K (a smaller epilogue register budget): one half at a time
