@@ -70,8 +70,9 @@ def parse_args():
 # DRAM bytes (read + write) of one launch of the roofline kernels, from one ncu capture of the
 # current kernels (dram__bytes_read.sum + dram__bytes_write.sum); set to None whenever a kernel
 # changes until it is captured again.
-TRAFFIC_GEMM_Q4K_GATE = 95.565824e6 + 205.278720e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
-TRAFFIC_GEMV_Q6K_LMHEAD = 447.181568e6 + 3.106560e6   # 152064x3584 Q6_K, M=1
+TRAFFIC_GEMM_Q4K_GATE = 97.276928e6 + 209.093120e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
+TRAFFIC_GEMM_Q6K_DOWN = 359.300352e6 + 42.797568e6      # 3584x18944 Q6_K, M=3314
+TRAFFIC_GEMV_Q6K_LMHEAD = None                          # 152064x3584 Q6_K, M=1 (kernel changed: re-capture)
 # the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs): context
 # only -- the GEMM does not use that instruction
 INT8_MMA_SYNC_PEAK_TOPS = 158.1
@@ -680,6 +681,10 @@ def main():
                      "peak_probe": TCGEN05_F16_PROBE_TFLOPS, "frac_of_probe": q4k_tflops / TCGEN05_F16_PROBE_TFLOPS,
                      "vs_int8_mma_sync_peak": q4k_tflops / INT8_MMA_SYNC_PEAK_TOPS,
                      "vs_int8_mma_sync_note": "context only: the legacy int8 instruction is not what the kernel runs"},
+        "roofline_q6k": {"bound": "tensor", "kernel": "mq_gemm_q6k (3584x18944, M=3314)", "achieved": q6k_tflops,
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": q6k_tflops / bf16_peak,
+                         "traffic": TRAFFIC_GEMM_Q6K_DOWN,
+                         "peak_kind": f"{peak_kind} dense bf16 (f16 MMA has the same nominal rate)"},
         "e2e": e2e, "gpu_launches": pf.launches * K, "clocks": clk,
     }
 
