@@ -108,8 +108,8 @@ struct GmCfg {
     // per-warpgroup register budgets (launch: 512 x 128 = the whole 64K register file), chosen
     // per format by measurement (spill reloads in a pipeline loop cost an L2 trip each)
     static constexpr int REGS_CTL = TMW ? 56 : 48;
-    static constexpr int REGS_UNPACK = TMW ? 72 : 80;
-    static constexpr int REGS_EPI = 192;
+    static constexpr int REGS_UNPACK = TMW ? 72 : 112;
+    static constexpr int REGS_EPI = TMW ? 192 : 176;
     static_assert(128 * REGS_CTL + 128 * REGS_UNPACK + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 };
 
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int sb = 0; sb < R && sb < nsb; ++sb) issue_raw(sb);
         }
 
-        uint32_t dirty = (1u << S) - 1;      // Q6_K correction rows that may hold non-zero data
+        uint32_t dirty = (1u << S) - 1;      // Q6_K: stage slots whose correction rows may hold non-zero data (per warp)
         int issued = (FMT == FMT_Q6K) ? (R < nsb ? R : nsb) : 0;
         int sb = 0;
         for (; sb < nsb; ++sb) {
@@ -503,6 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int sc[16];
             int mn[8];
             float dw[8], mw[8];          // 32-value formats: each block's d and m (m = 0 without one)
+            bool wbig = false;           // Q6_K: some row of the warp has a big scale in this super-block
+            // Q6_K: the 16 int8 scales (big ones made even) and the correction factors (1 where the
+            // scale is big, else 0), four per word
+            uint32_t scw[4], cw[4];
             if constexpr (C::B32) {
                 // block j's fp16 d at byte BS j of the group (2-byte aligned), m right after it
                 constexpr int BS = b32_bytes(FMT);
@@ -542,9 +546,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 5; ++i) tail[i] = 0;
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sc[i] = (int)(int8_t)((tail[i >> 2] >> (8 * (i & 3))) & 0xff);
                 d = __half2float(__ushort_as_half((unsigned short)(tail[4] & 0xffff)));
+                // an odd |sc| > 64 (13 bits with q - 32) keeps sc - 1 in the main tile and marks the
+                // correction tile, which then carries q - 32 itself.  For an int8 byte that is bit 0
+                // and (bit 6 xor bit 7): 65..127 and -128..-65 are the bytes whose bits 6 and 7 differ.
+                uint32_t any = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cw[i] = tail[i] & ((tail[i] >> 6) ^ (tail[i] >> 7)) & 0x01010101u;
+                    scw[i] = tail[i] & ~cw[i];
+                    any |= cw[i];
+                }
+                wbig = __any_sync(kFull, any != 0);
             }
             // ---- per-row factors of this super-block: d for the epilogue, -dmin m_j for the min MMA
             if (!__all_sync(kFull, mbar_wait(&bars.info_empty[sb & 1], ((sb >> 1) & 1) ^ 1, err, ERR_GEMM_INFO_EMPTY,
@@ -696,19 +709,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     const int nsh = (g0 >= 2) ? 4 : 0;
-                    bool need_corr = false;
                     const __half2 bias = __float2half2_rn(1056.0f);
                     const uint32_t bct = bc_tile0 + s * kTile;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    // the 8 values of chunk c as (q - 32) pairs
+                    auto chunk_t = [&](int c, __half2 (&t)[4]) {
                         const int g = g0 + (c >> 2), l = 8 * (c & 3);
-                        const int si = 8 * h + 2 * g + (l >= 16 ? 1 : 0);
-                        const int scv = valid ? sc[si] : 0;
-                        const bool big = (scv > 64 || scv < -64) && (scv & 1);
-                        const int se = big ? (scv & ~1) : scv;
-                        need_corr |= big;
-                        const __half2 s2 = __float2half2_rn((float)se);
-                        uint32_t o[4], oc[4];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const uint32_t lw = ql[8 * (g & 1) + (l >> 2) + e];
@@ -716,20 +721,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t v = ((lw >> nsh) & 0x0f0f0f0fu) | (((hw >> (2 * g)) & 0x03030303u) << 4);
                             uint32_t b0, b1;
                             bytes_to_h2_biased(v, b0, b1);
-                            const __half2 t0 = __hsub2(u32_as_h2(b0), bias);   // q - 32, exact
-                            const __half2 t1 = __hsub2(u32_as_h2(b1), bias);
-                            o[2 * e] = h2_as_u32(__hmul2(t0, s2));
-                            o[2 * e + 1] = h2_as_u32(__hmul2(t1, s2));
-                            oc[2 * e] = big ? h2_as_u32(t0) : 0u;
-                            oc[2 * e + 1] = big ? h2_as_u32(t1) : 0u;
+                            t[2 * e] = __hsub2(u32_as_h2(b0), bias);      // q - 32, exact
+                            t[2 * e + 1] = __hsub2(u32_as_h2(b1), bias);
                         }
-                        sts128(sw128_chunk(btile, r, c), make_uint4(o[0], o[1], o[2], o[3]));
-                        if (need_corr || ((dirty >> s) & 1)) sts128(sw128_chunk(bct, r, c), make_uint4(oc[0], oc[1], oc[2], oc[3]));
+                    };
+                    auto chunk_si = [&](int c) { return 8 * h + 2 * (g0 + (c >> 2)) + ((c & 3) >= 2 ? 1 : 0); };
+                    // pass 0 writes the main tile, (q - 32) times the scale (made even if big); pass 1
+                    // (only while the warp has big scales in this super-block, and once more after it,
+                    // to zero its rows) the correction tile, (q - 32) times 1 where the scale is big, else 0
+                    const int npass = (wbig || ((dirty >> s) & 1)) ? 2 : 1;
+#pragma unroll 1
+                    for (int pass = 0; pass < npass; ++pass) {
+                        uint32_t fw[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) fw[i] = pass ? cw[i] : scw[i];
+                        const uint32_t tile = pass ? bct : btile;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int si = chunk_si(c);
+                            const __half2 s2 = __float2half2_rn((float)(int)(int8_t)(fw[si >> 2] >> (8 * (si & 3))));
+                            __half2 t[4];
+                            chunk_t(c, t);
+                            sts128(sw128_chunk(tile, r, c),
+                                   make_uint4(h2_as_u32(__hmul2(t[0], s2)), h2_as_u32(__hmul2(t[1], s2)),
+                                              h2_as_u32(__hmul2(t[2], s2)), h2_as_u32(__hmul2(t[3], s2))));
+                        }
                     }
-                    // rows written with correction data stay dirty until rewritten with zeros
-                    if (need_corr) dirty |= 1u << s; else dirty &= ~(1u << s);
-                    const bool any = __any_sync(kFull, need_corr);
-                    if (lane == 0) corr_flags[4 * s + (warp - kWarpUnpack0)] = any ? 1u : 0u;
+                    if (wbig) dirty |= 1u << s; else dirty &= ~(1u << s);
+                    if (lane == 0) corr_flags[4 * s + (warp - kWarpUnpack0)] = wbig ? 1u : 0u;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
