@@ -49,17 +49,8 @@ struct SmCfg {
     static constexpr bool TMW = FMT != FMT_Q6K;                         // raw rows by TMA
     static constexpr bool CORR = FMT == FMT_Q6K;                        // odd |sc| > 64 correction tile
     static constexpr int BB = block_bytes(FMT);
-#ifndef SMALL_S
-#define SMALL_S 4
-#endif
-#ifndef SMALL_R6
-#define SMALL_R6 2
-#endif
-#ifndef SMALL_R4
-#define SMALL_R4 3
-#endif
-    static constexpr int S = SMALL_S;                                    // 64-value stages in flight
-    static constexpr int R = FMT == FMT_Q6K ? SMALL_R6 : SMALL_R4;       // raw super-block slots
+    static constexpr int S = 4;                                          // 64-value stages in flight
+    static constexpr int R = FMT == FMT_Q6K ? 2 : 3;                     // raw super-block slots
     static constexpr int RAW_ROW = TMW ? BB : 240;                       // Q6_K: 16-B aligned superset
     static constexpr int XTILE = NT * SBK * 2;                           // token codes of one stage
     // the token tiles have their own, deeper ring: they come from L2 with a latency of a few stages
