@@ -302,6 +302,11 @@ GEMV_GROUPED = {"q4k": mq_gemv_grouped_q4k, "q5k": mq_gemv_grouped_q5k, "q6k": m
 # the small-M band (1 <= M <= 32) on the tensor cores, k-quant weights
 GEMM_SMALL = {"q4k": mq_gemm_small_q4k, "q5k": mq_gemm_small_q5k, "q6k": mq_gemm_small_q6k}
 SMALL_MAX_M = 32
+# the fewest tokens at which the size dispatch prefers the small-M kernel to the GEMV: measured on a
+# 152064 x 3584 LM head (GB300), the GEMV's time grows with its passes over W (8 tokens a pass for
+# Q4_K / Q5_K, 4 for Q6_K) while the small-M kernel's is flat up to 32 tokens; Q4_K: GEMV 0.168 ms at
+# 5 tokens, 0.256 at 8, small-M 0.213; Q6_K: GEMV 0.168 at 4, 0.334 at 8, small-M 0.321
+SMALL_MIN_M = {"q4k": 7, "q5k": 7, "q6k": 8}
 # debug op of each (kind, format) for mq_debug_blockdots
 DEBUG_OP = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv", "q6k"): 3, ("gemv", "q5k"): 4,
             ("gemm", "q5k"): 5, ("gemv", "q4_0"): 6, ("gemv", "q4_1"): 7, ("gemv", "q5_0"): 8, ("gemv", "q5_1"): 9,
@@ -312,16 +317,18 @@ DEBUG_OP = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv",
 
 def matmul_path(fmt: str, M: int) -> str:
     """The entry point family the size dispatch picks: the pages' gate (MMVQ for one token, MMQ from 16),
-    with the band 2 <= M <= 32 on the small-M tensor-core kernel where the format has one."""
-    if M == 1:
-        return "gemv"
-    if M <= SMALL_MAX_M and fmt in GEMM_SMALL:
-        return "small"
+    with the band up to 32 tokens on the small-M tensor-core kernel where the format has one and it is
+    the faster path (SMALL_MIN_M[fmt] .. 32 tokens)."""
+    if fmt in GEMM_SMALL:
+        if M < SMALL_MIN_M[fmt]:
+            return "gemv"
+        return "small" if M <= SMALL_MAX_M else "gemm"
     return "gemv" if M < 16 else "gemm"
 
 
 def matmul(fmt: str, w, N: int, K: int, plane, M: int, y, stream=None):
-    """Size dispatch (matmul_path): GEMV for one token, the small-M tensor-core GEMM for 2 .. 32 tokens
-    (k-quants), the GEMV below 16 tokens and the GEMM from 16 on otherwise."""
+    """Size dispatch (matmul_path): k-quants take the GEMV below SMALL_MIN_M tokens, the small-M
+    tensor-core GEMM up to 32 tokens and the GEMM beyond; the 32-value formats take the GEMV below
+    16 tokens and the GEMM from 16 on."""
     table = {"gemv": GEMV, "gemm": GEMM, "small": GEMM_SMALL}[matmul_path(fmt, M)]
     return table[fmt](w, N, K, plane, M, y, stream)

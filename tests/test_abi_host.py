@@ -153,12 +153,17 @@ def test_matmul_argument_errors(L, name):
 
 
 def test_size_dispatch():
-    # the pages' gate: one token -> MMVQ; the band up to 32 tokens -> the small-M tensor-core GEMM for the
-    # k-quants; otherwise MMVQ below 16 tokens and MMQ from 16
-    assert B.matmul_path("q6k", 1) == "gemv"
-    for m in (2, 5, 9, 15, 16, 17, 32):
-        assert B.matmul_path("q4k", m) == "small" and B.matmul_path("q6k", m) == "small"
-    assert B.matmul_path("q4k", 33) == "gemm"
+    # the pages' gate: one token -> MMVQ; for the k-quants the GEMV while it is the faster path (below
+    # SMALL_MIN_M tokens), then the small-M tensor-core GEMM up to 32 tokens, then MMQ; the 32-value
+    # formats: MMVQ below 16 tokens and MMQ from 16
+    for fmt in ("q4k", "q5k", "q6k"):
+        lo = B.SMALL_MIN_M[fmt]
+        assert 2 <= lo <= 16
+        for m in range(1, lo):
+            assert B.matmul_path(fmt, m) == "gemv"
+        for m in range(lo, B.SMALL_MAX_M + 1):
+            assert B.matmul_path(fmt, m) == "small"
+        assert B.matmul_path(fmt, B.SMALL_MAX_M + 1) == "gemm"
     assert B.matmul_path("q8_0", 8) == "gemv" and B.matmul_path("q8_0", 16) == "gemm"
 
 

@@ -446,10 +446,10 @@ def test_small_m_decode_shapes():
         _sampled("small", c["fmt"], c["w"], plane, ref_plane, 8, K, N, ms, ns, dump_window=(0, 8, N - 64, 64))
 
 
-@pytest.mark.parametrize("M", [2, 5, 16, 32])
+@pytest.mark.parametrize("M", [2, 5, 7, 8, 16, 32])
 def test_small_m_size_dispatch_agrees(M):
-    # matmul() routes 2 <= M <= 32 to the small-M kernel: same bar against the oracle, and the
-    # GEMV / GEMM on the same inputs meet it too
+    # matmul() routes the band to the GEMV or the small-M kernel (matmul_path): the path it picks meets
+    # the bar against the oracle, and every path on the same inputs meets it too
     import torch
     N, K = 300, 1024
     for fmt in ("q4k", "q6k"):
@@ -457,13 +457,13 @@ def test_small_m_size_dispatch_agrees(M):
         x = inputs.activations(np.random.default_rng(94 + M), M, K)
         plane, _ = G.gpu_plane(x)
         ref = oracle.matmul(w, fmt, G.oracle_plane(x))
-        assert B.matmul_path(fmt, M) == "small"
+        assert B.matmul_path(fmt, M) == ("small" if M >= B.SMALL_MIN_M[fmt] else "gemv")
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         B.matmul(fmt, G.dev(w.reshape(N, -1)), N, K, plane, M, y)
         torch.cuda.synchronize()
         B.mq_device_status()
         assert G.rel_err(y.cpu().numpy(), ref) <= G.REL_TOL
-        for path in ("gemv", "gemm"):
+        for path in ("gemv", "gemm", "small"):
             y2, _ = G.run_matmul(path, fmt, w, plane, M, K, N)
             assert G.rel_err(y2, ref) <= G.REL_TOL, path
 
