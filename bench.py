@@ -98,6 +98,8 @@ CASES = {
     "gemm_swiglu_ffn": "7B FFN prefill fused gate|up GEMM: Q4_K 2 x 18944x3584, M=3314, SwiGLU epilogue -> down plane",
     "quantize_rms": "7B FFN prefill RMSNorm-fused Q8 quantize: 3314x3584",
     "decode_sweep": "decode sweep: the 196 quantize + GEMV pairs of one decode token, plain launches",
+    "decode_sweep_grouped": "decode sweep: one decode token with one grouped quantize and one grouped GEMV launch per "
+                            "layer level and format (238 launches), plain launches",
     "quantize_ffn": "7B FFN prefill plain Q8 quantize: 3314x18944",
 }
 
@@ -117,6 +119,14 @@ def run_case(args):
         torch.cuda.synchronize()
         B.mq_device_status()
         print(json.dumps({"case": name, "what": CASES[name], "launches": (1 + args.reps) * 2 * len(sw.items)}))
+        return
+    if name == "decode_sweep_grouped":
+        sw = DecodeSweep(torch, B, I)
+        for _ in range(1 + args.reps):
+            sw.run_grouped(True)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+        print(json.dumps({"case": name, "what": CASES[name]}))
         return
     if name.startswith("gemm_q4k_gate") or name.startswith("gemm_q6k_down") or name.startswith("quantize"):
         c = I.ffn_prefill()
