@@ -551,6 +551,30 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
+def bind_gpu_local_cpus(torch, dev):
+    """Run this process (and so first-touch its pinned host buffers) on the CPUs local to the GPU, as
+    sysfs lists them for the GPU's PCI function; returns that CPU list, or None where it is not known."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return spec
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
 def main():
     args = parse_args()
     if args.case:
@@ -564,6 +588,7 @@ def main():
     import torch
     torch.cuda.set_device(dist.local)
     dist.init(use_cuda=True)
+    host_cpus = bind_gpu_local_cpus(torch, dist.local)
     import __graft_entry__
     __graft_entry__.build()
     from quantized_q8_activation_quantize_gb300 import binding as B
@@ -671,7 +696,7 @@ def main():
         "data": "synthetic (seeded, 7B q4_K_m shapes)",
         "config": {"workload": "7B FFN prefill, 3314 tokens: RMSNorm-Q8, gate/up Q4_K 18944x3584, "
                                "Q8, down Q6_K 3584x18944", "tokens": pf.M, "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas x{dist.world}"},
+                   "parallelism": f"replicas x{dist.world}", "host_cpus": host_cpus},
         "prefill_tok_per_s": dist.world * pf.M / (ms_step * 1e-3),
         "kernels_ms": {"rms_quantize": k_ms[0], "gemm_q4k_gate": k_ms[1], "gemm_q4k_up": k_ms[2],
                        "quantize": k_ms[3], "gemm_q6k_down": k_ms[4]},
