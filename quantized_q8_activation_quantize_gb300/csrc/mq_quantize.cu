@@ -189,14 +189,73 @@ __device__ __forceinline__ void add_square(float v, float &hi, float &lo) {
     lo = __fadd_rn(lo, __fadd_rn(err, e));
 }
 
+// Error-free sum a + b = s + e (Knuth's two-sum, branch-free, any order of magnitudes).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bv = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bv)), __fsub_rn(b, bv));
+}
+
+// (ah, al) += (bh, bl) for pairs of f32 (a value and its small correction): the high parts add
+// error-free, the corrections add rounded, and the result is renormalised (|al| <= ulp(ah) / 2).
+// The result does not depend on the order of the operands, so a butterfly over the lanes leaves
+// the same pair in every lane.
+__device__ __forceinline__ void pair_add(float &ah, float &al, float bh, float bl) {
+    float s, e;
+    two_sum(ah, bh, s, e);
+    e = __fadd_rn(e, __fadd_rn(al, bl));
+    ah = __fadd_rn(s, e);
+    al = __fsub_rn(e, __fsub_rn(ah, s));
+}
+
+// r = 1 / sqrt(t / K + eps) rounded once to f32, from the per-lane pairs of the sum of squares, in
+// f32 arithmetic only.  The lanes' pairs add as f32 pairs (relative error below 2^-43 for these
+// non-negative sums), t / K is an f32 pair (the remainder t - q K of the quotient q is exact for
+// K < 2^22), and one Newton step on rsqrtf's estimate y0 (error below 2^-21) gives y0 + yl within
+// 2^-41 of the value the same lane pairs give in f64.  When every point within 2^-38 y0 of
+// y0 + yl rounds to the same f32, that is r, and it equals the rounding of the f64 evaluation;
+// otherwise (about one token in 10^4: the value lies near a rounding boundary) or outside the
+// normal range the function returns false and the caller evaluates r in f64.  The f64 pipe of
+// this GPU issues ~1.7 operations per clock per SM, so its square root and divide (dozens of
+// operations each) cost more than the rest of a token's arithmetic.
+__device__ __forceinline__ bool rms_scale_f32(float hi0, float lo0, float hi1, float lo1, int64_t K, float eps,
+                                              float &r) {
+    float th = hi0, tl = lo0;
+    pair_add(th, tl, hi1, lo1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float bh = __shfl_xor_sync(kFull, th, o), bl = __shfl_xor_sync(kFull, tl, o);
+        pair_add(th, tl, bh, bl);
+    }
+    const float kf = (float)K;
+    const float ik = __frcp_rn(kf);
+    const float qh = __fmul_rn(th, ik);
+    const float rem = __fmaf_rn(-qh, kf, th);
+    const float ql = __fmul_rn(__fadd_rn(rem, tl), ik);
+    float vh, vl;
+    two_sum(qh, eps, vh, vl);
+    vl = __fadd_rn(vl, ql);
+    // Newton step for 1/sqrt(v): y1 = y0 + y0 (1 - v y0^2) / 2, with y0^2 = p + pe exactly
+    const float y0 = rsqrtf(vh);
+    const float p = __fmul_rn(y0, y0);
+    const float pe = __fmaf_rn(y0, y0, -p);
+    const float a = __fmaf_rn(-vh, p, 1.0f);
+    const float c = __fsub_rn(a, __fmaf_rn(vh, pe, __fmul_rn(vl, p)));
+    const float yl = __fmul_rn(__fmul_rn(0.5f, y0), c);
+    const float dl = __fmul_rn(y0, 0x1p-38f);
+    const float ra = __fadd_rn(y0, __fsub_rn(yl, dl));
+    const float rb = __fadd_rn(y0, __fadd_rn(yl, dl));
+    r = ra;
+    return ra == rb && vh >= 0x1p-100f && vh <= 0x1p100f;
+}
+
 // RMSNorm producer: one warp per token.  Pass 1 sums x^2 per lane as an f32 pair (hi, lo)
-// carrying about 48 significant bits (every square and every addition's rounding error kept),
-// then combines the lanes in f64 in a fixed order; r = (float)(1 / sqrt(sum/K + eps)) is rounded
-// once (f64 sums of the same squares in another order give the same f32 r but with probability
-// ~1e-7 per token).  The f64 pipe of this GPU issues ~1.7 ops per clock per SM, so only the 32
-// lane sums per token and one lane's square root and divide go through it.  Pass 2 re-reads the
-// row (cache-resident) and quantizes y = fl(fl(x * r) * w) with the layout of quantize_kernel
-// (lane l holds values 8l .. 8l + 7 of each 256-value chunk).
+// carrying about 48 significant bits (every square and every addition's rounding error kept);
+// r = 1 / sqrt(sum/K + eps) rounded once to f32 comes from rms_scale_f32, or, when that declines,
+// from the lanes' pairs combined in f64 in a fixed order (f64 sums of the same squares in another
+// order give the same f32 r but with probability ~1e-7 per token).  Pass 2 re-reads the row
+// (cache-resident) and quantizes y = fl(fl(x * r) * w) with the layout of quantize_kernel (lane l
+// holds values 8l .. 8l + 7 of each 256-value chunk).
 template <unsigned SECT>
 __global__ void __launch_bounds__(256) rms_quantize_kernel(const float *__restrict__ x, int64_t M, int64_t K,
                                                            const float *__restrict__ w, float eps, Plane p) {
@@ -220,14 +279,17 @@ __global__ void __launch_bounds__(256) rms_quantize_kernel(const float *__restri
             add_square(b.z, hi0, lo0);
             add_square(b.w, hi1, lo1);
         }
-        double t = ((double)hi0 + (double)lo0) + ((double)hi1 + (double)lo1);
+        float r;
+        if (!rms_scale_f32(hi0, lo0, hi1, lo1, K, eps, r)) {
+            // every lane holds the same f64 sum; one lane takes the square root and divide and
+            // broadcasts r
+            double t = ((double)hi0 + (double)lo0) + ((double)hi1 + (double)lo1);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
-        // every lane holds the same sum; one lane takes the f64 square root and divide (dozens of
-        // f64 operations each) and broadcasts r
-        float r = 0.0f;
-        if (lane == 0) r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
-        r = __shfl_sync(kFull, r, 0);
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+            r = 0.0f;
+            if (lane == 0) r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
+            r = __shfl_sync(kFull, r, 0);
+        }
 #pragma unroll 2
         for (int64_t c = 0; c < nch; ++c) {
             const int64_t k0 = c * 256 + lane * 8;

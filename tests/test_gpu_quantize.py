@@ -40,12 +40,33 @@ def test_edge_values():
 
 def test_rms_quantize_bit_exact_small():
     r = np.random.default_rng(3)
-    for M, K in ((1, 3584), (5, 256), (64, 3584), (3, 18944)):
+    for M, K in ((1, 3584), (5, 256), (64, 3584), (9, 4096), (7, 8192), (2, 18432), (3, 18944)):
         x = inputs.activations(r, M, K)
         w = inputs.rms_weight(r, K)
         plane, got = G.gpu_plane(x, w, 1e-6)
         G.assert_plane_equal(got, G.oracle_plane(x, w, 1e-6))
         G.assert_ds_consistent(plane, M, K)
+
+
+def test_rms_scale_near_rounding_boundary():
+    # Rows whose 1/sqrt(mean(x^2)) lies within 2^-40 of the midpoint between two f32 values: 255 ones
+    # and one 1 - 2^-16 give mean 1 - 2^-23 + 2^-40, so r = 1 + 2^-24 - 2^-41 + O(2^-48), just below
+    # the midpoint of 1 and 1 + 2^-23; r must round to 1 (the producer's f32 evaluation of r declines
+    # such rows and evaluates them in f64).  Scaling a row by 2^k scales r by 2^-k exactly.  The rows
+    # sit among random tokens, so the warps that take them also quantize ordinary rows.
+    M, K = 40, 256
+    r = np.random.default_rng(21)
+    x = inputs.activations(r, M, K)
+    w = np.ones(K, np.float32)
+    near = np.ones(K, np.float32)
+    near[100] = np.float32(1 - 2.0 ** -16)
+    for i, k in enumerate((0, 3, -5, 10, -20)):
+        x[7 * i + 1] = np.ldexp(np.roll(near, 31 * i), k).astype(np.float32)
+    plane, got = G.gpu_plane(x, w, 0.0)
+    G.assert_plane_equal(got, G.oracle_plane(x, w, 0.0))
+    # the codes of a near row are those of the row itself (r rounds to 1, w = 1)
+    _, plain = G.gpu_plane(x[1:2])
+    assert np.array_equal(got[0][1], plain[0][0]) and np.array_equal(got[2][1], plain[2][0])
 
 
 def test_ffn_prefill_full_size_planes():
