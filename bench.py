@@ -12,10 +12,12 @@ than the 129 MB L2, so consecutive steps do not hit L2 for their inputs (no flus
 
 Also reported, measured in the same run:
   "decode":  the decode sweep, one decode token through all 196 per-layer matmuls of a 28-layer
-             7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph whose
-             branches run a layer's independent matmuls -- q|k|v, gate|up -- side by side; the
-             linear chain is reported as "serial"), weight GB/s and tok/s; 3.9 GB of weights,
-             far larger than L2.
+             7B q4_K_m stack (Q8 quantize + dp4a GEMV each, captured in one CUDA graph): one
+             grouped GEMV launch per layer level (q|k|v, o, gate|up, down), the K = 3584 levels
+             quantizing their activation inside the GEMV, down's through a quantize launch;
+             the variants (a quantize launch before every level, per-matrix launches on
+             parallel branches, one linear chain as "serial") are reported beside it; weight
+             GB/s and tok/s; 3.9 GB of weights, far larger than L2.
   "lm_head": the 152064 x 3584 Q6_K LM head at M = 1 (GEMV) and M = 16 (GEMV and GEMM).
   "gemm_q5k", "gemv_q5k": the Q5_K prefill GEMM on the gate shape and the Q5_K decode GEMV on a
              matrix of the LM-head shape (synthetic Q5_K weights).
@@ -100,6 +102,8 @@ CASES = {
     "decode_sweep": "decode sweep: the 196 quantize + GEMV pairs of one decode token, plain launches",
     "decode_sweep_grouped": "decode sweep: one decode token with one grouped quantize and one grouped GEMV launch per "
                             "layer level and format (238 launches), plain launches",
+    "decode_sweep_fused": "decode sweep: one decode token, the K = 3584 levels' activations quantized inside their "
+                          "grouped GEMVs, down's by a grouped quantize launch (154 launches), plain launches",
     "quantize_ffn": "7B FFN prefill plain Q8 quantize: 3314x18944",
 }
 
@@ -120,10 +124,10 @@ def run_case(args):
         B.mq_device_status()
         print(json.dumps({"case": name, "what": CASES[name], "launches": (1 + args.reps) * 2 * len(sw.items)}))
         return
-    if name == "decode_sweep_grouped":
+    if name in ("decode_sweep_grouped", "decode_sweep_fused"):
         sw = DecodeSweep(torch, B, I)
         for _ in range(1 + args.reps):
-            sw.run_grouped(True)
+            sw.run_grouped(True, I.HIDDEN if name == "decode_sweep_fused" else 0)
         torch.cuda.synchronize()
         B.mq_device_status()
         print(json.dumps({"case": name, "what": CASES[name]}))
@@ -426,10 +430,16 @@ class DecodeSweep:
         else:
             self.B.GEMV_GROUPED[group[0][0]]([(w, n, plane, y) for (_, w, _, plane, y, n, _) in group], group[0][6], 1)
 
-    def run_grouped(self, quantize=True):
+    def _gemv_group_x(self, group):
+        fmt, k = group[0][0], group[0][6]
+        self.B.GEMV_GROUPED_X[fmt]([(w, n, x, y) for (_, w, x, _, y, n, _) in group], k)
+
+    def run_grouped(self, quantize=True, xq_max_k=0):
         """The sweep with one launch per layer level and weight format: q|k|v from the layer input (one
         grouped quantize; one grouped Q4_K GEMV, and in the Q6_K layers v's GEMV on a parallel branch),
-        then o, gate|up (grouped quantize and GEMV), down -- the dependency order of a real layer."""
+        then o, gate|up (grouped quantize and GEMV), down -- the dependency order of a real layer.
+        Levels with K <= xq_max_k skip the quantize launch: their grouped GEMV quantizes the f32
+        activations itself (mq_gemv_grouped_x_*)."""
         t, B = self.torch, self.B
         main = t.cuda.current_stream()
         if not hasattr(self, "side"):
@@ -437,35 +447,37 @@ class DecodeSweep:
         for layer in range(len(self.items) // 7):
             li = self.items[7 * layer:7 * layer + 7]           # q, k, v, o, gate, up, down
             for group in (li[0:3], li[3:4], li[4:6], li[6:7]):
-                if quantize:
+                fused = quantize and group[0][6] <= xq_max_k
+                gemv = self._gemv_group_x if fused else self._gemv_group
+                if quantize and not fused:
                     B.mq_quantize_q8_grouped([(it[2], it[3]) for it in group], 1, group[0][6], B.PLANE_FOR_GEMV)
                 by_fmt = {}
                 for it in group:
                     by_fmt.setdefault(it[0], []).append(it)
                 if len(by_fmt) == 1:
-                    self._gemv_group(group)
+                    gemv(group)
                     continue
                 fork = t.cuda.Event()
                 fork.record(main)
                 self.side[0].wait_event(fork)
                 with t.cuda.stream(self.side[0]):
-                    self._gemv_group(by_fmt["q6k"])
-                self._gemv_group(by_fmt["q4k"])
+                    gemv(by_fmt["q6k"])
+                gemv(by_fmt["q4k"])
                 join = t.cuda.Event()
                 join.record(self.side[0])
                 main.wait_event(join)
 
-    def capture_grouped(self, quantize=True):
+    def capture_grouped(self, quantize=True, xq_max_k=0):
         t = self.torch
         s = t.cuda.Stream()
         s.wait_stream(t.cuda.current_stream())
         with t.cuda.stream(s):
-            self.run_grouped(True)
+            self.run_grouped(True, xq_max_k)
         t.cuda.current_stream().wait_stream(s)
         t.cuda.synchronize()
         g = t.cuda.CUDAGraph()
         with t.cuda.graph(g):
-            self.run_grouped(quantize)
+            self.run_grouped(quantize, xq_max_k)
         t.cuda.synchronize()
         return g
 
@@ -784,21 +796,41 @@ def main():
         torch.cuda.synchronize()
         if not all(torch.equal(a, it[4]) for a, it in zip(outs, sw.items)):
             raise RuntimeError("grouped decode sweep differs from the per-matrix sweep")
+        # the sweep with the activations of the K = 3584 levels (q|k|v, o, gate|up) quantized inside
+        # their grouped GEMVs, and with every level's (down too): the same outputs, bit for bit
+        xq = {}
+        for xk in (I.HIDDEN, I.FFN):
+            gx = sw.capture_grouped(True, xk)
+            for it in sw.items:
+                it[4].fill_(float("nan"))
+            gx.replay()
+            torch.cuda.synchronize()
+            if not all(torch.equal(a, it[4]) for a, it in zip(outs, sw.items)):
+                raise RuntimeError("decode sweep with in-GEMV quantization differs from the per-matrix sweep")
+            xq[xk] = time_events(torch, gx.replay, max(5, K), W)
+            del gx
         B.mq_device_status()
         gemv_bytes = sw.bytes - 4 * sum(k for *_, k in sw.items)          # without the f32 activations
         lm_ms = lm["m1_gemv"]["ms"]
         n_layers = len(sw.items) // 7
         gr_launches = 4 * n_layers + 4 * n_layers + (n_layers + 1) // 2      # quantize + GEMV per level (+ v)
+        gx_launches = gr_launches - 3 * n_layers                             # no quantize launch before q|k|v, o, gate|up
+        ms_gx = xq[I.HIDDEN]
         line["decode"] = {"workload": "7B decode sweep: 28 layers x 7 matmuls, M=1, Q8 quantize + GEMV each, one CUDA graph; "
-                                      "one grouped launch per layer level and format (q|k|v from the layer input, o, "
-                                      "gate|up from the post-attention input, down), v's Q6_K GEMV on a parallel branch",
-                          "ms_per_token": ms_gr, "tok_per_s": 1e3 / ms_gr, "weight_bytes": sw.weight_bytes,
-                          "GB/s": sw.bytes / (ms_gr * 1e-3) / 1e9,
-                          "frac_of_hbm": sw.bytes / (ms_gr * 1e-3) / 1e9 / hbm_peak,
-                          "launches_per_token": gr_launches,
+                                      "one grouped GEMV launch per layer level and format (q|k|v from the layer input, o, "
+                                      "gate|up from the post-attention input, down), v's Q6_K GEMV on a parallel branch; the "
+                                      "K = 3584 levels quantize their activation inside the GEMV, down's takes a quantize launch",
+                          "ms_per_token": ms_gx, "tok_per_s": 1e3 / ms_gx, "weight_bytes": sw.weight_bytes,
+                          "GB/s": sw.bytes / (ms_gx * 1e-3) / 1e9,
+                          "frac_of_hbm": sw.bytes / (ms_gx * 1e-3) / 1e9 / hbm_peak,
+                          "launches_per_token": gx_launches,
                           "gemv_only": {"what": "the grouped GEMVs alone (planes already quantized)",
                                         "ms_per_token": ms_gr_gemv, "GB/s": gemv_bytes / (ms_gr_gemv * 1e-3) / 1e9,
                                         "tok_per_s_with_lm_head": 1e3 / (ms_gr_gemv + lm_ms)},
+                          "quantize_launches": {"what": "a grouped quantize launch before every grouped GEMV",
+                                                "ms_per_token": ms_gr, "launches_per_token": gr_launches},
+                          "in_gemv_quantize_all_levels": {"what": "down's activation quantized inside its GEMV too",
+                                                          "ms_per_token": xq[I.FFN]},
                           "per_matrix": {"what": "one quantize + one GEMV launch per matmul (392 launches), "
                                                  "q|k|v and gate|up on parallel branches",
                                          "ms_per_token": ms_br, "GB/s": sw.bytes / (ms_br * 1e-3) / 1e9,

@@ -284,6 +284,37 @@ MQ_API int mq_gemv_grouped_q5k(const mq_gemv_job *jobs, int n_jobs, int64_t K, i
 MQ_API int mq_gemv_grouped_q6k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t M, mq_stream_t stream);
 
 /*
+ * mq_gemv_grouped_x_q4k / _q5k / _q6k -- the grouped decode GEMV for one token (M = 1) straight from
+ * f32 activations: every CTA quantizes its job's x with the arithmetic of mq_quantize_q8 (no
+ * RMSNorm) into shared memory and runs the GEMV on those codes, so a layer level takes one launch
+ * instead of a quantize launch and a GEMV launch ("Features > GPU -- CUDA": activation quantization
+ * fused into the kernels of the path; decode uses the MMVQ weight-streaming kernel).  No plane is
+ * written.
+ *
+ *   jobs     HOST array of n_jobs descriptors {w, N, x, y}, read during the call and not retained:
+ *            w, N and y as for mq_gemv_q4k / _q5k / _q6k with M = 1; x f32 [K], 16-byte aligned
+ *            (device); jobs may share one x
+ *   n_jobs   0 .. 8 (0: nothing to do); a job with N == 0 is skipped
+ *   K        shared by every job; one token's staged codes must fit a CTA's shared memory
+ *            (K below about 100 000)
+ *
+ * Each job's y is, bit for bit, the y of mq_quantize_q8(x) followed by mq_gemv_q4k / _q5k / _q6k
+ * on that plane.  Errors: MQ_ERR_ARG for n_jobs outside 0 .. 8, a NULL table or pointer, negative
+ * N, or an output overlapping any input or other output; MQ_ERR_ALIGN for a misaligned w, x or y;
+ * MQ_ERR_SHAPE for an invalid K, N >= 2^31, or K too large to stage.
+ */
+typedef struct {
+    const void *w;       /* raw weight blocks [N][K/256], 16-byte aligned (device) */
+    int64_t N;           /* rows of this job's weight matrix */
+    const float *x;      /* f32 [K] activation of the token (device) */
+    float *y;            /* f32 [N] output (device) */
+} mq_gemv_xjob;
+
+MQ_API int mq_gemv_grouped_x_q4k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream);
+MQ_API int mq_gemv_grouped_x_q5k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream);
+MQ_API int mq_gemv_grouped_x_q6k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream);
+
+/*
  * mq_quantize_q8_grouped -- the plain mq_quantize_q8_ex over several independent activations of one
  * shape [M][K] in one launch (the inputs of one level of a decoder layer in the decode sweep).
  *

@@ -38,6 +38,10 @@ class GemvJob(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("N", ctypes.c_int64), ("plane", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
+class GemvXJob(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("N", ctypes.c_int64), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
 class QuantizeJob(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("plane", ctypes.c_void_p)]
 
@@ -77,6 +81,8 @@ def lib():
         L.mq_gemm_q4k_swiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
         for name in ("mq_gemv_grouped_q4k", "mq_gemv_grouped_q5k", "mq_gemv_grouped_q6k"):
             getattr(L, name).argtypes = [ctypes.POINTER(GemvJob), I32, I64, I64, P]
+        for name in ("mq_gemv_grouped_x_q4k", "mq_gemv_grouped_x_q5k", "mq_gemv_grouped_x_q6k"):
+            getattr(L, name).argtypes = [ctypes.POINTER(GemvXJob), I32, I64, P]
         L.mq_quantize_q8_grouped.argtypes = [ctypes.POINTER(QuantizeJob), I32, I64, I64, ctypes.c_uint, P]
         L.mq_device_status.argtypes = [P]
         L.mq_debug_blockdots.argtypes = [I32, P, I64, I64, P, I64, P, I64, I64, I64, I64, P, P]
@@ -255,6 +261,25 @@ def mq_gemv_grouped_q6k(jobs, K: int, M: int, stream=None):
     return _gemv_grouped("mq_gemv_grouped_q6k", jobs, K, M, stream)
 
 
+def _gemv_grouped_x(name, jobs, K, stream):
+    arr = (GemvXJob * max(1, len(jobs)))(*[GemvXJob(_ptr(w), N, _ptr(x), _ptr(y)) for (w, N, x, y) in jobs])
+    return _check(getattr(lib(), name)(arr, len(jobs), K, _stream(stream)))
+
+
+def mq_gemv_grouped_x_q4k(jobs, K: int, stream=None):
+    """jobs: a list of (w, N, x, y) for one token (x f32 [K]); the activations are quantized in the
+    kernel, one launch for all of them."""
+    return _gemv_grouped_x("mq_gemv_grouped_x_q4k", jobs, K, stream)
+
+
+def mq_gemv_grouped_x_q5k(jobs, K: int, stream=None):
+    return _gemv_grouped_x("mq_gemv_grouped_x_q5k", jobs, K, stream)
+
+
+def mq_gemv_grouped_x_q6k(jobs, K: int, stream=None):
+    return _gemv_grouped_x("mq_gemv_grouped_x_q6k", jobs, K, stream)
+
+
 def mq_quantize_q8_grouped(jobs, M: int, K: int, sections: int, stream=None):
     """jobs: a list of (x, plane); the plain quantizer over all of them in one launch."""
     arr = (QuantizeJob * max(1, len(jobs)))(*[QuantizeJob(_ptr(x), _ptr(p)) for (x, p) in jobs])
@@ -299,6 +324,7 @@ GEMM = {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q5k": mq_gemm_q5k, "q4_0": mq_g
 GEMV = {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k, "q4_0": mq_gemv_q4_0, "q4_1": mq_gemv_q4_1,
         "q5_0": mq_gemv_q5_0, "q5_1": mq_gemv_q5_1, "q8_0": mq_gemv_q8_0}
 GEMV_GROUPED = {"q4k": mq_gemv_grouped_q4k, "q5k": mq_gemv_grouped_q5k, "q6k": mq_gemv_grouped_q6k}
+GEMV_GROUPED_X = {"q4k": mq_gemv_grouped_x_q4k, "q5k": mq_gemv_grouped_x_q5k, "q6k": mq_gemv_grouped_x_q6k}
 # the small-M band (1 <= M <= 32) on the tensor cores, k-quant weights
 GEMM_SMALL = {"q4k": mq_gemm_small_q4k, "q5k": mq_gemm_small_q5k, "q6k": mq_gemm_small_q6k}
 SMALL_MAX_M = 32

@@ -447,6 +447,64 @@ int mq_gemv_grouped_q6k(const mq_gemv_job *jobs, int n_jobs, int64_t K, int64_t 
     return run_gemv_grouped("mq_gemv_grouped_q6k", FMT_Q6K, jobs, n_jobs, K, M, stream);
 }
 
+// the grouped GEMV from f32 activations (M = 1): every job validated as a GEMV call with x in place of
+// the plane, and no output may overlap any input or other output of the call
+static int run_gemv_grouped_x(const char *fn, Fmt fmt, const mq_gemv_xjob *jobs, int n_jobs, int64_t K,
+                              mq_stream_t stream) {
+    if (n_jobs < 0 || n_jobs > 8) return set_error(MQ_ERR_ARG, "%s: n_jobs=%d not in 0 .. 8", fn, n_jobs);
+    if (n_jobs == 0) return MQ_OK;
+    if (jobs == nullptr) return set_error(MQ_ERR_ARG, "%s: NULL job table", fn);
+    int rc = check_k(K);
+    if (rc != MQ_OK) return rc;
+    const uint8_t *w[8];
+    int64_t N[8];
+    Plane p[8];
+    float *y[8];
+    const float *x[8];
+    int nj = 0;
+    for (int i = 0; i < n_jobs; ++i) {
+        const mq_gemv_xjob &j = jobs[i];
+        if (j.N < 0) return set_error(MQ_ERR_ARG, "%s: job %d: negative N=%lld", fn, i, (long long)j.N);
+        if (j.N >= kMaxDim) return set_error(MQ_ERR_SHAPE, "%s: job %d: N=%lld must be below 2^31", fn, i, (long long)j.N);
+        if (j.N == 0) continue;                      // an empty job launches nothing
+        if (!j.w || !j.x || !j.y)
+            return set_error(MQ_ERR_ARG, "%s: job %d: NULL pointer (w=%p x=%p y=%p)", fn, i, j.w, (const void *)j.x,
+                             (const void *)j.y);
+        if (!aligned(j.w, 16)) return set_error(MQ_ERR_ALIGN, "%s: job %d: weights %p not 16-byte aligned", fn, i, j.w);
+        if (!aligned(j.x, 16)) return set_error(MQ_ERR_ALIGN, "%s: job %d: x %p not 16-byte aligned", fn, i, (const void *)j.x);
+        if (!aligned(j.y, 4)) return set_error(MQ_ERR_ALIGN, "%s: job %d: y %p not 4-byte aligned", fn, i, (const void *)j.y);
+        const size_t yb = (size_t)j.N * 4;
+        for (int k = 0; k < n_jobs; ++k) {
+            if (jobs[k].N <= 0) continue;
+            const size_t wb = (size_t)jobs[k].N * (size_t)(K / kQK) * (size_t)block_bytes(fmt);
+            if (overlaps(j.y, yb, jobs[k].w, wb) || overlaps(j.y, yb, jobs[k].x, (size_t)K * 4) ||
+                (k != i && overlaps(j.y, yb, jobs[k].y, (size_t)jobs[k].N * 4)))
+                return set_error(MQ_ERR_ARG, "%s: output of job %d overlaps an input or output of job %d", fn, i, k);
+        }
+        w[nj] = static_cast<const uint8_t *>(j.w);
+        N[nj] = j.N;
+        memset(&p[nj], 0, sizeof p[nj]);
+        y[nj] = j.y;
+        x[nj] = j.x;
+        ++nj;
+    }
+    if (nj == 0) return MQ_OK;
+    unsigned int *err = nullptr;
+    rc = device_state(&err);
+    if (rc != MQ_OK) return rc;
+    return launch_gemv_grouped(fmt, nj, w, N, p, y, K, 1, err, reinterpret_cast<cudaStream_t>(stream), x);
+}
+
+int mq_gemv_grouped_x_q4k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream) {
+    return run_gemv_grouped_x("mq_gemv_grouped_x_q4k", FMT_Q4K, jobs, n_jobs, K, stream);
+}
+int mq_gemv_grouped_x_q5k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream) {
+    return run_gemv_grouped_x("mq_gemv_grouped_x_q5k", FMT_Q5K, jobs, n_jobs, K, stream);
+}
+int mq_gemv_grouped_x_q6k(const mq_gemv_xjob *jobs, int n_jobs, int64_t K, mq_stream_t stream) {
+    return run_gemv_grouped_x("mq_gemv_grouped_x_q6k", FMT_Q6K, jobs, n_jobs, K, stream);
+}
+
 int mq_quantize_q8_grouped(const mq_quantize_job *jobs, int n_jobs, int64_t M, int64_t K, unsigned sections,
                            mq_stream_t stream) {
     const char *fn = "mq_quantize_q8_grouped";

@@ -389,6 +389,50 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
 }
 
 
+// Q8 quantization of a 32-value block held by four consecutive lanes (lane 4i + j holds values
+// 8j .. 8j + 7 of block i; every lane of the warp takes part): amax over the block, d = amax / 127
+// (IEEE divide), the codes q = clamp(round_half_away(y * (1 / d)), -127, 127) as exact floats (+0
+// for a zero code; 0 when d = 0), and the code sums of the lane pair (lane, lane ^ 1: values 0 .. 15
+// or 16 .. 31 of the block) and of the whole block -- exact integers, |S| <= 4064.
+struct Q8Lane {
+    float r[8];
+    float d;
+    float s16;
+    float s;
+};
+__device__ __forceinline__ void q8_lane(const float (&v)[8], Q8Lane &o) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    o.d = __fdiv_rn(amax, 127.0f);
+    const float id = (o.d != 0.0f) ? __fdiv_rn(1.0f, o.d) : 0.0f;
+    float fs = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // half away from zero, clamped; + 0 turns a -0 code into +0 (the f16 code of 0 is 0x0000)
+        o.r[i] = __fadd_rn(fminf(fmaxf(roundf(__fmul_rn(v[i], id)), -127.0f), 127.0f), 0.0f);
+        fs = __fadd_rn(fs, o.r[i]);
+    }
+    fs = __fadd_rn(fs, __shfl_xor_sync(0xffffffffu, fs, 1));
+    o.s16 = fs;
+    o.s = __fadd_rn(fs, __shfl_xor_sync(0xffffffffu, fs, 2));
+}
+
+// the int8 bytes of eight codes held as exact floats in [-127, 127], without conversion
+// instructions: r + 1.5 * 2^23 holds r in the low mantissa bits, so its low byte is r in two's
+// complement
+__device__ __forceinline__ uint2 q8_bytes(const float (&r)[8]) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__fadd_rn(r[i], 12582912.0f));
+    uint2 b8;
+    b8.x = __byte_perm(__byte_perm(w[0], w[1], 0x0040), __byte_perm(w[2], w[3], 0x0040), 0x5410);
+    b8.y = __byte_perm(__byte_perm(w[4], w[5], 0x0040), __byte_perm(w[6], w[7], 0x0040), 0x5410);
+    return b8;
+}
+
 // Q8 quantization of one 32-value block held by one thread, with the same operations as the
 // warp-cooperative quantizer (amax, d = amax / 127, q = round_half_away(x * (1 / d)) clamped to
 // +-127, S = sum q, and d * S as a tf32 (hi, lo) pair), so equal inputs give equal planes.

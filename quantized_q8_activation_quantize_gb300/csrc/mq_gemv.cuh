@@ -146,6 +146,9 @@ struct GvArgs {
     float *y;
     Dump dump;
     unsigned int *err;
+    // M = 1 only: the token's f32 activation, quantized by every CTA into its staged records
+    // (instead of the plane p, which is then not read)
+    const float *x = nullptr;
 };
 
 // A grouped launch: up to kMaxJobs independent matrices of the same format and K, each with its own
@@ -158,6 +161,7 @@ struct GvJobs {
     int64_t N[kMaxJobs];
     Plane p[kMaxJobs];
     float *y[kMaxJobs];
+    const float *x[kMaxJobs];    // GvArgs::x of each job
 };
 
 // shared-memory addresses of the staged activations (ACT kernels): codes [MT][K], table
@@ -518,6 +522,55 @@ __device__ __forceinline__ void b32_half(const GvArgs &a, const GvAct &at, const
     for (int t = 0; t < MT; ++t) part[t] = acc[t];
 }
 
+// One token (M = 1): its f32 activation x quantized straight into the staged records with the
+// arithmetic of mq_quantize_q8 (q8_lane), so the records hold exactly what staging its plane
+// would give.  Warp w takes super-blocks w, w + CW, ...; lane l holds values 8l .. 8l + 7 of one:
+// half l / 16, block (l / 4) % 4 of the half, bytes 8 (l % 16) .. of the half's codes.  The block
+// entries: (d_a, d_a S) for Q4_K / Q5_K, (d_a, -32 S16, -32 S16') for Q6_K.
+template <int FMT>
+__device__ __forceinline__ void stage_x_one(const float (&v)[8], const GvAct &at, uint32_t sbi, int lane) {
+    using C = GvCfg<FMT>;
+    Q8Lane q;
+    q8_lane(v, q);
+    const uint2 b8 = q8_bytes(q.r);
+    const uint32_t rec = at.codes + sbi * C::SB_STRIDE + C::HALF * (uint32_t)(lane >> 4);
+    sts64u(rec + 8u * (uint32_t)(lane & 15), b8.x, b8.y);
+    const uint32_t g = (uint32_t)(lane >> 2) & 3u;
+    if constexpr (FMT == FMT_Q6K) {
+        const uint32_t ent = rec + 128u + 16u * g;
+        const uint32_t o32 = (uint32_t)(-32 * __float2int_rn(q.s16));
+        if ((lane & 3) == 0)
+            sts64u(ent, __float_as_uint(q.d), o32);
+        else if ((lane & 3) == 2)
+            sts32(ent + 8u, o32);
+    } else {
+        if ((lane & 3) == 0) sts64u(rec + 128u + 8u * g, __float_as_uint(q.d), __float_as_uint(q.d * q.s));
+    }
+}
+
+// (two super-blocks' loads in flight per warp before either is quantized)
+template <int FMT>
+__device__ __forceinline__ void stage_x(const float *__restrict__ x, const GvAct &at, uint32_t nb, int warp,
+                                        int lane) {
+    using C = GvCfg<FMT>;
+    for (uint32_t sbi = (uint32_t)warp; sbi < nb; sbi += 2 * C::CW) {
+        const bool two = sbi + C::CW < nb;
+        const float4 *src = reinterpret_cast<const float4 *>(x + (int64_t)sbi * kQK + lane * 8);
+        const float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        float4 p2 = make_float4(0.f, 0.f, 0.f, 0.f), p3 = p2;
+        if (two) {
+            p2 = __ldg(src + C::CW * kQK / 4);
+            p3 = __ldg(src + C::CW * kQK / 4 + 1);
+        }
+        const float v0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        stage_x_one<FMT>(v0, at, sbi, lane);
+        if (two) {
+            const float v1[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+            stage_x_one<FMT>(v1, at, sbi + C::CW, lane);
+        }
+    }
+}
+
 // Hand a ring stage back to the producer once this warp's reads of it are done.  Every lane
 // first waits for its own shared-memory loads to complete (membar.cta): the loaded registers
 // are consumed only after the release, and without the fence a lane's loads could still be
@@ -545,6 +598,7 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
                 a.N = jobs.N[i];
                 a.p = jobs.p[i];
                 a.y = jobs.y[i];
+                a.x = jobs.x[i];
                 cta = blockIdx.x - jobs.cta0[i];
                 ncta = jobs.cta0[i + 1] - jobs.cta0[i];
             }
@@ -651,7 +705,14 @@ __global__ void __launch_bounds__(GvCfg<FMT>::THREADS, GvCfg<FMT>::ctas_per_sm(M
         // stage the tokens' codes (padded layout) and their scale data
         at.codes = smem_u32(partbuf) + (uint32_t)C::part_bytes(MT);
         at.ck = nb * C::SB_STRIDE;
-        const uint32_t nch = nb * 16u;                // 16-byte chunks of codes per token
+        bool staged = false;
+        if constexpr (MT == 1 && !is_b32(FMT)) {
+            if (a.x != nullptr) {
+                stage_x<FMT>(a.x, at, nb, warp, lane);
+                staged = true;
+            }
+        }
+        const uint32_t nch = staged ? 0u : nb * 16u;  // 16-byte chunks of codes per token
         for (int t = 0; t < a.mt; ++t) {
             const int64_t m = a.t0 + t;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.p.q8 + m * a.K);

@@ -97,8 +97,9 @@ int launch_gemm_small(Fmt fmt, const uint8_t *w, int64_t N, int64_t K, const Pla
                       const Dump &dump, unsigned int *err, cudaStream_t stream);
 // one launch over nj independent matrices of one format (k-quants) and K, each with its own plane
 // (M tokens) and output
+// x: nullptr (each job reads its plane p), or each job's f32 activation (M = 1; quantized in the kernel)
 int launch_gemv_grouped(Fmt fmt, int nj, const uint8_t *const *w, const int64_t *N, const Plane *p, float *const *y,
-                        int64_t K, int64_t M, unsigned int *err, cudaStream_t stream);
+                        int64_t K, int64_t M, unsigned int *err, cudaStream_t stream, const float *const *x = nullptr);
 // one launch quantizing nj activations [M][K] (plain Q8, no RMSNorm) into their own planes
 int launch_quantize_grouped(int nj, const float *const *x, const Plane *p, int64_t M, int64_t K, unsigned sections,
                             cudaStream_t stream);

@@ -26,33 +26,12 @@ constexpr unsigned kFull = 0xffffffffu;
 template <unsigned SECT>
 __device__ __forceinline__ void quantize8(const float (&v)[8], int lane, const Plane &p, int64_t M, int64_t K,
                                           int64_t m, int64_t k0) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-    // the codes as floats holding integers in [-127, 127]; their sum is exact in f32 (|S| <= 4064)
-    float r[8];
-    float fs = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        // half away from zero, clamped; + 0 turns a -0 code into +0 (the f16 code of 0 is 0x0000)
-        r[i] = __fadd_rn(fminf(fmaxf(roundf(__fmul_rn(v[i], id)), -127.0f), 127.0f), 0.0f);
-        fs = __fadd_rn(fs, r[i]);
-    }
-    fs = __fadd_rn(fs, __shfl_xor_sync(kFull, fs, 1));
-    fs = __fadd_rn(fs, __shfl_xor_sync(kFull, fs, 2));
-    const int s = __float2int_rn(fs);
-    // int8 bytes without conversion instructions: r + 1.5 * 2^23 holds r in the low mantissa bits,
-    // so its low byte is r in two's complement
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__fadd_rn(r[i], 12582912.0f));
-    uint2 b8;
-    b8.x = __byte_perm(__byte_perm(w[0], w[1], 0x0040), __byte_perm(w[2], w[3], 0x0040), 0x5410);
-    b8.y = __byte_perm(__byte_perm(w[4], w[5], 0x0040), __byte_perm(w[6], w[7], 0x0040), 0x5410);
+    Q8Lane q;
+    q8_lane(v, q);
+    const float(&r)[8] = q.r;
+    const float d = q.d;
+    const int s = __float2int_rn(q.s);
+    const uint2 b8 = q8_bytes(r);
     // f16 codes: each integer is exact in f16, so the packed conversion is exact
     uint4 h;
     __half2 t;

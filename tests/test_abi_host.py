@@ -24,7 +24,7 @@ EXPECTED = {"mq_last_error", "mq_q8_plane_bytes", "mq_q8_plane_layout", "mq_quan
             "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemm_q5_0", "mq_gemm_q5_1", "mq_gemm_q8_0", "mq_gemm_q4k_swiglu",
             "mq_quantize_q8_ex", "mq_quantize_swiglu_q8_ex", "mq_gemm_small_q4k", "mq_gemm_small_q5k",
             "mq_gemm_small_q6k", "mq_gemv_grouped_q4k", "mq_gemv_grouped_q5k", "mq_gemv_grouped_q6k",
-            "mq_quantize_q8_grouped"}
+            "mq_quantize_q8_grouped", "mq_gemv_grouped_x_q4k", "mq_gemv_grouped_x_q5k", "mq_gemv_grouped_x_q6k"}
 
 
 def test_header_declares_the_boundary():
@@ -181,6 +181,19 @@ def test_grouped_argument_errors():
     assert "overlaps" in B.last_error()
     bad = (J * 1)(J(8, 8, 1 << 24, 1 << 28))
     assert L.mq_gemv_grouped_q5k(bad, 1, 256, 4, None) == B.MQ_ERR_ALIGN
+    X = B.GemvXJob
+    xj = (X * 2)(X(1 << 20, 8, 1 << 24, 1 << 28), X(1 << 21, 8, 1 << 25, (1 << 28) + 16))
+    assert L.mq_gemv_grouped_x_q4k(xj, 9, 256, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_x_q4k(None, 2, 256, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_x_q4k(xj, 0, 256, None) == B.MQ_OK
+    assert L.mq_gemv_grouped_x_q4k(xj, 2, 300, None) == B.MQ_ERR_SHAPE
+    assert L.mq_gemv_grouped_x_q6k(xj, 2, 256, None) == B.MQ_ERR_ARG     # job 0's y overlaps job 1's y
+    assert "overlaps" in B.last_error()
+    over_x = (X * 1)(X(1 << 20, 64, 1 << 28, (1 << 28) + 512))           # y inside x
+    assert L.mq_gemv_grouped_x_q5k(over_x, 1, 256, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_x_q5k((X * 1)(X(1 << 20, 8, (1 << 24) + 4, 1 << 28)), 1, 256, None) == B.MQ_ERR_ALIGN
+    assert L.mq_gemv_grouped_x_q5k((X * 1)(X(1 << 20, 8, None, 1 << 28)), 1, 256, None) == B.MQ_ERR_ARG
+    assert L.mq_gemv_grouped_x_q6k((X * 1)(X(1 << 20, -1, 1 << 24, 1 << 28)), 1, 256, None) == B.MQ_ERR_ARG
     Q = B.QuantizeJob
     q = (Q * 2)(Q(1 << 20, 1 << 24), Q(1 << 21, (1 << 24) + 256))
     assert L.mq_quantize_q8_grouped(q, 9, 4, 256, B.PLANE_ALL, None) == B.MQ_ERR_ARG

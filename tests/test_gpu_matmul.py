@@ -497,6 +497,39 @@ def test_grouped_gemv_matches_single_calls(M):
             assert G.rel_err(ys[i].cpu().numpy(), ref) <= G.REL_TOL
 
 
+def test_grouped_gemv_from_f32_activations():
+    # one token, the activation quantized inside the GEMV (mq_gemv_grouped_x_*): every job's output
+    # equals, bit for bit, the plane quantizer followed by the grouped GEMV, and meets the bar against
+    # the oracle; jobs may share an x (q|k|v of a layer), and ragged, edge-valued and zero activations
+    # take the same codes as the plane quantizer
+    import torch
+    cases = [("q4k", 3584, [3584, 512, 512], True), ("q4k", 3584, [18944, 18944], False),
+             ("q6k", 18944, [3584, 1000], False), ("q6k", 3584, [512, 7], True), ("q5k", 512, [7, 300, 129], False),
+             ("q4k", 256, [33], False)]
+    for fmt, K, Ns, shared in cases:
+        r = np.random.default_rng(K * 7 + len(Ns))
+        ws = [_weights(fmt, n, K, 900 + i + K) for i, n in enumerate(Ns)]
+        x0 = inputs.activations(r, 1, K)
+        xs = [x0 if shared else inputs.activations(r, 1, K) for _ in Ns]
+        if not shared:
+            xs[0][0, :32] = 0.0                                   # an all-zero block: d = 0, codes 0
+            xs[0][0, 32:40] = [0.5, -0.5, 2.5, -2.5, 126.5, -126.5, 127.0, 0.49999997]
+        xds = [G.dev(x.reshape(-1)) for x in xs]
+        wds = [G.dev(w.reshape(n, -1)) for w, n in zip(ws, Ns)]
+        ys = [torch.full((1, n), float("nan"), dtype=torch.float32, device="cuda") for n in Ns]
+        B.GEMV_GROUPED_X[fmt]([(wd, n, xd, y) for wd, n, xd, y in zip(wds, Ns, xds, ys)], K)
+        torch.cuda.synchronize()
+        B.mq_device_status()
+        planes = [G.gpu_plane(x)[0] for x in xs]
+        yp = [torch.empty((1, n), dtype=torch.float32, device="cuda") for n in Ns]
+        B.GEMV_GROUPED[fmt]([(wd, n, p, y) for wd, n, p, y in zip(wds, Ns, planes, yp)], K, 1)
+        torch.cuda.synchronize()
+        for i, n in enumerate(Ns):
+            assert torch.equal(ys[i], yp[i]), (fmt, K, n)
+            ref = oracle.matmul(ws[i], fmt, G.oracle_plane(xs[i]), threads=8)
+            assert G.rel_err(ys[i].cpu().numpy(), ref) <= G.REL_TOL
+
+
 def test_grouped_quantize_matches_single_calls():
     import torch
     for M, K, n in ((1, 3584, 3), (1, 18944, 1), (5, 512, 8)):
