@@ -295,8 +295,8 @@ MQ_API int mq_gemv_grouped_q6k(const mq_gemv_job *jobs, int n_jobs, int64_t K, i
  *            w, N and y as for mq_gemv_q4k / _q5k / _q6k with M = 1; x f32 [K], 16-byte aligned
  *            (device); jobs may share one x
  *   n_jobs   0 .. 8 (0: nothing to do); a job with N == 0 is skipped
- *   K        shared by every job; one token's staged codes must fit a CTA's shared memory
- *            (K below about 100 000)
+ *   K        shared by every job; one token's staged codes must fit a CTA's shared memory:
+ *            K <= 101888 (Q4_K), 96768 (Q5_K), 81920 (Q6_K)
  *
  * Each job's y is, bit for bit, the y of mq_quantize_q8(x) followed by mq_gemv_q4k / _q5k / _q6k
  * on that plane.  Errors: MQ_ERR_ARG for n_jobs outside 0 .. 8, a NULL table or pointer, negative

@@ -530,6 +530,32 @@ def test_grouped_gemv_from_f32_activations():
             assert G.rel_err(ys[i].cpu().numpy(), ref) <= G.REL_TOL
 
 
+def test_grouped_gemv_from_f32_staging_limit():
+    # the largest K whose staged codes fit one CTA, per format (include/mq.h); one super-block more
+    # is MQ_ERR_SHAPE before any launch
+    import torch
+    for fmt, kmax, bb in (("q4k", 101888, 144), ("q5k", 96768, 176), ("q6k", 81920, 210)):
+        K = kmax + 256
+        x = torch.zeros(K, dtype=torch.float32, device="cuda")
+        w = torch.zeros(K // 256 * bb, dtype=torch.uint8, device="cuda")
+        y = torch.zeros(8, dtype=torch.float32, device="cuda")
+        with pytest.raises(B.MQError) as e:
+            B.GEMV_GROUPED_X[fmt]([(w, 1, x, y)], K)
+        assert e.value.status == B.MQ_ERR_SHAPE, (fmt, e.value)
+    r = np.random.default_rng(77)
+    K = 81920
+    wt = _weights("q6k", 3, K, 78)
+    xk = inputs.activations(r, 1, K)
+    wd, xd = G.dev(wt.reshape(3, -1)), G.dev(xk.reshape(-1))
+    yx = torch.full((1, 3), float("nan"), dtype=torch.float32, device="cuda")
+    B.GEMV_GROUPED_X["q6k"]([(wd, 3, xd, yx)], K)
+    torch.cuda.synchronize()
+    yp = torch.empty_like(yx)
+    B.GEMV["q6k"](wd, 3, K, G.gpu_plane(xk)[0], 1, yp)
+    torch.cuda.synchronize()
+    assert torch.equal(yx, yp)
+
+
 def test_grouped_quantize_matches_single_calls():
     import torch
     for M, K, n in ((1, 3584, 3), (1, 18944, 1), (5, 512, 8)):
