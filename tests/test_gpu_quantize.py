@@ -40,7 +40,10 @@ def test_edge_values():
 
 def test_rms_quantize_bit_exact_small():
     r = np.random.default_rng(3)
-    for M, K in ((1, 3584), (5, 256), (64, 3584), (9, 4096), (7, 8192), (2, 18432), (3, 18944)):
+    # K <= 8192: rows in registers, 1 / 2 / 4 / 8 warps per token (K = 256 .. 1024, 1280 .. 2048,
+    # 2304 .. 4096, 4352 .. 8192); above, the warp-per-token producer
+    for M, K in ((1, 3584), (5, 256), (64, 3584), (6, 1536), (3, 2048), (9, 4096), (7, 8192), (2, 18432),
+                 (3, 18944)):
         x = inputs.activations(r, M, K)
         w = inputs.rms_weight(r, K)
         plane, got = G.gpu_plane(x, w, 1e-6)
