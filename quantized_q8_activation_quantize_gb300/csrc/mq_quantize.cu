@@ -188,10 +188,10 @@ __device__ __forceinline__ void pair_add(float &ah, float &al, float bh, float b
 }
 
 // r = 1 / sqrt(t / K + eps) rounded once to f32, from the sum of squares t = th + tl (reduced
-// from the lanes' pairs by pair_add), in f32 arithmetic only.  The lanes' pairs add as f32 pairs (relative error below 2^-43 for these
-// non-negative sums), t / K is an f32 pair (the remainder t - q K of the quotient q is exact for
-// K < 2^22), and one Newton step on rsqrtf's estimate y0 (error below 2^-21) gives y0 + yl within
-// 2^-41 of the value the same lane pairs give in f64.  When every point within 2^-38 y0 of
+// from the lanes' pairs by pair_add), in f32 arithmetic only.  The lanes' pairs add as f32 pairs
+// (relative error below 2^-43 for these non-negative sums), t / K is an f32 pair (the remainder
+// t - q K of the quotient q is exact for K < 2^22), and one Newton step on rsqrtf's estimate y0
+// (error below 2^-21) gives y0 + yl within 2^-41 of the value the same lane pairs give in f64.  When every point within 2^-38 y0 of
 // y0 + yl rounds to the same f32, that is r, and it equals the rounding of the f64 evaluation;
 // otherwise (about one token in 10^4: the value lies near a rounding boundary) or outside the
 // normal range the function returns false and the caller evaluates r in f64.  The f64 pipe of
