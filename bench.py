@@ -73,7 +73,7 @@ def parse_args():
 # current kernels (dram__bytes_read.sum + dram__bytes_write.sum); set to None whenever a kernel
 # changes until it is captured again.
 TRAFFIC_GEMM_Q4K_GATE = 97.276928e6 + 209.093120e6      # 18944x3584 Q4_K, M=3314 (Y is 251 MB)
-TRAFFIC_GEMM_Q6K_DOWN = 409.452288e6 + 43.629568e6      # 3584x18944 Q6_K, M=3314
+TRAFFIC_GEMM_Q6K_DOWN = 420.704000e6 + 43.702784e6      # 3584x18944 Q6_K, M=3314
 TRAFFIC_GEMV_Q6K_LMHEAD = 447.188736e6 + 3.509760e6     # 152064x3584 Q6_K, M=1
 # the legacy int8 tensor instruction's measured peak on this GPU (mma.sync.m16n8k32.s8, 152 SMs): context
 # only -- the GEMM does not use that instruction

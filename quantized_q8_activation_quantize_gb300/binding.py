@@ -331,8 +331,9 @@ SMALL_MAX_M = 32
 # the fewest tokens at which the size dispatch prefers the small-M kernel to the GEMV: measured on a
 # 152064 x 3584 LM head (GB300), the GEMV's time grows with its passes over W (8 tokens a pass for
 # Q4_K / Q5_K, 4 for Q6_K) while the small-M kernel's is flat up to 32 tokens; Q4_K: GEMV 0.168 ms at
-# 5 tokens, 0.256 at 8, small-M 0.213; Q6_K: GEMV 0.168 at 4, 0.334 at 8, small-M 0.321
-SMALL_MIN_M = {"q4k": 7, "q5k": 7, "q6k": 8}
+# 5 tokens, 0.256 at 8, small-M 0.213; Q6_K (int8 scales over the whole range): GEMV 0.168 at 4, 0.334
+# at 8 (two passes), 0.5 at 9 (three), small-M 0.348
+SMALL_MIN_M = {"q4k": 7, "q5k": 7, "q6k": 9}
 # debug op of each (kind, format) for mq_debug_blockdots
 DEBUG_OP = {("gemm", "q4k"): 0, ("gemm", "q6k"): 1, ("gemv", "q4k"): 2, ("gemv", "q6k"): 3, ("gemv", "q5k"): 4,
             ("gemm", "q5k"): 5, ("gemv", "q4_0"): 6, ("gemv", "q4_1"): 7, ("gemv", "q5_0"): 8, ("gemv", "q5_1"): 9,

@@ -115,12 +115,15 @@ def b32_weights(r: np.random.Generator, n_rows: int, k: int, fmt: str,
 
 
 def q6k_weights(r: np.random.Generator, n_rows: int, k: int,
-                scale_range=(-64, 63), d_range=(1e-3, 1e-2)) -> np.ndarray:
+                scale_range=(-128, 127), d_range=(1e-3, 1e-2)) -> np.ndarray:
     """Q6_K weight matrix as raw bytes, shape [n_rows, k/256, 210].
 
     The 128 low-bit bytes and 64 high-bit bytes are uniform random bytes; the
     16 int8 sub-block scales are uniform integers in ``scale_range``
-    (inclusive); d is fp16 drawn uniform in ``d_range``.
+    (inclusive; by default the whole int8 range, as a quantizer that maps each
+    super-block's largest sub-block scale to the end of the range produces:
+    a quarter of them odd with magnitude above 64); d is fp16 drawn uniform in
+    ``d_range``.
     """
     assert k % QK_K == 0
     nb = k // QK_K

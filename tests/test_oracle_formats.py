@@ -158,7 +158,10 @@ def test_generated_value_ranges():
         for b in range(w6.shape[1]):
             d, sc, q = oracle.q6k_fields(w6[n, b])
             assert 1e-3 * 0.999 <= d <= 1e-2 * 1.001
-            assert sc.min() >= -64 and sc.max() <= 63 and q.min() >= -32 and q.max() <= 31
+            assert sc.min() >= -128 and sc.max() <= 127 and q.min() >= -32 and q.max() <= 31
+    # the default scale range is the whole int8 range: odd scales above 64 in magnitude occur
+    sc_all = np.array([oracle.q6k_fields(w6[n, b])[1] for n in range(4) for b in range(w6.shape[1])])
+    assert ((np.abs(sc_all.astype(int)) > 64) & (sc_all % 2 != 0)).any()
 
 
 
