@@ -182,7 +182,7 @@ def qproj_prefill():
 
 
 def ffn_prefill(m: int = PREFILL_TOKENS):
-    """7B FFN prefill: gate/up W 18944 x 3584 (Q4_K), down W 3584 x 18944 (Q6_K, scales [-64, 63]).
+    """7B FFN prefill: gate/up W 18944 x 3584 (Q4_K), down W 3584 x 18944 (Q6_K, int8 scales over the whole range).
 
     x_hidden [m, 3584] N(0,1) goes through the RMSNorm producer (weight N(1, 0.1), eps 1e-6)
     for gate and up; x_ffn [m, 18944] N(0,1) is the down projection's plain input.
@@ -239,7 +239,7 @@ def b32_vocab_weights(fmt: str):
 
 
 def lm_head_weights():
-    """LM head weights: 152064 x 3584 Q6_K (scales [-64, 63]), 447,068,160 bytes."""
+    """LM head weights: 152064 x 3584 Q6_K (int8 scales over the whole range), 447,068,160 bytes."""
     return q6k_weights(rng(4, STREAM_W), VOCAB, HIDDEN)
 
 
@@ -254,5 +254,5 @@ def lm_head_x(m: int):
 
 
 def lm_head_case(m: int):
-    """LM head: W 152064 x 3584 (Q6_K, scales [-64, 63]), X m x 3584 N(0,1), m in {1, 16, 3314}."""
+    """LM head: W 152064 x 3584 (Q6_K, int8 scales over the whole range), X m x 3584 N(0,1), m in {1, 16, 3314}."""
     return {"w": lm_head_weights(), "x": lm_head_x(m), "fmt": "q6k"}
